@@ -1,0 +1,385 @@
+"""Benchmark of the sparse top-k MoE training step on GB300.
+
+One step = one full pass of the training step (router, dispatch, expert MLPs,
+combine, MSE + aux losses, the full backward including dX, SGD) through the C
+ABI entry point moe_train_step, on one synthetic batch already resident in HBM.
+
+Prints ONE JSON line (rank 0).  Default workload: the large layer (T=65536,
+D=4096, E=128, k=8, SwiGLU F=2048, bf16 with fp32 masters).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle on a sample
+
+N > 1 (under torchrun): every rank runs an independent replica of the step on
+its own GPU (replicas only: the layer has no cross-GPU exchange step here);
+value = all ranks' tokens / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "MoE train-step tokens/sec (fwd+bwd+SGD) at 1 GB300; expert-GEMM TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GB300_SMS = 152
+FFMA_PER_SM_PER_CLK = 128
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def expert_flops_per_step(wl: W.Workload) -> float:
+    """Algorithmic active-row FLOPs of the expert GEMMs in one training step:
+    per routed row 2*D*F per projection, SwiGLU has 3 projections (W1, W3, W2),
+    the two-layer MLP 2; backward is twice the forward."""
+    proj = 3 if wl.act == "swiglu" else 2
+    return 3.0 * proj * 2.0 * wl.D * wl.F * wl.R
+
+
+def router_flops_per_step(wl: W.Workload) -> float:
+    return 3.0 * 2.0 * wl.T * wl.D * wl.E
+
+
+def hbm_bytes(wl: W.Workload) -> dict:
+    """Algorithmic bytes per launch of the HBM-bound passes."""
+    es = 2 if wl.dtype == "bf16" else 4
+    T, D, R = wl.T, wl.D, wl.R
+    n_exp = (3 if wl.act == "swiglu" else 2) * wl.E * wl.D * wl.F
+    return {
+        "gather": T * D * es + R * D * es,                 # X once, Xe written
+        "combine_loss": R * D * es + 2 * T * D * 4,       # Ye, target read; dY written
+        "combine_bwd": T * D * 4 + 2 * R * D * es,        # dY, Ye read; dYe written
+        "sgd_experts": n_exp * (12 + (2 if wl.dtype == "bf16" else 0)) / (3 if wl.act == "swiglu" else 2),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
+    """One oracle training step on a bounded sample of the workload: T_s tokens
+    of the same layer width (D, F, k, activation, scores) over its first E_s
+    experts.  Returns (seconds, description)."""
+    import numpy as np
+    import torch
+    from oracle import moe_oracle as O
+
+    E_s = max(E_s, wl.k)
+    if wl.n_groups > 1:
+        per = wl.E // wl.n_groups
+        E_s = max(E_s, per * wl.topk_groups)
+        E_s = (E_s + per - 1) // per * per
+    n_groups = wl.n_groups if wl.n_groups == 1 else E_s // (wl.E // wl.n_groups)
+    topk_groups = min(wl.topk_groups, n_groups)
+    sub = W.Workload(wl.name + "_sample", T=T_s, D=wl.D, F=wl.F, E=E_s, k=wl.k, act=wl.act,
+                     score=wl.score, n_groups=n_groups, topk_groups=topk_groups,
+                     has_bias=wl.has_bias, dtype=wl.dtype, aux_alpha=wl.aux_alpha, lr=wl.lr,
+                     router_init=wl.router_init)
+    inp = W.make_inputs(sub, seed=seed)
+    f64 = lambda t: None if t is None else t.detach().double().numpy()  # noqa: E731
+    lp = wl.dtype == "bf16"
+    w = dict(w_gate=f64(inp["w_gate"]), w1=f64(inp["w1_bf16"] if lp else inp["w1"]),
+             w2=f64(inp["w2_bf16"] if lp else inp["w2"]),
+             w3=f64(inp["w3_bf16"] if lp and inp["w3"] is not None else inp["w3"]),
+             b1=f64(inp["b1"]), b2=f64(inp["b2"]), logit_bias=None)
+    x = f64(inp["x_bf16"] if lp else inp["x"])
+    tgt = f64(inp["target"])
+    cfg = O.OracleConfig(T=T_s, D=wl.D, F=wl.F, E=E_s, k=wl.k, act=wl.act, score=wl.score,
+                         n_groups=n_groups, topk_groups=topk_groups, has_bias=wl.has_bias,
+                         aux_alpha=wl.aux_alpha)
+    t0 = time.perf_counter()
+    O.train_step(cfg, w, x, tgt, wl.lr)
+    dt = time.perf_counter() - t0
+    desc = (f"oracle train step (fwd+bwd+SGD, float64 numpy) on {T_s} tokens of the "
+            f"{wl.name} layer (D={wl.D}, F={wl.F}, k={wl.k}) over {E_s} of its {wl.E} experts")
+    return dt, desc
+
+
+def sample_size(wl: W.Workload):
+    """Tokens / experts of the CPU sample: about 10-30 s of float64 work."""
+    per_tok = 3 * (3 if wl.act == "swiglu" else 2) * 2 * wl.D * wl.F * wl.k
+    T_s = int(max(16, min(wl.T, 2.0e11 / per_tok)))
+    E_s = min(wl.E, 16)
+    return T_s, E_s
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    T_s, E_s = sample_size(wl)
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        dt, desc = oracle_sample_step(wl, T_s, E_s)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = T_s * len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl: W.Workload) -> dict:
+    return {"workload": wl.name, "tokens": wl.T, "d_model": wl.D, "d_ff": wl.F, "experts": wl.E,
+            "top_k": wl.k, "activation": wl.act, "scores": wl.score, "n_groups": wl.n_groups,
+            "topk_groups": wl.topk_groups, "expert_dtype": wl.dtype, "aux_alpha": wl.aux_alpha,
+            "lr": wl.lr, "global_batch": wl.T, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (weights and expert-major activations >> 129 MB)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="large", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernels", action="store_true", help="print per-kernel times to stderr")
+    args = ap.parse_args()
+    wl = W.WORKLOADS[args.workload]
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from sparse_mixture_experts_softmax_gb300 import binding as B
+    from sparse_mixture_experts_softmax_gb300.layer import MoELayer
+
+    inp = W.make_inputs(wl, seed=0, device=str(dev))
+    lp = wl.dtype == "bf16"
+    layer = MoELayer(wl.T, wl.D, wl.F, wl.E, wl.k, wl.act, wl.score, wl.dtype, wl.has_bias,
+                     wl.aux_alpha, inp["w_gate"], inp["w1"], inp["w2"], w3=inp["w3"],
+                     b1=inp["b1"], b2=inp["b2"], logit_bias=inp["logit_bias"],
+                     n_groups=wl.n_groups, topk_groups=wl.topk_groups,
+                     w1_lp=inp.get("w1_bf16"), w3_lp=inp.get("w3_bf16"),
+                     w2_lp=inp.get("w2_bf16"), device=str(dev))
+    x = (inp["x_bf16"] if lp else inp["x"]).contiguous()
+    tgt = inp["target"].contiguous()
+    dx = torch.empty(wl.T, wl.D, device=dev)
+    for k_ in ("w1", "w2", "w3", "w1_bf16", "w2_bf16", "w3_bf16"):
+        inp.pop(k_, None)
+    torch.cuda.empty_cache()
+
+    for _ in range(args.warmup):
+        layer.train_step(x, tgt, wl.lr, dx=dx)
+    torch.cuda.synchronize()
+    launches = B.moe_last_launch_count()
+
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    B.moe_profile_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(args.steps):
+        layer.train_step(x, tgt, wl.lr, dx=dx)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = start.elapsed_time(end)
+    prof = B.moe_profile_read()
+    B.moe_profile_enable(False)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = wl.T * world * args.steps / (ms_total / 1e3)
+    loss = layer.d_loss.cpu().tolist()
+
+    # per-kernel times over the timed region
+    per_kernel = {}
+    for name, ms in prof:
+        per_kernel[name] = per_kernel.get(name, 0.0) + ms
+    for k_ in per_kernel:
+        per_kernel[k_] /= args.steps
+    gemm_ms = sum(v for k_, v in per_kernel.items()
+                  if k_.startswith("gemm_") and not k_.startswith("gemm_router"))
+    peaks = load_peaks()
+    eflops = expert_flops_per_step(wl)
+    if lp:
+        achieved = eflops / (gemm_ms / 1e3) / 1e12
+        peak = float(peaks["bf16_tflops_sustained"])
+        bound, unit = "tensor", "TFLOP/s"
+    else:
+        achieved = eflops / (gemm_ms / 1e3) / 1e12
+        mhz = clk.get("sm_max_mhz") or 2070.0
+        peak = GB300_SMS * FFMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
+        bound, unit = "alu", "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None,
+                "kernel": "grouped expert GEMMs (all launches of one step)",
+                "peak_source": f"{peaks['source']} ({'bf16_tflops_sustained' if lp else 'FFMA at max clock'})"}
+    hb = hbm_bytes(wl)
+    hbm = {}
+    for name, key in (("gather", "gather"), ("combine_loss", "combine_loss"),
+                      ("combine_bwd", "combine_bwd")):
+        if name in per_kernel and per_kernel[name] > 0:
+            gbs = hb[key] / (per_kernel[name] / 1e3) / 1e9
+            hbm[name] = {"ms": per_kernel[name], "GB/s": gbs, "frac": gbs / float(peaks["hbm_gbs"])}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if lp else "f32", "data": "synthetic", "config": workload_config(wl),
+            "expert_gemm_tflops": achieved, "router_gflop_per_step": router_flops_per_step(wl) / 1e9,
+            "expert_gflop_per_step": eflops / 1e9, "roofline": roofline, "hbm_passes": hbm,
+            "gpu_launches": launches * args.steps, "clocks": clk,
+            "loss": {"mse": loss[0], "aux": loss[1]},
+            "kernels_ms_per_step": {k_: round(v, 4) for k_, v in sorted(per_kernel.items())}}
+
+    # end to end through the host-buffer entry point
+    if not args.no_e2e:
+        staging = torch.empty(B.moe_host_staging_size(layer.cfg), dtype=torch.uint8, device=dev)
+        x_host = x.cpu().pin_memory()
+        t_host = tgt.cpu().pin_memory()
+        l_host = torch.zeros(2, dtype=torch.float32).pin_memory()
+        for _ in range(1):
+            B.moe_train_step_host(layer.cfg, layer.params(), x_host, t_host, wl.lr, l_host,
+                                  staging, layer.workspace)
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            B.moe_train_step_host(layer.cfg, layer.params(), x_host, t_host, wl.lr, l_host,
+                                  staging, layer.workspace)
+        e2e_s = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        line["e2e"] = {"value": wl.T * world * args.steps / e2e_s, "unit": "tokens/s",
+                       "h2d_bytes_per_step": x_host.numel() * x_host.element_size()
+                       + t_host.numel() * 4, "d2h_bytes_per_step": 8}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        T_s, E_s = sample_size(wl)
+        dt, desc = oracle_sample_step(wl, T_s, E_s)
+        line["cpu_baseline"] = {"value": T_s / dt, "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": desc}
+    if args.kernels and rank == 0:
+        for k_, v in sorted(per_kernel.items(), key=lambda kv: -kv[1]):
+            print(f"{k_:20s} {v:9.3f} ms", file=sys.stderr)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse top-k mixture-of-experts layer.
+ *
+ * One training step of a sparse top-k MoE layer, as the course "Trainable MoE
+ * in CUDA" lays it out (Parts 1-7): router gate matmul -> scores (softmax, or
+ * the sigmoid group-limited variant of "AI Infra Kernel Lab", "Project status")
+ * -> per-token top-k and renormalisation -> dispatch (per-expert histogram,
+ * exclusive-scan slot offsets, gather into expert-major rows) -> each expert's
+ * two-layer MLP (ReLU / GELU-tanh with biases, or SwiGLU W2(SiLU(W1 x) * W3 x),
+ * "AI Infra Kernel Lab", "Numerical contracts") -> gate-weighted combine ->
+ * MSE task loss + load-balancing aux loss -> the full backward -> SGD.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Shapes: T tokens, D model width, F expert hidden width, E experts, k
+ *   experts per token, R = T*k routed rows.  All tensors are dense, row-major
+ *   and contiguous.  x is [T,D]; the router weight W_g is [E,D]; expert
+ *   weights use the [out,in] layout: W1, W3 [E,F,D], W2 [E,D,F], b1 [E,F],
+ *   b2 [E,D].  Index tensors are int32.
+ * - Memory: every pointer is a DEVICE pointer unless its comment says "host".
+ *   The caller owns all memory, including the workspace; the library never
+ *   allocates or frees.  Pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT).
+ * - Streams: all work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream).  No entry point synchronises the host except
+ *   moe_train_step_host, which waits for its own loss read-back.
+ * - Validation: every call checks its arguments on the host before the first
+ *   launch and returns a status; an unsupported request fails, it never falls
+ *   back to another code path.
+ * - Determinism: no floating-point atomics anywhere; the same inputs give the
+ *   same bits on every call.  Routing ties go to the smaller expert id (and
+ *   the smaller group id), as the grouped gate of "AI Infra Kernel Lab"
+ *   specifies; rows of one expert keep ascending token order.
+ * - Inputs are not modified, except the parameters moe_train_step updates.
+ *   Repeated calls are independent (course lesson "Define Expert Mlp Forward
+ *   And Backward", "Prove it works").
+ * - Precision: MOE_F32 computes in fp32 on CUDA cores.  MOE_BF16 feeds the
+ *   expert GEMMs bf16 operands with fp32 accumulation (tcgen05 tensor cores);
+ *   scores, gates, Y, dY, losses and every gradient of a parameter are fp32.
+ *
+ * Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= E <= 256, 1 <= k <= 32,
+ * k <= E; n_groups divides E and is <= 32; D and F are multiples of 8;
+ * T*k < 2^31.  SwiGLU experts carry no biases.  T = 0 is accepted and does no
+ * work (train step losses read 0).  The device must be sm_103.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* NULL pointer, negative size, inconsistent shape     */
+  MOE_ERR_UNSUPPORTED = 2,          /* dtype / activation / limits / device arch           */
+  MOE_ERR_ALIGNMENT = 3,            /* a pointer is not 16-byte aligned                    */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace smaller than moe_workspace_size()         */
+  MOE_ERR_CUDA = 5,                 /* a CUDA runtime/driver call failed                   */
+  MOE_ERR_TIMEOUT = 6               /* a bounded device-side wait expired                  */
+} moe_status;
+
+enum { MOE_ACT_RELU = 0, MOE_ACT_GELU_TANH = 1, MOE_ACT_SWIGLU = 2 };
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+/* Group score of the group-limited router: the pages do not define it; the
+ * default sums the two largest scores of a group, the alternative takes the
+ * group maximum. */
+enum { MOE_GROUP_TOP2_SUM = 0, MOE_GROUP_MAX = 1 };
+enum { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* Layer configuration.  n_groups = topk_groups = 1 selects plain top-k. */
+typedef struct {
+  int32_t T, D, F, E, k;
+  int32_t n_groups, topk_groups, group_score;
+  int32_t act;        /* MOE_ACT_*                                           */
+  int32_t score;      /* MOE_SCORE_*                                         */
+  int32_t dtype;      /* MOE_F32 | MOE_BF16: element type of x and expert W  */
+  int32_t has_bias;   /* expert biases b1, b2 (not with SwiGLU)              */
+  float aux_alpha;    /* L = L_mse + aux_alpha * aux                         */
+} moe_config;
+
+/* Read-only weights for moe_forward / moe_backward. */
+typedef struct {
+  const float* w_gate;      /* [E,D] fp32 router weight (the router has no bias)   */
+  const void* w1;           /* [E,F,D] in cfg.dtype                                */
+  const void* w3;           /* [E,F,D] in cfg.dtype, SwiGLU only, else NULL         */
+  const void* w2;           /* [E,D,F] in cfg.dtype                                */
+  const float* b1;          /* [E,F] fp32 or NULL (has_bias = 0)                   */
+  const float* b2;          /* [E,D] fp32 or NULL                                  */
+  const float* logit_bias;  /* [E] fixed, non-trainable bias added to the logits
+                               before the score, or NULL; -INFINITY never routes  */
+} moe_weights;
+
+/* fp32 gradient buffers, overwritten (never accumulated into) by each call:
+ * zeroing them beforehand is not needed.  Experts that receive no rows get
+ * exact zeros. */
+typedef struct {
+  float* dw_gate;   /* [E,D]              */
+  float* dw1;       /* [E,F,D]            */
+  float* dw3;       /* [E,F,D] or NULL    */
+  float* dw2;       /* [E,D,F]            */
+  float* db1;       /* [E,F] or NULL      */
+  float* db2;       /* [E,D] or NULL      */
+} moe_grads;
+
+/* Trainable parameters for moe_train_step.  The fp32 masters are updated in
+ * place by SGD; for MOE_BF16 the bf16 working copies (used by the expert GEMMs)
+ * are rewritten from the updated masters with round-to-nearest-even.  The
+ * router always uses its fp32 master. */
+typedef struct {
+  float* w_gate;            /* [E,D] fp32 master                         */
+  float* w1;                /* [E,F,D] fp32 master                       */
+  float* w3;                /* [E,F,D] fp32 master or NULL               */
+  float* w2;                /* [E,D,F] fp32 master                       */
+  float* b1;                /* [E,F] or NULL                             */
+  float* b2;                /* [E,D] or NULL                             */
+  void* w1_lp;              /* [E,F,D] bf16 copy (MOE_BF16) or NULL      */
+  void* w3_lp;              /* [E,F,D] bf16 copy or NULL                 */
+  void* w2_lp;              /* [E,D,F] bf16 copy or NULL                 */
+  const float* logit_bias;  /* [E] or NULL                               */
+  moe_grads grads;          /* gradient buffers, written by the step     */
+} moe_params;
+
+/* Bytes of device workspace the forward / backward / train step need for one
+ * configuration: routing state, expert-major activations saved for the
+ * backward, and reduction partials.  0 on an invalid configuration. */
+MOE_API size_t moe_workspace_size(const moe_config* cfg);
+
+/* Forward (course Parts 3, 4 and 5): router, dispatch, expert MLPs, combine.
+ * x [T,D] in cfg.dtype; y [T,D] fp32 output.  The routing and the activations
+ * the backward needs stay in `workspace`, which must then be passed unchanged
+ * to moe_backward. */
+MOE_API moe_status moe_forward(const moe_config* cfg, const moe_weights* w, const void* x, float* y,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of L = L_task + aux_alpha * aux given dy = dL_task/dy [T,D] fp32,
+ * using the state moe_forward left in `workspace` (same cfg, w and x).  Writes
+ * every gradient in `g` and, when dx is not NULL, dx [T,D] fp32 (expert path
+ * scattered back plus the router term).  The aux gradient to the router
+ * scores is aux_alpha * E * f_e / T with f_e = count_e / (T k) held constant
+ * (course Part 6, "Load Balancing Auxiliary Loss"). */
+MOE_API moe_status moe_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                        const float* dy, const moe_grads* g, float* dx,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* One training step (course Part 7, "Loss, Optimizer, and Training Loop"):
+ * forward, L_mse = mean over T*D of (y - y_target)^2, aux = E sum_e f_e P_e
+ * with P_e the mean router score of expert e, the full backward of
+ * L = L_mse + aux_alpha * aux (dx included), then theta <- theta - lr * grad
+ * for W_g, W1, W3, W2, b1, b2.  x is in cfg.dtype (it must equal the bf16
+ * rounding the expert weights' copies use for MOE_BF16); y_target [T,D] fp32.
+ * d_loss: device float[2] receiving (L_mse, aux) of the forward, before the
+ * update.  dx, when not NULL, receives dL/dx [T,D] fp32. */
+MOE_API moe_status moe_train_step(const moe_config* cfg, const moe_params* p, const void* x,
+                          const float* y_target, float lr, float* d_loss, float* dx,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device staging moe_train_step_host needs for x and y_target. */
+MOE_API size_t moe_host_staging_size(const moe_config* cfg);
+
+/* moe_train_step from HOST buffers: copies x_host [T,D] (cfg.dtype) and
+ * y_target_host [T,D] fp32 into `staging` (device, moe_host_staging_size
+ * bytes), runs the step on `stream`, copies the two losses back into
+ * loss_host[2] and waits for that copy.  Host buffers should be pinned for
+ * full copy bandwidth; pageable memory works but is slower. */
+MOE_API moe_status moe_train_step_host(const moe_config* cfg, const moe_params* p, const void* x_host,
+                               const float* y_target_host, float lr, float* loss_host,
+                               void* staging, size_t staging_bytes,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Copies the routing the last forward left in `workspace` into caller buffers
+ * (device, any may be NULL): scores [T,E] fp32, idx [T,k], gate [T,k] fp32,
+ * counts [E], offsets [E+1], src_tok [R] (slot -> token), slot_of [T,k]
+ * (token, j -> slot).  Device-to-device copies on `stream`. */
+MOE_API moe_status moe_get_routing(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                           float* scores, int32_t* idx, float* gate, int32_t* counts,
+                           int32_t* offsets, int32_t* src_tok, int32_t* slot_of, void* stream);
+
+/* Copies expert-major intermediates of the last forward/backward out of the
+ * workspace for inspection (device, any may be NULL): ye [R,D] and dxe [R,D]
+ * in cfg.dtype, dlogits [T,E] fp32. */
+MOE_API moe_status moe_get_intermediates(const moe_config* cfg, const void* workspace,
+                                 size_t workspace_bytes, void* ye, void* dxe, float* dlogits,
+                                 void* stream);
+
+/* Static text for a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Launch statistics of the last forward/backward/train-step call on this host
+ * thread: the number of kernels it enqueued.  Host-side bookkeeping only. */
+MOE_API int32_t moe_last_launch_count(void);
+
+/* Kernel timing for measurement tools.  While enabled, every kernel launch of
+ * the calling host thread is bracketed by two CUDA events on the launch
+ * stream.  Records accumulate over calls from the moe_profile_enable(1) that
+ * started them (at most 4096 kernels are kept); moe_profile_ms waits for the
+ * i-th recorded kernel to finish and returns its duration in milliseconds (-1
+ * for an invalid index). */
+MOE_API void moe_profile_enable(int32_t on);
+MOE_API int32_t moe_profile_count(void);
+MOE_API const char* moe_profile_name(int32_t i);
+MOE_API float moe_profile_ms(int32_t i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

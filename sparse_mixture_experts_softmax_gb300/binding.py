@@ -1,0 +1,219 @@
+"""ctypes binding of ``libmoe_gb300.so`` (the C ABI declared in ``include/moe.h``).
+
+Argument marshalling only: every function here forwards torch tensors' device
+pointers and sizes to the entry point of the same name, and raises
+``MoEError`` when the library returns a status other than ``MOE_OK``.  No step
+of the layer is computed in Python, and there is no fallback: if the library
+is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_ALIGNMENT = 3
+MOE_ERR_WORKSPACE_TOO_SMALL = 4
+MOE_ERR_CUDA = 5
+MOE_ERR_TIMEOUT = 6
+
+ACT = {"relu": 0, "gelu_tanh": 1, "swiglu": 2}
+SCORE = {"softmax": 0, "sigmoid": 1}
+GROUP_SCORE = {"top2_sum": 0, "max": 1}
+DTYPE = {"f32": 0, "bf16": 1}
+
+c_int32, c_float, c_void_p, c_size_t = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T", c_int32), ("D", c_int32), ("F", c_int32), ("E", c_int32), ("k", c_int32),
+                ("n_groups", c_int32), ("topk_groups", c_int32), ("group_score", c_int32),
+                ("act", c_int32), ("score", c_int32), ("dtype", c_int32), ("has_bias", c_int32),
+                ("aux_alpha", c_float)]
+
+
+class moe_weights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2", "logit_bias")]
+
+
+class moe_grads(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("dw_gate", "dw1", "dw3", "dw2", "db1", "db2")]
+
+
+class moe_params(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2",
+                                        "w1_lp", "w3_lp", "w2_lp", "logit_bias")] + \
+               [("grads", moe_grads)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn}: {text} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "sparse_mixture_experts_softmax_gb300.build.build_library()")
+        L = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.POINTER
+        L.moe_workspace_size.argtypes = [P(moe_config)]
+        L.moe_workspace_size.restype = c_size_t
+        L.moe_host_staging_size.argtypes = [P(moe_config)]
+        L.moe_host_staging_size.restype = c_size_t
+        L.moe_forward.argtypes = [P(moe_config), P(moe_weights), c_void_p, c_void_p, c_void_p,
+                                  c_size_t, c_void_p]
+        L.moe_backward.argtypes = [P(moe_config), P(moe_weights), c_void_p, c_void_p, P(moe_grads),
+                                   c_void_p, c_void_p, c_size_t, c_void_p]
+        L.moe_train_step.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p, c_float,
+                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+        L.moe_train_step_host.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p,
+                                          c_float, c_void_p, c_void_p, c_size_t, c_void_p,
+                                          c_size_t, c_void_p]
+        L.moe_get_routing.argtypes = [P(moe_config), c_void_p, c_size_t] + [c_void_p] * 8
+        L.moe_get_intermediates.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
+                                            c_void_p, c_void_p]
+        L.moe_status_string.argtypes = [c_int32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_last_launch_count.argtypes = []
+        L.moe_last_launch_count.restype = c_int32
+        L.moe_profile_enable.argtypes = [c_int32]
+        L.moe_profile_enable.restype = None
+        L.moe_profile_count.argtypes = []
+        L.moe_profile_count.restype = c_int32
+        L.moe_profile_name.argtypes = [c_int32]
+        L.moe_profile_name.restype = ctypes.c_char_p
+        L.moe_profile_ms.argtypes = [c_int32]
+        L.moe_profile_ms.restype = c_float
+        for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
+                   "moe_get_routing", "moe_get_intermediates"):
+            getattr(L, fn).restype = c_int32
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status, lib().moe_status_string(status).decode())
+
+
+def make_config(T, D, F, E, k, act="relu", score="softmax", n_groups=1, topk_groups=1,
+                group_score="top2_sum", dtype="f32", has_bias=True, aux_alpha=0.0) -> moe_config:
+    return moe_config(T, D, F, E, k, n_groups, topk_groups, GROUP_SCORE[group_score], ACT[act],
+                      SCORE[score], DTYPE[dtype], int(bool(has_bias)), float(aux_alpha))
+
+
+def make_weights(w_gate, w1, w2, w3=None, b1=None, b2=None, logit_bias=None) -> moe_weights:
+    return moe_weights(_ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(b1), _ptr(b2),
+                       _ptr(logit_bias))
+
+
+def make_grads(dw_gate, dw1, dw2, dw3=None, db1=None, db2=None) -> moe_grads:
+    return moe_grads(_ptr(dw_gate), _ptr(dw1), _ptr(dw3), _ptr(dw2), _ptr(db1), _ptr(db2))
+
+
+def make_params(w_gate, w1, w2, grads: moe_grads, w3=None, b1=None, b2=None, w1_lp=None,
+                w3_lp=None, w2_lp=None, logit_bias=None) -> moe_params:
+    return moe_params(_ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(b1), _ptr(b2),
+                      _ptr(w1_lp), _ptr(w3_lp), _ptr(w2_lp), _ptr(logit_bias), grads)
+
+
+def moe_workspace_size(cfg: moe_config) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_host_staging_size(cfg: moe_config) -> int:
+    return int(lib().moe_host_staging_size(ctypes.byref(cfg)))
+
+
+def moe_forward(cfg, weights, x, y, workspace, stream=None):
+    _check("moe_forward", lib().moe_forward(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x),
+                                            _ptr(y), _ptr(workspace), workspace.numel(),
+                                            _stream(stream)))
+
+
+def moe_backward(cfg, weights, x, dy, grads, dx, workspace, stream=None):
+    _check("moe_backward", lib().moe_backward(ctypes.byref(cfg), ctypes.byref(weights), _ptr(x),
+                                              _ptr(dy), ctypes.byref(grads), _ptr(dx),
+                                              _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_train_step(cfg, params, x, y_target, lr, d_loss, workspace, dx=None, stream=None):
+    _check("moe_train_step", lib().moe_train_step(ctypes.byref(cfg), ctypes.byref(params), _ptr(x),
+                                                  _ptr(y_target), float(lr), _ptr(d_loss),
+                                                  _ptr(dx), _ptr(workspace), workspace.numel(),
+                                                  _stream(stream)))
+
+
+def moe_train_step_host(cfg, params, x_host, y_target_host, lr, loss_host, staging, workspace,
+                        stream=None):
+    """x_host / y_target_host / loss_host are CPU tensors (pinned for full speed)."""
+    _check("moe_train_step_host",
+           lib().moe_train_step_host(ctypes.byref(cfg), ctypes.byref(params), _ptr(x_host),
+                                     _ptr(y_target_host), float(lr), _ptr(loss_host),
+                                     _ptr(staging), staging.numel(), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)))
+
+
+def moe_get_routing(cfg, workspace, scores=None, idx=None, gate=None, counts=None, offsets=None,
+                    src_tok=None, slot_of=None, stream=None):
+    _check("moe_get_routing",
+           lib().moe_get_routing(ctypes.byref(cfg), _ptr(workspace), workspace.numel(),
+                                 _ptr(scores), _ptr(idx), _ptr(gate), _ptr(counts), _ptr(offsets),
+                                 _ptr(src_tok), _ptr(slot_of), _stream(stream)))
+
+
+def moe_get_intermediates(cfg, workspace, ye=None, dxe=None, dlogits=None, stream=None):
+    _check("moe_get_intermediates",
+           lib().moe_get_intermediates(ctypes.byref(cfg), _ptr(workspace), workspace.numel(),
+                                       _ptr(ye), _ptr(dxe), _ptr(dlogits), _stream(stream)))
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_last_launch_count() -> int:
+    return int(lib().moe_last_launch_count())
+
+
+def moe_profile_enable(on: bool):
+    lib().moe_profile_enable(1 if on else 0)
+
+
+def moe_profile_read():
+    """[(kernel name, milliseconds)] of the last call on this thread (waits)."""
+    L = lib()
+    return [(L.moe_profile_name(i).decode(), float(L.moe_profile_ms(i)))
+            for i in range(L.moe_profile_count())]

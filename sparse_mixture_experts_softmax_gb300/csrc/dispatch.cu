@@ -1,0 +1,450 @@
+// Token dispatch and combine (course "Trainable MoE in CUDA", Part 4), the
+// losses (Parts 6 and 7) and the SGD update (Part 7).  No floating-point
+// atomics: every reduction has a fixed order, so results are bit-reproducible.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+// ---------------------------------------------------------------- dispatch --
+
+// Per-chunk expert histogram of the routed assignments (t, j) in token order.
+__global__ void __launch_bounds__(256)
+route_count_kernel(const int* __restrict__ idx, long long R, int E, int* __restrict__ chunk_counts) {
+  __shared__ int hist[256];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const long long lo = (long long)blockIdx.x * ROUTE_CHUNK;
+  const long long hi = min(lo + ROUTE_CHUNK, R);
+  for (long long f = lo + threadIdx.x; f < hi; f += blockDim.x) {
+    int e = idx[f];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);   // integer: order-independent
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// counts[e] = sum over chunks; offsets = exclusive scan of counts (offsets[E] = R);
+// chunk_counts[c][e] becomes the first slot of chunk c's rows for expert e.
+__global__ void __launch_bounds__(256)
+route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int* __restrict__ counts,
+                  int* __restrict__ offsets) {
+  __shared__ int tot[256];
+  __shared__ int scan[257];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int c = 0; c < nchunks; ++c) total += cc[(size_t)c * E + e];
+  }
+  tot[e] = (e < E) ? total : 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < E; ++i) { scan[i] = run; run += tot[i]; }
+    scan[E] = run;
+  }
+  __syncthreads();
+  if (e < E) {
+    counts[e] = total;
+    offsets[e] = scan[e];
+    int run = scan[e];
+    for (int c = 0; c < nchunks; ++c) {
+      int v = cc[(size_t)c * E + e];
+      cc[(size_t)c * E + e] = run;
+      run += v;
+    }
+  }
+  if (threadIdx.x == 0) offsets[E] = scan[E];
+}
+
+// Stable scatter: one warp walks its chunk in token order; lanes holding the
+// same expert are ranked by lane id (match_any), so slots keep token order.
+__global__ void __launch_bounds__(32)
+route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E,
+                     const int* __restrict__ chunk_base, int* __restrict__ src_tok,
+                     int* __restrict__ slot_of) {
+  __shared__ int cursor[256];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[(size_t)blockIdx.x * E + e];
+  __syncwarp();
+  const long long lo = (long long)blockIdx.x * ROUTE_CHUNK;
+  const long long hi = min(lo + ROUTE_CHUNK, R);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (long long base = lo; base < hi; base += 32) {
+    const long long f = base + lane;
+    const bool valid = f < hi;
+    int e = valid ? idx[f] : -1;
+    if ((unsigned)e >= (unsigned)E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    int slot = 0;
+    if (e >= 0) {
+      slot = cursor[e] + rank;
+      src_tok[slot] = (int)(f / k);
+      slot_of[f] = slot;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) cursor[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Xe[s, :] = X[src_tok[s], :] with 16-byte vectors, one warp per row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+gather_kernel(const T* __restrict__ x, const int* __restrict__ src_tok, long long R, int D,
+              T* __restrict__ xe) {
+  constexpr int VN = 16 / sizeof(T);
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int nv = D / VN;
+  for (long long s = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < R; s += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)src_tok[s] * D);
+    uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)s * D);
+    int v = lane;
+    for (; v + 96 < nv; v += 128) {
+      uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
+      dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
+    }
+    for (; v < nv; v += 32) dst[v] = src[v];
+  }
+}
+
+// ------------------------------------------------------------------ combine --
+
+constexpr int CB_TOK = 32;   // tokens per block (4 per warp)
+
+// Y[t] = sum_j g_tj Ye[slot(t, j)] in j order (fp32).  With a target it also
+// forms dY = 2 (Y - target) / (T D) and a per-block sum of squared errors.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
+               const int* __restrict__ slot_of, int Tn, int D, int k, float* __restrict__ y,
+               const float* __restrict__ target, float* __restrict__ dy, float inv_n,
+               double* __restrict__ sq_partial) {
+  constexpr int VN = Vec<T>::N;
+  __shared__ float wpart[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float sq = 0.f;
+  for (int tt = 0; tt < CB_TOK / 8; ++tt) {
+    const int t = blockIdx.x * CB_TOK + warp * (CB_TOK / 8) + tt;
+    if (t >= Tn) break;
+    for (int d = lane * VN; d < D; d += 32 * VN) {
+      float acc[VN];
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int s = slot_of[(size_t)t * k + j];
+        const float g = gate[(size_t)t * k + j];
+        Vec<T> v;
+        v.load(ye + (size_t)s * D + d);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] = fmaf(g, v.get(i), acc[i]);
+      }
+      if (y != nullptr) {
+#pragma unroll
+        for (int i = 0; i < VN; i += 4)
+          *reinterpret_cast<float4*>(y + (size_t)t * D + d + i) =
+              make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+      }
+      if (target != nullptr) {
+#pragma unroll
+        for (int i = 0; i < VN; i += 4) {
+          float4 tg = *reinterpret_cast<const float4*>(target + (size_t)t * D + d + i);
+          float d0 = acc[i] - tg.x, d1 = acc[i + 1] - tg.y, d2 = acc[i + 2] - tg.z,
+                d3 = acc[i + 3] - tg.w;
+          sq += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+          *reinterpret_cast<float4*>(dy + (size_t)t * D + d + i) =
+              make_float4(2.f * d0 * inv_n, 2.f * d1 * inv_n, 2.f * d2 * inv_n, 2.f * d3 * inv_n);
+        }
+      }
+    }
+  }
+  if (sq_partial != nullptr) {
+    sq = warp_sum(sq);
+    if (lane == 0) wpart[warp] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double s = 0.0;
+      for (int w = 0; w < 8; ++w) s += (double)wpart[w];
+      sq_partial[blockIdx.x] = s;
+    }
+  }
+}
+
+// L_mse = sum(sq_partial) / (T D);  P_e = sum_b psum[b][e] / T;  f_e = c_e / (T k);
+// aux = E sum_e f_e P_e;  aux_row[e] = alpha E f_e / T (d aux / d s_te, f constant).
+__global__ void __launch_bounds__(256)
+finalize_losses_kernel(const double* __restrict__ sq_partial, int n_sq,
+                       const float* __restrict__ psum, int n_ps, const int* __restrict__ counts,
+                       int T, int D, int E, int k, float alpha, float* __restrict__ d_loss,
+                       float* __restrict__ aux_row) {
+  __shared__ double red[256];
+  const int tid = threadIdx.x;
+  double s = 0.0;
+  for (int i = tid; i < n_sq; i += 256) s += sq_partial[i];
+  red[tid] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (tid < w) red[tid] += red[tid + w];
+    __syncthreads();
+  }
+  const double mse = red[0] / ((double)T * (double)D);
+  __syncthreads();
+  double term = 0.0;
+  for (int e = tid; e < E; e += 256) {
+    double P = 0.0;
+    for (int b = 0; b < n_ps; ++b) P += (double)psum[(size_t)b * E + e];
+    P /= (double)T;
+    const double f = (double)counts[e] / ((double)T * (double)k);
+    term += f * P;
+    if (aux_row != nullptr) aux_row[e] = (float)((double)alpha * (double)E * f / (double)T);
+  }
+  red[tid] = term;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (tid < w) red[tid] += red[tid + w];
+    __syncthreads();
+  }
+  if (tid == 0 && d_loss != nullptr) {
+    d_loss[0] = (float)mse;
+    d_loss[1] = (float)((double)E * red[0]);
+  }
+}
+
+// dYe[slot(t,j)] = g_tj dY[t];  dg_tj = <dY[t], Ye[slot(t,j)]>; one warp per token.
+template <typename T, int MAXK>
+__global__ void __launch_bounds__(256)
+combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
+                   const float* __restrict__ gate, const int* __restrict__ slot_of, int Tn, int D,
+                   int k, T* __restrict__ dye, float* __restrict__ dgate) {
+  constexpr int VN = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  int slot[MAXK];
+  float g[MAXK], dot[MAXK];
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j) {
+    slot[j] = (j < k) ? slot_of[(size_t)t * k + j] : 0;
+    g[j] = (j < k) ? gate[(size_t)t * k + j] : 0.f;
+    dot[j] = 0.f;
+  }
+  for (int d = lane * VN; d < D; d += 32 * VN) {
+    float dv[VN];
+#pragma unroll
+    for (int i = 0; i < VN; i += 4) {
+      float4 q = *reinterpret_cast<const float4*>(dy + (size_t)t * D + d + i);
+      dv[i] = q.x; dv[i + 1] = q.y; dv[i + 2] = q.z; dv[i + 3] = q.w;
+    }
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      if (j < k) {
+        Vec<T> v, o;
+        v.load(ye + (size_t)slot[j] * D + d);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) {
+          dot[j] = fmaf(dv[i], v.get(i), dot[j]);
+          o.set(i, g[j] * dv[i]);
+        }
+        o.store(dye + (size_t)slot[j] * D + d);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j) {
+    if (j < k) {
+      float s = warp_sum(dot[j]);
+      if (lane == 0) dgate[(size_t)t * k + j] = s;
+    }
+  }
+}
+
+// out[e, n] = sum over rows of segment e of src[r, n] (fixed order), for db.
+template <typename T>
+__global__ void __launch_bounds__(256)
+segment_colsum_kernel(const T* __restrict__ src, const int* __restrict__ offsets, int N,
+                      float* __restrict__ out) {
+  __shared__ float part[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int e = blockIdx.y;
+  const int n = blockIdx.x * 32 + tx;
+  const int lo = offsets[e], hi = offsets[e + 1];
+  float s = 0.f;
+  if (n < N)
+    for (int r = lo + ty; r < hi; r += 8) s += to_f(src[(size_t)r * N + n]);
+  part[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && n < N) {
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += part[i][tx];
+    out[(size_t)e * N + n] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+sum_partials_kernel(const float* __restrict__ p, int nparts, long long n, float* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int q = 0; q < nparts; ++q) s += p[(size_t)q * n + i];
+    out[i] = s;
+  }
+}
+
+// theta <- theta - lr * grad (fp32 master); optional bf16 working copy (RNE).
+__global__ void __launch_bounds__(256)
+sgd_kernel(float* __restrict__ w, const float* __restrict__ g, long long n4, float lr,
+           bf16* __restrict__ w_lp) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 wv = reinterpret_cast<float4*>(w)[i];
+    const float4 gv = reinterpret_cast<const float4*>(g)[i];
+    wv.x = fmaf(-lr, gv.x, wv.x);
+    wv.y = fmaf(-lr, gv.y, wv.y);
+    wv.z = fmaf(-lr, gv.z, wv.z);
+    wv.w = fmaf(-lr, gv.w, wv.w);
+    reinterpret_cast<float4*>(w)[i] = wv;
+    if (w_lp != nullptr) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(wv.x, wv.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(wv.z, wv.w);
+      uint2 q;
+      q.x = *reinterpret_cast<uint32_t*>(&lo);
+      q.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(w_lp)[i] = q;
+    }
+  }
+}
+
+inline int grid_for(long long n, int per_block, int cap) {
+  long long b = (n + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  return (int)(b < cap ? b : cap);
+}
+
+}  // namespace
+
+int route_chunks(long long R) { return (int)((R + ROUTE_CHUNK - 1) / ROUTE_CHUNK); }
+
+cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
+                               cudaStream_t st) {
+  int nc = route_chunks(R);
+  if (nc == 0) return cudaSuccess;
+  route_count_kernel<<<nc, 256, 0, st>>>(idx, R, E, chunk_counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int* counts, int* offsets,
+                              cudaStream_t st) {
+  route_scan_kernel<<<1, 256, 0, st>>>(chunk_counts, nchunks, E, counts, offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, const int* chunk_base,
+                                 int* src_tok, int* slot_of, cudaStream_t st) {
+  int nc = route_chunks(R);
+  if (nc == 0) return cudaSuccess;
+  route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, k, E, chunk_base, src_tok, slot_of);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(int dtype, const void* x, const int* src_tok, long long R, int D,
+                          void* xe, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  int grid = grid_for(R, 8, 152 * 16);
+  if (dtype == 1)
+    gather_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(x), src_tok, R, D,
+                                              static_cast<bf16*>(xe));
+  else
+    gather_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), src_tok, R, D,
+                                               static_cast<float*>(xe));
+  return cudaGetLastError();
+}
+
+int combine_blocks(int T) { return (T + CB_TOK - 1) / CB_TOK; }
+
+cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of, int T,
+                           int D, int k, float* y, const float* target, float* dy,
+                           double* sq_partial, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  float inv_n = 1.0f / ((float)T * (float)D);
+  int grid = combine_blocks(T);
+  if (dtype == 1)
+    combine_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T, D, k,
+                                               y, target, dy, inv_n, sq_partial);
+  else
+    combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(ye), gate, slot_of, T, D,
+                                                k, y, target, dy, inv_n, sq_partial);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
+                                   int n_ps, const int* counts, int T, int D, int E, int k,
+                                   float alpha, float* d_loss, float* aux_row, cudaStream_t st) {
+  finalize_losses_kernel<<<1, 256, 0, st>>>(sq_partial, n_sq, psum_partial, n_ps, counts, T, D, E,
+                                            k, alpha, d_loss, aux_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
+                               const int* slot_of, int T, int D, int k, void* dye, float* dgate,
+                               cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  int grid = (T + 7) / 8;
+  if (dtype == 1) {
+    if (k <= 8)
+      combine_bwd_kernel<bf16, 8><<<grid, 256, 0, st>>>(dy, static_cast<const bf16*>(ye), gate,
+                                                        slot_of, T, D, k, static_cast<bf16*>(dye),
+                                                        dgate);
+    else
+      combine_bwd_kernel<bf16, 32><<<grid, 256, 0, st>>>(dy, static_cast<const bf16*>(ye), gate,
+                                                         slot_of, T, D, k, static_cast<bf16*>(dye),
+                                                         dgate);
+  } else {
+    if (k <= 8)
+      combine_bwd_kernel<float, 8><<<grid, 256, 0, st>>>(dy, static_cast<const float*>(ye), gate,
+                                                         slot_of, T, D, k,
+                                                         static_cast<float*>(dye), dgate);
+    else
+      combine_bwd_kernel<float, 32><<<grid, 256, 0, st>>>(dy, static_cast<const float*>(ye), gate,
+                                                          slot_of, T, D, k,
+                                                          static_cast<float*>(dye), dgate);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets, int E, int N,
+                                  float* out, cudaStream_t st) {
+  dim3 grid((N + 31) / 32, E);
+  if (dtype == 1)
+    segment_colsum_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), offsets, N, out);
+  else
+    segment_colsum_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(src), offsets, N,
+                                                       out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,
+                                cudaStream_t st) {
+  sum_partials_kernel<<<grid_for(n, 256, 152 * 8), 256, 0, st>>>(partials, nparts, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sgd(float* w, const float* g, long long n, float lr, void* w_lp,
+                       cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  long long n4 = n / 4;   // every parameter tensor holds a multiple of 8 elements
+  sgd_kernel<<<grid_for(n4, 256, 152 * 16), 256, 0, st>>>(w, g, n4, lr, static_cast<bf16*>(w_lp));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t st) {
+  return cudaMemsetAsync(p, 0, bytes, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,261 @@
+// Grouped GEMMs on CUDA cores (fp32 FFMA), used where the operands are fp32:
+// the expert MLPs of fp32 layers and the router's dW_g / dX products.  Course
+// "Trainable MoE in CUDA", Part 1 (matmul variants, bias add) and Part 5
+// (expert MLP forward and backward over each expert's slice of rows).
+//
+// Tile 128x128x8, 256 threads, 8x8 outputs per thread, register-prefetched
+// double buffering.  Three operand forms (see GemmArgs in kernels.h):
+//   FORM 0  C[r,n] = sum_k A[r,k] B_e[n,k]   ragged M (x W^T)
+//   FORM 1  C[r,n] = sum_k A[r,k] B_e[k,n]   ragged M (x W)
+//   FORM 2  C_e[m,n] = sum_{r in e} A[r,m] B[r,n]   ragged K (weight gradients)
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace simt {
+
+constexpr int BM = 128, BN = 128, BK = 8, NT = 256;
+
+template <typename T>
+__device__ __forceinline__ float ld_f(const void* p, size_t i) {
+  return to_f(static_cast<const T*>(p)[i]);
+}
+__device__ __forceinline__ float ld_rt(const void* p, size_t i, int type) {
+  return type == 1 ? ld_f<bf16>(p, i) : ld_f<float>(p, i);
+}
+__device__ __forceinline__ void st_rt(void* p, size_t i, float v, int type) {
+  if (type == 1) static_cast<bf16*>(p)[i] = __float2bfloat16_rn(v);
+  else static_cast<float*>(p)[i] = v;
+}
+
+__device__ __forceinline__ int seg_lo(const GemmArgs& g, int e, int total) {
+  if (g.offsets) return g.offsets[e];
+  long long v = (long long)e * g.seg_len;
+  return (int)(v < total ? v : total);
+}
+__device__ __forceinline__ int seg_hi(const GemmArgs& g, int e, int total) {
+  if (g.offsets) return g.offsets[e + 1];
+  long long v = (long long)(e + 1) * g.seg_len;
+  return (int)(v < total ? v : total);
+}
+
+template <typename TA, typename TB, int FORM, int EPI>
+__global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
+  constexpr bool AK = FORM != 2;   // A element (m, k) has k contiguous
+  constexpr bool BKC = FORM == 0;  // B element (k, n) has k contiguous
+  constexpr bool RAGK = FORM == 2;
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
+  __shared__ int tile_start[258];
+  __shared__ int sel[3];
+
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int n0 = blockIdx.y * BN;
+  int e, m0, lo, hi;   // ragged-M: rows [lo, hi) of expert e; ragged-K: reduction rows
+  if (!RAGK) {
+    // map the linear tile index onto (expert, m-tile)
+    const int E = g.E;
+    for (int i = tid; i < E; i += NT) {
+      int l = seg_lo(g, i, g.M), h = seg_hi(g, i, g.M);
+      tile_start[i + 1] = (h - l + BM - 1) / BM;
+    }
+    if (tid == 0) { tile_start[0] = 0; sel[0] = -1; }
+    __syncthreads();
+    if (tid == 0)
+      for (int i = 1; i <= E; ++i) tile_start[i] += tile_start[i - 1];
+    __syncthreads();
+    const int tile = blockIdx.x;
+    for (int i = tid; i < E; i += NT)
+      if (tile >= tile_start[i] && tile < tile_start[i + 1]) {
+        sel[0] = i;
+        sel[1] = tile - tile_start[i];
+      }
+    __syncthreads();
+    e = sel[0];
+    if (e < 0) return;
+    lo = seg_lo(g, e, g.M);
+    hi = seg_hi(g, e, g.M);
+    m0 = lo + sel[1] * BM;
+  } else {
+    e = blockIdx.z;
+    m0 = blockIdx.x * BM;
+    lo = seg_lo(g, e, g.K0);
+    hi = seg_hi(g, e, g.K0);
+  }
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  // one or two (A, B, K) pairs; ragged-K has a single pair over rows [lo, hi)
+  const int npairs = (!RAGK && g.A1 != nullptr && g.K1 > 0) ? 2 : 1;
+  for (int pair = 0; pair < npairs; ++pair) {
+    const TA* A = static_cast<const TA*>(pair == 0 ? g.A0 : g.A1);
+    const TB* B = static_cast<const TB*>(pair == 0 ? g.B0 : g.B1);
+    if (!RAGK) B += (size_t)e * g.sBe;
+    const int kbeg = RAGK ? lo : 0;
+    const int kend = RAGK ? hi : (pair == 0 ? g.K0 : g.K1);
+    const int mlim = RAGK ? g.M : hi;
+    if (kend <= kbeg) continue;
+
+    float ra[4], rb[4];
+    auto load_tiles = [&](int k0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int l = tid + q * NT;
+        int m, kk;
+        if (AK) { m = l / BK; kk = l % BK; } else { m = l % BM; kk = l / BM; }
+        const int gm = m0 + m, gk = k0 + kk;
+        float v = 0.f;
+        if (gm < mlim && gk < kend)
+          v = to_f(AK ? A[(size_t)gm * g.lda + gk] : A[(size_t)gk * g.lda + gm]);
+        ra[q] = v;
+        int n, kb;
+        if (BKC) { n = l / BK; kb = l % BK; } else { n = l % BN; kb = l / BN; }
+        const int gn = n0 + n, gk2 = k0 + kb;
+        float w = 0.f;
+        if (gn < g.N && gk2 < kend)
+          w = to_f(BKC ? B[(size_t)gn * g.ldb + gk2] : B[(size_t)gk2 * g.ldb + gn]);
+        rb[q] = w;
+      }
+    };
+    auto store_tiles = [&](int buf) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int l = tid + q * NT;
+        int m, kk;
+        if (AK) { m = l / BK; kk = l % BK; } else { m = l % BM; kk = l / BM; }
+        As[buf][kk][m] = ra[q];
+        int n, kb;
+        if (BKC) { n = l / BK; kb = l % BK; } else { n = l % BN; kb = l / BN; }
+        Bs[buf][kb][n] = rb[q];
+      }
+    };
+
+    __syncthreads();
+    load_tiles(kbeg);
+    store_tiles(0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = kbeg; k0 < kend; k0 += BK) {
+      const bool more = k0 + BK < kend;
+      if (more) load_tiles(k0 + BK);
+#pragma unroll
+      for (int kk = 0; kk < BK; ++kk) {
+        float a[8], b[8];
+        const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
+        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+        a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      if (more) {
+        store_tiles(buf ^ 1);
+        __syncthreads();
+        buf ^= 1;
+      }
+    }
+  }
+
+  // epilogue
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    const bool rok = RAGK ? (r < g.M) : (r < hi);
+    if (!rok) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+      if (c >= g.N) continue;
+      float v = acc[i][j];
+      const size_t ci = RAGK ? (size_t)e * g.sCe + (size_t)r * g.ldc + c : (size_t)r * g.ldc + c;
+      const size_t ai = (size_t)r * g.ld_aux + c;
+      switch (EPI) {
+        case EPI_STORE:
+          if (g.bias) v += g.bias[(size_t)e * g.N + c];
+          st_rt(g.C, ci, v, g.c_type);
+          break;
+        case EPI_ACT_FWD: {
+          float h = v + (g.bias ? g.bias[(size_t)e * g.N + c] : 0.f);
+          st_rt(g.out1, ci, h, g.c_type);
+          st_rt(g.C, ci, g.act == 0 ? fmaxf(h, 0.f) : gelu_tanh_f(h), g.c_type);
+          break;
+        }
+        case EPI_SWIGLU_FWD: {
+          float h1 = ld_rt(g.aux0, ai, g.c_type);
+          st_rt(g.out1, ci, v, g.c_type);
+          st_rt(g.C, ci, silu_f(h1) * v, g.c_type);
+          break;
+        }
+        case EPI_ACT_BWD: {
+          float h = ld_rt(g.aux0, ai, g.c_type);
+          float dh = g.act == 0 ? (h > 0.f ? v : 0.f) : v * gelu_tanh_grad_f(h);
+          st_rt(g.C, ci, dh, g.c_type);
+          break;
+        }
+        case EPI_SWIGLU_BWD: {
+          float h1 = ld_rt(g.aux0, ai, g.c_type);
+          float h3 = ld_rt(g.aux1, ai, g.c_type);
+          st_rt(g.C, ci, v * h3 * silu_grad_f(h1), g.c_type);
+          st_rt(g.out1, ci, v * silu_f(h1), g.c_type);
+          break;
+        }
+        case EPI_SCATTER_ADD: {
+          float s = v;
+          for (int jj = 0; jj < g.k; ++jj) {
+            const int slot = g.slot_of[(size_t)r * g.k + jj];
+            s += ld_rt(g.src, (size_t)slot * g.N + c, g.src_type);
+          }
+          static_cast<float*>(g.C)[ci] = s;
+          break;
+        }
+      }
+    }
+  }
+}
+
+// FORM 0 / 1 are ragged-M (B k-contiguous / n-contiguous), FORM 2 ragged-K.
+template <typename TA, typename TB, int FORM, int EPI>
+cudaError_t launch_form(const GemmArgs& g, cudaStream_t st) {
+  if constexpr (FORM != 2) {
+    dim3 grid((g.M + BM - 1) / BM + g.E, (g.N + BN - 1) / BN);
+    gemm_simt_kernel<TA, TB, FORM, EPI><<<grid, NT, 0, st>>>(g);
+  } else {
+    dim3 grid((g.M + BM - 1) / BM, (g.N + BN - 1) / BN, g.E);
+    gemm_simt_kernel<TA, TB, 2, EPI><<<grid, NT, 0, st>>>(g);
+  }
+  return cudaGetLastError();
+}
+
+// Only the (form, epilogue) pairs the layer uses are instantiated.
+template <typename TA, typename TB>
+cudaError_t launch_expert_forms(const GemmArgs& g, cudaStream_t st) {
+  const int form = g.ragged_k ? 2 : (g.b_kcontig ? 0 : 1);
+  if (form == 0) {
+    if (g.epi == EPI_STORE) return launch_form<TA, TB, 0, EPI_STORE>(g, st);
+    if (g.epi == EPI_ACT_FWD) return launch_form<TA, TB, 0, EPI_ACT_FWD>(g, st);
+    if (g.epi == EPI_SWIGLU_FWD) return launch_form<TA, TB, 0, EPI_SWIGLU_FWD>(g, st);
+  } else if (form == 1) {
+    if (g.epi == EPI_STORE) return launch_form<TA, TB, 1, EPI_STORE>(g, st);
+    if (g.epi == EPI_ACT_BWD) return launch_form<TA, TB, 1, EPI_ACT_BWD>(g, st);
+    if (g.epi == EPI_SWIGLU_BWD) return launch_form<TA, TB, 1, EPI_SWIGLU_BWD>(g, st);
+  } else {
+    if (g.epi == EPI_STORE) return launch_form<TA, TB, 2, EPI_STORE>(g, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace simt
+}  // namespace moe

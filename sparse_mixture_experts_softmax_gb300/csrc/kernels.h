@@ -1,0 +1,110 @@
+// Host-side launchers of the MoE kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct RouterArgs {
+  int T, D, E, k;
+  int score;         // 0 softmax, 1 sigmoid
+  int n_groups, topk_groups, group_score;
+};
+
+// ---- router (router.cu)
+int router_fwd_blocks(int T);
+cudaError_t launch_router_fwd(int dtype, const void* x, const float* wg, const float* logit_bias,
+                              const RouterArgs& a, float* scores, int* idx, float* gate,
+                              float* psum_partial, cudaStream_t st);
+cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* gate,
+                              const float* dgate, const float* aux_row, const RouterArgs& a,
+                              float* dlogits, cudaStream_t st);
+
+// ---- dispatch, combine, losses, optimizer (dispatch.cu)
+constexpr int ROUTE_CHUNK = 1024;   // routed assignments per scatter chunk
+int route_chunks(long long R);
+cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
+                               cudaStream_t st);
+cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int* counts, int* offsets,
+                              cudaStream_t st);
+cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E,
+                                 const int* chunk_base, int* src_tok, int* slot_of,
+                                 cudaStream_t st);
+cudaError_t launch_gather(int dtype, const void* x, const int* src_tok, long long R, int D,
+                          void* xe, cudaStream_t st);
+int combine_blocks(int T);
+cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of,
+                           int T, int D, int k, float* y, const float* target, float* dy,
+                           double* sq_partial, cudaStream_t st);
+cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
+                                   int n_ps, const int* counts, int T, int D, int E, int k,
+                                   float alpha, float* d_loss, float* aux_row, cudaStream_t st);
+cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
+                               const int* slot_of, int T, int D, int k, void* dye, float* dgate,
+                               cudaStream_t st);
+cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets, int E, int N,
+                                  float* out, cudaStream_t st);
+cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,
+                                cudaStream_t st);
+cudaError_t launch_sgd(float* w, const float* g, long long n, float lr, void* w_lp,
+                       cudaStream_t st);
+cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t st);
+
+// ---- grouped GEMMs (gemm_simt.cu for fp32; gemm_tc.cu for bf16 on tcgen05)
+enum Epi {
+  EPI_STORE = 0,        // C = acc (+ bias[e, n])
+  EPI_ACT_FWD = 1,      // out1 = H = acc + bias;  C = act(H)
+  EPI_SWIGLU_FWD = 2,   // acc = H3; H1 read from aux0;  out1 = H3;  C = SiLU(H1) * H3
+  EPI_ACT_BWD = 3,      // acc = dA; H from aux0;  C = dA * act'(H)
+  EPI_SWIGLU_BWD = 4,   // acc = dA; H1 aux0, H3 aux1;  C = dH1;  out1 = dH3
+  EPI_SCATTER_ADD = 5   // C(fp32) = acc + sum_j src[slot_of[r, j], n]
+};
+
+// One grouped GEMM.  Ragged-M form (ragged_k = 0): rows [off_e, off_{e+1}) of
+// A use expert e's B;  C[r, n] = sum_k A(r, k) B_e(k, n).  Ragged-K form
+// (ragged_k = 1): C_e[m, n] = sum_{r in segment e} A(r, m) B(r, n).
+// Operand element (row, col) addresses: a_kcontig ? A[m*lda + k] : A[k*lda + m],
+// b_kcontig ? B_e[n*ldb + k] : B_e[k*ldb + n].  A second operand pair
+// (A1, B1, K1) extends the reduction (ragged-M only).  offsets == nullptr
+// means segments of seg_len rows.
+struct GemmArgs {
+  int a_type, b_type, c_type;   // 0 fp32, 1 bf16
+  const void* A0;
+  const void* B0;
+  int K0;
+  const void* A1;
+  const void* B1;
+  int K1;
+  long long lda, ldb, sBe;
+  bool a_kcontig, b_kcontig;
+  bool ragged_k;
+  int M, N;                     // ragged-M: M = total rows R; ragged-K: per-expert output M
+  const int* offsets;
+  int E;
+  int seg_len;
+  void* C;
+  long long ldc, sCe;
+  int epi;
+  int act;                      // 0 relu, 1 gelu_tanh
+  const float* bias;            // [E, N] or nullptr
+  const void* aux0;
+  const void* aux1;
+  void* out1;
+  long long ld_aux;
+  const int* slot_of;
+  int k;
+  const void* src;
+  int src_type;
+};
+
+cudaError_t launch_gemm_simt_f32(const GemmArgs& g, cudaStream_t st);
+cudaError_t launch_gemm_simt_bf16(const GemmArgs& g, cudaStream_t st);
+inline cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st) {
+  if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
+  if (g.a_type == 0 && g.b_type == 0) return launch_gemm_simt_f32(g, st);
+  return launch_gemm_simt_bf16(g, st);
+}
+
+}  // namespace moe

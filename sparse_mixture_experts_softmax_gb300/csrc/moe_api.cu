@@ -1,0 +1,703 @@
+// C ABI of the MoE layer: validation, workspace layout and the launch
+// sequence of forward, backward and the training step (course "Trainable MoE
+// in CUDA", Part 7: host orchestration of the forward pass, the backward pass
+// and one training step).  Every step runs in this library's kernels; there is
+// no host-side arithmetic on tensors and no fallback path.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local int g_launches = 0;
+
+// Optional per-kernel timing: CUDA events recorded around every kernel launch
+// of the calling thread's last entry-point call.
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+thread_local bool g_prof = false;
+thread_local std::vector<ProfRec> g_prof_recs;
+thread_local int g_prof_n = 0;
+
+inline void prof_begin(const char* name, cudaStream_t st) {
+  if (!g_prof || g_prof_n >= 4096) return;
+  if (g_prof_n == (int)g_prof_recs.size()) {
+    ProfRec r{name, nullptr, nullptr};
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+    g_prof_recs.push_back(r);
+  }
+  g_prof_recs[g_prof_n].name = name;
+  cudaEventRecord(g_prof_recs[g_prof_n].a, st);
+}
+inline void prof_end(cudaStream_t st) {
+  if (!g_prof || g_prof_n >= 4096 || g_prof_n >= (int)g_prof_recs.size()) return;
+  cudaEventRecord(g_prof_recs[g_prof_n].b, st);
+  ++g_prof_n;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline size_t esize(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// split-K factor of the router weight gradient dW_g = dlogits^T x
+inline int dwg_splits(int T) {
+  int s = T / 2048;
+  if (s < 1) s = 1;
+  if (s > 32) s = 32;
+  return s;
+}
+
+struct Layout {
+  size_t scores, idx, gate, counts, offsets, chunk, src_tok, slot_of, psum, sq, aux_row;
+  size_t xe, h1, h3, a, ye, dy, dye, dgate, dh1, dh3, dxe, dlogits, dwg_part, dx;
+  size_t total;
+};
+
+Layout make_layout(const moe_config& c) {
+  Layout L{};
+  const size_t T = (size_t)c.T, D = (size_t)c.D, F = (size_t)c.F, E = (size_t)c.E;
+  const size_t R = T * (size_t)c.k;
+  const size_t es = esize(c.dtype);
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o += align_up(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  L.scores = take(T * E * 4);
+  L.idx = take(R * 4);
+  L.gate = take(R * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.chunk = take((size_t)route_chunks((long long)R) * E * 4);
+  L.src_tok = take(R * 4);
+  L.slot_of = take(R * 4);
+  L.psum = take((size_t)router_fwd_blocks(c.T) * E * 4);
+  L.sq = take((size_t)combine_blocks(c.T) * 8);
+  L.aux_row = take(E * 4);
+  L.xe = take(R * D * es);
+  L.h1 = take(R * F * es);
+  L.h3 = swiglu ? take(R * F * es) : 0;
+  L.a = take(R * F * es);
+  L.ye = take(R * D * es);
+  L.dy = take(T * D * 4);
+  L.dye = take(R * D * es);
+  L.dgate = take(R * 4);
+  L.dh1 = take(R * F * es);
+  L.dh3 = swiglu ? take(R * F * es) : 0;
+  L.dxe = take(R * D * es);
+  L.dlogits = take(T * E * 4);
+  L.dwg_part = take((size_t)dwg_splits(c.T) * E * D * 4);
+  L.dx = take(T * D * 4);
+  L.total = o;
+  return L;
+}
+
+moe_status validate_config(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->D <= 0 || c->F <= 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (c->act < 0 || c->act > 2 || c->score < 0 || c->score > 1 || c->dtype < 0 || c->dtype > 1 ||
+      c->group_score < 0 || c->group_score > 1)
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_groups <= 0 || c->topk_groups <= 0 || c->topk_groups > c->n_groups)
+    return MOE_ERR_INVALID_ARG;
+  if (c->E > 256 || c->k > 32 || c->k > c->E) return MOE_ERR_UNSUPPORTED;
+  if (c->E % c->n_groups != 0 || c->n_groups > 32) return MOE_ERR_UNSUPPORTED;
+  if ((long long)c->k > (long long)c->topk_groups * (c->E / c->n_groups)) return MOE_ERR_UNSUPPORTED;
+  if (c->D % 8 != 0 || c->F % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
+  if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((long long)c->T * c->D >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Device check, once per device: sm_103 only.
+moe_status check_device() {
+  static std::mutex mu;
+  static int checked[64] = {0};   // 0 unknown, 1 ok, 2 bad
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (checked[dev] == 0) {
+    int maj = 0, min = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    checked[dev] = (maj == 10 && min == 3) ? 1 : 2;
+  }
+  return checked[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+// KL: a named kernel launch on stream `st` (counted, optionally timed);
+// CK: any other CUDA call.
+#define KL(name, expr)                           \
+  do {                                           \
+    prof_begin(name, st);                        \
+    cudaError_t _e = (expr);                     \
+    prof_end(st);                                \
+    ++g_launches;                                \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;  \
+  } while (0)
+#define CK(expr)                                 \
+  do {                                           \
+    cudaError_t _e = (expr);                     \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;  \
+  } while (0)
+
+struct Ptrs {
+  char* base;
+  const Layout* L;
+  template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+};
+
+struct ExpertW {
+  const float* w_gate;
+  const void* w1;
+  const void* w3;
+  const void* w2;
+  const float* b1;
+  const float* b2;
+  const float* logit_bias;
+};
+
+RouterArgs router_args(const moe_config& c) {
+  RouterArgs a;
+  a.T = c.T; a.D = c.D; a.E = c.E; a.k = c.k; a.score = c.score;
+  a.n_groups = c.n_groups; a.topk_groups = c.topk_groups; a.group_score = c.group_score;
+  return a;
+}
+
+GemmArgs gemm_base(const moe_config& c, const Ptrs& P) {
+  GemmArgs g{};
+  g.a_type = g.b_type = g.c_type = c.dtype;
+  g.offsets = P.at<int>(P.L->offsets);
+  g.E = c.E;
+  g.src_type = c.dtype;
+  g.act = c.act == MOE_ACT_GELU_TANH ? 1 : 0;
+  return g;
+}
+
+cudaError_t run_gemm(const moe_config& c, const GemmArgs& g, cudaStream_t st) {
+  (void)c;
+  return launch_gemm_simt(g, st);
+}
+
+// Forward: router -> dispatch -> experts -> combine.  With a target, combine
+// also forms dY and the squared-error partials, and the losses are finalised.
+moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, float* y,
+                       const float* target, float* d_loss, const Ptrs& P, cudaStream_t st) {
+  const Layout& L = *P.L;
+  const long long R = (long long)c.T * c.k;
+  const RouterArgs ra = router_args(c);
+  KL("router_fwd", launch_router_fwd(c.dtype, x, w.w_gate, w.logit_bias, ra, P.at<float>(L.scores),
+                       P.at<int>(L.idx), P.at<float>(L.gate), P.at<float>(L.psum), st));
+  KL("route_count", launch_route_count(P.at<int>(L.idx), R, c.E, P.at<int>(L.chunk), st));
+  KL("route_scan", launch_route_scan(P.at<int>(L.chunk), route_chunks(R), c.E, P.at<int>(L.counts),
+                       P.at<int>(L.offsets), st));
+  KL("route_scatter", launch_route_scatter(P.at<int>(L.idx), R, c.k, c.E, P.at<int>(L.chunk),
+                          P.at<int>(L.src_tok), P.at<int>(L.slot_of), st));
+  KL("gather", launch_gather(c.dtype, x, P.at<int>(L.src_tok), R, c.D, P.at<void>(L.xe), st));
+
+  // expert up-projection (+ activation)
+  GemmArgs g = gemm_base(c, P);
+  g.ragged_k = false;
+  g.a_kcontig = true;
+  g.b_kcontig = true;
+  g.M = (int)R;
+  g.N = c.F;
+  g.A0 = P.at<void>(L.xe);
+  g.lda = c.D;
+  g.K0 = c.D;
+  g.B0 = w.w1;
+  g.ldb = c.D;
+  g.sBe = (long long)c.F * c.D;
+  g.ldc = c.F;
+  g.ld_aux = c.F;
+  if (c.act == MOE_ACT_SWIGLU) {
+    g.epi = EPI_STORE;
+    g.C = P.at<void>(L.h1);
+    KL("gemm_up", run_gemm(c, g, st));
+    g.B0 = w.w3;
+    g.epi = EPI_SWIGLU_FWD;
+    g.aux0 = P.at<void>(L.h1);
+    g.out1 = P.at<void>(L.h3);
+    g.C = P.at<void>(L.a);
+    KL("gemm_up_w3", run_gemm(c, g, st));
+  } else {
+    g.epi = EPI_ACT_FWD;
+    g.bias = w.b1;
+    g.out1 = P.at<void>(L.h1);
+    g.C = P.at<void>(L.a);
+    KL("gemm_up", run_gemm(c, g, st));
+  }
+  // expert down-projection (+ bias)
+  GemmArgs d = gemm_base(c, P);
+  d.ragged_k = false;
+  d.a_kcontig = true;
+  d.b_kcontig = true;
+  d.M = (int)R;
+  d.N = c.D;
+  d.A0 = P.at<void>(L.a);
+  d.lda = c.F;
+  d.K0 = c.F;
+  d.B0 = w.w2;
+  d.ldb = c.F;
+  d.sBe = (long long)c.D * c.F;
+  d.ldc = c.D;
+  d.epi = EPI_STORE;
+  d.bias = w.b2;
+  d.C = P.at<void>(L.ye);
+  KL("gemm_down", run_gemm(c, d, st));
+
+  const bool train = target != nullptr;
+  KL("combine_loss", launch_combine(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of), c.T,
+                    c.D, c.k, y, target, train ? P.at<float>(L.dy) : nullptr,
+                    train ? P.at<double>(L.sq) : nullptr, st));
+  if (train)
+    KL("finalize_losses", launch_finalize_losses(P.at<double>(L.sq), combine_blocks(c.T), P.at<float>(L.psum),
+                              router_fwd_blocks(c.T), P.at<int>(L.counts), c.T, c.D, c.E, c.k,
+                              c.aux_alpha, d_loss, P.at<float>(L.aux_row), st));
+  return MOE_OK;
+}
+
+// Backward of L = L_task + alpha aux given dY (course Parts 4-6).
+moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, const float* dy,
+                        const moe_grads& gr, float* dx, bool aux_ready, const Ptrs& P,
+                        cudaStream_t st) {
+  const Layout& L = *P.L;
+  const long long R = (long long)c.T * c.k;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  if (!aux_ready)
+    KL("finalize_losses", launch_finalize_losses(P.at<double>(L.sq), 0, P.at<float>(L.psum), router_fwd_blocks(c.T),
+                              P.at<int>(L.counts), c.T, c.D, c.E, c.k, c.aux_alpha, nullptr,
+                              P.at<float>(L.aux_row), st));
+  KL("combine_bwd", launch_combine_bwd(c.dtype, dy, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of),
+                        c.T, c.D, c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st));
+  // dA = dYe W2_e with the activation backward in the epilogue
+  GemmArgs g = gemm_base(c, P);
+  g.ragged_k = false;
+  g.a_kcontig = true;
+  g.b_kcontig = false;
+  g.M = (int)R;
+  g.N = c.F;
+  g.A0 = P.at<void>(L.dye);
+  g.lda = c.D;
+  g.K0 = c.D;
+  g.B0 = w.w2;
+  g.ldb = c.F;
+  g.sBe = (long long)c.D * c.F;
+  g.ldc = c.F;
+  g.ld_aux = c.F;
+  g.aux0 = P.at<void>(L.h1);
+  g.C = P.at<void>(L.dh1);
+  if (swiglu) {
+    g.epi = EPI_SWIGLU_BWD;
+    g.aux1 = P.at<void>(L.h3);
+    g.out1 = P.at<void>(L.dh3);
+  } else {
+    g.epi = EPI_ACT_BWD;
+  }
+  KL("gemm_dA", run_gemm(c, g, st));
+  // dW2_e = dYe_e^T A_e  (ragged K)
+  GemmArgs w2g = gemm_base(c, P);
+  w2g.ragged_k = true;
+  w2g.a_kcontig = false;
+  w2g.b_kcontig = false;
+  w2g.c_type = MOE_F32;
+  w2g.M = c.D;
+  w2g.N = c.F;
+  w2g.A0 = P.at<void>(L.dye);
+  w2g.lda = c.D;
+  w2g.B0 = P.at<void>(L.a);
+  w2g.ldb = c.F;
+  w2g.K0 = (int)R;
+  w2g.C = gr.dw2;
+  w2g.ldc = c.F;
+  w2g.sCe = (long long)c.D * c.F;
+  w2g.epi = EPI_STORE;
+  KL("gemm_dw2", run_gemm(c, w2g, st));
+  if (gr.db2) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dye), P.at<int>(L.offsets), c.E, c.D, gr.db2, st));
+  // dXe = dH1 W1_e (+ dH3 W3_e)
+  GemmArgs xg = gemm_base(c, P);
+  xg.ragged_k = false;
+  xg.a_kcontig = true;
+  xg.b_kcontig = false;
+  xg.M = (int)R;
+  xg.N = c.D;
+  xg.A0 = P.at<void>(L.dh1);
+  xg.lda = c.F;
+  xg.K0 = c.F;
+  xg.B0 = w.w1;
+  xg.ldb = c.D;
+  xg.sBe = (long long)c.F * c.D;
+  if (swiglu) {
+    xg.A1 = P.at<void>(L.dh3);
+    xg.B1 = w.w3;
+    xg.K1 = c.F;
+  }
+  xg.ldc = c.D;
+  xg.epi = EPI_STORE;
+  xg.C = P.at<void>(L.dxe);
+  KL("gemm_dxe", run_gemm(c, xg, st));
+  // dW1_e = dH1_e^T Xe_e (dW3 likewise)
+  GemmArgs w1g = gemm_base(c, P);
+  w1g.ragged_k = true;
+  w1g.a_kcontig = false;
+  w1g.b_kcontig = false;
+  w1g.c_type = MOE_F32;
+  w1g.M = c.F;
+  w1g.N = c.D;
+  w1g.A0 = P.at<void>(L.dh1);
+  w1g.lda = c.F;
+  w1g.B0 = P.at<void>(L.xe);
+  w1g.ldb = c.D;
+  w1g.K0 = (int)R;
+  w1g.C = gr.dw1;
+  w1g.ldc = c.D;
+  w1g.sCe = (long long)c.F * c.D;
+  w1g.epi = EPI_STORE;
+  KL("gemm_dw1", run_gemm(c, w1g, st));
+  if (swiglu) {
+    w1g.A0 = P.at<void>(L.dh3);
+    w1g.C = gr.dw3;
+    KL("gemm_dw3", run_gemm(c, w1g, st));
+  }
+  if (gr.db1) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dh1), P.at<int>(L.offsets), c.E, c.F, gr.db1, st));
+
+  // router: renormalisation + aux + score backward
+  const RouterArgs ra = router_args(c);
+  KL("router_bwd", launch_router_bwd(P.at<float>(L.scores), P.at<int>(L.idx), P.at<float>(L.gate),
+                       P.at<float>(L.dgate), c.aux_alpha != 0.f ? P.at<float>(L.aux_row) : nullptr,
+                       ra, P.at<float>(L.dlogits), st));
+  // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
+  const int S = dwg_splits(c.T);
+  GemmArgs rg{};
+  rg.a_type = MOE_F32;
+  rg.b_type = c.dtype;
+  rg.c_type = MOE_F32;
+  rg.ragged_k = true;
+  rg.a_kcontig = false;
+  rg.b_kcontig = false;
+  rg.M = c.E;
+  rg.N = c.D;
+  rg.A0 = P.at<void>(L.dlogits);
+  rg.lda = c.E;
+  rg.B0 = x;
+  rg.ldb = c.D;
+  rg.K0 = c.T;
+  rg.offsets = nullptr;
+  rg.E = S;
+  rg.seg_len = (c.T + S - 1) / S;
+  rg.C = P.at<void>(L.dwg_part);
+  rg.ldc = c.D;
+  rg.sCe = (long long)c.E * c.D;
+  rg.epi = EPI_STORE;
+  KL("gemm_router_dwg", launch_gemm_simt(rg, st));
+  KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D, gr.dw_gate, st));
+  // dX = dlogits W_g + sum_j dXe[slot(t, j)]
+  GemmArgs dg{};
+  dg.a_type = MOE_F32;
+  dg.b_type = MOE_F32;
+  dg.c_type = MOE_F32;
+  dg.ragged_k = false;
+  dg.a_kcontig = true;
+  dg.b_kcontig = false;
+  dg.M = c.T;
+  dg.N = c.D;
+  dg.A0 = P.at<void>(L.dlogits);
+  dg.lda = c.E;
+  dg.K0 = c.E;
+  dg.B0 = w.w_gate;
+  dg.ldb = c.D;
+  dg.sBe = 0;
+  dg.offsets = nullptr;
+  dg.E = 1;
+  dg.seg_len = c.T;
+  dg.C = dx;
+  dg.ldc = c.D;
+  dg.epi = EPI_SCATTER_ADD;
+  dg.slot_of = P.at<int>(L.slot_of);
+  dg.k = c.k;
+  dg.src = P.at<void>(L.dxe);
+  dg.src_type = c.dtype;
+  KL("gemm_router_dx", launch_gemm_simt(dg, st));
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_config& c, const void* ws, size_t bytes) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MOE_ERR_ALIGNMENT;
+  if (bytes < make_layout(c).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+moe_status check_weights(const moe_config& c, const ExpertW& w) {
+  if (!w.w_gate || !w.w1 || !w.w2) return MOE_ERR_INVALID_ARG;
+  if (c.act == MOE_ACT_SWIGLU && !w.w3) return MOE_ERR_INVALID_ARG;
+  if (c.has_bias && (!w.b1 || !w.b2)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {w.w_gate, w.w1, w.w3, w.w2, w.b1, w.b2, w.logit_bias};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+moe_status check_grads(const moe_config& c, const moe_grads& g) {
+  if (!g.dw_gate || !g.dw1 || !g.dw2) return MOE_ERR_INVALID_ARG;
+  if (c.act == MOE_ACT_SWIGLU && !g.dw3) return MOE_ERR_INVALID_ARG;
+  if (c.has_bias && (!g.db1 || !g.db2)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {g.dw_gate, g.dw1, g.dw3, g.dw2, g.db1, g.db2};
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+#define RET_IF(expr)                \
+  do {                              \
+    moe_status _s = (expr);         \
+    if (_s != MOE_OK) return _s;    \
+  } while (0)
+
+moe_status zero_grads(const moe_config& c, const moe_grads& g, cudaStream_t st) {
+  const size_t E = c.E, D = c.D, F = c.F;
+  CK(launch_fill_zero(g.dw_gate, E * D * 4, st));
+  CK(launch_fill_zero(g.dw1, E * F * D * 4, st));
+  if (g.dw3) CK(launch_fill_zero(g.dw3, E * F * D * 4, st));
+  CK(launch_fill_zero(g.dw2, E * D * F * 4, st));
+  if (g.db1) CK(launch_fill_zero(g.db1, E * F * 4, st));
+  if (g.db2) CK(launch_fill_zero(g.db2, E * D * 4, st));
+  return MOE_OK;
+}
+
+moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const void* x,
+                           const float* y_target, float lr, float* d_loss, float* dx,
+                           void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  if (!p->w_gate || !p->w1 || !p->w2 || (c.act == MOE_ACT_SWIGLU && !p->w3))
+    return MOE_ERR_INVALID_ARG;
+  if (c.has_bias && (!p->b1 || !p->b2)) return MOE_ERR_INVALID_ARG;
+  if (c.dtype == MOE_BF16 && (!p->w1_lp || !p->w2_lp || (c.act == MOE_ACT_SWIGLU && !p->w3_lp)))
+    return MOE_ERR_INVALID_ARG;
+  RET_IF(check_grads(c, p->grads));
+  const void* ps[] = {p->w_gate, p->w1, p->w3, p->w2, p->b1, p->b2, p->w1_lp, p->w3_lp, p->w2_lp,
+                      p->logit_bias, x, y_target, d_loss, dx};
+  for (const void* q : ps)
+    if (q && !aligned16(q)) return MOE_ERR_ALIGNMENT;
+  if (c.T > 0 && (!x || !y_target)) return MOE_ERR_INVALID_ARG;
+  if (!d_loss) return MOE_ERR_INVALID_ARG;
+  RET_IF(check_device());
+
+  Layout L = make_layout(c);
+  Ptrs P{static_cast<char*>(workspace), &L};
+  if (c.T == 0) {
+    CK(cudaMemsetAsync(d_loss, 0, 2 * sizeof(float), st));
+    return zero_grads(c, p->grads, st);
+  }
+  ExpertW w;
+  w.w_gate = p->w_gate;
+  w.w1 = c.dtype == MOE_BF16 ? p->w1_lp : p->w1;
+  w.w3 = c.dtype == MOE_BF16 ? p->w3_lp : p->w3;
+  w.w2 = c.dtype == MOE_BF16 ? p->w2_lp : p->w2;
+  w.b1 = p->b1;
+  w.b2 = p->b2;
+  w.logit_bias = p->logit_bias;
+  RET_IF(run_forward(c, w, x, nullptr, y_target, d_loss, P, st));
+  float* dxp = dx ? dx : P.at<float>(L.dx);
+  RET_IF(run_backward(c, w, x, P.at<float>(L.dy), p->grads, dxp, true, P, st));
+  // SGD on the fp32 masters; bf16 working copies rewritten from the result
+  const long long E = c.E, D = c.D, F = c.F;
+  const moe_grads& g = p->grads;
+  KL("sgd", launch_sgd(p->w_gate, g.dw_gate, E * D, lr, nullptr, st));
+  KL("sgd", launch_sgd(p->w1, g.dw1, E * F * D, lr, c.dtype == MOE_BF16 ? p->w1_lp : nullptr, st));
+  if (c.act == MOE_ACT_SWIGLU)
+    KL("sgd", launch_sgd(p->w3, g.dw3, E * F * D, lr, c.dtype == MOE_BF16 ? p->w3_lp : nullptr, st));
+  KL("sgd", launch_sgd(p->w2, g.dw2, E * D * F, lr, c.dtype == MOE_BF16 ? p->w2_lp : nullptr, st));
+  if (c.has_bias) {
+    KL("sgd", launch_sgd(p->b1, g.db1, E * F, lr, nullptr, st));
+    KL("sgd", launch_sgd(p->b2, g.db2, E * D, lr, nullptr, st));
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg) {
+  if (validate_config(cfg) != MOE_OK) return 0;
+  return make_layout(*cfg).total;
+}
+
+moe_status moe_forward(const moe_config* cfg, const moe_weights* w, const void* x, float* y,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  g_launches = 0;
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias};
+  RET_IF(check_weights(c, ew));
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  if (c.T > 0 && (!x || !y)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (y && !aligned16(y))) return MOE_ERR_ALIGNMENT;
+  RET_IF(check_device());
+  if (c.T == 0) return MOE_OK;
+  Layout L = make_layout(c);
+  Ptrs P{static_cast<char*>(workspace), &L};
+  return run_forward(c, ew, x, y, nullptr, nullptr, P, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                        const float* dy, const moe_grads* g, float* dx, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  g_launches = 0;
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  if (w == nullptr || g == nullptr) return MOE_ERR_INVALID_ARG;
+  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias};
+  RET_IF(check_weights(c, ew));
+  RET_IF(check_grads(c, *g));
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  if (c.T > 0 && (!x || !dy)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || (dy && !aligned16(dy)) || (dx && !aligned16(dx)))
+    return MOE_ERR_ALIGNMENT;
+  RET_IF(check_device());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c.T == 0) return zero_grads(c, *g, st);
+  Layout L = make_layout(c);
+  Ptrs P{static_cast<char*>(workspace), &L};
+  float* dxp = dx ? dx : P.at<float>(L.dx);
+  return run_backward(c, ew, x, dy, *g, dxp, false, P, st);
+}
+
+moe_status moe_train_step(const moe_config* cfg, const moe_params* p, const void* x,
+                          const float* y_target, float lr, float* d_loss, float* dx,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  g_launches = 0;
+  return train_step_impl(cfg, p, x, y_target, lr, d_loss, dx, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_host_staging_size(const moe_config* cfg) {
+  if (validate_config(cfg) != MOE_OK) return 0;
+  const size_t n = (size_t)cfg->T * cfg->D;
+  return align_up(n * esize(cfg->dtype)) + align_up(n * 4) + kAlign;
+}
+
+moe_status moe_train_step_host(const moe_config* cfg, const moe_params* p, const void* x_host,
+                               const float* y_target_host, float lr, float* loss_host,
+                               void* staging, size_t staging_bytes, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  g_launches = 0;
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  if (!staging || !loss_host || (c.T > 0 && (!x_host || !y_target_host)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(staging)) return MOE_ERR_ALIGNMENT;
+  if (staging_bytes < moe_host_staging_size(cfg)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t n = (size_t)c.T * c.D;
+  char* sbase = static_cast<char*>(staging);
+  void* xd = sbase;
+  float* td = reinterpret_cast<float*>(sbase + align_up(n * esize(c.dtype)));
+  float* ld = reinterpret_cast<float*>(sbase + align_up(n * esize(c.dtype)) + align_up(n * 4));
+  if (n > 0) {
+    if (cudaMemcpyAsync(xd, x_host, n * esize(c.dtype), cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (cudaMemcpyAsync(td, y_target_host, n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  moe_status s = train_step_impl(cfg, p, xd, td, lr, ld, nullptr, workspace, workspace_bytes, st);
+  if (s != MOE_OK) return s;
+  if (cudaMemcpyAsync(loss_host, ld, 2 * sizeof(float), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_get_routing(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                           float* scores, int32_t* idx, float* gate, int32_t* counts,
+                           int32_t* offsets, int32_t* src_tok, int32_t* slot_of, void* stream) {
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  Layout L = make_layout(c);
+  const char* b = static_cast<const char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t T = c.T, E = c.E, R = (size_t)c.T * c.k;
+  struct Cp { void* dst; size_t off; size_t bytes; } cps[] = {
+      {scores, L.scores, T * E * 4}, {idx, L.idx, R * 4},       {gate, L.gate, R * 4},
+      {counts, L.counts, E * 4},     {offsets, L.offsets, (E + 1) * 4},
+      {src_tok, L.src_tok, R * 4},   {slot_of, L.slot_of, R * 4}};
+  for (const Cp& cp : cps)
+    if (cp.dst && cp.bytes)
+      if (cudaMemcpyAsync(cp.dst, b + cp.off, cp.bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_get_intermediates(const moe_config* cfg, const void* workspace,
+                                 size_t workspace_bytes, void* ye, void* dxe, float* dlogits,
+                                 void* stream) {
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  Layout L = make_layout(c);
+  const char* b = static_cast<const char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t R = (size_t)c.T * c.k, es = esize(c.dtype);
+  struct Cp { void* dst; size_t off; size_t bytes; } cps[] = {
+      {ye, L.ye, R * c.D * es}, {dxe, L.dxe, R * c.D * es}, {dlogits, L.dlogits, (size_t)c.T * c.E * 4}};
+  for (const Cp& cp : cps)
+    if (cp.dst && cp.bytes)
+      if (cudaMemcpyAsync(cp.dst, b + cp.off, cp.bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration, dtype or device";
+    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "bounded device wait expired";
+  }
+  return "unknown status";
+}
+
+int32_t moe_last_launch_count(void) { return g_launches; }
+
+void moe_profile_enable(int32_t on) {
+  g_prof = on != 0;
+  g_prof_n = 0;
+}
+
+int32_t moe_profile_count(void) { return g_prof_n; }
+
+const char* moe_profile_name(int32_t i) {
+  return (i >= 0 && i < g_prof_n) ? g_prof_recs[i].name : "";
+}
+
+float moe_profile_ms(int32_t i) {
+  if (i < 0 || i >= g_prof_n) return -1.f;
+  float ms = -1.f;
+  if (cudaEventSynchronize(g_prof_recs[i].b) != cudaSuccess) return -1.f;
+  if (cudaEventElapsedTime(&ms, g_prof_recs[i].a, g_prof_recs[i].b) != cudaSuccess) return -1.f;
+  return ms;
+}
+
+}  // extern "C"

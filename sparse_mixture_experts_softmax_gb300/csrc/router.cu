@@ -1,0 +1,363 @@
+// Router kernels: gate matmul -> scores -> top-k -> renormalised gates, and
+// the router backward (course "Trainable MoE in CUDA", Parts 2, 3 and 6;
+// group-limited sigmoid selection and its tie rule from "AI Infra Kernel Lab",
+// "Project status").
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int RT_TOK = 64;    // tokens per block
+constexpr int RT_BK = 32;     // D chunk staged in shared memory
+constexpr int RT_THREADS = 256;
+
+template <int NJ>
+struct RouterSmem {
+  static constexpr int EP = 16 * NJ;
+  static constexpr int stage_floats = RT_BK * (RT_TOK + 1) + RT_BK * (EP + 1);
+  static constexpr int logit_floats = RT_TOK * (EP + 1);
+  static constexpr int main_floats = stage_floats > logit_floats ? stage_floats : logit_floats;
+  static constexpr size_t bytes = sizeof(float) * (size_t)(main_floats + (RT_THREADS / 32) * EP);
+};
+
+struct Cand {
+  float v;
+  int id;
+};
+
+// (v, id) beats (v', id'): larger score, equal score -> smaller id.
+__device__ __forceinline__ bool better(float v, int id, float v2, int id2) {
+  return v > v2 || (v == v2 && id < id2);
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float v2 = __shfl_xor_sync(0xffffffffu, c.v, o);
+    int id2 = __shfl_xor_sync(0xffffffffu, c.id, o);
+    if (better(v2, id2, c.v, c.id)) { c.v = v2; c.id = id2; }
+  }
+  return c;
+}
+
+// Logits for RT_TOK tokens x E_pad experts (E_pad = 16*NJ), then one warp per
+// token for score, selection and renormalisation.
+template <typename XT, int NJ>
+__global__ void __launch_bounds__(RT_THREADS)
+router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
+                  const float* __restrict__ logit_bias, RouterArgs a,
+                  float* __restrict__ scores, int* __restrict__ idx, float* __restrict__ gate,
+                  float* __restrict__ psum_partial) {
+  constexpr int EP = 16 * NJ;
+  constexpr int NC = (EP + 31) / 32;   // scores per lane
+  // dynamic shared memory: the logits tile ls aliases the staging tiles xs/ws
+  extern __shared__ __align__(16) float rsm[];
+  float(*xs)[RT_TOK + 1] = reinterpret_cast<float(*)[RT_TOK + 1]>(rsm);
+  float(*ws)[EP + 1] = reinterpret_cast<float(*)[EP + 1]>(rsm + RT_BK * (RT_TOK + 1));
+  float(*ls)[EP + 1] = reinterpret_cast<float(*)[EP + 1]>(rsm);
+  float(*wsum)[EP] = reinterpret_cast<float(*)[EP]>(rsm + RouterSmem<NJ>::main_floats);
+
+  const int T = a.T, D = a.D, E = a.E;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * RT_TOK;
+
+  float acc[4][NJ];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) acc[i][j] = 0.f;
+
+  for (int d0 = 0; d0 < D; d0 += RT_BK) {
+    for (int l = tid; l < RT_TOK * RT_BK; l += RT_THREADS) {
+      int tk = l / RT_BK, dd = l % RT_BK;
+      int t = t0 + tk, d = d0 + dd;
+      xs[dd][tk] = (t < T && d < D) ? to_f(x[(size_t)t * D + d]) : 0.f;
+    }
+    for (int l = tid; l < EP * RT_BK; l += RT_THREADS) {
+      int e = l / RT_BK, dd = l % RT_BK;
+      int d = d0 + dd;
+      ws[dd][e] = (e < E && d < D) ? wg[(size_t)e * D + d] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < RT_BK; ++kk) {
+      float av[4], bv[NJ];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = xs[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) bv[j] = ws[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      int e = tx + 16 * j;
+      float bias = (logit_bias != nullptr && e < E) ? logit_bias[e] : 0.f;
+      ls[ty + 16 * i][e] = acc[i][j] + bias;
+    }
+  __syncthreads();
+
+  const int warp = tid >> 5, lane = tid & 31;
+  constexpr int TOK_PER_WARP = RT_TOK / (RT_THREADS / 32);
+  float colsum[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) colsum[c] = 0.f;
+
+  const int per = E / a.n_groups;
+  for (int tt = 0; tt < TOK_PER_WARP; ++tt) {
+    const int tk = warp * TOK_PER_WARP + tt;
+    const int t = t0 + tk;
+    if (t >= T) break;
+    float s[NC];
+    // score: softmax with max subtraction, or sigmoid
+    if (a.score == 0) {
+      float m = -FLT_MAX;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        s[c] = (e < E) ? ls[tk][e] : -INFINITY;
+        m = fmaxf(m, s[c]);
+      }
+      m = warp_max(m);
+      float z = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        s[c] = (e < E) ? expf(s[c] - m) : 0.f;
+        z += s[c];
+      }
+      z = warp_sum(z);
+      float inv = 1.0f / z;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) s[c] *= inv;
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        s[c] = (e < E) ? sigmoidf_(ls[tk][e]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      int e = lane + 32 * c;
+      if (e < E) {
+        scores[(size_t)t * E + e] = s[c];
+        ls[tk][e] = s[c];   // the warp's own row now holds the scores
+        colsum[c] += s[c];
+      }
+    }
+    __syncwarp();
+
+    // candidate mask: plain top-k = every expert; grouped = kept groups only
+    bool allowed[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) allowed[c] = (lane + 32 * c) < E;
+    if (a.n_groups > 1) {
+      float gs = -INFINITY;
+      if (lane < a.n_groups) {
+        float m1 = -INFINITY, m2 = -INFINITY;
+        for (int e = lane * per; e < (lane + 1) * per; ++e) {
+          float v = ls[tk][e];
+          if (v > m1) { m2 = m1; m1 = v; } else if (v > m2) { m2 = v; }
+        }
+        gs = (per == 1 || a.group_score == 1) ? m1 : m1 + m2;
+      }
+      bool taken = false;
+      unsigned keep = 0u;
+      for (int r = 0; r < a.topk_groups; ++r) {
+        Cand c;
+        c.v = (lane < a.n_groups && !taken) ? gs : -INFINITY;
+        c.id = (lane < a.n_groups && !taken) ? lane : 0x7fffffff;
+        c = warp_best(c);
+        int gsel = c.id;
+        if (gsel >= a.n_groups) {   // only reachable with NaN scores
+          gsel = __ffs(~keep & ((a.n_groups >= 32) ? 0xffffffffu : ((1u << a.n_groups) - 1u))) - 1;
+        }
+        keep |= 1u << gsel;
+        if (lane == gsel) taken = true;
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        allowed[c] = allowed[c] && ((keep >> (e / per)) & 1u);
+      }
+    }
+    // k rounds of a warp-wide arg-max; ties -> smaller id
+    float selv = 0.f, ssum = 0.f;
+    int selid = 0;
+    for (int j = 0; j < a.k; ++j) {
+      Cand best;
+      best.v = -INFINITY;
+      best.id = 0x7fffffff;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        if (allowed[c] && better(s[c], e, best.v, best.id)) { best.v = s[c]; best.id = e; }
+      }
+      best = warp_best(best);
+      if (best.id >= E) {
+        // no comparable candidate left (NaN scores): take the smallest allowed id
+        int cand = 0x7fffffff;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (allowed[c]) cand = min(cand, lane + 32 * c);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+        best.id = (cand < E) ? cand : 0;
+        best.v = __shfl_sync(0xffffffffu, s[0], 0);
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (lane + 32 * c == best.id) best.v = s[c];
+        best.v = __shfl_sync(0xffffffffu, best.v, best.id & 31);
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (lane + 32 * c == best.id) allowed[c] = false;
+      if (lane == j) { selv = best.v; selid = best.id; }
+      ssum += best.v;   // j order, identical on every lane
+    }
+    if (lane < a.k) {
+      idx[(size_t)t * a.k + lane] = selid;
+      gate[(size_t)t * a.k + lane] = selv / ssum;
+    }
+  }
+  // deterministic per-block column sums of the scores (for the aux loss)
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    int e = lane + 32 * c;
+    if (e < EP) wsum[warp][e] = colsum[c];
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += RT_THREADS) {
+    float sacc = 0.f;
+#pragma unroll
+    for (int w = 0; w < RT_THREADS / 32; ++w) sacc += wsum[w][e];
+    psum_partial[(size_t)blockIdx.x * E + e] = sacc;
+  }
+}
+
+// Router backward, one warp per token:
+//   dsel_j = (dg_j - sum_i dg_i g_i) / S,  S = sum_j s_{idx_j}
+//   ds_e   = aux_row_e + [e selected] dsel
+//   softmax: dl = s (ds - <ds, s>);  sigmoid: dl = ds s (1 - s)
+template <int NC>
+__global__ void __launch_bounds__(256)
+router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
+                  const float* __restrict__ gate, const float* __restrict__ dgate,
+                  const float* __restrict__ aux_row, RouterArgs a,
+                  float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const int E = a.E, k = a.k;
+  float s[NC], ds[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    int e = lane + 32 * c;
+    s[c] = (e < E) ? scores[(size_t)t * E + e] : 0.f;
+    ds[c] = (e < E && aux_row != nullptr) ? aux_row[e] : 0.f;
+  }
+  // gather S and <dg, g> in j order (identical on every lane)
+  float S = 0.f, inner = 0.f;
+  for (int j = 0; j < k; ++j) {
+    int e = idx[(size_t)t * k + j];
+    float sv = __shfl_sync(0xffffffffu, s[0], e & 31);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) {
+      float v = __shfl_sync(0xffffffffu, s[c], e & 31);
+      if ((e >> 5) == c) sv = v;
+    }
+    S += sv;
+    inner += dgate[(size_t)t * k + j] * gate[(size_t)t * k + j];
+  }
+  for (int j = 0; j < k; ++j) {
+    int e = idx[(size_t)t * k + j];
+    float dsel = (dgate[(size_t)t * k + j] - inner) / S;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (lane + 32 * c == e) ds[c] += dsel;
+  }
+  if (a.score == 0) {
+    float dot = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) dot += ds[c] * s[c];
+    dot = warp_sum(dot);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      int e = lane + 32 * c;
+      if (e < E) dlogits[(size_t)t * E + e] = s[c] * (ds[c] - dot);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      int e = lane + 32 * c;
+      if (e < E) dlogits[(size_t)t * E + e] = ds[c] * s[c] * (1.0f - s[c]);
+    }
+  }
+}
+
+}  // namespace
+
+int router_fwd_blocks(int T) { return (T + RT_TOK - 1) / RT_TOK; }
+
+template <typename XT, int NJ>
+static cudaError_t launch_fwd_nj(const void* x, const float* wg, const float* lb,
+                                 const RouterArgs& a, float* scores, int* idx, float* gate,
+                                 float* psum, cudaStream_t st) {
+  dim3 grid(router_fwd_blocks(a.T));
+  const size_t smem = RouterSmem<NJ>::bytes;
+  static bool attr_set = false;   // per instantiation; benign race (idempotent)
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(router_fwd_kernel<XT, NJ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  router_fwd_kernel<XT, NJ><<<grid, RT_THREADS, smem, st>>>(
+      static_cast<const XT*>(x), wg, lb, a, scores, idx, gate, psum);
+  return cudaGetLastError();
+}
+
+template <typename XT>
+static cudaError_t launch_fwd_t(const void* x, const float* wg, const float* lb,
+                                const RouterArgs& a, float* scores, int* idx, float* gate,
+                                float* psum, cudaStream_t st) {
+  if (a.E <= 16) return launch_fwd_nj<XT, 1>(x, wg, lb, a, scores, idx, gate, psum, st);
+  if (a.E <= 32) return launch_fwd_nj<XT, 2>(x, wg, lb, a, scores, idx, gate, psum, st);
+  if (a.E <= 64) return launch_fwd_nj<XT, 4>(x, wg, lb, a, scores, idx, gate, psum, st);
+  if (a.E <= 128) return launch_fwd_nj<XT, 8>(x, wg, lb, a, scores, idx, gate, psum, st);
+  return launch_fwd_nj<XT, 16>(x, wg, lb, a, scores, idx, gate, psum, st);
+}
+
+cudaError_t launch_router_fwd(int dtype, const void* x, const float* wg, const float* logit_bias,
+                              const RouterArgs& a, float* scores, int* idx, float* gate,
+                              float* psum_partial, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  if (dtype == 1)
+    return launch_fwd_t<bf16>(x, wg, logit_bias, a, scores, idx, gate, psum_partial, st);
+  return launch_fwd_t<float>(x, wg, logit_bias, a, scores, idx, gate, psum_partial, st);
+}
+
+cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* gate,
+                              const float* dgate, const float* aux_row, const RouterArgs& a,
+                              float* dlogits, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  dim3 grid((a.T + 7) / 8);
+  if (a.E <= 32) router_bwd_kernel<1><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
+  else if (a.E <= 64) router_bwd_kernel<2><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
+  else if (a.E <= 128) router_bwd_kernel<4><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
+  else router_bwd_kernel<8><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

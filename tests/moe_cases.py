@@ -1,0 +1,115 @@
+"""Shared helpers of the parity tests: build the oracle's view and the CUDA
+layer's view of one seeded workload, and compare them.
+
+The oracle side receives exactly the values the CUDA side computes with:
+fp32 draws for fp32 layers; for bf16 layers the bf16-rounded x and expert
+weights (widened to float64) and the fp32 router master.  Nothing the oracle
+consumes comes out of the CUDA library, except a routing that has first been
+validated against the oracle's own (see ``validated_routing``).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads as W
+from oracle import moe_oracle as O
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def oracle_config(wl: W.Workload, group_score="top2_sum") -> O.OracleConfig:
+    return O.OracleConfig(T=wl.T, D=wl.D, F=wl.F, E=wl.E, k=wl.k, act=wl.act, score=wl.score,
+                          n_groups=wl.n_groups, topk_groups=wl.topk_groups,
+                          group_score=group_score, has_bias=wl.has_bias,
+                          aux_alpha=wl.aux_alpha)
+
+
+def np64(t):
+    if t is None:
+        return None
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def oracle_inputs(wl: W.Workload, inp: dict):
+    """(weights used by forward/backward, fp32 master weights, x, target) in float64."""
+    lp = wl.dtype == "bf16"
+    w_fwd = dict(w_gate=np64(inp["w_gate"]),
+                 w1=np64(inp["w1_bf16"] if lp else inp["w1"]),
+                 w2=np64(inp["w2_bf16"] if lp else inp["w2"]),
+                 w3=np64(inp["w3_bf16"] if lp else inp["w3"]) if inp["w3"] is not None else None,
+                 b1=np64(inp["b1"]), b2=np64(inp["b2"]), logit_bias=np64(inp["logit_bias"]))
+    master = dict(w_gate=np64(inp["w_gate"]), w1=np64(inp["w1"]), w2=np64(inp["w2"]),
+                  w3=np64(inp["w3"]), b1=np64(inp["b1"]), b2=np64(inp["b2"]))
+    x = np64(inp["x_bf16"] if lp else inp["x"])
+    return w_fwd, master, x, np64(inp["target"])
+
+
+def make_layer(wl: W.Workload, inp: dict, device="cuda", group_score="top2_sum"):
+    from sparse_mixture_experts_softmax_gb300.layer import MoELayer
+    lp = wl.dtype == "bf16"
+    return MoELayer(wl.T, wl.D, wl.F, wl.E, wl.k, wl.act, wl.score, wl.dtype, wl.has_bias,
+                    wl.aux_alpha, inp["w_gate"], inp["w1"], inp["w2"], w3=inp["w3"],
+                    b1=inp["b1"], b2=inp["b2"], logit_bias=inp["logit_bias"],
+                    n_groups=wl.n_groups, topk_groups=wl.topk_groups, group_score=group_score,
+                    w1_lp=inp.get("w1_bf16") if lp else None,
+                    w3_lp=inp.get("w3_bf16") if lp else None,
+                    w2_lp=inp.get("w2_bf16") if lp else None, device=device)
+
+
+def device_x(wl: W.Workload, inp: dict, device="cuda"):
+    return (inp["x_bf16"] if wl.dtype == "bf16" else inp["x"]).to(device).contiguous()
+
+
+def rel_err(a, b) -> float:
+    """max |a - b| / max |b| over a tensor (0 when both are all zero)."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.max(np.abs(b)) if b.size else 0.0
+    num = np.max(np.abs(a - b)) if b.size else 0.0
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return float(num / den)
+
+
+def assert_close(name, got, want, tol):
+    err = rel_err(got, want)
+    assert err <= tol, f"{name}: max-norm relative error {err:.3e} > {tol:.1e}"
+    return err
+
+
+def check_routing_exact(cfg: O.OracleConfig, r: dict):
+    """Given the GPU's own fp32 scores, the oracle's selection and dispatch must
+    reproduce idx, counts, offsets and both slot maps bit for bit."""
+    scores = r["scores"].cpu().numpy()            # float32, the kernel's precision
+    idx_gpu = r["idx"].cpu().numpy()
+    idx_o = O.route(cfg, scores)
+    np.testing.assert_array_equal(idx_gpu, idx_o)
+    counts, offsets, src_tok, _, slot_of = O.dispatch(idx_gpu, cfg.E)
+    np.testing.assert_array_equal(r["counts"].cpu().numpy(), counts)
+    np.testing.assert_array_equal(r["offsets"].cpu().numpy(), offsets)
+    R = cfg.T * cfg.k
+    np.testing.assert_array_equal(r["src_tok"].cpu().numpy()[:R], src_tok)
+    np.testing.assert_array_equal(r["slot_of"].cpu().numpy(), slot_of)
+    # gates: renormalised selected scores, in the kernel's fp32
+    g = O.renormalize(scores.astype(np.float64), idx_gpu)
+    assert rel_err(r["gate"].cpu().numpy(), g) <= 1e-6
+
+
+def validated_routing(cfg: O.OracleConfig, scores64: np.ndarray, idx_gpu: np.ndarray,
+                      margin_tol: float = 1e-5) -> np.ndarray:
+    """Routing for the oracle's float values: its own fp64 selection, except on
+    tokens where fp64 and the GPU's fp32 disagree AND the fp64 scores of the two
+    choices lie within ``margin_tol`` of each other (a near-tie that rounding may
+    legitimately flip).  Any other disagreement fails."""
+    idx_o = O.route(cfg, scores64)
+    bad = np.nonzero(np.any(idx_o != idx_gpu, axis=1))[0]
+    for t in bad:
+        a = np.sort(scores64[t, idx_o[t]])
+        b = np.sort(scores64[t, idx_gpu[t]])
+        assert np.max(np.abs(a - b)) <= margin_tol * max(1.0, np.max(np.abs(scores64[t]))), \
+            f"token {t}: GPU routing {idx_gpu[t]} vs oracle {idx_o[t]} is not a near-tie"
+    out = idx_o.copy()
+    out[bad] = idx_gpu[bad]
+    return out

@@ -1,0 +1,118 @@
+"""The C ABI library loads, exports every entry point include/moe.h declares,
+and rejects bad arguments on the host (no GPU needed: validation runs before
+any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mixture_experts_softmax_gb300 import binding as B
+from sparse_mixture_experts_softmax_gb300.build import INCLUDE, LIB, build_library
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(LIB):
+        build_library()
+    return B.lib()
+
+
+def _declared():
+    names = []
+    for f in os.listdir(INCLUDE):
+        if f.endswith(".h"):
+            txt = open(os.path.join(INCLUDE, f)).read()
+            names += re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def _cfg(**kw):
+    base = dict(T=64, D=32, F=64, E=4, k=2, act="relu", score="softmax", dtype="f32",
+                has_bias=True, aux_alpha=0.01)
+    base.update(kw)
+    return B.make_config(**base)
+
+
+def test_workspace_size_valid_and_invalid(L):
+    assert B.moe_workspace_size(_cfg()) > 0
+    assert B.moe_workspace_size(_cfg(T=0)) > 0
+    assert B.moe_workspace_size(_cfg(k=0)) == 0
+    assert B.moe_workspace_size(_cfg(k=5)) == 0                 # k > E
+    assert B.moe_workspace_size(_cfg(E=300, k=2)) == 0          # E > 256
+    assert B.moe_workspace_size(_cfg(D=30)) == 0                # D % 8
+    assert B.moe_workspace_size(_cfg(act="swiglu", has_bias=True)) == 0
+    assert B.moe_workspace_size(_cfg(E=8, n_groups=3, topk_groups=1)) == 0
+    assert B.moe_workspace_size(_cfg(E=8, k=4, n_groups=4, topk_groups=1)) == 0  # k > kept
+    assert B.moe_host_staging_size(_cfg()) >= 64 * 32 * 8
+
+
+def test_workspace_grows_with_tokens(L):
+    a = B.moe_workspace_size(_cfg(T=64))
+    b = B.moe_workspace_size(_cfg(T=6400))
+    assert b > a
+
+
+class _Fake:
+    """Stands in for a tensor: a fake, aligned address (never dereferenced)."""
+    def __init__(self, addr, n=1 << 40):
+        self.addr, self.n = addr, n
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.n
+
+
+def _status(fn, *a):
+    with pytest.raises(B.MoEError) as ei:
+        fn(*a)
+    return ei.value.status
+
+
+def test_host_validation_errors(L):
+    good = lambda i: _Fake(0x10000 * (i + 1))  # noqa: E731
+    w = B.make_weights(good(1), good(2), good(3), b1=good(4), b2=good(5))
+    ws = _Fake(0x900000, 1 << 40)
+    assert _status(B.moe_forward, _cfg(k=0), w, good(6), good(7), ws) == B.MOE_ERR_INVALID_ARG
+    assert _status(B.moe_forward, _cfg(E=512, k=2), w, good(6), good(7), ws) == B.MOE_ERR_UNSUPPORTED
+    # missing bias pointers for a biased layer
+    w_nob = B.make_weights(good(1), good(2), good(3))
+    assert _status(B.moe_forward, _cfg(), w_nob, good(6), good(7), ws) == B.MOE_ERR_INVALID_ARG
+    # misaligned weight / input
+    w_bad = B.make_weights(_Fake(0x10008), good(2), good(3), b1=good(4), b2=good(5))
+    assert _status(B.moe_forward, _cfg(), w_bad, good(6), good(7), ws) == B.MOE_ERR_ALIGNMENT
+    assert _status(B.moe_forward, _cfg(), w, _Fake(0x60004), good(7), ws) == B.MOE_ERR_ALIGNMENT
+    # workspace too small
+    small = _Fake(0x900000, 1024)
+    assert _status(B.moe_forward, _cfg(), w, good(6), good(7), small) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    # SwiGLU needs W3
+    cs = _cfg(act="swiglu", has_bias=False)
+    w_no3 = B.make_weights(good(1), good(2), good(3))
+    assert _status(B.moe_forward, cs, w_no3, good(6), good(7), ws) == B.MOE_ERR_INVALID_ARG
+    # backward: grads required
+    g_missing = B.make_grads(good(8), good(9), None)
+    assert _status(B.moe_backward, _cfg(), w, good(6), good(7), g_missing, None, ws) == B.MOE_ERR_INVALID_ARG
+    # train step: bf16 layer without bf16 copies
+    g = B.make_grads(good(8), good(9), good(10), db1=good(11), db2=good(12))
+    p = B.make_params(good(1), good(2), good(3), g, b1=good(4), b2=good(5))
+    assert _status(B.moe_train_step, _cfg(dtype="bf16"), p, good(6), good(7), 0.1, good(13), ws) \
+        == B.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert B.moe_status_string(s)
+    assert "workspace" in B.moe_status_string(B.MOE_ERR_WORKSPACE_TOO_SMALL)

@@ -1,0 +1,221 @@
+"""Parity of the CUDA library (through its C ABI) with the float64 oracle.
+
+Routing is bit-exact given the GPU's own fp32 scores; float results meet the
+max-norm relative tolerance 1e-4 (fp32 layers) or 2e-2 (bf16 layers), on
+outputs, losses, every gradient and the updated weights.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import moe_oracle as O
+from tests.moe_cases import (TOL, assert_close, check_routing_exact, device_x, make_layer, np64,
+                             oracle_config, oracle_inputs, rel_err, validated_routing)
+
+pytestmark = pytest.mark.gpu
+
+
+def _grad_keys(wl):
+    keys = ["dw_gate", "dw1", "dw2"]
+    if wl.act == "swiglu":
+        keys.append("dw3")
+    if wl.has_bias:
+        keys += ["db1", "db2"]
+    return keys
+
+
+def _one_step_parity(wl, seed=0, check_dx=True):
+    """One training step on both sides; returns the errors by tensor."""
+    inp = W.make_inputs(wl, seed=seed)
+    cfg = oracle_config(wl)
+    tol = TOL[wl.dtype]
+    layer = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    tgt = inp["target"].cuda()
+    dx = torch.empty(wl.T, wl.D, device="cuda")
+    w0 = {k: (v.clone() if v is not None else None) for k, v in layer.param_dict().items()}
+    layer.train_step(x, tgt, wl.lr, dx=dx)
+    torch.cuda.synchronize()
+    r = layer.routing()
+    check_routing_exact(cfg, r)
+
+    w_fwd, master, x64, t64 = oracle_inputs(wl, inp)
+    st0 = O.forward(cfg, w_fwd, x64)
+    idx = validated_routing(cfg, st0["scores"], r["idx"].cpu().numpy())
+    st = O.forward(cfg, w_fwd, x64, idx)
+    l_mse, aux, dy = O.losses(cfg, st, t64)
+    g = O.backward(cfg, w_fwd, x64, st, dy)
+    errs = {}
+    loss = layer.d_loss.cpu().numpy()
+    errs["mse"] = assert_close("mse", loss[0], l_mse, tol)
+    errs["aux"] = assert_close("aux", loss[1], aux, tol)
+    got = layer.grad_dict()
+    for key in _grad_keys(wl):
+        errs[key] = assert_close(key, np64(got[key]), g[key], tol)
+    if check_dx:
+        errs["dx"] = assert_close("dx", np64(dx), g["dx"], tol)
+    # SGD: theta_1 = theta_0 - lr * grad on the fp32 masters
+    new = layer.param_dict()
+    for key in ("w_gate", "w1", "w2", "w3", "b1", "b2"):
+        if master.get(key) is None:
+            continue
+        want = master[key] - wl.lr * g["d" + key]
+        errs[key] = assert_close(key, np64(new[key]), want, tol)
+    return errs, layer, inp
+
+
+def test_tiny_20_step_loop():
+    """The fp32 tiny layer trained for 20 SGD steps: routing bit-exact at every
+    step, losses / gradients / weights within 1e-4 at every step, and the
+    accumulated weight change W_20 - W_0 within 1e-4."""
+    wl = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(wl, seed=0)
+    cfg = oracle_config(wl)
+    layer = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    tgt = inp["target"].cuda()
+    w_fwd, master, x64, t64 = oracle_inputs(wl, inp)
+    w0 = {k: v.copy() for k, v in master.items() if v is not None}
+    wo = dict(w_fwd)
+    dx = torch.empty(wl.T, wl.D, device="cuda")
+    losses_gpu = []
+    for step in range(wl.steps):
+        layer.train_step(x, tgt, wl.lr, dx=dx)
+        torch.cuda.synchronize()
+        r = layer.routing()
+        check_routing_exact(cfg, r)
+        st0 = O.forward(cfg, wo, x64)
+        idx = validated_routing(cfg, st0["scores"], r["idx"].cpu().numpy())
+        wo_new, (l_mse, aux), st, g = O.train_step(cfg, wo, x64, t64, wl.lr, idx)
+        loss = layer.d_loss.cpu().numpy()
+        losses_gpu.append(float(loss[0] + wl.aux_alpha * loss[1]))
+        assert_close(f"mse@{step}", loss[0], l_mse, 1e-4)
+        assert_close(f"aux@{step}", loss[1], aux, 1e-4)
+        for key in _grad_keys(wl):
+            assert_close(f"{key}@{step}", np64(layer.grad_dict()[key]), g[key], 1e-4)
+        assert_close(f"dx@{step}", np64(dx), g["dx"], 1e-4)
+        wo = wo_new
+        for key, v in layer.param_dict().items():
+            if v is not None:
+                assert_close(f"{key}@{step}", np64(v), wo[key], 1e-4)
+    for key, v in layer.param_dict().items():
+        if v is not None:
+            assert_close(f"delta {key}", np64(v) - w0[key], wo[key] - w0[key], 1e-4)
+    assert losses_gpu[-1] < losses_gpu[0]
+
+
+def test_dense_f32_step():
+    errs, _, _ = _one_step_parity(W.WORKLOADS["dense_f32"])
+    assert max(errs.values()) <= 1e-4
+
+
+def test_dense_bf16_step():
+    errs, _, _ = _one_step_parity(W.WORKLOADS["dense_bf16"])
+    assert max(errs.values()) <= 2e-2
+
+
+@pytest.mark.parametrize("name,T", [("grouped", 2048), ("skewed", 768), ("large", 256)])
+def test_swiglu_layers_reduced_tokens(name, T):
+    """The SwiGLU layers at their full width (D, F, E, k) on fewer tokens, so
+    the oracle finishes in seconds: ragged expert segments, F = 704 tails,
+    empty experts (skewed), grouped sigmoid routing (grouped)."""
+    wl = W.WORKLOADS[name].with_tokens(T)
+    errs, layer, _ = _one_step_parity(wl)
+    if name == "skewed":
+        counts = layer.routing()["counts"].cpu().numpy()
+        assert (counts == 0).sum() >= 4
+        empty = np.nonzero(counts == 0)[0]
+        for e in empty:
+            assert torch.all(layer.dw1[e] == 0) and torch.all(layer.dw2[e] == 0)
+            assert torch.all(layer.dw3[e] == 0)
+
+
+def test_forward_backward_match_train_step():
+    """moe_forward + moe_backward give the same bits as the train step's
+    forward and backward; forward output y matches the oracle."""
+    wl = W.WORKLOADS["dense_f32"].with_tokens(1000)
+    inp = W.make_inputs(wl, seed=3)
+    cfg = oracle_config(wl)
+    layer = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    y = layer.forward(x)
+    w_fwd, _, x64, t64 = oracle_inputs(wl, inp)
+    st0 = O.forward(cfg, w_fwd, x64)
+    idx = validated_routing(cfg, st0["scores"], layer.routing()["idx"].cpu().numpy())
+    st = O.forward(cfg, w_fwd, x64, idx)
+    assert_close("y", np64(y), st["y"], 1e-4)
+    _, _, dy = O.losses(cfg, st, t64)
+    dyt = torch.from_numpy(dy.astype(np.float32)).cuda()
+    dx = torch.empty_like(dyt)
+    layer.backward(x, dyt, dx)
+    g = O.backward(cfg, w_fwd, x64, st, dy)
+    for key in _grad_keys(wl):
+        assert_close(key, np64(layer.grad_dict()[key]), g[key], 1e-4)
+    assert_close("dx", np64(dx), g["dx"], 1e-4)
+
+
+def test_deterministic_and_inputs_unchanged():
+    wl = W.WORKLOADS["dense_bf16"].with_tokens(1500)
+    inp = W.make_inputs(wl, seed=5)
+    layer = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    x_copy = x.clone()
+    w_copy = {k: v.clone() for k, v in layer.param_dict().items() if v is not None}
+    y1 = layer.forward(x).clone()
+    dy = torch.randn(wl.T, wl.D, device="cuda") * 1e-3
+    dx1 = layer.backward(x, dy, torch.empty_like(dy)).clone()
+    g1 = {k: v.clone() for k, v in layer.grad_dict().items() if v is not None}
+    y2 = layer.forward(x)
+    dx2 = layer.backward(x, dy, torch.empty_like(dy))
+    assert torch.equal(y1, y2) and torch.equal(dx1, dx2)
+    for k, v in layer.grad_dict().items():
+        if v is not None:
+            assert torch.equal(g1[k], v), k
+    assert torch.equal(x, x_copy)
+    for k, v in layer.param_dict().items():
+        if v is not None:
+            assert torch.equal(w_copy[k], v), k
+
+
+def test_host_entry_point_matches_device():
+    from sparse_mixture_experts_softmax_gb300 import binding as B
+    wl = W.WORKLOADS["dense_f32"].with_tokens(640)
+    inp = W.make_inputs(wl, seed=6)
+    a = make_layer(wl, inp)
+    b = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    tgt = inp["target"].cuda()
+    a.train_step(x, tgt, wl.lr)
+    staging = torch.empty(B.moe_host_staging_size(b.cfg), dtype=torch.uint8, device="cuda")
+    loss_host = torch.zeros(2, dtype=torch.float32).pin_memory()
+    B.moe_train_step_host(b.cfg, b.params(), x.cpu().pin_memory(), inp["target"].pin_memory(),
+                          wl.lr, loss_host, staging, b.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(a.d_loss.cpu(), loss_host)
+    for k, v in a.param_dict().items():
+        if v is not None:
+            assert torch.equal(v, b.param_dict()[k]), k
+
+
+def test_empty_tokens():
+    wl = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(wl, seed=0)
+    layer = make_layer(wl.with_tokens(0), {**inp, "x": inp["x"][:0], "target": inp["target"][:0]})
+    x = torch.empty(0, wl.D, device="cuda")
+    layer.dw1.fill_(1.0)
+    layer.train_step(x, torch.empty(0, wl.D, device="cuda"), wl.lr)
+    torch.cuda.synchronize()
+    assert layer.d_loss.abs().sum().item() == 0.0
+    assert torch.all(layer.dw1 == 0)
+
+
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (1, 2, 4), (37, 4, 4), (130, 1, 3)])
+def test_edge_shapes(T, k, E):
+    """Single token, single expert, k = E, odd token counts."""
+    base = W.WORKLOADS["tiny"]
+    import dataclasses
+    wl = dataclasses.replace(base, T=T, k=k, E=E)
+    errs, _, _ = _one_step_parity(wl, seed=11)
+    assert max(errs.values()) <= 1e-4
