@@ -209,6 +209,27 @@ MOE_API int32_t moe_profile_count(void);
 MOE_API const char* moe_profile_name(int32_t i);
 MOE_API float moe_profile_ms(int32_t i);
 
+/* Dispatch without a workspace, for callers that may not allocate device
+ * memory when they route (for example while a stream is being captured into a
+ * CUDA graph, inside a runtime whose memory pool forbids outside allocations,
+ * or in a loop where an allocation could synchronise the device).  The pages
+ * have no counterpart of this entry point: it is a deployment convenience.
+ *
+ * Given idx [T,k] (each entry in [0,E)), writes counts [E], offsets [E+1],
+ * src_tok [T*k] and slot_of [T,k] exactly as moe_forward's dispatch does.  The
+ * per-chunk scratch counts live in one fixed device array inside the library
+ * (1 MiB on every GPU that loads it, held until the process exits), so T*k
+ * must not exceed MOE_NOALLOC_MAX_ROUTED (MOE_ERR_UNSUPPORTED otherwise).  It
+ * calls no allocating routine.  The first call on a device looks up that
+ * array's device address (with the device current); make that first call
+ * before any stream capture.  All calls share the array: calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race
+ * and must be serialised by the caller. */
+#define MOE_NOALLOC_MAX_ROUTED (1024 * 1024)
+MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* idx,
+                                        int32_t* counts, int32_t* offsets, int32_t* src_tok,
+                                        int32_t* slot_of, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -100,8 +100,9 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_name.restype = ctypes.c_char_p
         L.moe_profile_ms.argtypes = [c_int32]
         L.moe_profile_ms.restype = c_float
+        L.moe_dispatch_noalloc.argtypes = [P(moe_config)] + [c_void_p] * 6
         for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
-                   "moe_get_routing", "moe_get_intermediates"):
+                   "moe_get_routing", "moe_get_intermediates", "moe_dispatch_noalloc"):
             getattr(L, fn).restype = c_int32
         _lib = L
     return _lib
@@ -217,3 +218,14 @@ def moe_profile_read():
     L = lib()
     return [(L.moe_profile_name(i).decode(), float(L.moe_profile_ms(i)))
             for i in range(L.moe_profile_count())]
+
+
+MOE_NOALLOC_MAX_ROUTED = 1024 * 1024
+
+
+def moe_dispatch_noalloc(cfg, idx, counts, offsets, src_tok, slot_of, stream=None):
+    """Dispatch with the library's fixed scratch array (no allocation, no
+    workspace); see include/moe.h."""
+    _check("moe_dispatch_noalloc",
+           lib().moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(idx), _ptr(counts), _ptr(offsets),
+                                      _ptr(src_tok), _ptr(slot_of), _stream(stream)))
