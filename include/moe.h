@@ -191,6 +191,29 @@ MOE_API moe_status moe_get_intermediates(const moe_config* cfg, const void* work
                                  size_t workspace_bytes, void* ye, void* dxe, float* dlogits,
                                  void* stream);
 
+/* Reads the device status word of the last call that used `workspace`: 0, or
+ * MOE_ERR_TIMEOUT when a bounded device-side wait of a tensor-core kernel
+ * expired (that kernel then stopped early and its outputs are invalid).
+ * Synchronises `stream`. */
+MOE_API moe_status moe_device_status(const moe_config* cfg, const void* workspace,
+                                     size_t workspace_bytes, int32_t* status_host, void* stream);
+
+/* Grouped GEMM over contiguous expert row segments on the tcgen05 tensor
+ * cores, bf16 operands, fp32 accumulation (course "Trainable MoE in CUDA",
+ * Part 1 matmul variants, applied per expert as in Part 5).  Segment e holds
+ * rows [offsets[e], offsets[e+1]) of the row-indexed operands (offsets [E+1],
+ * device, non-decreasing, offsets[E] = total rows).
+ *   form 0: C[r,n] = sum_k A[r,k] B[e,n,k]    A [M,K], B [E,N,K], C [M,N] bf16
+ *   form 1: C[r,n] = sum_k A[r,k] B[e,k,n]    A [M,K], B [E,K,N], C [M,N] bf16
+ *   form 2: C[e,m,n] = sum_{r in e} A[r,m] B[r,n]
+ *                                            A [K,M], B [K,N], C [E,M,N] fp32
+ * (forms 0/1: M = total rows; form 2: K = total rows).  N, K (and M for form
+ * 2) must be multiples of 8.  dev_status: device int32, set to
+ * MOE_ERR_TIMEOUT if a bounded wait expired (the caller zeroes it). */
+MOE_API moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
+                                    const int32_t* offsets, const void* A, const void* B,
+                                    void* C, int32_t* dev_status, void* stream);
+
 /* Static text for a status code. */
 MOE_API const char* moe_status_string(moe_status s);
 

@@ -101,8 +101,11 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_ms.argtypes = [c_int32]
         L.moe_profile_ms.restype = c_float
         L.moe_dispatch_noalloc.argtypes = [P(moe_config)] + [c_void_p] * 6
+        L.moe_device_status.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p]
+        L.moe_grouped_gemm.argtypes = [c_int32] * 5 + [c_void_p] * 6
         for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
-                   "moe_get_routing", "moe_get_intermediates", "moe_dispatch_noalloc"):
+                   "moe_get_routing", "moe_get_intermediates", "moe_dispatch_noalloc",
+                   "moe_device_status", "moe_grouped_gemm"):
             getattr(L, fn).restype = c_int32
         _lib = L
     return _lib
@@ -229,3 +232,18 @@ def moe_dispatch_noalloc(cfg, idx, counts, offsets, src_tok, slot_of, stream=Non
     _check("moe_dispatch_noalloc",
            lib().moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(idx), _ptr(counts), _ptr(offsets),
                                       _ptr(src_tok), _ptr(slot_of), _stream(stream)))
+
+
+def moe_device_status(cfg, workspace, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check("moe_device_status",
+           lib().moe_device_status(ctypes.byref(cfg), _ptr(workspace), workspace.numel(),
+                                   ctypes.addressof(out), _stream(stream)))
+    return int(out.value)
+
+
+def moe_grouped_gemm(form, M, N, K, E, offsets, A, B, C, dev_status, stream=None):
+    """Grouped bf16 GEMM on the tensor cores (see include/moe.h)."""
+    _check("moe_grouped_gemm",
+           lib().moe_grouped_gemm(int(form), int(M), int(N), int(K), int(E), _ptr(offsets),
+                                  _ptr(A), _ptr(B), _ptr(C), _ptr(dev_status), _stream(stream)))

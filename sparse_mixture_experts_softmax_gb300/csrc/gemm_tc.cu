@@ -1,0 +1,740 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (sm_103a), bf16
+// operands with fp32 accumulation in tensor memory.  Course "Trainable MoE in
+// CUDA", Part 5 ("Expert MLP Forward and Backward": up/down projections,
+// biases, activation, and the backward for inputs, weights and biases over
+// each expert's slice of rows); the SwiGLU form W2(SiLU(W1 x) * W3 x) is the
+// one of "AI Infra Kernel Lab", "Numerical contracts".
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: 2-D / 3-D tiled bulk-tensor loads, 128-byte
+//               swizzle, into a 4-stage shared-memory ring (mbarrier tx count);
+//   warp 1      allocates 512 TMEM columns, issues tcgen05.mma (M=128, N=256,
+//               K=16) from one lane, frees ring stages with tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane =
+//               one output row per thread), bias / activation / SwiGLU (and
+//               their backward) applied in registers, stores to HBM.
+// Two 256-column accumulators let the epilogue of one tile overlap the main
+// loop of the next.
+//
+// Forms (tile = 128 rows x 256 columns of the output):
+//   NT  C[r, n]   = sum_k A[r, k] W_e[n, k]        A, W both K-major   (x W^T)
+//   NN  C[r, n]   = sum_k A[r, k] W_e[k, n]        W N-major           (dY W)
+//   TN  C_e[m, n] = sum_{r in e} A[r, m] B[r, n]   both M/N-major, ragged K (dW)
+// Rows of expert e are [off_e, off_{e+1}) of the expert-major buffers.  A
+// 128-row tile that runs past its expert's last row computes junk rows that are
+// never stored; a ragged-K tail block has the rows past the expert zeroed in
+// shared memory before its MMAs.  Experts without rows get exact-zero dW.
+//
+// Every wait is bounded (about 2 s of %globaltimer); on expiry the CTA sets
+// an abort flag and the device status word, drains its own copies and MMAs
+// in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;                  // one 128-byte swizzle row of bf16
+constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = BN * BK * 2;    // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_E = 256;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4096;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
+constexpr int EPI_STORE_F32_TAG = 100;   // TN: fp32 weight-gradient tile store
+
+struct TcParams {
+  int M, N, E;          // ragged-M: M = total rows; TN: output rows per expert
+  int K0, K1;           // reduction lengths of pair 0 / pair 1 (ragged-M)
+  int nM, nN;           // tiles along M (TN) and N
+  int ntile_n;          // columns of one N tile in output space (128 for SwiGLU up)
+  const int* offsets;   // [E+1]
+  void* C;
+  long long ldc, sCe;
+  const float* bias;
+  const bf16* aux0;
+  const bf16* aux1;
+  void* out1;
+  void* out2;
+  long long ld_aux;
+  int act;              // 0 relu, 1 gelu_tanh
+  int* status;
+};
+
+// ------------------------------------------------------------ PTX helpers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false once the CTA has aborted or the limit expired (which
+// aborts the CTA and records a timeout in the device status word).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      if (status) atomicExch(status, DEV_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+// Bounded wait used while draining (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 layout type 2,
+// descriptor version 1): start address, leading / stride byte offsets.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 D, bf16 A and B, K- or MN-major
+// operands, N >> 3 at bit 17, M >> 4 at bit 24.
+template <int FORM>
+__host__ __device__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((FORM == FORM_TN ? 1u : 0u) << 15) |
+         ((FORM == FORM_NT ? 0u : 1u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 q;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 c = __floats2bfloat162_rn(v[4], v[5]);
+  __nv_bfloat162 d = __floats2bfloat162_rn(v[6], v[7]);
+  q.x = *reinterpret_cast<uint32_t*>(&a);
+  q.y = *reinterpret_cast<uint32_t*>(&b);
+  q.z = *reinterpret_cast<uint32_t*>(&c);
+  q.w = *reinterpret_cast<uint32_t*>(&d);
+  return q;
+}
+__device__ __forceinline__ void unpack8_bf16(uint4 q, float* v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __low2float(h[i]);
+    v[2 * i + 1] = __high2float(h[i]);
+  }
+}
+
+struct Tile {
+  int e, m0, n0, row_hi, kbeg, kend, nkb, nkb0;
+};
+
+template <int FORM>
+__device__ __forceinline__ Tile map_tile(int t, const TcParams& p, const int* offs,
+                                         const int* tpre) {
+  Tile T;
+  if (FORM != FORM_TN) {
+    const int mt = t / p.nN, nt = t % p.nN;
+    int lo = 0, hi = p.E;   // largest lo with tpre[lo] <= mt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tpre[mid] <= mt) lo = mid; else hi = mid;
+    }
+    T.e = lo;
+    T.m0 = offs[lo] + (mt - tpre[lo]) * BM;
+    T.row_hi = offs[lo + 1];
+    T.n0 = nt * p.ntile_n;
+    T.kbeg = 0;
+    T.kend = 0;
+    T.nkb0 = (p.K0 + BK - 1) / BK;
+    T.nkb = T.nkb0 + (p.K1 > 0 ? (p.K1 + BK - 1) / BK : 0);
+  } else {
+    const int per = p.nM * p.nN;
+    T.e = t / per;
+    const int rem = t % per;
+    T.m0 = (rem / p.nN) * BM;
+    T.n0 = (rem % p.nN) * BN;
+    T.row_hi = p.M;
+    T.kbeg = offs[T.e];
+    T.kend = offs[T.e + 1];
+    T.nkb = (T.kend - T.kbeg + BK - 1) / BK;
+    T.nkb0 = T.nkb;
+  }
+  return T;
+}
+
+template <int FORM, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmA1,
+               const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t bar0 = sbase + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* offs = reinterpret_cast<int*>(tmem_slot + 4);
+  int* tpre = offs + (MAX_E + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA0);
+    prefetch_tmap(&tmB0);
+    if (EPI == EPI_SWIGLU_UP) prefetch_tmap(&tmB0x);
+    if (p.K1 > 0) {
+      prefetch_tmap(&tmA1);
+      prefetch_tmap(&tmB1);
+    }
+  }
+  for (int i = tid; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
+  __syncthreads();
+  if (FORM != FORM_TN && tid == 0) {
+    tpre[0] = 0;
+    for (int e = 0; e < p.E; ++e) tpre[e + 1] = tpre[e] + (offs[e + 1] - offs[e] + BM - 1) / BM;
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = (FORM != FORM_TN) ? tpre[p.E] * p.nN : p.E * p.nM * p.nN;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      uint32_t last_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile T = map_tile<FORM>(t, p, offs, tpre);
+        for (int kb = 0; kb < T.nkb; ++kb) {
+          if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t fb = full_bar(s);
+          const uint32_t a_dst = sbase + s * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          if (FORM == FORM_NT) {
+            const int k0 = kb * BK;
+            tma_load_2d(a_dst, &tmA0, fb, k0, T.m0);
+            if (EPI == EPI_SWIGLU_UP) {
+              tma_load_3d(b_dst, &tmB0, fb, k0, T.n0, T.e);
+              tma_load_3d(b_dst + BM * BK * 2, &tmB0x, fb, k0, T.n0, T.e);
+            } else {
+              tma_load_3d(b_dst, &tmB0, fb, k0, T.n0, T.e);
+              tma_load_3d(b_dst + BM * BK * 2, &tmB0, fb, k0, T.n0 + 128, T.e);
+            }
+          } else if (FORM == FORM_NN) {
+            const bool second = kb >= T.nkb0;
+            const int k0 = (second ? kb - T.nkb0 : kb) * BK;
+            tma_load_2d(a_dst, second ? &tmA1 : &tmA0, fb, k0, T.m0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_3d(b_dst + j * (64 * BK * 2), second ? &tmB1 : &tmB0, fb, T.n0 + 64 * j, k0,
+                          T.e);
+          } else {
+            const int r0 = T.kbeg + kb * BK;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_2d(a_dst + j * (64 * BK * 2), &tmA0, fb, T.m0 + 64 * j, r0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + j * (64 * BK * 2), &tmB0, fb, T.n0 + 64 * j, r0);
+          }
+          issued |= 1 << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      // drain: every stage's last load must have landed before the CTA exits
+      for (int q = 0; q < STAGES; ++q)
+        if (issued & (1 << q)) drain_wait(full_bar(q), (last_par >> q) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = instr_desc<FORM>();
+    int s = 0;
+    uint32_t ph = 0;
+    int buf = 0;
+    uint32_t aph = 0;
+    bool ok = true, any_mma = false;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile T = map_tile<FORM>(t, p, offs, tpre);
+      if (T.nkb == 0) continue;
+      if (!__all_sync(0xffffffffu, wait_bar(tempty_bar(buf), aph ^ 1u, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      for (int kb = 0; kb < T.nkb; ++kb) {
+        if (!__all_sync(0xffffffffu, wait_bar(full_bar(s), ph, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_base = sbase + s * STAGE_BYTES;
+        const uint32_t b_base = a_base + A_BYTES;
+        if (FORM == FORM_TN && kb == T.nkb - 1) {
+          const int valid = T.kend - (T.kbeg + kb * BK);
+          if (valid < BK) {
+            // rows past the expert's last row: zero them in both A boxes
+            const int nchunk = (BK - valid) * 8;   // 16-byte chunks per box
+            for (int j = 0; j < 2; ++j) {
+              uint4* dst = reinterpret_cast<uint4*>(smem + s * STAGE_BYTES + j * (64 * BK * 2) + valid * 128);
+              for (int c = lane; c < nchunk; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            uint64_t adesc, bdesc;
+            if (FORM == FORM_TN) adesc = smem_desc(a_base + kk * 2048, 64 * BK * 2, 1024);
+            else adesc = smem_desc(a_base + kk * 32, 16, 1024);
+            if (FORM == FORM_NT) bdesc = smem_desc(b_base + kk * 32, 16, 1024);
+            else bdesc = smem_desc(b_base + kk * 2048, 64 * BK * 2, 1024);
+            mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(s));
+        }
+        any_mma = true;
+        __syncwarp();
+        if (++s == STAGES) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(tfull_bar(buf));
+      __syncwarp();
+      if (++buf == 2) { buf = 0; aph ^= 1u; }
+    }
+    if (any_mma && lane == 0) {
+      mma_commit(drain_bar);
+      drain_wait(drain_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int lane_base = (warp & 3) * 32;
+    const int row = lane_base + lane;
+    int buf = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile T = map_tile<FORM>(t, p, offs, tpre);
+      const int r = T.m0 + row;
+      const bool rok = r < T.row_hi;
+      if (T.nkb == 0) {
+        // ragged K with an empty expert: dW tile is exactly zero
+        if (FORM == FORM_TN && rok) {
+          float* c = static_cast<float*>(p.C) + (size_t)T.e * p.sCe + (size_t)r * p.ldc;
+          for (int n = T.n0; n < T.n0 + BN && n < p.N; n += 4)
+            *reinterpret_cast<float4*>(c + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      // warp-uniform: the tcgen05.ld below is a warp-collective instruction
+      if (!__all_sync(0xffffffffu, wait_bar(tfull_bar(buf), aph, abort_flag, p.status))) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
+      if (EPI == EPI_SWIGLU_UP) {
+        for (int c = 0; c < 128; c += 16) {
+          float h1[16], h3[16];
+          tmem_ld16(t_row + c, h1);
+          tmem_ld16(t_row + 128 + c, h3);
+          tmem_ld_wait();
+          const int f = T.n0 + c;
+          if (rok) {
+#pragma unroll
+            for (int g = 0; g < 16; g += 8) {
+              if (f + g < p.N) {
+                float av[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) av[i] = silu_f(h1[g + i]) * h3[g + i];
+                const size_t o = (size_t)r * p.ldc + f + g;
+                *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out1) + o) = pack8_bf16(h1 + g);
+                *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out2) + o) = pack8_bf16(h3 + g);
+                *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + o) = pack8_bf16(av);
+              }
+            }
+          }
+        }
+      } else {
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          tmem_ld_wait();
+          const int n = T.n0 + c;
+          if (!rok || n >= p.N) continue;
+#pragma unroll
+          for (int g = 0; g < 16; g += 8) {
+            if (n + g >= p.N) break;
+            float* x = v + g;
+            const int nn = n + g;
+            if (EPI == EPI_STORE_F32_TAG) {
+              float* cp = static_cast<float*>(p.C) + (size_t)T.e * p.sCe + (size_t)r * p.ldc + nn;
+              *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
+              *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            } else if (EPI == EPI_STORE) {
+              if (p.bias) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] += p.bias[(size_t)T.e * p.N + nn + i];
+              }
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + (size_t)r * p.ldc + nn) = pack8_bf16(x);
+            } else if (EPI == EPI_ACT_FWD) {
+              float a[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (p.bias) x[i] += p.bias[(size_t)T.e * p.N + nn + i];
+                a[i] = p.act == 0 ? fmaxf(x[i], 0.f) : gelu_tanh_f(x[i]);
+              }
+              const size_t o = (size_t)r * p.ldc + nn;
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out1) + o) = pack8_bf16(x);
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + o) = pack8_bf16(a);
+            } else if (EPI == EPI_ACT_BWD) {
+              float h[8], dh[8];
+              unpack8_bf16(*reinterpret_cast<const uint4*>(p.aux0 + (size_t)r * p.ld_aux + nn), h);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_tanh_grad_f(h[i]);
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + (size_t)r * p.ldc + nn) = pack8_bf16(dh);
+            } else if (EPI == EPI_SWIGLU_BWD) {
+              float h1[8], h3[8], d1[8], d3[8];
+              unpack8_bf16(*reinterpret_cast<const uint4*>(p.aux0 + (size_t)r * p.ld_aux + nn), h1);
+              unpack8_bf16(*reinterpret_cast<const uint4*>(p.aux1 + (size_t)r * p.ld_aux + nn), h3);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                d1[i] = x[i] * h3[i] * silu_grad_f(h1[i]);
+                d3[i] = x[i] * silu_f(h1[i]);
+              }
+              const size_t o = (size_t)r * p.ldc + nn;
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + o) = pack8_bf16(d1);
+              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out1) + o) = pack8_bf16(d3);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (++buf == 2) { buf = 0; aph ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------- host --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle, zero fill out of bounds.  dims[0] is
+// the contiguous dimension; strides are in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t d[3], s[2];
+  cuuint32_t b[3];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), d, s,
+                  b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int FORM, int EPI>
+cudaError_t launch_inst(const CUtensorMap* maps, const TcParams& p, int tiles_upper,
+                        cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<FORM, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  int grid = sm_count();
+  if (tiles_upper < grid) grid = tiles_upper;
+  if (grid < 1) return cudaSuccess;
+  tc_gemm_kernel<FORM, EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(maps[0], maps[1], maps[2],
+                                                                   maps[3], maps[4], p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
+  using namespace tc;
+  if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
+  if (g.a_type != 1 || g.b_type != 1 || g.offsets == nullptr || g.E > MAX_E)
+    return cudaErrorInvalidValue;
+  CUtensorMap maps[5];
+  TcParams p{};
+  p.M = g.M;
+  p.N = g.N;
+  p.E = g.E;
+  p.K0 = g.K0;
+  p.K1 = (g.A1 != nullptr) ? g.K1 : 0;
+  p.offsets = g.offsets;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.sCe = g.sCe;
+  p.bias = g.bias;
+  p.aux0 = static_cast<const bf16*>(g.aux0);
+  p.aux1 = static_cast<const bf16*>(g.aux1);
+  p.out1 = g.out1;
+  p.out2 = g.out2;
+  p.ld_aux = g.ld_aux;
+  p.act = g.act;
+  p.status = g.status;
+  int tiles_upper = 0;
+  const uint64_t R = (uint64_t)g.M;
+  if (!g.ragged_k && g.b_kcontig) {
+    // NT: A [R, K0] K-major; W [E, N, K0] K-major (3-D so tiles never cross experts)
+    const uint64_t ad[2] = {(uint64_t)g.K0, R}, as[1] = {(uint64_t)g.lda * 2};
+    const uint32_t ab[2] = {BK, BM};
+    const uint64_t bd[3] = {(uint64_t)g.K0, (uint64_t)g.N, (uint64_t)g.E};
+    const uint64_t bs[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.sBe * 2};
+    const uint32_t bb[3] = {BK, 128, 1};
+    if (!make_map(&maps[0], g.A0, 2, ad, as, ab) || !make_map(&maps[1], g.B0, 3, bd, bs, bb))
+      return cudaErrorInvalidValue;
+    const bool swiglu = g.epi == EPI_SWIGLU_UP;
+    if (swiglu) {
+      if (!make_map(&maps[2], g.B0x, 3, bd, bs, bb)) return cudaErrorInvalidValue;
+    } else {
+      maps[2] = maps[1];
+    }
+    maps[3] = maps[0];
+    maps[4] = maps[1];
+    p.ntile_n = swiglu ? 128 : BN;
+    p.nN = (g.N + p.ntile_n - 1) / p.ntile_n;
+    p.nM = 0;
+    p.K1 = 0;
+    tiles_upper = (int)(((R + BM - 1) / BM + g.E) * p.nN);
+    switch (g.epi) {
+      case EPI_SWIGLU_UP: return launch_inst<FORM_NT, EPI_SWIGLU_UP>(maps, p, tiles_upper, st);
+      case EPI_ACT_FWD: return launch_inst<FORM_NT, EPI_ACT_FWD>(maps, p, tiles_upper, st);
+      case EPI_STORE: return launch_inst<FORM_NT, EPI_STORE>(maps, p, tiles_upper, st);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (!g.ragged_k) {
+    // NN: A [R, K] K-major; W [E, K, N] N-major
+    const uint64_t ad[2] = {(uint64_t)g.K0, R}, as[1] = {(uint64_t)g.lda * 2};
+    const uint32_t ab[2] = {BK, BM};
+    const uint64_t bd[3] = {(uint64_t)g.N, (uint64_t)g.K0, (uint64_t)g.E};
+    const uint64_t bs[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.sBe * 2};
+    const uint32_t bb[3] = {64, BK, 1};
+    if (!make_map(&maps[0], g.A0, 2, ad, as, ab) || !make_map(&maps[1], g.B0, 3, bd, bs, bb))
+      return cudaErrorInvalidValue;
+    maps[2] = maps[1];
+    if (p.K1 > 0) {
+      const uint64_t ad1[2] = {(uint64_t)g.K1, R};
+      const uint64_t bd1[3] = {(uint64_t)g.N, (uint64_t)g.K1, (uint64_t)g.E};
+      if (!make_map(&maps[3], g.A1, 2, ad1, as, ab) || !make_map(&maps[4], g.B1, 3, bd1, bs, bb))
+        return cudaErrorInvalidValue;
+    } else {
+      maps[3] = maps[0];
+      maps[4] = maps[1];
+    }
+    p.ntile_n = BN;
+    p.nN = (g.N + BN - 1) / BN;
+    tiles_upper = (int)(((R + BM - 1) / BM + g.E) * p.nN);
+    switch (g.epi) {
+      case EPI_SWIGLU_BWD: return launch_inst<FORM_NN, EPI_SWIGLU_BWD>(maps, p, tiles_upper, st);
+      case EPI_ACT_BWD: return launch_inst<FORM_NN, EPI_ACT_BWD>(maps, p, tiles_upper, st);
+      case EPI_STORE: return launch_inst<FORM_NN, EPI_STORE>(maps, p, tiles_upper, st);
+    }
+    return cudaErrorInvalidValue;
+  }
+  // TN (ragged K): A [Rk, M] M-major, B [Rk, N] N-major; Rk = K0 rows in total
+  if (g.c_type != 0 || g.epi != EPI_STORE) return cudaErrorInvalidValue;
+  const uint64_t Rk = (uint64_t)g.K0;
+  if (Rk == 0) {
+    // no rows at all: every expert's gradient is zero
+    return cudaMemsetAsync(g.C, 0, (size_t)g.E * g.sCe * sizeof(float), st);
+  }
+  const uint64_t ad[2] = {(uint64_t)g.M, Rk}, as[1] = {(uint64_t)g.lda * 2};
+  const uint64_t bd[2] = {(uint64_t)g.N, Rk}, bs[1] = {(uint64_t)g.ldb * 2};
+  const uint32_t box[2] = {64, BK};
+  if (!make_map(&maps[0], g.A0, 2, ad, as, box) || !make_map(&maps[1], g.B0, 2, bd, bs, box))
+    return cudaErrorInvalidValue;
+  maps[2] = maps[3] = maps[0];
+  maps[4] = maps[1];
+  p.ntile_n = BN;
+  p.nM = (g.M + BM - 1) / BM;
+  p.nN = (g.N + BN - 1) / BN;
+  p.K1 = 0;
+  tiles_upper = g.E * p.nM * p.nN;
+  return launch_inst<FORM_TN, EPI_STORE_F32_TAG>(maps, p, tiles_upper, st);
+}
+
+}  // namespace moe

@@ -59,7 +59,9 @@ enum Epi {
   EPI_SWIGLU_FWD = 2,   // acc = H3; H1 read from aux0;  out1 = H3;  C = SiLU(H1) * H3
   EPI_ACT_BWD = 3,      // acc = dA; H from aux0;  C = dA * act'(H)
   EPI_SWIGLU_BWD = 4,   // acc = dA; H1 aux0, H3 aux1;  C = dH1;  out1 = dH3
-  EPI_SCATTER_ADD = 5   // C(fp32) = acc + sum_j src[slot_of[r, j], n]
+  EPI_SCATTER_ADD = 5,  // C(fp32) = acc + sum_j src[slot_of[r, j], n]
+  EPI_SWIGLU_UP = 6     // tcgen05 only: B0 = W1, B0x = W3 in one N = 2 x 128 tile;
+                        //   out1 = H1, out2 = H3, C = SiLU(H1) * H3
 };
 
 // One grouped GEMM.  Ragged-M form (ragged_k = 0): rows [off_e, off_{e+1}) of
@@ -97,6 +99,9 @@ struct GemmArgs {
   int k;
   const void* src;
   int src_type;
+  const void* B0x;              // second B operand of EPI_SWIGLU_UP (W3)
+  void* out2;                   // second extra output (H3 of EPI_SWIGLU_UP)
+  int* status;                  // device status word (bounded-wait timeouts), tcgen05 only
 };
 
 cudaError_t launch_gemm_simt_f32(const GemmArgs& g, cudaStream_t st);
@@ -106,5 +111,10 @@ inline cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st) {
   if (g.a_type == 0 && g.b_type == 0) return launch_gemm_simt_f32(g, st);
   return launch_gemm_simt_bf16(g, st);
 }
+
+// tcgen05 / TMA grouped GEMM for bf16 operands (gemm_tc.cu).
+cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st);
+// Device status word values written by kernels (0 = ok).
+constexpr int DEV_STATUS_TIMEOUT = 6;
 
 }  // namespace moe

@@ -57,7 +57,7 @@ inline int dwg_splits(int T) {
 }
 
 struct Layout {
-  size_t scores, idx, gate, counts, offsets, chunk, src_tok, slot_of, psum, sq, aux_row;
+  size_t status, scores, idx, gate, counts, offsets, chunk, src_tok, slot_of, psum, sq, aux_row;
   size_t xe, h1, h3, a, ye, dy, dye, dgate, dh1, dh3, dxe, dlogits, dwg_part, dx;
   size_t total;
 };
@@ -74,6 +74,7 @@ Layout make_layout(const moe_config& c) {
     o += align_up(bytes > 0 ? bytes : 1);
     return at;
   };
+  L.status = take(16);
   L.scores = take(T * E * 4);
   L.idx = take(R * 4);
   L.gate = take(R * 4);
@@ -179,6 +180,7 @@ RouterArgs router_args(const moe_config& c) {
 
 GemmArgs gemm_base(const moe_config& c, const Ptrs& P) {
   GemmArgs g{};
+  g.status = P.at<int>(P.L->status);
   g.a_type = g.b_type = g.c_type = c.dtype;
   g.offsets = P.at<int>(P.L->offsets);
   g.E = c.E;
@@ -187,8 +189,9 @@ GemmArgs gemm_base(const moe_config& c, const Ptrs& P) {
   return g;
 }
 
+// Expert GEMMs: tcgen05 tensor cores for bf16 layers, CUDA cores for fp32.
 cudaError_t run_gemm(const moe_config& c, const GemmArgs& g, cudaStream_t st) {
-  (void)c;
+  if (c.dtype == MOE_BF16) return launch_gemm_tc(g, st);
   return launch_gemm_simt(g, st);
 }
 
@@ -199,6 +202,7 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   const Layout& L = *P.L;
   const long long R = (long long)c.T * c.k;
   const RouterArgs ra = router_args(c);
+  CK(cudaMemsetAsync(P.at<void>(L.status), 0, 16, st));
   KL("router_fwd", launch_router_fwd(c.dtype, x, w.w_gate, w.logit_bias, ra, P.at<float>(L.scores),
                        P.at<int>(L.idx), P.at<float>(L.gate), P.at<float>(L.psum), st));
   KL("route_count", launch_route_count(P.at<int>(L.idx), R, c.E, P.at<int>(L.chunk), st));
@@ -223,7 +227,15 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   g.sBe = (long long)c.F * c.D;
   g.ldc = c.F;
   g.ld_aux = c.F;
-  if (c.act == MOE_ACT_SWIGLU) {
+  if (c.act == MOE_ACT_SWIGLU && c.dtype == MOE_BF16) {
+    // one launch: W1 and W3 tiles side by side in a 2 x 128-column accumulator
+    g.epi = EPI_SWIGLU_UP;
+    g.B0x = w.w3;
+    g.out1 = P.at<void>(L.h1);
+    g.out2 = P.at<void>(L.h3);
+    g.C = P.at<void>(L.a);
+    KL("gemm_up", run_gemm(c, g, st));
+  } else if (c.act == MOE_ACT_SWIGLU) {
     g.epi = EPI_STORE;
     g.C = P.at<void>(L.h1);
     KL("gemm_up", run_gemm(c, g, st));
@@ -663,6 +675,67 @@ moe_status moe_get_intermediates(const moe_config* cfg, const void* workspace,
     if (cp.dst && cp.bytes)
       if (cudaMemcpyAsync(cp.dst, b + cp.off, cp.bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_device_status(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                             int32_t* status_host, void* stream) {
+  RET_IF(validate_config(cfg));
+  RET_IF(check_ws(*cfg, workspace, workspace_bytes));
+  if (!status_host) return MOE_ERR_INVALID_ARG;
+  Layout L = make_layout(*cfg);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaMemcpyAsync(status_host, static_cast<const char*>(workspace) + L.status, 4,
+                     cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
+                            const int32_t* offsets, const void* A, const void* B, void* C,
+                            int32_t* dev_status, void* stream) {
+  g_launches = 0;
+  if (form < 0 || form > 2 || M < 0 || N <= 0 || K < 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > 256 || N % 8 != 0 || K % 8 != 0 || (form == 2 && M % 8 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (!offsets || !A || !B || !C || !dev_status) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {offsets, A, B, C, dev_status};
+  for (const void* q : ps)
+    if (!aligned16(q)) return MOE_ERR_ALIGNMENT;
+  RET_IF(check_device());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmArgs g{};
+  g.a_type = g.b_type = MOE_BF16;
+  g.offsets = offsets;
+  g.E = E;
+  g.status = dev_status;
+  g.epi = EPI_STORE;
+  g.A0 = A;
+  g.B0 = B;
+  if (form == 2) {
+    // C[e][m][n] = sum over rows r of segment e of A[r, m] B[r, n]; K = total rows
+    g.ragged_k = true;
+    g.c_type = MOE_F32;
+    g.M = M;
+    g.N = N;
+    g.K0 = K;
+    g.lda = M;
+    g.ldb = N;
+    g.ldc = N;
+    g.sCe = (long long)M * N;
+  } else {
+    // C[r, n] = sum_k A[r, k] B_e(k, n); M = total rows, B [E, N, K] or [E, K, N]
+    g.ragged_k = false;
+    g.c_type = MOE_BF16;
+    g.b_kcontig = form == 0;
+    g.M = M;
+    g.N = N;
+    g.K0 = K;
+    g.lda = K;
+    g.ldb = form == 0 ? K : N;
+    g.sBe = (long long)N * K;
+    g.ldc = N;
+  }
+  KL("grouped_gemm", launch_gemm_tc(g, st));
   return MOE_OK;
 }
 

@@ -1,0 +1,95 @@
+"""The tcgen05 grouped GEMM (moe_grouped_gemm) against a plain PyTorch fp32
+matmul of the same operands, per expert segment.  Segments include empty
+experts, one-row experts and ragged tails; N and K include non-multiples of
+the 256 / 64 tile sizes."""
+
+import pytest
+import torch
+
+from sparse_mixture_experts_softmax_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+
+
+def _offsets(counts):
+    off = [0]
+    for c in counts:
+        off.append(off[-1] + c)
+    return torch.tensor(off, dtype=torch.int32, device="cuda")
+
+
+def _rel(a, b):
+    den = b.abs().max().item()
+    return (a - b).abs().max().item() / den if den > 0 else (a - b).abs().max().item()
+
+
+CASES = [
+    ([300, 0, 129, 1, 570], 704, 1024),
+    ([128, 256, 0, 0, 77], 256, 64),
+    ([5], 512, 200),
+    ([1000, 24, 0, 333], 1408, 2048),
+]
+
+
+@pytest.mark.parametrize("counts,N,K", CASES)
+@pytest.mark.parametrize("form", [0, 1])
+def test_ragged_m_forms(form, counts, N, K):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    E, M = len(counts), sum(counts)
+    off = _offsets(counts)
+    A = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    Bw = (torch.randn(E, N, K, generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
+    Bt = Bw if form == 0 else Bw.transpose(1, 2).contiguous()     # [E, K, N] for form 1
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_grouped_gemm(form, M, N, K, E, off, A, Bt, C, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = off.tolist()
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        ref = A[o[e]:o[e + 1]].float() @ Bw[e].float().T
+        got = C[o[e]:o[e + 1]].float()
+        assert torch.isfinite(got).all(), e
+        assert _rel(got, ref) <= 1e-2, (e, _rel(got, ref))
+
+
+@pytest.mark.parametrize("counts,Mo,N", [([300, 0, 129, 1, 570], 1024, 704),
+                                         ([64, 65, 0, 127], 704, 256),
+                                         ([2000, 3], 512, 2048)])
+def test_ragged_k_form(counts, Mo, N):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2)
+    E, R = len(counts), sum(counts)
+    off = _offsets(counts)
+    A = torch.randn(R, Mo, generator=g, device="cuda").to(torch.bfloat16)
+    Bm = torch.randn(R, N, generator=g, device="cuda").to(torch.bfloat16)
+    C = torch.full((E, Mo, N), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_grouped_gemm(2, Mo, N, R, E, off, A, Bm, C, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = off.tolist()
+    for e in range(E):
+        ref = A[o[e]:o[e + 1]].float().T @ Bm[o[e]:o[e + 1]].float()
+        if counts[e] == 0:
+            assert torch.equal(C[e], torch.zeros_like(C[e])), e
+        else:
+            assert _rel(C[e], ref) <= 1e-4, (e, _rel(C[e], ref))
+
+
+def test_repeatable_bits():
+    counts, N, K = [200, 0, 313], 512, 512
+    E, M = len(counts), sum(counts)
+    off = _offsets(counts)
+    A = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    Bw = torch.randn(E, N, K, device="cuda").to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    C1 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    C2 = torch.empty_like(C1)
+    B.moe_grouped_gemm(0, M, N, K, E, off, A, Bw, C1, st)
+    B.moe_grouped_gemm(0, M, N, K, E, off, A, Bw, C2, st)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
