@@ -207,8 +207,8 @@ MOE_API moe_status moe_device_status(const moe_config* cfg, const void* workspac
  *   form 1: C[r,n] = sum_k A[r,k] B[e,k,n]    A [M,K], B [E,K,N], C [M,N] bf16
  *   form 2: C[e,m,n] = sum_{r in e} A[r,m] B[r,n]
  *                                            A [K,M], B [K,N], C [E,M,N] fp32
- * (forms 0/1: M = total rows; form 2: K = total rows).  N, K (and M for form
- * 2) must be multiples of 8.  dev_status: device int32, set to
+ * (forms 0/1: M = total rows; form 2: K = total rows).  The contiguous
+ * dimensions must be multiples of 8: N always, K for forms 0/1, M for form 2.  dev_status: device int32, set to
  * MOE_ERR_TIMEOUT if a bounded wait expired (the caller zeroes it). */
 MOE_API moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
                                     const int32_t* offsets, const void* A, const void* B,

@@ -50,7 +50,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 256;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4096;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;   // + alignment slack
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
@@ -144,9 +144,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
-}
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -281,57 +278,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  const uint32_t sbase = raw + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  const uint32_t bar0 = sbase + STAGES * STAGE_BYTES;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* offs = reinterpret_cast<int*>(tmem_slot + 4);
-  int* tpre = offs + (MAX_E + 4);
+  // stage ring in dynamic shared memory (1024-byte aligned for the 128-byte
+  // swizzle); barriers, the TMEM address slot and the segment tables static
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_mb[STAGES], empty_mb[STAGES], tfull_mb[2], tempty_mb[2], drain_mb;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_word;
+  __shared__ int offs[MAX_E + 1];
+  __shared__ int tpre[MAX_E + 1];
+  volatile int* abort_flag = &abort_word;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t drain_bar = smem_u32(&drain_mb);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(smem_u32(&full_mb[s]), 1);
+      mbar_init(smem_u32(&empty_mb[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(smem_u32(&tfull_mb[b]), 1);
+      mbar_init(smem_u32(&tempty_mb[b]), 4);
     }
     mbar_init(drain_bar, 1);
-    *abort_flag = 0;
+    abort_word = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA0);
-    prefetch_tmap(&tmB0);
-    if (EPI == EPI_SWIGLU_UP) prefetch_tmap(&tmB0x);
-    if (p.K1 > 0) {
-      prefetch_tmap(&tmA1);
-      prefetch_tmap(&tmB1);
-    }
-  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
   for (int i = tid; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   if (FORM != FORM_TN && tid == 0) {
     tpre[0] = 0;
     for (int e = 0; e < p.E; ++e) tpre[e + 1] = tpre[e] + (offs[e + 1] - offs[e] + BM - 1) / BM;
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_base = tmem_slot;
   const int total = (FORM != FORM_TN) ? tpre[p.E] * p.nN : p.E * p.nM * p.nN;
 
   if (warp == 0) {
@@ -345,8 +328,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile T = map_tile<FORM>(t, p, offs, tpre);
         for (int kb = 0; kb < T.nkb; ++kb) {
-          if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          const uint32_t fb = full_bar(s);
+          if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full_mb[s]);
           const uint32_t a_dst = sbase + s * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -382,7 +365,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       }
       // drain: every stage's last load must have landed before the CTA exits
       for (int q = 0; q < STAGES; ++q)
-        if (issued & (1 << q)) drain_wait(full_bar(q), (last_par >> q) & 1u);
+        if (issued & (1 << q)) drain_wait(smem_u32(&full_mb[q]), (last_par >> q) & 1u);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -396,14 +379,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
       if (T.nkb == 0) continue;
-      if (!__all_sync(0xffffffffu, wait_bar(tempty_bar(buf), aph ^ 1u, abort_flag, p.status))) {
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tempty_mb[buf]), aph ^ 1u, abort_flag, p.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
       for (int kb = 0; kb < T.nkb; ++kb) {
-        if (!__all_sync(0xffffffffu, wait_bar(full_bar(s), ph, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&full_mb[s]), ph, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -432,14 +415,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             else bdesc = smem_desc(b_base + kk * 2048, 64 * BK * 2, 1024);
             mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(empty_bar(s));
+          mma_commit(smem_u32(&empty_mb[s]));
         }
         any_mma = true;
         __syncwarp();
         if (++s == STAGES) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(tfull_bar(buf));
+      if (lane == 0) mma_commit(smem_u32(&tfull_mb[buf]));
       __syncwarp();
       if (++buf == 2) { buf = 0; aph ^= 1u; }
     }
@@ -468,7 +451,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         continue;
       }
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
-      if (!__all_sync(0xffffffffu, wait_bar(tfull_bar(buf), aph, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
       if (EPI == EPI_SWIGLU_UP) {
@@ -550,7 +533,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) mbar_arrive(smem_u32(&tempty_mb[buf]));
       if (++buf == 2) { buf = 0; aph ^= 1u; }
     }
   }
@@ -635,6 +618,13 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   using namespace tc;
   if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
   if (g.a_type != 1 || g.b_type != 1 || g.offsets == nullptr || g.E > MAX_E)
+    return cudaErrorInvalidValue;
+  // every pointer the chosen epilogue dereferences must be set
+  if (g.A0 == nullptr || g.B0 == nullptr || g.C == nullptr) return cudaErrorInvalidValue;
+  if ((g.epi == EPI_SWIGLU_UP && (g.B0x == nullptr || g.out1 == nullptr || g.out2 == nullptr)) ||
+      (g.epi == EPI_ACT_FWD && g.out1 == nullptr) || (g.epi == EPI_ACT_BWD && g.aux0 == nullptr) ||
+      (g.epi == EPI_SWIGLU_BWD && (g.aux0 == nullptr || g.aux1 == nullptr || g.out1 == nullptr)) ||
+      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)))
     return cudaErrorInvalidValue;
   CUtensorMap maps[5];
   TcParams p{};

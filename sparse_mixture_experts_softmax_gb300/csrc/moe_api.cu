@@ -696,7 +696,10 @@ moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32
                             int32_t* dev_status, void* stream) {
   g_launches = 0;
   if (form < 0 || form > 2 || M < 0 || N <= 0 || K < 0 || E <= 0) return MOE_ERR_INVALID_ARG;
-  if (E > 256 || N % 8 != 0 || K % 8 != 0 || (form == 2 && M % 8 != 0)) return MOE_ERR_UNSUPPORTED;
+  // inner (contiguous) dimensions must be multiples of 8 elements; form 2's K
+  // counts rows and has no alignment requirement
+  if (E > 256 || N % 8 != 0 || (form != 2 && K % 8 != 0) || (form == 2 && M % 8 != 0))
+    return MOE_ERR_UNSUPPORTED;
   if (!offsets || !A || !B || !C || !dev_status) return MOE_ERR_INVALID_ARG;
   const void* ps[] = {offsets, A, B, C, dev_status};
   for (const void* q : ps)
@@ -711,6 +714,7 @@ moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32
   g.epi = EPI_STORE;
   g.A0 = A;
   g.B0 = B;
+  g.C = C;
   if (form == 2) {
     // C[e][m][n] = sum over rows r of segment e of A[r, m] B[r, n]; K = total rows
     g.ragged_k = true;

@@ -24,6 +24,7 @@ def _rel(a, b):
 
 
 CASES = [
+    ([256], 256, 128),
     ([300, 0, 129, 1, 570], 704, 1024),
     ([128, 256, 0, 0, 77], 256, 64),
     ([5], 512, 200),
