@@ -231,8 +231,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="print per-kernel times to stderr")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (profiling a smaller case of the same layer)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (profiling a smaller case of the same layer)")
     args = ap.parse_args()
     wl = W.WORKLOADS[args.workload]
+    if args.tokens is not None or args.experts is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, T=args.tokens or wl.T, E=args.experts or wl.E,
+                                 zipf_empty=min(wl.zipf_empty, max(0, (args.experts or wl.E) - wl.k)),
+                                 name=f"{wl.name}(T={args.tokens or wl.T},E={args.experts or wl.E})")
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
