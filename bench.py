@@ -156,7 +156,8 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
     inp = W.make_inputs(sub, seed=seed)
     f64 = lambda t: None if t is None else t.detach().double().numpy()  # noqa: E731
     lp = wl.dtype == "bf16"
-    w = dict(w_gate=f64(inp["w_gate"]), w1=f64(inp["w1_bf16"] if lp else inp["w1"]),
+    w = dict(w_gate=f64(inp["w_gate"].to(torch.bfloat16) if lp else inp["w_gate"]),
+             w1=f64(inp["w1_bf16"] if lp else inp["w1"]),
              w2=f64(inp["w2_bf16"] if lp else inp["w2"]),
              w3=f64(inp["w3_bf16"] if lp and inp["w3"] is not None else inp["w3"]),
              b1=f64(inp["b1"]), b2=f64(inp["b2"]), logit_bias=None)

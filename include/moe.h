@@ -34,12 +34,13 @@
  *   Repeated calls are independent (course lesson "Define Expert Mlp Forward
  *   And Backward", "Prove it works").
  * - Precision: MOE_F32 computes in fp32 on CUDA cores.  MOE_BF16 feeds the
- *   expert GEMMs bf16 operands with fp32 accumulation (tcgen05 tensor cores);
+ *   expert and router GEMMs bf16 operands with fp32 accumulation (tcgen05
+ *   tensor cores; the router multiplies with a bf16 copy of its fp32 master);
  *   scores, gates, Y, dY, losses and every gradient of a parameter are fp32.
  *
  * Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= E <= 256, 1 <= k <= 32,
  * k <= E; n_groups divides E and is <= 32; D and F are multiples of 8;
- * T*k < 2^31.  SwiGLU experts carry no biases.  T = 0 is accepted and does no
+ * for MOE_BF16 also E; T*k < 2^31.  SwiGLU experts carry no biases.  T = 0 is accepted and does no
  * work (train step losses read 0).  The device must be sm_103.
  */
 #ifndef MOE_GB300_H
@@ -114,7 +115,7 @@ typedef struct {
 /* Trainable parameters for moe_train_step.  The fp32 masters are updated in
  * place by SGD; for MOE_BF16 the bf16 working copies (used by the expert GEMMs)
  * are rewritten from the updated masters with round-to-nearest-even.  The
- * router always uses its fp32 master. */
+ * router reads its fp32 master (MOE_BF16 casts it to bf16 for its GEMMs). */
 typedef struct {
   float* w_gate;            /* [E,D] fp32 master                         */
   float* w1;                /* [E,F,D] fp32 master                       */

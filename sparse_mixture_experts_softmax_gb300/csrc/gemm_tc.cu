@@ -55,6 +55,7 @@ constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
 constexpr int EPI_STORE_F32_TAG = 100;   // TN: fp32 weight-gradient tile store
+constexpr int EPI_ROWS_F32_TAG = 101;    // NT: fp32 row store (+ bias[n]), e.g. router logits
 
 struct TcParams {
   int M, N, E;          // ragged-M: M = total rows; TN: output rows per expert
@@ -72,6 +73,11 @@ struct TcParams {
   long long ld_aux;
   int act;              // 0 relu, 1 gelu_tanh
   int* status;
+  int seg_len;          // offsets == nullptr: segment e = [e*seg_len, min((e+1)*seg_len, rows))
+  int seg_rows;         // total rows of the implicit segments
+  const int* slot_of;   // EPI_SCATTER_ADD: [rows, k] slots of the rows to add
+  int k;
+  const bf16* src;      // EPI_SCATTER_ADD: [R, N] rows added to the fp32 result
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -305,7 +311,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
-  for (int i = tid; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
+  for (int i = tid; i <= p.E; i += NUM_THREADS)
+    offs[i] = p.offsets ? p.offsets[i] : min(i * p.seg_len, p.seg_rows);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -492,6 +499,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
               float* cp = static_cast<float*>(p.C) + (size_t)T.e * p.sCe + (size_t)r * p.ldc + nn;
               *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
               *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            } else if (EPI == EPI_ROWS_F32_TAG) {
+              if (p.bias) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] += p.bias[(size_t)T.e * p.N + nn + i];
+              }
+              float* cp = static_cast<float*>(p.C) + (size_t)r * p.ldc + nn;
+              *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
+              *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            } else if (EPI == EPI_SCATTER_ADD) {
+              // dX[t] = acc + sum_j dXe[slot(t, j)] in j order
+              for (int j = 0; j < p.k; ++j) {
+                const int slot = p.slot_of[(size_t)r * p.k + j];
+                float sv[8];
+                unpack8_bf16(*reinterpret_cast<const uint4*>(p.src + (size_t)slot * p.N + nn), sv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] += sv[i];
+              }
+              float* cp = static_cast<float*>(p.C) + (size_t)r * p.ldc + nn;
+              *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
+              *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
             } else if (EPI == EPI_STORE) {
               if (p.bias) {
 #pragma unroll
@@ -617,14 +644,15 @@ cudaError_t launch_inst(const CUtensorMap* maps, const TcParams& p, int tiles_up
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   using namespace tc;
   if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
-  if (g.a_type != 1 || g.b_type != 1 || g.offsets == nullptr || g.E > MAX_E)
-    return cudaErrorInvalidValue;
+  if (g.a_type != 1 || g.b_type != 1 || g.E > MAX_E) return cudaErrorInvalidValue;
+  if (g.offsets == nullptr && g.seg_len <= 0) return cudaErrorInvalidValue;
   // every pointer the chosen epilogue dereferences must be set
   if (g.A0 == nullptr || g.B0 == nullptr || g.C == nullptr) return cudaErrorInvalidValue;
   if ((g.epi == EPI_SWIGLU_UP && (g.B0x == nullptr || g.out1 == nullptr || g.out2 == nullptr)) ||
       (g.epi == EPI_ACT_FWD && g.out1 == nullptr) || (g.epi == EPI_ACT_BWD && g.aux0 == nullptr) ||
       (g.epi == EPI_SWIGLU_BWD && (g.aux0 == nullptr || g.aux1 == nullptr || g.out1 == nullptr)) ||
-      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)))
+      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)) ||
+      (g.epi == EPI_SCATTER_ADD && (g.slot_of == nullptr || g.src == nullptr || g.src_type != 1)))
     return cudaErrorInvalidValue;
   CUtensorMap maps[5];
   TcParams p{};
@@ -645,6 +673,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   p.ld_aux = g.ld_aux;
   p.act = g.act;
   p.status = g.status;
+  p.seg_len = g.seg_len;
+  p.seg_rows = g.ragged_k ? g.K0 : g.M;
+  p.slot_of = g.slot_of;
+  p.k = g.k;
+  p.src = static_cast<const bf16*>(g.src);
   int tiles_upper = 0;
   const uint64_t R = (uint64_t)g.M;
   if (!g.ragged_k && g.b_kcontig) {
@@ -672,7 +705,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     switch (g.epi) {
       case EPI_SWIGLU_UP: return launch_inst<FORM_NT, EPI_SWIGLU_UP>(maps, p, tiles_upper, st);
       case EPI_ACT_FWD: return launch_inst<FORM_NT, EPI_ACT_FWD>(maps, p, tiles_upper, st);
-      case EPI_STORE: return launch_inst<FORM_NT, EPI_STORE>(maps, p, tiles_upper, st);
+      case EPI_STORE:
+        if (g.c_type == 0) return launch_inst<FORM_NT, EPI_ROWS_F32_TAG>(maps, p, tiles_upper, st);
+        return launch_inst<FORM_NT, EPI_STORE>(maps, p, tiles_upper, st);
     }
     return cudaErrorInvalidValue;
   }
@@ -702,6 +737,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
       case EPI_SWIGLU_BWD: return launch_inst<FORM_NN, EPI_SWIGLU_BWD>(maps, p, tiles_upper, st);
       case EPI_ACT_BWD: return launch_inst<FORM_NN, EPI_ACT_BWD>(maps, p, tiles_upper, st);
       case EPI_STORE: return launch_inst<FORM_NN, EPI_STORE>(maps, p, tiles_upper, st);
+      case EPI_SCATTER_ADD: return launch_inst<FORM_NN, EPI_SCATTER_ADD>(maps, p, tiles_upper, st);
     }
     return cudaErrorInvalidValue;
   }

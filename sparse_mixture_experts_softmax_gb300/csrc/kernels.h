@@ -20,7 +20,11 @@ cudaError_t launch_router_fwd(int dtype, const void* x, const float* wg, const f
                               float* psum_partial, cudaStream_t st);
 cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* gate,
                               const float* dgate, const float* aux_row, const RouterArgs& a,
-                              float* dlogits, cudaStream_t st);
+                              float* dlogits, void* dlogits_lp, cudaStream_t st);
+// selection from precomputed logits (bias already added) and the bf16 weight cast
+cudaError_t launch_router_select(const float* logits, const RouterArgs& a, float* scores, int* idx,
+                                 float* gate, float* psum_partial, cudaStream_t st);
+cudaError_t launch_cast_bf16(const float* src, void* dst, long long n, cudaStream_t st);
 
 // ---- dispatch, combine, losses, optimizer (dispatch.cu)
 constexpr int ROUTE_CHUNK = 1024;   // routed assignments per scatter chunk
@@ -52,7 +56,7 @@ cudaError_t launch_sgd(float* w, const float* g, long long n, float lr, void* w_
                        cudaStream_t st);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t st);
 
-// ---- grouped GEMMs (gemm_simt.cu for fp32; gemm_tc.cu for bf16 on tcgen05)
+// ---- grouped GEMMs (gemm_simt_f32.cu for fp32; gemm_tc.cu for bf16 on tcgen05)
 enum Epi {
   EPI_STORE = 0,        // C = acc (+ bias[e, n])
   EPI_ACT_FWD = 1,      // out1 = H = acc + bias;  C = act(H)
@@ -104,12 +108,12 @@ struct GemmArgs {
   int* status;                  // device status word (bounded-wait timeouts), tcgen05 only
 };
 
+// CUDA-core GEMMs serve fp32 layers only; bf16 operands go to the tensor cores.
 cudaError_t launch_gemm_simt_f32(const GemmArgs& g, cudaStream_t st);
-cudaError_t launch_gemm_simt_bf16(const GemmArgs& g, cudaStream_t st);
 inline cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
-  if (g.a_type == 0 && g.b_type == 0) return launch_gemm_simt_f32(g, st);
-  return launch_gemm_simt_bf16(g, st);
+  if (g.a_type != 0 || g.b_type != 0) return cudaErrorInvalidValue;
+  return launch_gemm_simt_f32(g, st);
 }
 
 // tcgen05 / TMA grouped GEMM for bf16 operands (gemm_tc.cu).

@@ -59,6 +59,7 @@ inline int dwg_splits(int T) {
 struct Layout {
   size_t status, scores, idx, gate, counts, offsets, chunk, src_tok, slot_of, psum, sq, aux_row;
   size_t xe, h1, h3, a, ye, dy, dye, dgate, dh1, dh3, dxe, dlogits, dwg_part, dx;
+  size_t logits, wg_lp, dl_lp;   // bf16 layers: router logits, bf16 W_g, bf16 dlogits
   size_t total;
 };
 
@@ -100,6 +101,10 @@ Layout make_layout(const moe_config& c) {
   L.dlogits = take(T * E * 4);
   L.dwg_part = take((size_t)dwg_splits(c.T) * E * D * 4);
   L.dx = take(T * D * 4);
+  const bool lp = c.dtype == MOE_BF16;
+  L.logits = lp ? take(T * E * 4) : 0;
+  L.wg_lp = lp ? take(E * D * 2) : 0;
+  L.dl_lp = lp ? take(T * E * 2) : 0;
   L.total = o;
   return L;
 }
@@ -117,6 +122,7 @@ moe_status validate_config(const moe_config* c) {
   if ((long long)c->k > (long long)c->topk_groups * (c->E / c->n_groups)) return MOE_ERR_UNSUPPORTED;
   if (c->D % 8 != 0 || c->F % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_BF16 && c->E % 8 != 0) return MOE_ERR_UNSUPPORTED;   // TMA row alignment
   if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if ((long long)c->T * c->D >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -203,8 +209,38 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   const long long R = (long long)c.T * c.k;
   const RouterArgs ra = router_args(c);
   CK(cudaMemsetAsync(P.at<void>(L.status), 0, 16, st));
-  KL("router_fwd", launch_router_fwd(c.dtype, x, w.w_gate, w.logit_bias, ra, P.at<float>(L.scores),
-                       P.at<int>(L.idx), P.at<float>(L.gate), P.at<float>(L.psum), st));
+  if (c.dtype == MOE_BF16) {
+    // logits = x W_g^T (+ logit bias) on the tensor cores, then selection
+    KL("cast_wg", launch_cast_bf16(w.w_gate, P.at<void>(L.wg_lp), (long long)c.E * c.D, st));
+    GemmArgs r{};
+    r.a_type = r.b_type = MOE_BF16;
+    r.c_type = MOE_F32;
+    r.status = P.at<int>(L.status);
+    r.ragged_k = false;
+    r.b_kcontig = true;
+    r.M = c.T;
+    r.N = c.E;
+    r.K0 = c.D;
+    r.A0 = x;
+    r.lda = c.D;
+    r.B0 = P.at<void>(L.wg_lp);
+    r.ldb = c.D;
+    r.sBe = (long long)c.E * c.D;
+    r.offsets = nullptr;
+    r.E = 1;
+    r.seg_len = c.T;
+    r.C = P.at<void>(L.logits);
+    r.ldc = c.E;
+    r.bias = w.logit_bias;
+    r.epi = EPI_STORE;
+    KL("router_logits", launch_gemm_tc(r, st));
+    KL("router_select", launch_router_select(P.at<float>(L.logits), ra, P.at<float>(L.scores),
+                                             P.at<int>(L.idx), P.at<float>(L.gate),
+                                             P.at<float>(L.psum), st));
+  } else {
+    KL("router_fwd", launch_router_fwd(c.dtype, x, w.w_gate, w.logit_bias, ra, P.at<float>(L.scores),
+                                       P.at<int>(L.idx), P.at<float>(L.gate), P.at<float>(L.psum), st));
+  }
   KL("route_count", launch_route_count(P.at<int>(L.idx), R, c.E, P.at<int>(L.chunk), st));
   KL("route_scan", launch_route_scan(P.at<int>(L.chunk), route_chunks(R), c.E, P.at<int>(L.counts),
                        P.at<int>(L.offsets), st));
@@ -388,9 +424,64 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
 
   // router: renormalisation + aux + score backward
   const RouterArgs ra = router_args(c);
+  const bool lp = c.dtype == MOE_BF16;
   KL("router_bwd", launch_router_bwd(P.at<float>(L.scores), P.at<int>(L.idx), P.at<float>(L.gate),
                        P.at<float>(L.dgate), c.aux_alpha != 0.f ? P.at<float>(L.aux_row) : nullptr,
-                       ra, P.at<float>(L.dlogits), st));
+                       ra, P.at<float>(L.dlogits), lp ? P.at<void>(L.dl_lp) : nullptr, st));
+  if (lp) {
+    // tensor-core router products: dW_g = dlogits^T x (split over token
+    // chunks, fixed-order sum) and dX = dlogits W_g + scatter-back of dXe
+    KL("cast_wg", launch_cast_bf16(w.w_gate, P.at<void>(L.wg_lp), (long long)c.E * c.D, st));
+    const int S = dwg_splits(c.T);
+    GemmArgs rg{};
+    rg.a_type = rg.b_type = MOE_BF16;
+    rg.c_type = MOE_F32;
+    rg.status = P.at<int>(L.status);
+    rg.ragged_k = true;
+    rg.M = c.E;
+    rg.N = c.D;
+    rg.A0 = P.at<void>(L.dl_lp);
+    rg.lda = c.E;
+    rg.B0 = x;
+    rg.ldb = c.D;
+    rg.K0 = c.T;
+    rg.offsets = nullptr;
+    rg.E = S;
+    rg.seg_len = (c.T + S - 1) / S;
+    rg.C = P.at<void>(L.dwg_part);
+    rg.ldc = c.D;
+    rg.sCe = (long long)c.E * c.D;
+    rg.epi = EPI_STORE;
+    KL("gemm_router_dwg", launch_gemm_tc(rg, st));
+    KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D,
+                                             gr.dw_gate, st));
+    GemmArgs dg{};
+    dg.a_type = dg.b_type = MOE_BF16;
+    dg.c_type = MOE_F32;
+    dg.status = P.at<int>(L.status);
+    dg.ragged_k = false;
+    dg.b_kcontig = false;
+    dg.M = c.T;
+    dg.N = c.D;
+    dg.K0 = c.E;
+    dg.A0 = P.at<void>(L.dl_lp);
+    dg.lda = c.E;
+    dg.B0 = P.at<void>(L.wg_lp);
+    dg.ldb = c.D;
+    dg.sBe = (long long)c.E * c.D;
+    dg.offsets = nullptr;
+    dg.E = 1;
+    dg.seg_len = c.T;
+    dg.C = dx;
+    dg.ldc = c.D;
+    dg.epi = EPI_SCATTER_ADD;
+    dg.slot_of = P.at<int>(L.slot_of);
+    dg.k = c.k;
+    dg.src = P.at<void>(L.dxe);
+    dg.src_type = MOE_BF16;
+    KL("gemm_router_dx", launch_gemm_tc(dg, st));
+    return MOE_OK;
+  }
   // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
   const int S = dwg_splits(c.T);
   GemmArgs rg{};

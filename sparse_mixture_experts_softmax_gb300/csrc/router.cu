@@ -246,6 +246,150 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
   }
 }
 
+// Score, selection and renormalisation from precomputed logits (the bf16
+// layers compute logits = x W_g^T + logit_bias on the tensor cores).  One warp
+// per token; a warp-private shared row serves the group-limited selection.
+// Per-block column sums of the scores feed the aux loss.
+template <int NC>
+__global__ void __launch_bounds__(256)
+router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __restrict__ scores,
+                     int* __restrict__ idx, float* __restrict__ gate,
+                     float* __restrict__ psum_partial) {
+  constexpr int EP = 32 * NC;
+  __shared__ float rows[8][EP];
+  __shared__ float wsum[8][EP];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, T = a.T;
+  const int per = E / a.n_groups;
+  float colsum[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) colsum[c] = 0.f;
+  for (int tt = 0; tt < RT_TOK / 8; ++tt) {
+    const int t = blockIdx.x * RT_TOK + warp * (RT_TOK / 8) + tt;
+    if (t >= T) break;
+    float s[NC];
+    if (a.score == 0) {
+      float m = -FLT_MAX;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        s[c] = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+        m = fmaxf(m, s[c]);
+      }
+      m = warp_max(m);
+      float z = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        s[c] = (e < E) ? expf(s[c] - m) : 0.f;
+        z += s[c];
+      }
+      z = warp_sum(z);
+      float inv = 1.0f / z;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) s[c] *= inv;
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        s[c] = (e < E) ? sigmoidf_(logits[(size_t)t * E + e]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      int e = lane + 32 * c;
+      if (e < E) {
+        scores[(size_t)t * E + e] = s[c];
+        rows[warp][e] = s[c];
+        colsum[c] += s[c];
+      }
+    }
+    __syncwarp();
+    bool allowed[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) allowed[c] = (lane + 32 * c) < E;
+    if (a.n_groups > 1) {
+      float gs = -INFINITY;
+      if (lane < a.n_groups) {
+        float m1 = -INFINITY, m2 = -INFINITY;
+        for (int e = lane * per; e < (lane + 1) * per; ++e) {
+          float v = rows[warp][e];
+          if (v > m1) { m2 = m1; m1 = v; } else if (v > m2) { m2 = v; }
+        }
+        gs = (per == 1 || a.group_score == 1) ? m1 : m1 + m2;
+      }
+      bool taken = false;
+      unsigned keep = 0u;
+      for (int r = 0; r < a.topk_groups; ++r) {
+        Cand c;
+        c.v = (lane < a.n_groups && !taken) ? gs : -INFINITY;
+        c.id = (lane < a.n_groups && !taken) ? lane : 0x7fffffff;
+        c = warp_best(c);
+        int gsel = c.id;
+        if (gsel >= a.n_groups)
+          gsel = __ffs(~keep & ((a.n_groups >= 32) ? 0xffffffffu : ((1u << a.n_groups) - 1u))) - 1;
+        keep |= 1u << gsel;
+        if (lane == gsel) taken = true;
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        allowed[c] = allowed[c] && ((keep >> (e / per)) & 1u);
+      }
+    }
+    float selv = 0.f, ssum = 0.f;
+    int selid = 0;
+    for (int j = 0; j < a.k; ++j) {
+      Cand best;
+      best.v = -INFINITY;
+      best.id = 0x7fffffff;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        int e = lane + 32 * c;
+        if (allowed[c] && better(s[c], e, best.v, best.id)) { best.v = s[c]; best.id = e; }
+      }
+      best = warp_best(best);
+      if (best.id >= E) {
+        int cand = 0x7fffffff;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (allowed[c]) cand = min(cand, lane + 32 * c);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+        best.id = (cand < E) ? cand : 0;
+        best.v = rows[warp][best.id];
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (lane + 32 * c == best.id) allowed[c] = false;
+      if (lane == j) { selv = best.v; selid = best.id; }
+      ssum += best.v;
+    }
+    if (lane < a.k) {
+      idx[(size_t)t * a.k + lane] = selid;
+      gate[(size_t)t * a.k + lane] = selv / ssum;
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int c = 0; c < NC; ++c) wsum[warp][lane + 32 * c] = colsum[c];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 256) {
+    float sacc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sacc += wsum[w][e];
+    psum_partial[(size_t)blockIdx.x * E + e] = sacc;
+  }
+}
+
+// Round-to-nearest-even bf16 copy of an fp32 tensor (the router weight).
+__global__ void __launch_bounds__(256)
+cast_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
+}
+
 // Router backward, one warp per token:
 //   dsel_j = (dg_j - sum_i dg_i g_i) / S,  S = sum_j s_{idx_j}
 //   ds_e   = aux_row_e + [e selected] dsel
@@ -255,7 +399,7 @@ __global__ void __launch_bounds__(256)
 router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
                   const float* __restrict__ gate, const float* __restrict__ dgate,
                   const float* __restrict__ aux_row, RouterArgs a,
-                  float* __restrict__ dlogits) {
+                  float* __restrict__ dlogits, bf16* __restrict__ dlogits_lp) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= a.T) return;
@@ -295,13 +439,21 @@ router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       int e = lane + 32 * c;
-      if (e < E) dlogits[(size_t)t * E + e] = s[c] * (ds[c] - dot);
+      if (e < E) {
+        const float v = s[c] * (ds[c] - dot);
+        dlogits[(size_t)t * E + e] = v;
+        if (dlogits_lp) dlogits_lp[(size_t)t * E + e] = __float2bfloat16_rn(v);
+      }
     }
   } else {
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       int e = lane + 32 * c;
-      if (e < E) dlogits[(size_t)t * E + e] = ds[c] * s[c] * (1.0f - s[c]);
+      if (e < E) {
+        const float v = ds[c] * s[c] * (1.0f - s[c]);
+        dlogits[(size_t)t * E + e] = v;
+        if (dlogits_lp) dlogits_lp[(size_t)t * E + e] = __float2bfloat16_rn(v);
+      }
     }
   }
 }
@@ -339,24 +491,44 @@ static cudaError_t launch_fwd_t(const void* x, const float* wg, const float* lb,
   return launch_fwd_nj<XT, 16>(x, wg, lb, a, scores, idx, gate, psum, st);
 }
 
+// fp32 layers: logits on CUDA cores inside the fused router kernel.
 cudaError_t launch_router_fwd(int dtype, const void* x, const float* wg, const float* logit_bias,
                               const RouterArgs& a, float* scores, int* idx, float* gate,
                               float* psum_partial, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  if (dtype == 1)
-    return launch_fwd_t<bf16>(x, wg, logit_bias, a, scores, idx, gate, psum_partial, st);
+  if (dtype != 0) return cudaErrorInvalidValue;
   return launch_fwd_t<float>(x, wg, logit_bias, a, scores, idx, gate, psum_partial, st);
 }
 
 cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* gate,
                               const float* dgate, const float* aux_row, const RouterArgs& a,
-                              float* dlogits, cudaStream_t st) {
+                              float* dlogits, void* dlogits_lp, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   dim3 grid((a.T + 7) / 8);
-  if (a.E <= 32) router_bwd_kernel<1><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
-  else if (a.E <= 64) router_bwd_kernel<2><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
-  else if (a.E <= 128) router_bwd_kernel<4><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
-  else router_bwd_kernel<8><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits);
+  bf16* lp = static_cast<bf16*>(dlogits_lp);
+  if (a.E <= 32) router_bwd_kernel<1><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
+  else if (a.E <= 64) router_bwd_kernel<2><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
+  else if (a.E <= 128) router_bwd_kernel<4><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
+  else router_bwd_kernel<8><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_select(const float* logits, const RouterArgs& a, float* scores, int* idx,
+                                 float* gate, float* psum_partial, cudaStream_t st) {
+  if (a.T == 0) return cudaSuccess;
+  dim3 grid(router_fwd_blocks(a.T));
+  if (a.E <= 32) router_select_kernel<1><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
+  else if (a.E <= 64) router_select_kernel<2><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
+  else if (a.E <= 128) router_select_kernel<4><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
+  else router_select_kernel<8><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_bf16(const float* src, void* dst, long long n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  cast_bf16_kernel<<<(int)blocks, 256, 0, st>>>(src, static_cast<bf16*>(dst), n);
   return cudaGetLastError();
 }
 

@@ -3,9 +3,10 @@ layer's view of one seeded workload, and compare them.
 
 The oracle side receives exactly the values the CUDA side computes with:
 fp32 draws for fp32 layers; for bf16 layers the bf16-rounded x and expert
-weights (widened to float64) and the fp32 router master.  Nothing the oracle
-consumes comes out of the CUDA library, except a routing that has first been
-validated against the oracle's own (see ``validated_routing``).
+weights (widened to float64), the bf16 copy of the router weight that the
+router GEMM multiplies with, and the fp32 masters for the SGD update.  Nothing
+the oracle consumes comes out of the CUDA library, except a routing that has
+first been validated against the oracle's own (see ``validated_routing``).
 """
 
 from __future__ import annotations
@@ -35,7 +36,8 @@ def np64(t):
 def oracle_inputs(wl: W.Workload, inp: dict):
     """(weights used by forward/backward, fp32 master weights, x, target) in float64."""
     lp = wl.dtype == "bf16"
-    w_fwd = dict(w_gate=np64(inp["w_gate"]),
+    # bf16 layers feed the router GEMM a bf16 copy of the fp32 master W_g
+    w_fwd = dict(w_gate=np64(inp["w_gate"].to(torch.bfloat16) if lp else inp["w_gate"]),
                  w1=np64(inp["w1_bf16"] if lp else inp["w1"]),
                  w2=np64(inp["w2_bf16"] if lp else inp["w2"]),
                  w3=np64(inp["w3_bf16"] if lp else inp["w3"]) if inp["w3"] is not None else None,

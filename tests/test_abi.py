@@ -108,8 +108,11 @@ def test_host_validation_errors(L):
     # train step: bf16 layer without bf16 copies
     g = B.make_grads(good(8), good(9), good(10), db1=good(11), db2=good(12))
     p = B.make_params(good(1), good(2), good(3), g, b1=good(4), b2=good(5))
-    assert _status(B.moe_train_step, _cfg(dtype="bf16"), p, good(6), good(7), 0.1, good(13), ws) \
+    assert _status(B.moe_train_step, _cfg(dtype="bf16", E=8), p, good(6), good(7), 0.1, good(13), ws) \
         == B.MOE_ERR_INVALID_ARG
+    # bf16 layers need E % 8 == 0 (16-byte rows of the bf16 router operands)
+    assert _status(B.moe_train_step, _cfg(dtype="bf16", E=4), p, good(6), good(7), 0.1, good(13), ws) \
+        == B.MOE_ERR_UNSUPPORTED
 
 
 def test_status_strings(L):
