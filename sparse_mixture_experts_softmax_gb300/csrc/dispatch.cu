@@ -93,24 +93,31 @@ route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E,
   }
 }
 
-// Xe[s, :] = X[src_tok[s], :] with 16-byte vectors, one warp per row.
+// Xe[slot(t, j), :] = X[t, :] for j < k: one warp per token reads its row
+// once (16-byte vectors, 4 in flight per lane) and writes it to its k slots.
 template <typename T>
 __global__ void __launch_bounds__(256)
-gather_kernel(const T* __restrict__ x, const int* __restrict__ src_tok, long long R, int D,
+gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, int k, int D,
               T* __restrict__ xe) {
   constexpr int VN = 16 / sizeof(T);
   const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int warps = gridDim.x * (blockDim.x >> 5);
   const int nv = D / VN;
-  for (long long s = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < R; s += warps) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)src_tok[s] * D);
-    uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)s * D);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < Tn; t += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * D);
+    const int* so = slot_of + (size_t)t * k;
     int v = lane;
     for (; v + 96 < nv; v += 128) {
-      uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
-      dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
+      const uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
+      for (int j = 0; j < k; ++j) {
+        uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)so[j] * D);
+        dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
+      }
     }
-    for (; v < nv; v += 32) dst[v] = src[v];
+    for (; v < nv; v += 32) {
+      const uint4 a = src[v];
+      for (int j = 0; j < k; ++j) reinterpret_cast<uint4*>(xe + (size_t)so[j] * D)[v] = a;
+    }
   }
 }
 
@@ -264,6 +271,36 @@ combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
   }
 }
 
+// dX[t] += sum_j dXe[slot(t, j)] in j order (scatter-back of the expert rows
+// onto the router's dX term); one warp per token, 16-byte vectors along D.
+template <typename T>
+__global__ void __launch_bounds__(256)
+scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
+                        const int* __restrict__ slot_of, int Tn, int D, int k) {
+  constexpr int VN = Vec<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  for (int d = lane * VN; d < D; d += 32 * VN) {
+    float acc[VN];
+#pragma unroll
+    for (int i = 0; i < VN; i += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(dx + (size_t)t * D + d + i);
+      acc[i] = q.x; acc[i + 1] = q.y; acc[i + 2] = q.z; acc[i + 3] = q.w;
+    }
+    for (int j = 0; j < k; ++j) {
+      Vec<T> v;
+      v.load(dxe + (size_t)slot_of[(size_t)t * k + j] * D + d);
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] += v.get(i);
+    }
+#pragma unroll
+    for (int i = 0; i < VN; i += 4)
+      *reinterpret_cast<float4*>(dx + (size_t)t * D + d + i) =
+          make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+  }
+}
+
 // out[e, n] = sum over rows of segment e of src[r, n] (fixed order), for db.
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -353,15 +390,15 @@ cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(int dtype, const void* x, const int* src_tok, long long R, int D,
+cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, int k, int D,
                           void* xe, cudaStream_t st) {
-  if (R == 0) return cudaSuccess;
-  int grid = grid_for(R, 8, 152 * 16);
+  if (T == 0) return cudaSuccess;
+  int grid = grid_for(T, 8, 152 * 16);
   if (dtype == 1)
-    gather_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(x), src_tok, R, D,
+    gather_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(x), slot_of, T, k, D,
                                               static_cast<bf16*>(xe));
   else
-    gather_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), src_tok, R, D,
+    gather_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), slot_of, T, k, D,
                                                static_cast<float*>(xe));
   return cudaGetLastError();
 }
@@ -415,6 +452,19 @@ cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const
                                                           slot_of, T, D, k,
                                                           static_cast<float*>(dye), dgate);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const int* slot_of,
+                                    int T, int D, int k, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int grid = (T + 7) / 8;
+  if (dtype == 1)
+    scatter_back_add_kernel<bf16><<<grid, 256, 0, st>>>(dx, static_cast<const bf16*>(dxe), slot_of,
+                                                         T, D, k);
+  else
+    scatter_back_add_kernel<float><<<grid, 256, 0, st>>>(dx, static_cast<const float*>(dxe),
+                                                          slot_of, T, D, k);
   return cudaGetLastError();
 }
 

@@ -55,7 +55,7 @@ constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
 constexpr int EPI_STORE_F32_TAG = 100;   // TN: fp32 weight-gradient tile store
-constexpr int EPI_ROWS_F32_TAG = 101;    // NT: fp32 row store (+ bias[n]), e.g. router logits
+constexpr int EPI_ROWS_F32_TAG = 101;    // fp32 row store (+ bias[n]): router logits, router dX
 
 struct TcParams {
   int M, N, E;          // ragged-M: M = total rows; TN: output rows per expert
@@ -75,9 +75,6 @@ struct TcParams {
   int* status;
   int seg_len;          // offsets == nullptr: segment e = [e*seg_len, min((e+1)*seg_len, rows))
   int seg_rows;         // total rows of the implicit segments
-  const int* slot_of;   // EPI_SCATTER_ADD: [rows, k] slots of the rows to add
-  int k;
-  const bf16* src;      // EPI_SCATTER_ADD: [R, N] rows added to the fp32 result
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -507,18 +504,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
               float* cp = static_cast<float*>(p.C) + (size_t)r * p.ldc + nn;
               *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
               *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
-            } else if (EPI == EPI_SCATTER_ADD) {
-              // dX[t] = acc + sum_j dXe[slot(t, j)] in j order
-              for (int j = 0; j < p.k; ++j) {
-                const int slot = p.slot_of[(size_t)r * p.k + j];
-                float sv[8];
-                unpack8_bf16(*reinterpret_cast<const uint4*>(p.src + (size_t)slot * p.N + nn), sv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] += sv[i];
-              }
-              float* cp = static_cast<float*>(p.C) + (size_t)r * p.ldc + nn;
-              *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
-              *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
             } else if (EPI == EPI_STORE) {
               if (p.bias) {
 #pragma unroll
@@ -651,8 +636,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if ((g.epi == EPI_SWIGLU_UP && (g.B0x == nullptr || g.out1 == nullptr || g.out2 == nullptr)) ||
       (g.epi == EPI_ACT_FWD && g.out1 == nullptr) || (g.epi == EPI_ACT_BWD && g.aux0 == nullptr) ||
       (g.epi == EPI_SWIGLU_BWD && (g.aux0 == nullptr || g.aux1 == nullptr || g.out1 == nullptr)) ||
-      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)) ||
-      (g.epi == EPI_SCATTER_ADD && (g.slot_of == nullptr || g.src == nullptr || g.src_type != 1)))
+      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)) || g.epi == EPI_SCATTER_ADD)
     return cudaErrorInvalidValue;
   CUtensorMap maps[5];
   TcParams p{};
@@ -675,9 +659,6 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.seg_len = g.seg_len;
   p.seg_rows = g.ragged_k ? g.K0 : g.M;
-  p.slot_of = g.slot_of;
-  p.k = g.k;
-  p.src = static_cast<const bf16*>(g.src);
   int tiles_upper = 0;
   const uint64_t R = (uint64_t)g.M;
   if (!g.ragged_k && g.b_kcontig) {
@@ -736,8 +717,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     switch (g.epi) {
       case EPI_SWIGLU_BWD: return launch_inst<FORM_NN, EPI_SWIGLU_BWD>(maps, p, tiles_upper, st);
       case EPI_ACT_BWD: return launch_inst<FORM_NN, EPI_ACT_BWD>(maps, p, tiles_upper, st);
-      case EPI_STORE: return launch_inst<FORM_NN, EPI_STORE>(maps, p, tiles_upper, st);
-      case EPI_SCATTER_ADD: return launch_inst<FORM_NN, EPI_SCATTER_ADD>(maps, p, tiles_upper, st);
+      case EPI_STORE:
+        if (g.c_type == 0) return launch_inst<FORM_NN, EPI_ROWS_F32_TAG>(maps, p, tiles_upper, st);
+        return launch_inst<FORM_NN, EPI_STORE>(maps, p, tiles_upper, st);
     }
     return cudaErrorInvalidValue;
   }

@@ -36,7 +36,7 @@ cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int* counts
 cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E,
                                  const int* chunk_base, int* src_tok, int* slot_of,
                                  cudaStream_t st);
-cudaError_t launch_gather(int dtype, const void* x, const int* src_tok, long long R, int D,
+cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, int k, int D,
                           void* xe, cudaStream_t st);
 int combine_blocks(int T);
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of,
@@ -48,6 +48,8 @@ cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const flo
 cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
                                const int* slot_of, int T, int D, int k, void* dye, float* dgate,
                                cudaStream_t st);
+cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const int* slot_of,
+                                    int T, int D, int k, cudaStream_t st);
 cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets, int E, int N,
                                   float* out, cudaStream_t st);
 cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,
@@ -63,7 +65,7 @@ enum Epi {
   EPI_SWIGLU_FWD = 2,   // acc = H3; H1 read from aux0;  out1 = H3;  C = SiLU(H1) * H3
   EPI_ACT_BWD = 3,      // acc = dA; H from aux0;  C = dA * act'(H)
   EPI_SWIGLU_BWD = 4,   // acc = dA; H1 aux0, H3 aux1;  C = dH1;  out1 = dH3
-  EPI_SCATTER_ADD = 5,  // C(fp32) = acc + sum_j src[slot_of[r, j], n]
+  EPI_SCATTER_ADD = 5,  // C(fp32) = acc + sum_j src[slot_of[r, j], n]  (CUDA-core GEMM only)
   EPI_SWIGLU_UP = 6     // tcgen05 only: B0 = W1, B0x = W3 in one N = 2 x 128 tile;
                         //   out1 = H1, out2 = H3, C = SiLU(H1) * H3
 };

@@ -246,7 +246,7 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
                        P.at<int>(L.offsets), st));
   KL("route_scatter", launch_route_scatter(P.at<int>(L.idx), R, c.k, c.E, P.at<int>(L.chunk),
                           P.at<int>(L.src_tok), P.at<int>(L.slot_of), st));
-  KL("gather", launch_gather(c.dtype, x, P.at<int>(L.src_tok), R, c.D, P.at<void>(L.xe), st));
+  KL("gather", launch_gather(c.dtype, x, P.at<int>(L.slot_of), c.T, c.k, c.D, P.at<void>(L.xe), st));
 
   // expert up-projection (+ activation)
   GemmArgs g = gemm_base(c, P);
@@ -474,12 +474,10 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
     dg.seg_len = c.T;
     dg.C = dx;
     dg.ldc = c.D;
-    dg.epi = EPI_SCATTER_ADD;
-    dg.slot_of = P.at<int>(L.slot_of);
-    dg.k = c.k;
-    dg.src = P.at<void>(L.dxe);
-    dg.src_type = MOE_BF16;
+    dg.epi = EPI_STORE;
     KL("gemm_router_dx", launch_gemm_tc(dg, st));
+    KL("scatter_back", launch_scatter_back_add(c.dtype, dx, P.at<void>(L.dxe), P.at<int>(L.slot_of),
+                                               c.T, c.D, c.k, st));
     return MOE_OK;
   }
   // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
