@@ -1,0 +1,172 @@
+"""Parity at the full sizes of the SwiGLU layers, in the launch configuration
+bench.py times (whole layer, all tokens, one training step through the C ABI).
+
+The oracle cannot run a whole step at these sizes, so it checks what it can
+compute exactly or one token at a time:
+  * routing over ALL tokens, bit-exact given the GPU's own fp32 scores;
+  * the scores and the aux loss against the oracle's fp64 router (cheap);
+  * the MSE loss against the mean of (y - target)^2 of the GPU's own y;
+  * y and dX on sampled tokens, each token's k expert rows run by the oracle;
+  * the weight gradients of the smallest non-empty expert (every token routed
+    to it runs through the oracle), and exact zeros for experts with no rows.
+Expert weights are pulled to float64 one expert at a time.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import moe_oracle as O
+from tests.moe_cases import (assert_close, check_routing_exact, make_layer, np64, oracle_config,
+                             validated_routing)
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+class LazyExperts:
+    """[E, ...] device tensor seen as float64 experts fetched on demand."""
+
+    def __init__(self, t):
+        self.t = t
+        self.cache = {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = self.t[e].float().cpu().numpy().astype(np.float64)
+        return self.cache[e]
+
+
+def _oracle_weights(inp, lb):
+    return dict(w_gate=np64(inp["w_gate"].to(torch.bfloat16)), w1=LazyExperts(inp["w1_bf16"]),
+                w2=LazyExperts(inp["w2_bf16"]),
+                w3=LazyExperts(inp["w3_bf16"]) if inp["w3_bf16"] is not None else None,
+                b1=None, b2=None, logit_bias=lb)
+
+
+def _rows_forward(cfg, w, x64, pairs):
+    """Expert rows (t, e) through the oracle's expert MLP, batched per expert.
+    Returns {(t, e): forward dict of that single row}."""
+    out = {}
+    by_e = {}
+    for t, e in pairs:
+        by_e.setdefault(int(e), []).append(int(t))
+    for e, ts in by_e.items():
+        fe = O.expert_forward(cfg, e, x64[ts], w)
+        for i, t in enumerate(ts):
+            out[(t, e)] = {k_: v[i:i + 1] for k_, v in fe.items()}
+    return out
+
+
+def _tokens_y(cfg, w, x64, scores64, idx, tokens):
+    """y[t] for the given tokens (oracle gates from its own scores)."""
+    pairs = [(t, idx[t, j]) for t in tokens for j in range(cfg.k)]
+    fw = _rows_forward(cfg, w, x64, pairs)
+    gate = O.renormalize(scores64[tokens], idx[tokens])
+    ys = {}
+    for i, t in enumerate(tokens):
+        y = np.zeros(cfg.D)
+        for j in range(cfg.k):
+            y = y + gate[i, j] * fw[(t, int(idx[t, j]))]["ye"][0]
+        ys[t] = y
+    return ys, fw, gate
+
+
+def _run_full(name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl, seed=0, device="cuda")
+    cfg = oracle_config(wl)
+    layer = make_layer(wl, inp)
+    x = inp["x_bf16"]
+    tgt = inp["target"]
+    y = layer.forward(x).clone()
+    dx = torch.empty(wl.T, wl.D, device="cuda")
+    layer.train_step(x, tgt, wl.lr, dx=dx)
+    torch.cuda.synchronize()
+    r = layer.routing()
+    return wl, inp, cfg, layer, y, dx, r
+
+
+@pytest.mark.parametrize("name,n_sample", [("grouped", 8), ("skewed", 6), ("large", 4)])
+def test_full_size_layer(name, n_sample):
+    wl, inp, cfg, layer, y, dx, r = _run_full(name)
+    T, D, E, k = wl.T, wl.D, wl.E, wl.k
+    # 1. routing over all tokens, bit-exact given the GPU's scores
+    check_routing_exact(cfg, r)
+    idx = r["idx"].cpu().numpy()
+    counts = r["counts"].cpu().numpy().astype(np.int64)
+    offsets = r["offsets"].cpu().numpy()
+    src_tok = r["src_tok"].cpu().numpy()
+    # 2. scores and aux against the oracle's fp64 router on all tokens
+    lb = np64(inp["logit_bias"])
+    w = _oracle_weights(inp, lb)
+    x64 = np64(inp["x_bf16"])
+    scores64 = O.router_scores(cfg, O.router_logits(x64, w["w_gate"], lb))
+    assert_close("scores", r["scores"].cpu().numpy(), scores64, 1e-4)
+    aux, f, _ = O.aux_loss(counts, scores64, k)
+    loss = layer.d_loss.cpu().numpy()
+    assert_close("aux", loss[1], aux, 1e-4)
+    # 3. the MSE reduction against the GPU's own y
+    y64 = y.double()
+    mse_of_y = float(((y64 - inp["target"].double()) ** 2).mean())
+    assert_close("mse", loss[0], mse_of_y, 1e-4)
+    # 4. sampled tokens: y and dX
+    tokens = W.sample_tokens(T, n_sample).tolist()
+    idx_v = validated_routing(cfg, scores64[tokens], idx[tokens])
+    idx_s = idx.copy()
+    idx_s[tokens] = idx_v
+    ys, fw, gate = _tokens_y(cfg, w, x64, scores64, idx_s, tokens)
+    t64 = inp["target"][tokens].double().cpu().numpy()
+    aux_row = cfg.aux_alpha * O.aux_loss_score_grad(counts / float(T * k), T)
+    for i, t in enumerate(tokens):
+        assert_close(f"y[{t}]", y[t].double().cpu().numpy(), ys[t], TOL)
+        dy = 2.0 * (ys[t] - t64[i]) / float(T * D)
+        dxt = np.zeros(D)
+        dgate = np.zeros(k)
+        for j in range(k):
+            e = int(idx_s[t, j])
+            fe = fw[(t, e)]
+            be = O.expert_backward(cfg, e, x64[t:t + 1], fe, (gate[i, j] * dy)[None], w)
+            dxt = dxt + be["dxe"][0]
+            dgate[j] = float(np.dot(dy, fe["ye"][0]))
+        ds = O.renormalize_backward(scores64[t:t + 1], idx_s[t:t + 1], gate[i:i + 1], dgate[None])
+        ds = ds + aux_row[None, :]
+        if cfg.score == "softmax":
+            dl = O.softmax_rows_backward(scores64[t:t + 1], ds)
+        else:
+            dl = O.sigmoid_backward(scores64[t:t + 1], ds)
+        dxt = dxt + (dl @ w["w_gate"])[0]
+        assert_close(f"dx[{t}]", dx[t].double().cpu().numpy(), dxt, TOL)
+    # 5. empty experts: exact zero gradients
+    for e in np.nonzero(counts == 0)[0]:
+        assert torch.all(layer.dw1[e] == 0) and torch.all(layer.dw2[e] == 0)
+        assert torch.all(layer.dw3[e] == 0)
+    # 6. the smallest non-empty expert's weight gradients (when cheap enough)
+    nonzero = np.nonzero(counts)[0]
+    e_min = int(nonzero[np.argmin(counts[nonzero])])
+    n_rows = int(counts[e_min])
+    checked_dw = n_rows * k * 6 * D * wl.F <= 4e11
+    print(f"\n{name}: T={T} R={T * k} routed rows checked bit-exact; sampled tokens {tokens}; "
+          f"{int((counts == 0).sum())} empty experts; smallest expert {e_min} with {n_rows} rows "
+          f"{'checked' if checked_dw else 'skipped (too costly for the oracle)'}")
+    if checked_dw:
+        rows_tok = src_tok[offsets[e_min]:offsets[e_min + 1]].tolist()
+        idx_v = validated_routing(cfg, scores64[rows_tok], idx[rows_tok])
+        idx_m = idx.copy()
+        idx_m[rows_tok] = idx_v
+        ys_m, fw_m, gate_m = _tokens_y(cfg, w, x64, scores64, idx_m, rows_tok)
+        t_rows = inp["target"][rows_tok].double().cpu().numpy()
+        dye = np.zeros((n_rows, D))
+        for i, t in enumerate(rows_tok):
+            j = int(np.nonzero(idx_m[t] == e_min)[0][0])
+            dye[i] = gate_m[i, j] * 2.0 * (ys_m[t] - t_rows[i]) / float(T * D)
+        xe = x64[rows_tok]
+        fe = O.expert_forward(cfg, e_min, xe, w)
+        be = O.expert_backward(cfg, e_min, xe, fe, dye, w)
+        assert_close(f"dw1[{e_min}]", np64(layer.dw1[e_min]), be["dw1"], TOL)
+        assert_close(f"dw3[{e_min}]", np64(layer.dw3[e_min]), be["dw3"], TOL)
+        assert_close(f"dw2[{e_min}]", np64(layer.dw2[e_min]), be["dw2"], TOL)
+    del layer, inp
+    torch.cuda.empty_cache()
