@@ -67,12 +67,32 @@ def hbm_bytes(wl: W.Workload) -> dict:
     es = 2 if wl.dtype == "bf16" else 4
     T, D, R = wl.T, wl.D, wl.R
     n_exp = (3 if wl.act == "swiglu" else 2) * wl.E * wl.D * wl.F
+    n_bias = wl.E * (wl.F + wl.D) if wl.has_bias else 0
     return {
         "gather": T * D * es + R * D * es,                 # X once, Xe written
         "combine_loss": R * D * es + 2 * T * D * 4,       # Ye, target read; dY written
         "combine_bwd": T * D * 4 + 2 * R * D * es,        # dY, Ye read; dYe written
-        "sgd_experts": n_exp * (12 + (2 if wl.dtype == "bf16" else 0)) / (3 if wl.act == "swiglu" else 2),
+        # every fp32 parameter: master and gradient read, master written; bf16
+        # layers also write the bf16 copy of each expert weight (all launches)
+        "sgd": (wl.E * D + n_exp + n_bias) * 12 + (n_exp * 2 if wl.dtype == "bf16" else 0),
     }
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (x itself with a single process)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, seconds: float) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling:
+    every rank runs its own replica of the step on its own batch)."""
+    return units_per_rank * world * steps / seconds
 
 
 class ClockSampler:
@@ -264,7 +284,7 @@ def main():
     from sparse_mixture_experts_softmax_gb300 import binding as B
     from sparse_mixture_experts_softmax_gb300.layer import MoELayer
 
-    inp = W.make_inputs(wl, seed=0, device=str(dev))
+    inp = W.make_inputs(wl, seed=rank, device=str(dev))   # each replica its own batch
     lp = wl.dtype == "bf16"
     layer = MoELayer(wl.T, wl.D, wl.F, wl.E, wl.k, wl.act, wl.score, wl.dtype, wl.has_bias,
                      wl.aux_alpha, inp["w_gate"], inp["w1"], inp["w2"], w3=inp["w3"],
@@ -304,12 +324,9 @@ def main():
     ms_total = start.elapsed_time(end)
     prof = B.moe_profile_read()
     B.moe_profile_enable(False)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
-    value = wl.T * world * args.steps / (ms_total / 1e3)
+    value = whole_job_rate(wl.T, world, args.steps, ms_total / 1e3)
     loss = layer.d_loss.cpu().tolist()
 
     # per-kernel times over the timed region
@@ -338,7 +355,7 @@ def main():
     hb = hbm_bytes(wl)
     hbm = {}
     for name, key in (("gather", "gather"), ("combine_loss", "combine_loss"),
-                      ("combine_bwd", "combine_bwd")):
+                      ("combine_bwd", "combine_bwd"), ("sgd", "sgd")):
         if name in per_kernel and per_kernel[name] > 0:
             gbs = hb[key] / (per_kernel[name] / 1e3) / 1e9
             hbm[name] = {"ms": per_kernel[name], "GB/s": gbs, "frac": gbs / float(peaks["hbm_gbs"])}
@@ -369,11 +386,8 @@ def main():
             B.moe_train_step_host(layer.cfg, layer.params(), x_host, t_host, wl.lr, l_host,
                                   staging, layer.workspace)
         e2e_s = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        line["e2e"] = {"value": wl.T * world * args.steps / e2e_s, "unit": "tokens/s",
+        e2e_s = max_over_ranks(e2e_s, dev)
+        line["e2e"] = {"value": whole_job_rate(wl.T, world, args.steps, e2e_s), "unit": "tokens/s",
                        "h2d_bytes_per_step": x_host.numel() * x_host.element_size()
                        + t_host.numel() * 4, "d2h_bytes_per_step": 8}
 

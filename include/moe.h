@@ -215,6 +215,16 @@ MOE_API moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t 
                                     const int32_t* offsets, const void* A, const void* B,
                                     void* C, int32_t* dev_status, void* stream);
 
+/* Self-test of the bounded device waits: runs moe_grouped_gemm with every
+ * load withheld, so the tensor-core kernel's waits run out after limit_ns
+ * (0 < limit_ns <= 2e9).  The kernel then stops cleanly (drains, frees tensor
+ * memory) and writes MOE_ERR_TIMEOUT to *dev_status; C is left unwritten.
+ * The context stays usable.  Diagnostic only; the pages have no counterpart. */
+MOE_API moe_status moe_selftest_wait_timeout(int32_t form, int32_t M, int32_t N, int32_t K,
+                                             int32_t E, const int32_t* offsets, const void* A,
+                                             const void* B, void* C, int32_t* dev_status,
+                                             int64_t limit_ns, void* stream);
+
 /* Static text for a status code. */
 MOE_API const char* moe_status_string(moe_status s);
 

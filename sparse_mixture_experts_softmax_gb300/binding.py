@@ -103,9 +103,11 @@ def lib() -> ctypes.CDLL:
         L.moe_dispatch_noalloc.argtypes = [P(moe_config)] + [c_void_p] * 6
         L.moe_device_status.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p]
         L.moe_grouped_gemm.argtypes = [c_int32] * 5 + [c_void_p] * 6
+        L.moe_selftest_wait_timeout.argtypes = [c_int32] * 5 + [c_void_p] * 5 + [ctypes.c_int64,
+                                                                                c_void_p]
         for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
                    "moe_get_routing", "moe_get_intermediates", "moe_dispatch_noalloc",
-                   "moe_device_status", "moe_grouped_gemm"):
+                   "moe_device_status", "moe_grouped_gemm", "moe_selftest_wait_timeout"):
             getattr(L, fn).restype = c_int32
         _lib = L
     return _lib
@@ -247,3 +249,12 @@ def moe_grouped_gemm(form, M, N, K, E, offsets, A, B, C, dev_status, stream=None
     _check("moe_grouped_gemm",
            lib().moe_grouped_gemm(int(form), int(M), int(N), int(K), int(E), _ptr(offsets),
                                   _ptr(A), _ptr(B), _ptr(C), _ptr(dev_status), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(form, M, N, K, E, offsets, A, B, C, dev_status, limit_ns,
+                              stream=None):
+    """The grouped GEMM with its loads withheld: its bounded waits must expire."""
+    _check("moe_selftest_wait_timeout",
+           lib().moe_selftest_wait_timeout(int(form), int(M), int(N), int(K), int(E),
+                                           _ptr(offsets), _ptr(A), _ptr(B), _ptr(C),
+                                           _ptr(dev_status), int(limit_ns), _stream(stream)))

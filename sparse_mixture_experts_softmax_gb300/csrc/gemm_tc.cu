@@ -51,7 +51,7 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 256;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;   // + alignment slack
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+constexpr long long WAIT_LIMIT_NS = 2000000000ll;   // default bound of every wait
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
 constexpr int EPI_STORE_F32_TAG = 100;   // TN: fp32 weight-gradient tile store
@@ -75,6 +75,8 @@ struct TcParams {
   int* status;
   int seg_len;          // offsets == nullptr: segment e = [e*seg_len, min((e+1)*seg_len, rows))
   int seg_rows;         // total rows of the implicit segments
+  long long wait_ns;    // bound of every mbarrier wait
+  int stall;            // self-test: the producer withholds every load
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -112,13 +114,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait: false once the CTA has aborted or the limit expired (which
 // aborts the CTA and records a timeout in the device status word).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
+                                         int* status, long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > WAIT_LIMIT_NS) {
+    if ((long long)(global_ns() - t0) > limit_ns) {
       *abort_flag = 1;
       if (status) atomicExch(status, DEV_STATUS_TIMEOUT);
       return false;
@@ -126,10 +128,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 // Bounded wait used while draining (ignores the abort flag).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit_ns) {
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > WAIT_LIMIT_NS) return;
+    if ((long long)(global_ns() - t0) > limit_ns) return;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -328,11 +330,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       uint32_t ph = 0;
       int issued = 0;
       uint32_t last_par = 0;
-      bool ok = true;
+      bool ok = p.stall == 0;   // a stalled self-test issues nothing: the MMA waits run out
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile T = map_tile<FORM>(t, p, offs, tpre);
         for (int kb = 0; kb < T.nkb; ++kb) {
-          if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full_mb[s]);
           const uint32_t a_dst = sbase + s * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_BYTES;
@@ -369,7 +371,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       }
       // drain: every stage's last load must have landed before the CTA exits
       for (int q = 0; q < STAGES; ++q)
-        if (issued & (1 << q)) drain_wait(smem_u32(&full_mb[q]), (last_par >> q) & 1u);
+        if (issued & (1 << q)) drain_wait(smem_u32(&full_mb[q]), (last_par >> q) & 1u, p.wait_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -383,14 +385,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
       if (T.nkb == 0) continue;
-      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tempty_mb[buf]), aph ^ 1u, abort_flag, p.status))) {
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tempty_mb[buf]), aph ^ 1u, abort_flag, p.status, p.wait_ns))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
       for (int kb = 0; kb < T.nkb; ++kb) {
-        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&full_mb[s]), ph, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&full_mb[s]), ph, abort_flag, p.status, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -432,7 +434,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     }
     if (any_mma && lane == 0) {
       mma_commit(drain_bar);
-      drain_wait(drain_bar, 0);
+      drain_wait(drain_bar, 0, p.wait_ns);
     }
     __syncwarp();
   } else {
@@ -455,7 +457,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         continue;
       }
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
-      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
       if (EPI == EPI_SWIGLU_UP) {
@@ -659,6 +661,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.seg_len = g.seg_len;
   p.seg_rows = g.ragged_k ? g.K0 : g.M;
+  p.wait_ns = g.wait_ns > 0 ? g.wait_ns : WAIT_LIMIT_NS;
+  p.stall = g.stall;
   int tiles_upper = 0;
   const uint64_t R = (uint64_t)g.M;
   if (!g.ragged_k && g.b_kcontig) {

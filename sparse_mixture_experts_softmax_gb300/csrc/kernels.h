@@ -108,6 +108,8 @@ struct GemmArgs {
   const void* B0x;              // second B operand of EPI_SWIGLU_UP (W3)
   void* out2;                   // second extra output (H3 of EPI_SWIGLU_UP)
   int* status;                  // device status word (bounded-wait timeouts), tcgen05 only
+  long long wait_ns;            // bound of each device wait (0: the default, ~2 s)
+  int stall;                    // self-test of the timeout path: withhold every load
 };
 
 // CUDA-core GEMMs serve fp32 layers only; bf16 operands go to the tensor cores.

@@ -780,9 +780,28 @@ moe_status moe_device_status(const moe_config* cfg, const void* workspace, size_
   return MOE_OK;
 }
 
+static moe_status grouped_gemm_impl(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
+                                    const int32_t* offsets, const void* A, const void* B, void* C,
+                                    int32_t* dev_status, long long wait_ns, int stall,
+                                    void* stream);
+
 moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
                             const int32_t* offsets, const void* A, const void* B, void* C,
                             int32_t* dev_status, void* stream) {
+  return grouped_gemm_impl(form, M, N, K, E, offsets, A, B, C, dev_status, 0, 0, stream);
+}
+
+moe_status moe_selftest_wait_timeout(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
+                                     const int32_t* offsets, const void* A, const void* B, void* C,
+                                     int32_t* dev_status, int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 2000000000ll) return MOE_ERR_INVALID_ARG;
+  return grouped_gemm_impl(form, M, N, K, E, offsets, A, B, C, dev_status, limit_ns, 1, stream);
+}
+
+static moe_status grouped_gemm_impl(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
+                                    const int32_t* offsets, const void* A, const void* B, void* C,
+                                    int32_t* dev_status, long long wait_ns, int stall,
+                                    void* stream) {
   g_launches = 0;
   if (form < 0 || form > 2 || M < 0 || N <= 0 || K < 0 || E <= 0) return MOE_ERR_INVALID_ARG;
   // inner (contiguous) dimensions must be multiples of 8 elements; form 2's K
@@ -804,6 +823,8 @@ moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32
   g.A0 = A;
   g.B0 = B;
   g.C = C;
+  g.wait_ns = wait_ns;
+  g.stall = stall;
   if (form == 2) {
     // C[e][m][n] = sum over rows r of segment e of A[r, m] B[r, n]; K = total rows
     g.ragged_k = true;

@@ -115,6 +115,13 @@ def test_host_validation_errors(L):
         == B.MOE_ERR_UNSUPPORTED
 
 
+def test_selftest_rejects_unbounded_wait_limit(L):
+    good = lambda i: _Fake(0x10000 * (i + 1))  # noqa: E731
+    for bad in (0, -1, 3_000_000_000):
+        assert _status(B.moe_selftest_wait_timeout, 0, 1, 8, 8, 1, good(1), good(2), good(3),
+                       good(4), good(5), bad) == B.MOE_ERR_INVALID_ARG
+
+
 def test_status_strings(L):
     for s in range(7):
         assert B.moe_status_string(s)

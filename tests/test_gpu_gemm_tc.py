@@ -94,3 +94,32 @@ def test_repeatable_bits():
     B.moe_grouped_gemm(0, M, N, K, E, off, A, Bw, C2, st)
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """Failure detection without a fault: with every load withheld the kernel's
+    bounded waits expire, it stops cleanly and reports MOE_ERR_TIMEOUT in the
+    device status word; the same context then runs a normal GEMM correctly."""
+    counts, N, K = [300, 0, 129], 512, 256
+    E, M = len(counts), sum(counts)
+    off = _offsets(counts)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    A = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    Bw = (torch.randn(E, N, K, generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_selftest_wait_timeout(0, M, N, K, E, off, A, Bw, C, st, 20_000_000)   # 20 ms
+    torch.cuda.synchronize()
+    assert st.item() == 6                        # MOE_ERR_TIMEOUT
+    assert torch.isnan(C.float()).all()          # nothing was stored
+    st.zero_()
+    B.moe_grouped_gemm(0, M, N, K, E, off, A, Bw, C, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = off.tolist()
+    for e in range(E):
+        if counts[e]:
+            ref = A[o[e]:o[e + 1]].float() @ Bw[e].float().T
+            assert _rel(C[o[e]:o[e + 1]].float(), ref) <= 1e-2
+
