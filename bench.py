@@ -72,9 +72,10 @@ def hbm_bytes(wl: W.Workload) -> dict:
         "gather": T * D * es + R * D * es,                 # X once, Xe written
         "combine_loss": R * D * es + 2 * T * D * 4,       # Ye, target read; dY written
         "combine_bwd": T * D * 4 + 2 * R * D * es,        # dY, Ye read; dYe written
-        # every fp32 parameter: master and gradient read, master written; bf16
-        # layers also write the bf16 copy of each expert weight (all launches)
-        "sgd": (wl.E * D + n_exp + n_bias) * 12 + (n_exp * 2 if wl.dtype == "bf16" else 0),
+        # the stand-alone SGD launches: master and gradient read, master
+        # written.  bf16 layers update the expert weights inside the dW GEMM
+        # epilogues, so only the router weight and biases remain here.
+        "sgd": (wl.E * D + n_bias + (0 if wl.dtype == "bf16" else n_exp)) * 12,
     }
 
 
@@ -355,7 +356,7 @@ def main():
     hb = hbm_bytes(wl)
     hbm = {}
     for name, key in (("gather", "gather"), ("combine_loss", "combine_loss"),
-                      ("combine_bwd", "combine_bwd"), ("sgd", "sgd")):
+                      ("combine_bwd", "combine_bwd")) + ((("sgd", "sgd"),) if not lp else ()):
         if name in per_kernel and per_kernel[name] > 0:
             gbs = hb[key] / (per_kernel[name] / 1e3) / 1e9
             hbm[name] = {"ms": per_kernel[name], "GB/s": gbs, "frac": gbs / float(peaks["hbm_gbs"])}

@@ -50,12 +50,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 256;
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;   // + alignment slack
+constexpr int STG_BYTES = 32 * 32 * 4;    // epilogue staging buffer of one warp
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 4 * STG_BYTES + 1024;   // + alignment slack
 constexpr long long WAIT_LIMIT_NS = 2000000000ll;   // default bound of every wait
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
 constexpr int EPI_STORE_F32_TAG = 100;   // TN: fp32 weight-gradient tile store
 constexpr int EPI_ROWS_F32_TAG = 101;    // fp32 row store (+ bias[n]): router logits, router dX
+constexpr int EPI_SGD_F32_TAG = 102;     // TN: fp32 weight-gradient store + fused SGD step
 
 struct TcParams {
   int M, N, E;          // ragged-M: M = total rows; TN: output rows per expert
@@ -75,6 +77,9 @@ struct TcParams {
   int* status;
   int seg_len;          // offsets == nullptr: segment e = [e*seg_len, min((e+1)*seg_len, rows))
   int seg_rows;         // total rows of the implicit segments
+  float* sgd_w;         // EPI_SGD_F32_TAG: fp32 master weights, indexed like C
+  bf16* sgd_wlp;        //   and their bf16 copy (may be null)
+  float sgd_lr;
   long long wait_ns;    // bound of every mbarrier wait
   int stall;            // self-test: the producer withholds every load
 };
@@ -149,6 +154,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// Bulk prefetch of a 16-byte aligned range (a multiple of 16 bytes) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -231,12 +241,63 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   q.w = *reinterpret_cast<uint32_t*>(&d);
   return q;
 }
-__device__ __forceinline__ void unpack8_bf16(uint4 q, float* v) {
+__device__ __forceinline__ uint2 pack4_bf16(const float* v) {
+  uint2 q;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  q.x = *reinterpret_cast<uint32_t*>(&a);
+  q.y = *reinterpret_cast<uint32_t*>(&b);
+  return q;
+}
+__device__ __forceinline__ void unpack4_bf16(uint2 q, float* v) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+  v[0] = __low2float(h[0]);
+  v[1] = __high2float(h[0]);
+  v[2] = __low2float(h[1]);
+  v[3] = __high2float(h[1]);
+}
+
+// Four bf16 at column n of rows row0 + 4 j (j = 0..7) of a row-major
+// matrix with leading dimension ld; zeros for rows >= row_hi or n >= N.
+__device__ __forceinline__ void load_bf16x4_rows(const bf16* base, long long ld, int row0,
+                                                 int row_hi, int n, int N, uint2 (&d)[8]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __low2float(h[i]);
-    v[2 * i + 1] = __high2float(h[i]);
+  for (int j = 0; j < 8; ++j) {
+    const int g = row0 + 4 * j;
+    d[j] = (g < row_hi && n < N) ? __ldg(reinterpret_cast<const uint2*>(base + (size_t)g * ld + n))
+                                 : make_uint2(0u, 0u);
+  }
+}
+// The same for fp32 (plain loads: the SGD epilogue rewrites these weights).
+__device__ __forceinline__ void load_f32x4_rows(const float* base, long long ld, int row0,
+                                                int row_hi, int n, int N, float4 (&d)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int g = row0 + 4 * j;
+    d[j] = (g < row_hi && n < N) ? *reinterpret_cast<const float4*>(base + (size_t)g * ld + n)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// 32 accumulator columns from TMEM (row = this lane's TMEM lane) through a
+// 32 x 32 fp32 shared buffer of the warp, 16-byte pieces XOR-swizzled by
+// row so that both the row-wise writes and the column-wise reads are free of
+// bank conflicts.  out[j] = columns 4 (lane % 8) .. +3 of row lane / 8 + 4 j.
+__device__ __forceinline__ void stage_chunk(float* stg, int lane, uint32_t taddr, float4 (&out)[8]) {
+  float v[32];
+  tmem_ld16(taddr, v);
+  tmem_ld16(taddr + 16, v + 16);
+  tmem_ld_wait();
+  __syncwarp();   // the previous chunk's readers are done with the buffer
+  float4* mine = reinterpret_cast<float4*>(stg + lane * 32);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mine[q ^ (lane & 7)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  __syncwarp();
+  const int cq = lane & 7, cr = lane >> 3;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int rr = cr + 4 * j;
+    out[j] = reinterpret_cast<const float4*>(stg + rr * 32)[cq ^ (rr & 7)];
   }
 }
 
@@ -333,6 +394,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       bool ok = p.stall == 0;   // a stalled self-test issues nothing: the MMA waits run out
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile T = map_tile<FORM>(t, p, offs, tpre);
+        if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
+          // the epilogue of this tile reads its rows of H (H1, H3) about one
+          // tile's MMA time from now: stage them in L2 meanwhile
+          const int rhi = min(T.row_hi, T.m0 + BM);
+          const int ncols = min(BN, p.N - T.n0);
+          for (int rr = T.m0; rr < rhi && ncols > 0; ++rr) {
+            const size_t o = (size_t)rr * p.ld_aux + T.n0;
+            prefetch_l2(p.aux0 + o, (uint32_t)ncols * 2u);
+            if (EPI == EPI_SWIGLU_BWD) prefetch_l2(p.aux1 + o, (uint32_t)ncols * 2u);
+          }
+        }
+        if (EPI == EPI_SGD_F32_TAG) {
+          // the epilogue reads this tile of the fp32 master weights
+          const int rhi = min(T.row_hi, T.m0 + BM);
+          const int ncols = min(BN, p.N - T.n0);
+          for (int rr = T.m0; rr < rhi && ncols > 0; ++rr)
+            prefetch_l2(p.sgd_w + (size_t)T.e * p.sCe + (size_t)rr * p.ldc + T.n0,
+                        (uint32_t)ncols * 4u);
+        }
         for (int kb = 0; kb < T.nkb; ++kb) {
           if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full_mb[s]);
@@ -439,6 +519,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + (warp - 2) * STG_BYTES);
     const int lane_base = (warp & 3) * 32;
     const int row = lane_base + lane;
     int buf = 0;
@@ -448,100 +529,130 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       const int r = T.m0 + row;
       const bool rok = r < T.row_hi;
       if (T.nkb == 0) {
-        // ragged K with an empty expert: dW tile is exactly zero
+        // ragged K with an empty expert: dW tile is exactly zero (and the SGD
+        // step leaves W as it is; its bf16 copy is still rewritten from W)
         if (FORM == FORM_TN && rok) {
-          float* c = static_cast<float*>(p.C) + (size_t)T.e * p.sCe + (size_t)r * p.ldc;
+          const size_t o = (size_t)T.e * p.sCe + (size_t)r * p.ldc;
+          float* c = static_cast<float*>(p.C) + o;
           for (int n = T.n0; n < T.n0 + BN && n < p.N; n += 4)
             *reinterpret_cast<float4*>(c + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (EPI == EPI_SGD_F32_TAG && p.sgd_wlp) {
+            for (int n = T.n0; n < T.n0 + BN && n < p.N; n += 8) {
+              float w[8];
+              *reinterpret_cast<float4*>(w) = *reinterpret_cast<const float4*>(p.sgd_w + o + n);
+              *reinterpret_cast<float4*>(w + 4) = *reinterpret_cast<const float4*>(p.sgd_w + o + n + 4);
+              *reinterpret_cast<uint4*>(p.sgd_wlp + o + n) = pack8_bf16(w);
+            }
+          }
         }
         continue;
       }
+      // Each 32-column chunk of the accumulator goes TMEM -> registers (one
+      // row per lane) -> this warp's swizzled shared buffer -> registers in
+      // a coalesced layout: lane l then owns columns 4 (l % 8) .. +3 of rows
+      // l / 8 + 4 j, j = 0..7, so eight lanes cover 128 contiguous bytes of a
+      // row and every global load and store below is coalesced.
+      const int cq = lane & 7;
+      const int row0 = T.m0 + lane_base + (lane >> 3);
+      const int ncols = EPI == EPI_SWIGLU_UP ? 128 : BN;
+      // side inputs (H / H1, H3 of the backward epilogues, the fp32 master
+      // weights of the SGD epilogue) are fetched one chunk ahead
+      uint2 h1c[8], h3c[8], h1n[8], h3n[8];
+      float4 wc[8], wn[8];
+      const size_t wbase = (size_t)T.e * p.sCe;
+      if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
+        load_bf16x4_rows(p.aux0, p.ld_aux, row0, T.row_hi, T.n0 + 4 * cq, p.N, h1c);
+        if (EPI == EPI_SWIGLU_BWD) load_bf16x4_rows(p.aux1, p.ld_aux, row0, T.row_hi, T.n0 + 4 * cq, p.N, h3c);
+      }
+      if (EPI == EPI_SGD_F32_TAG) load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, T.n0 + 4 * cq, p.N, wc);
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
-      if (EPI == EPI_SWIGLU_UP) {
-        for (int c = 0; c < 128; c += 16) {
-          float h1[16], h3[16];
-          tmem_ld16(t_row + c, h1);
-          tmem_ld16(t_row + 128 + c, h3);
-          tmem_ld_wait();
-          const int f = T.n0 + c;
-          if (rok) {
+#pragma unroll 1
+      for (int cc = 0; cc < ncols; cc += 32) {
+        const int n = T.n0 + cc + 4 * cq;
+        const bool more = cc + 32 < ncols;
+        if (more && (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD)) {
+          load_bf16x4_rows(p.aux0, p.ld_aux, row0, T.row_hi, n + 32, p.N, h1n);
+          if (EPI == EPI_SWIGLU_BWD) load_bf16x4_rows(p.aux1, p.ld_aux, row0, T.row_hi, n + 32, p.N, h3n);
+        }
+        if (more && EPI == EPI_SGD_F32_TAG)
+          load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, n + 32, p.N, wn);
+        float4 acc[8], acc3[8];
+        stage_chunk(stg, lane, t_row + cc, acc);
+        if (EPI == EPI_SWIGLU_UP) stage_chunk(stg, lane, t_row + 128 + cc, acc3);
+        constexpr bool BIAS_EPI = EPI == EPI_STORE || EPI == EPI_ROWS_F32_TAG || EPI == EPI_ACT_FWD;
+        const bool add_bias = BIAS_EPI && p.bias != nullptr && n < p.N;
+        float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (add_bias) b4 = *reinterpret_cast<const float4*>(p.bias + (size_t)T.e * p.N + n);
 #pragma unroll
-            for (int g = 0; g < 16; g += 8) {
-              if (f + g < p.N) {
-                float av[8];
+        for (int j = 0; j < 8; ++j) {
+          const int g = row0 + 4 * j;
+          if (g >= T.row_hi || n >= p.N) continue;
+          float x[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+          if (add_bias) {
+            x[0] += b4.x;
+            x[1] += b4.y;
+            x[2] += b4.z;
+            x[3] += b4.w;
+          }
+          const size_t o = (size_t)g * p.ldc + n;
+          if (EPI == EPI_STORE) {
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(x);
+          } else if (EPI == EPI_ROWS_F32_TAG) {
+            *reinterpret_cast<float4*>(static_cast<float*>(p.C) + o) = make_float4(x[0], x[1], x[2], x[3]);
+          } else if (EPI == EPI_STORE_F32_TAG) {
+            *reinterpret_cast<float4*>(static_cast<float*>(p.C) + wbase + o) = acc[j];
+          } else if (EPI == EPI_SGD_F32_TAG) {
+            // dW stored as is; the update uses the same fused multiply-add and
+            // round-to-nearest bf16 conversion as the stand-alone SGD kernel
+            *reinterpret_cast<float4*>(static_cast<float*>(p.C) + wbase + o) = acc[j];
+            float w[4] = {wc[j].x, wc[j].y, wc[j].z, wc[j].w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) av[i] = silu_f(h1[g + i]) * h3[g + i];
-                const size_t o = (size_t)r * p.ldc + f + g;
-                *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out1) + o) = pack8_bf16(h1 + g);
-                *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out2) + o) = pack8_bf16(h3 + g);
-                *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + o) = pack8_bf16(av);
-              }
+            for (int i = 0; i < 4; ++i) w[i] = fmaf(-p.sgd_lr, x[i], w[i]);
+            *reinterpret_cast<float4*>(p.sgd_w + wbase + o) = make_float4(w[0], w[1], w[2], w[3]);
+            if (p.sgd_wlp) *reinterpret_cast<uint2*>(p.sgd_wlp + wbase + o) = pack4_bf16(w);
+          } else if (EPI == EPI_ACT_FWD) {
+            float a[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = p.act == 0 ? fmaxf(x[i], 0.f) : gelu_tanh_f(x[i]);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out1) + o) = pack4_bf16(x);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(a);
+          } else if (EPI == EPI_ACT_BWD) {
+            float h[4], dh[4];
+            unpack4_bf16(h1c[j], h);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_tanh_grad_f(h[i]);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(dh);
+          } else if (EPI == EPI_SWIGLU_BWD) {
+            float h1[4], h3[4], d1[4], d3[4];
+            unpack4_bf16(h1c[j], h1);
+            unpack4_bf16(h3c[j], h3);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              d1[i] = x[i] * h3[i] * silu_grad_f(h1[i]);
+              d3[i] = x[i] * silu_f(h1[i]);
             }
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(d1);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out1) + o) = pack4_bf16(d3);
+          } else if (EPI == EPI_SWIGLU_UP) {
+            const float h3[4] = {acc3[j].x, acc3[j].y, acc3[j].z, acc3[j].w};
+            float a[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = silu_f(x[i]) * h3[i];
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out1) + o) = pack4_bf16(x);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out2) + o) = pack4_bf16(h3);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(a);
           }
         }
-      } else {
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          tmem_ld16(t_row + c, v);
-          tmem_ld_wait();
-          const int n = T.n0 + c;
-          if (!rok || n >= p.N) continue;
+        if (more) {
 #pragma unroll
-          for (int g = 0; g < 16; g += 8) {
-            if (n + g >= p.N) break;
-            float* x = v + g;
-            const int nn = n + g;
-            if (EPI == EPI_STORE_F32_TAG) {
-              float* cp = static_cast<float*>(p.C) + (size_t)T.e * p.sCe + (size_t)r * p.ldc + nn;
-              *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
-              *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
-            } else if (EPI == EPI_ROWS_F32_TAG) {
-              if (p.bias) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] += p.bias[(size_t)T.e * p.N + nn + i];
-              }
-              float* cp = static_cast<float*>(p.C) + (size_t)r * p.ldc + nn;
-              *reinterpret_cast<float4*>(cp) = make_float4(x[0], x[1], x[2], x[3]);
-              *reinterpret_cast<float4*>(cp + 4) = make_float4(x[4], x[5], x[6], x[7]);
-            } else if (EPI == EPI_STORE) {
-              if (p.bias) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] += p.bias[(size_t)T.e * p.N + nn + i];
-              }
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + (size_t)r * p.ldc + nn) = pack8_bf16(x);
-            } else if (EPI == EPI_ACT_FWD) {
-              float a[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (p.bias) x[i] += p.bias[(size_t)T.e * p.N + nn + i];
-                a[i] = p.act == 0 ? fmaxf(x[i], 0.f) : gelu_tanh_f(x[i]);
-              }
-              const size_t o = (size_t)r * p.ldc + nn;
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out1) + o) = pack8_bf16(x);
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + o) = pack8_bf16(a);
-            } else if (EPI == EPI_ACT_BWD) {
-              float h[8], dh[8];
-              unpack8_bf16(*reinterpret_cast<const uint4*>(p.aux0 + (size_t)r * p.ld_aux + nn), h);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_tanh_grad_f(h[i]);
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + (size_t)r * p.ldc + nn) = pack8_bf16(dh);
-            } else if (EPI == EPI_SWIGLU_BWD) {
-              float h1[8], h3[8], d1[8], d3[8];
-              unpack8_bf16(*reinterpret_cast<const uint4*>(p.aux0 + (size_t)r * p.ld_aux + nn), h1);
-              unpack8_bf16(*reinterpret_cast<const uint4*>(p.aux1 + (size_t)r * p.ld_aux + nn), h3);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                d1[i] = x[i] * h3[i] * silu_grad_f(h1[i]);
-                d3[i] = x[i] * silu_f(h1[i]);
-              }
-              const size_t o = (size_t)r * p.ldc + nn;
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.C) + o) = pack8_bf16(d1);
-              *reinterpret_cast<uint4*>(static_cast<bf16*>(p.out1) + o) = pack8_bf16(d3);
-            }
+          for (int j = 0; j < 8; ++j) {
+            h1c[j] = h1n[j];
+            h3c[j] = h3n[j];
+            wc[j] = wn[j];
           }
         }
       }
@@ -661,6 +772,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.seg_len = g.seg_len;
   p.seg_rows = g.ragged_k ? g.K0 : g.M;
+  p.sgd_w = g.sgd_w;
+  p.sgd_wlp = static_cast<bf16*>(g.sgd_wlp);
+  p.sgd_lr = g.sgd_lr;
   p.wait_ns = g.wait_ns > 0 ? g.wait_ns : WAIT_LIMIT_NS;
   p.stall = g.stall;
   int tiles_upper = 0;
@@ -731,7 +845,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if (g.c_type != 0 || g.epi != EPI_STORE) return cudaErrorInvalidValue;
   const uint64_t Rk = (uint64_t)g.K0;
   if (Rk == 0) {
-    // no rows at all: every expert's gradient is zero
+    // no rows at all: every expert's gradient is zero (callers with no rows
+    // skip the SGD step, so a fused update has nothing to do here)
+    if (g.sgd_w != nullptr) return cudaErrorInvalidValue;
     return cudaMemsetAsync(g.C, 0, (size_t)g.E * g.sCe * sizeof(float), st);
   }
   const uint64_t ad[2] = {(uint64_t)g.M, Rk}, as[1] = {(uint64_t)g.lda * 2};
@@ -746,6 +862,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   p.nN = (g.N + BN - 1) / BN;
   p.K1 = 0;
   tiles_upper = g.E * p.nM * p.nN;
+  if (g.sgd_w != nullptr) return launch_inst<FORM_TN, EPI_SGD_F32_TAG>(maps, p, tiles_upper, st);
   return launch_inst<FORM_TN, EPI_STORE_F32_TAG>(maps, p, tiles_upper, st);
 }
 

@@ -110,6 +110,11 @@ struct GemmArgs {
   int* status;                  // device status word (bounded-wait timeouts), tcgen05 only
   long long wait_ns;            // bound of each device wait (0: the default, ~2 s)
   int stall;                    // self-test of the timeout path: withhold every load
+  // ragged-K weight gradients only: with sgd_w set, the epilogue also applies
+  // SGD, sgd_w -= sgd_lr * dW, and rewrites the bf16 copy sgd_wlp (same layout as C)
+  float* sgd_w;
+  void* sgd_wlp;
+  float sgd_lr;
 };
 
 // CUDA-core GEMMs serve fp32 layers only; bf16 operands go to the tensor cores.

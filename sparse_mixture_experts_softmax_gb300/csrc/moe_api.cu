@@ -318,10 +318,19 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   return MOE_OK;
 }
 
+// SGD folded into the weight-gradient GEMMs of a bf16 training step: each
+// expert weight is updated, and its bf16 copy rewritten, as soon as its
+// gradient tile exists (every GEMM reading that copy has run by then).
+struct SgdFuse {
+  float lr;
+  float *w1, *w3, *w2;
+  void *w1_lp, *w3_lp, *w2_lp;
+};
+
 // Backward of L = L_task + alpha aux given dY (course Parts 4-6).
 moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, const float* dy,
                         const moe_grads& gr, float* dx, bool aux_ready, const Ptrs& P,
-                        cudaStream_t st) {
+                        cudaStream_t st, const SgdFuse* sgd = nullptr) {
   const Layout& L = *P.L;
   const long long R = (long long)c.T * c.k;
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
@@ -373,6 +382,11 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
   w2g.ldc = c.F;
   w2g.sCe = (long long)c.D * c.F;
   w2g.epi = EPI_STORE;
+  if (sgd) {
+    w2g.sgd_w = sgd->w2;
+    w2g.sgd_wlp = sgd->w2_lp;
+    w2g.sgd_lr = sgd->lr;
+  }
   KL("gemm_dw2", run_gemm(c, w2g, st));
   if (gr.db2) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dye), P.at<int>(L.offsets), c.E, c.D, gr.db2, st));
   // dXe = dH1 W1_e (+ dH3 W3_e)
@@ -414,10 +428,19 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
   w1g.ldc = c.D;
   w1g.sCe = (long long)c.F * c.D;
   w1g.epi = EPI_STORE;
+  if (sgd) {
+    w1g.sgd_w = sgd->w1;
+    w1g.sgd_wlp = sgd->w1_lp;
+    w1g.sgd_lr = sgd->lr;
+  }
   KL("gemm_dw1", run_gemm(c, w1g, st));
   if (swiglu) {
     w1g.A0 = P.at<void>(L.dh3);
     w1g.C = gr.dw3;
+    if (sgd) {
+      w1g.sgd_w = sgd->w3;
+      w1g.sgd_wlp = sgd->w3_lp;
+    }
     KL("gemm_dw3", run_gemm(c, w1g, st));
   }
   if (gr.db1) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dh1), P.at<int>(L.offsets), c.E, c.F, gr.db1, st));
@@ -616,15 +639,20 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   w.logit_bias = p->logit_bias;
   RET_IF(run_forward(c, w, x, nullptr, y_target, d_loss, P, st));
   float* dxp = dx ? dx : P.at<float>(L.dx);
-  RET_IF(run_backward(c, w, x, P.at<float>(L.dy), p->grads, dxp, true, P, st));
+  // bf16 layers: the expert weights' SGD runs inside the dW GEMM epilogues
+  const bool fused = c.dtype == MOE_BF16;
+  const SgdFuse sf{lr, p->w1, p->w3, p->w2, p->w1_lp, p->w3_lp, p->w2_lp};
+  RET_IF(run_backward(c, w, x, P.at<float>(L.dy), p->grads, dxp, true, P, st,
+                      fused ? &sf : nullptr));
   // SGD on the fp32 masters; bf16 working copies rewritten from the result
   const long long E = c.E, D = c.D, F = c.F;
   const moe_grads& g = p->grads;
   KL("sgd", launch_sgd(p->w_gate, g.dw_gate, E * D, lr, nullptr, st));
-  KL("sgd", launch_sgd(p->w1, g.dw1, E * F * D, lr, c.dtype == MOE_BF16 ? p->w1_lp : nullptr, st));
-  if (c.act == MOE_ACT_SWIGLU)
-    KL("sgd", launch_sgd(p->w3, g.dw3, E * F * D, lr, c.dtype == MOE_BF16 ? p->w3_lp : nullptr, st));
-  KL("sgd", launch_sgd(p->w2, g.dw2, E * D * F, lr, c.dtype == MOE_BF16 ? p->w2_lp : nullptr, st));
+  if (!fused) {
+    KL("sgd", launch_sgd(p->w1, g.dw1, E * F * D, lr, nullptr, st));
+    if (c.act == MOE_ACT_SWIGLU) KL("sgd", launch_sgd(p->w3, g.dw3, E * F * D, lr, nullptr, st));
+    KL("sgd", launch_sgd(p->w2, g.dw2, E * D * F, lr, nullptr, st));
+  }
   if (c.has_bias) {
     KL("sgd", launch_sgd(p->b1, g.db1, E * F, lr, nullptr, st));
     KL("sgd", launch_sgd(p->b2, g.db2, E * D, lr, nullptr, st));

@@ -7,8 +7,10 @@ compute exactly or one token at a time:
   * the scores and the aux loss against the oracle's fp64 router (cheap);
   * the MSE loss against the mean of (y - target)^2 of the GPU's own y;
   * y and dX on sampled tokens, each token's k expert rows run by the oracle;
-  * the weight gradients of the smallest non-empty expert (every token routed
-    to it runs through the oracle), and exact zeros for experts with no rows.
+  * the weight gradients and SGD step of the smallest non-empty expert (every
+    token routed to it runs through the oracle), and exact zeros for experts
+    with no rows;
+  * every bf16 working copy equal to the bf16 rounding of its updated master.
 Expert weights are pulled to float64 one expert at a time.
 """
 
@@ -165,8 +167,20 @@ def test_full_size_layer(name, n_sample):
         xe = x64[rows_tok]
         fe = O.expert_forward(cfg, e_min, xe, w)
         be = O.expert_backward(cfg, e_min, xe, fe, dye, w)
-        assert_close(f"dw1[{e_min}]", np64(layer.dw1[e_min]), be["dw1"], TOL)
-        assert_close(f"dw3[{e_min}]", np64(layer.dw3[e_min]), be["dw3"], TOL)
-        assert_close(f"dw2[{e_min}]", np64(layer.dw2[e_min]), be["dw2"], TOL)
+        for key in ("w1", "w3", "w2"):
+            assert_close(f"d{key}[{e_min}]", np64(getattr(layer, "d" + key)[e_min]), be["d" + key],
+                         TOL)
+            # the SGD step of that expert: theta_1 - theta_0 against -lr * grad
+            # (tolerance widened by half an fp32 ulp of |theta|)
+            w0 = np64(inp[key][e_min])
+            step = np64(getattr(layer, key)[e_min]) - w0
+            want = -wl.lr * be["d" + key]
+            scale = np.max(np.abs(want))
+            assert_close(f"step {key}[{e_min}]", step, want,
+                         TOL + 2.0 ** -24 * np.max(np.abs(w0)) / scale)
+    # 7. every expert's bf16 working copy is the round-to-nearest image of its
+    #    updated fp32 master
+    for key in ("w1", "w3", "w2"):
+        assert torch.equal(getattr(layer, key + "_lp"), getattr(layer, key).to(torch.bfloat16)), key
     del layer, inp
     torch.cuda.empty_cache()

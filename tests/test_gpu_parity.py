@@ -63,6 +63,20 @@ def _one_step_parity(wl, seed=0, check_dx=True):
             continue
         want = master[key] - wl.lr * g["d" + key]
         errs[key] = assert_close(key, np64(new[key]), want, tol)
+        # the update itself: lr * grad is far below |theta|, so compare the
+        # step theta_1 - theta_0 with -lr * grad; storing theta_1 in fp32
+        # adds up to half an ulp of |theta| to it
+        step = np64(new[key]) - master[key]
+        want_step = -wl.lr * g["d" + key]
+        scale = np.max(np.abs(want_step))
+        step_tol = tol + 2.0 ** -24 * np.max(np.abs(master[key])) / scale if scale > 0 else tol
+        assert_close("step " + key, step, want_step, step_tol)
+    if wl.dtype == "bf16":
+        # the bf16 working copies are the round-to-nearest images of the masters
+        for key in ("w1", "w2", "w3"):
+            lp = getattr(layer, key + "_lp")
+            if lp is not None:
+                assert torch.equal(lp, new[key].to(torch.bfloat16)), key
     return errs, layer, inp
 
 
