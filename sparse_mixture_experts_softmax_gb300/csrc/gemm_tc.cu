@@ -10,9 +10,12 @@
 //               swizzle, into a 4-stage shared-memory ring (mbarrier tx count);
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma (M=128, N=256,
 //               K=16) from one lane, frees ring stages with tcgen05.commit;
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane =
-//               one output row per thread), bias / activation / SwiGLU (and
-//               their backward) applied in registers, stores to HBM.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (each takes half of
+//               the tile's columns): tcgen05.ld of the fp32 accumulator, a
+//               swizzled shared-memory transpose per 16-column chunk so that
+//               every global access is coalesced, bias / activation / SwiGLU
+//               (and their backward, and the fused SGD update of weight
+//               gradients) applied in registers.
 // Two 256-column accumulators let the epilogue of one tile overlap the main
 // loop of the next.
 //
@@ -47,11 +50,14 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BYTES = BN * BK * 2;    // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 256;
-constexpr int STG_BYTES = 32 * 32 * 4;    // epilogue staging buffer of one warp
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 4 * STG_BYTES + 1024;   // + alignment slack
+constexpr int CHUNK = 16;                // accumulator columns per epilogue step
+constexpr int STG_BYTES = 32 * CHUNK * 4; // epilogue staging buffer of one warp
+constexpr size_t SMEM_BYTES =
+    (size_t)STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES + 1024;   // + alignment slack
 constexpr long long WAIT_LIMIT_NS = 2000000000ll;   // default bound of every wait
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
@@ -257,47 +263,56 @@ __device__ __forceinline__ void unpack4_bf16(uint2 q, float* v) {
   v[3] = __high2float(h[1]);
 }
 
-// Four bf16 at column n of rows row0 + 4 j (j = 0..7) of a row-major
-// matrix with leading dimension ld; zeros for rows >= row_hi or n >= N.
+// Side inputs of one epilogue chunk in the coalesced layout (four rows per
+// lane): H or H1 / H3 for the backward epilogues, fp32 master weights for the
+// fused SGD.  Members an epilogue does not use are never touched.
+struct Side {
+  uint2 h1[4], h3[4];
+  float4 w[4];
+};
+
+// Four bf16 at column n of rows row0 + 8 j (j = 0..3) of a row-major matrix
+// with leading dimension ld; zeros for rows >= row_hi or n >= N.
 __device__ __forceinline__ void load_bf16x4_rows(const bf16* base, long long ld, int row0,
-                                                 int row_hi, int n, int N, uint2 (&d)[8]) {
+                                                 int row_hi, int n, int N, uint2 (&d)[4]) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int g = row0 + 4 * j;
+  for (int j = 0; j < 4; ++j) {
+    const int g = row0 + 8 * j;
     d[j] = (g < row_hi && n < N) ? __ldg(reinterpret_cast<const uint2*>(base + (size_t)g * ld + n))
                                  : make_uint2(0u, 0u);
   }
 }
 // The same for fp32 (plain loads: the SGD epilogue rewrites these weights).
 __device__ __forceinline__ void load_f32x4_rows(const float* base, long long ld, int row0,
-                                                int row_hi, int n, int N, float4 (&d)[8]) {
+                                                int row_hi, int n, int N, float4 (&d)[4]) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int g = row0 + 4 * j;
+  for (int j = 0; j < 4; ++j) {
+    const int g = row0 + 8 * j;
     d[j] = (g < row_hi && n < N) ? *reinterpret_cast<const float4*>(base + (size_t)g * ld + n)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
-// 32 accumulator columns from TMEM (row = this lane's TMEM lane) through a
-// 32 x 32 fp32 shared buffer of the warp, 16-byte pieces XOR-swizzled by
-// row so that both the row-wise writes and the column-wise reads are free of
-// bank conflicts.  out[j] = columns 4 (lane % 8) .. +3 of row lane / 8 + 4 j.
-__device__ __forceinline__ void stage_chunk(float* stg, int lane, uint32_t taddr, float4 (&out)[8]) {
-  float v[32];
+// 16 accumulator columns from TMEM (row = this lane's TMEM lane) through a
+// 32 x 16 fp32 shared buffer of the warp; 16-byte pieces are XOR-swizzled by
+// row pairs so that the row-wise writes and the column-wise reads are both
+// free of bank conflicts.  out[j] = columns 4 (lane % 4) .. +3 of row
+// lane / 4 + 8 j.
+__device__ __forceinline__ void stage_chunk(float* stg, int lane, uint32_t taddr, float4 (&out)[4]) {
+  float v[16];
   tmem_ld16(taddr, v);
-  tmem_ld16(taddr + 16, v + 16);
   tmem_ld_wait();
   __syncwarp();   // the previous chunk's readers are done with the buffer
-  float4* mine = reinterpret_cast<float4*>(stg + lane * 32);
+  float4* mine = reinterpret_cast<float4*>(stg + lane * CHUNK);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) mine[q ^ (lane & 7)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  for (int q = 0; q < 4; ++q)
+    mine[q ^ ((lane >> 1) & 3)] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   __syncwarp();
-  const int cq = lane & 7, cr = lane >> 3;
+  const int cq = lane & 3, cr = lane >> 2;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int rr = cr + 4 * j;
-    out[j] = reinterpret_cast<const float4*>(stg + rr * 32)[cq ^ (rr & 7)];
+  for (int j = 0; j < 4; ++j) {
+    const int rr = cr + 8 * j;
+    out[j] = reinterpret_cast<const float4*>(stg + rr * CHUNK)[cq ^ ((rr >> 1) & 3)];
   }
 }
 
@@ -364,7 +379,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_mb[b]), 1);
-      mbar_init(smem_u32(&tempty_mb[b]), 4);
+      mbar_init(smem_u32(&tempty_mb[b]), NUM_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     abort_word = 0;
@@ -386,6 +401,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the operand loads.  At the start of a tile it also stages
+    // in L2 the rows that tile's epilogue will read about one tile's MMA
+    // time later (H / H1, H3 of the backward epilogues, the fp32 masters of
+    // the fused SGD).
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
@@ -394,24 +413,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       bool ok = p.stall == 0;   // a stalled self-test issues nothing: the MMA waits run out
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile T = map_tile<FORM>(t, p, offs, tpre);
-        if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
-          // the epilogue of this tile reads its rows of H (H1, H3) about one
-          // tile's MMA time from now: stage them in L2 meanwhile
+        {
           const int rhi = min(T.row_hi, T.m0 + BM);
           const int ncols = min(BN, p.N - T.n0);
-          for (int rr = T.m0; rr < rhi && ncols > 0; ++rr) {
-            const size_t o = (size_t)rr * p.ld_aux + T.n0;
-            prefetch_l2(p.aux0 + o, (uint32_t)ncols * 2u);
-            if (EPI == EPI_SWIGLU_BWD) prefetch_l2(p.aux1 + o, (uint32_t)ncols * 2u);
+          if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
+            for (int rr = T.m0; rr < rhi && ncols > 0; ++rr) {
+              const size_t o = (size_t)rr * p.ld_aux + T.n0;
+              prefetch_l2(p.aux0 + o, (uint32_t)ncols * 2u);
+              if (EPI == EPI_SWIGLU_BWD) prefetch_l2(p.aux1 + o, (uint32_t)ncols * 2u);
+            }
           }
-        }
-        if (EPI == EPI_SGD_F32_TAG) {
-          // the epilogue reads this tile of the fp32 master weights
-          const int rhi = min(T.row_hi, T.m0 + BM);
-          const int ncols = min(BN, p.N - T.n0);
-          for (int rr = T.m0; rr < rhi && ncols > 0; ++rr)
-            prefetch_l2(p.sgd_w + (size_t)T.e * p.sCe + (size_t)rr * p.ldc + T.n0,
-                        (uint32_t)ncols * 4u);
+          if (EPI == EPI_SGD_F32_TAG) {
+            for (int rr = T.m0; rr < rhi && ncols > 0; ++rr)
+              prefetch_l2(p.sgd_w + (size_t)T.e * p.sCe + (size_t)rr * p.ldc + T.n0, (uint32_t)ncols * 4u);
+          }
         }
         for (int kb = 0; kb < T.nkb; ++kb) {
           if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
@@ -451,7 +466,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       }
       // drain: every stage's last load must have landed before the CTA exits
       for (int q = 0; q < STAGES; ++q)
-        if (issued & (1 << q)) drain_wait(smem_u32(&full_mb[q]), (last_par >> q) & 1u, p.wait_ns);
+          if (issued & (1 << q)) drain_wait(smem_u32(&full_mb[q]), (last_par >> q) & 1u, p.wait_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -520,7 +535,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
   } else {
     // ------------------------------------------------------------ epilogue
     float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + (warp - 2) * STG_BYTES);
+    // TMEM lane quarter of this warp (a warp may only read lanes
+    // 32 (warp % 4) .. +31) and which half of the tile's columns it takes
     const int lane_base = (warp & 3) * 32;
+    const int half = (warp - 2) >> 2;
     const int row = lane_base + lane;
     int buf = 0;
     uint32_t aph = 0;
@@ -534,10 +552,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         if (FORM == FORM_TN && rok) {
           const size_t o = (size_t)T.e * p.sCe + (size_t)r * p.ldc;
           float* c = static_cast<float*>(p.C) + o;
-          for (int n = T.n0; n < T.n0 + BN && n < p.N; n += 4)
+          const int nb = T.n0 + half * (BN / 2), ne = min(nb + BN / 2, p.N);
+          for (int n = nb; n < ne; n += 4)
             *reinterpret_cast<float4*>(c + n) = make_float4(0.f, 0.f, 0.f, 0.f);
           if (EPI == EPI_SGD_F32_TAG && p.sgd_wlp) {
-            for (int n = T.n0; n < T.n0 + BN && n < p.N; n += 8) {
+            for (int n = nb; n < ne; n += 8) {
               float w[8];
               *reinterpret_cast<float4*>(w) = *reinterpret_cast<const float4*>(p.sgd_w + o + n);
               *reinterpret_cast<float4*>(w + 4) = *reinterpret_cast<const float4*>(p.sgd_w + o + n + 4);
@@ -547,39 +566,34 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         }
         continue;
       }
-      // Each 32-column chunk of the accumulator goes TMEM -> registers (one
-      // row per lane) -> this warp's swizzled shared buffer -> registers in
-      // a coalesced layout: lane l then owns columns 4 (l % 8) .. +3 of rows
-      // l / 8 + 4 j, j = 0..7, so eight lanes cover 128 contiguous bytes of a
-      // row and every global load and store below is coalesced.
-      const int cq = lane & 7;
-      const int row0 = T.m0 + lane_base + (lane >> 3);
+      // Each 16-column chunk of the accumulator goes TMEM -> registers (one
+      // row per lane) -> this warp's swizzled shared buffer -> registers in a
+      // coalesced layout: lane l then owns columns 4 (l % 4) .. +3 of rows
+      // l / 4 + 8 j, j = 0..3, so four lanes cover 64 contiguous bytes of a
+      // fp32 row and every global load and store below is coalesced.
+      const int cq = lane & 3;
+      const int row0 = T.m0 + lane_base + (lane >> 2);
       const int ncols = EPI == EPI_SWIGLU_UP ? 128 : BN;
-      // side inputs (H / H1, H3 of the backward epilogues, the fp32 master
-      // weights of the SGD epilogue) are fetched one chunk ahead
-      uint2 h1c[8], h3c[8], h1n[8], h3n[8];
-      float4 wc[8], wn[8];
+      const int c_begin = half * (ncols / 2), c_end = c_begin + ncols / 2;
       const size_t wbase = (size_t)T.e * p.sCe;
-      if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
-        load_bf16x4_rows(p.aux0, p.ld_aux, row0, T.row_hi, T.n0 + 4 * cq, p.N, h1c);
-        if (EPI == EPI_SWIGLU_BWD) load_bf16x4_rows(p.aux1, p.ld_aux, row0, T.row_hi, T.n0 + 4 * cq, p.N, h3c);
-      }
-      if (EPI == EPI_SGD_F32_TAG) load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, T.n0 + 4 * cq, p.N, wc);
+      // side inputs are fetched one chunk ahead, alternating two buffers
+      auto load_side = [&](int n, Side& d) {
+        if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
+          load_bf16x4_rows(p.aux0, p.ld_aux, row0, T.row_hi, n, p.N, d.h1);
+          if (EPI == EPI_SWIGLU_BWD) load_bf16x4_rows(p.aux1, p.ld_aux, row0, T.row_hi, n, p.N, d.h3);
+        }
+        if (EPI == EPI_SGD_F32_TAG) load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, n, p.N, d.w);
+      };
+      Side sa, sb;
+      load_side(T.n0 + c_begin + 4 * cq, sa);
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
-#pragma unroll 1
-      for (int cc = 0; cc < ncols; cc += 32) {
+      auto chunk = [&](int cc, const Side& use, Side& fill) {
         const int n = T.n0 + cc + 4 * cq;
-        const bool more = cc + 32 < ncols;
-        if (more && (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD)) {
-          load_bf16x4_rows(p.aux0, p.ld_aux, row0, T.row_hi, n + 32, p.N, h1n);
-          if (EPI == EPI_SWIGLU_BWD) load_bf16x4_rows(p.aux1, p.ld_aux, row0, T.row_hi, n + 32, p.N, h3n);
-        }
-        if (more && EPI == EPI_SGD_F32_TAG)
-          load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, n + 32, p.N, wn);
-        float4 acc[8], acc3[8];
+        if (cc + CHUNK < c_end) load_side(n + CHUNK, fill);
+        float4 acc[4], acc3[4];
         stage_chunk(stg, lane, t_row + cc, acc);
         if (EPI == EPI_SWIGLU_UP) stage_chunk(stg, lane, t_row + 128 + cc, acc3);
         constexpr bool BIAS_EPI = EPI == EPI_STORE || EPI == EPI_ROWS_F32_TAG || EPI == EPI_ACT_FWD;
@@ -587,8 +601,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (add_bias) b4 = *reinterpret_cast<const float4*>(p.bias + (size_t)T.e * p.N + n);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int g = row0 + 4 * j;
+        for (int j = 0; j < 4; ++j) {
+          const int g = row0 + 8 * j;
           if (g >= T.row_hi || n >= p.N) continue;
           float x[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
           if (add_bias) {
@@ -608,7 +622,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             // dW stored as is; the update uses the same fused multiply-add and
             // round-to-nearest bf16 conversion as the stand-alone SGD kernel
             *reinterpret_cast<float4*>(static_cast<float*>(p.C) + wbase + o) = acc[j];
-            float w[4] = {wc[j].x, wc[j].y, wc[j].z, wc[j].w};
+            float w[4] = {use.w[j].x, use.w[j].y, use.w[j].z, use.w[j].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) w[i] = fmaf(-p.sgd_lr, x[i], w[i]);
             *reinterpret_cast<float4*>(p.sgd_w + wbase + o) = make_float4(w[0], w[1], w[2], w[3]);
@@ -621,15 +635,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(a);
           } else if (EPI == EPI_ACT_BWD) {
             float h[4], dh[4];
-            unpack4_bf16(h1c[j], h);
+            unpack4_bf16(use.h1[j], h);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_tanh_grad_f(h[i]);
             *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(dh);
           } else if (EPI == EPI_SWIGLU_BWD) {
             float h1[4], h3[4], d1[4], d3[4];
-            unpack4_bf16(h1c[j], h1);
-            unpack4_bf16(h3c[j], h3);
+            unpack4_bf16(use.h1[j], h1);
+            unpack4_bf16(use.h3[j], h3);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               d1[i] = x[i] * h3[i] * silu_grad_f(h1[i]);
@@ -647,14 +661,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(a);
           }
         }
-        if (more) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            h1c[j] = h1n[j];
-            h3c[j] = h3n[j];
-            wc[j] = wn[j];
-          }
-        }
+      };
+      // an even number of chunks per warp: 8 (64 for SwiGLU-up tiles: 4)
+#pragma unroll 1
+      for (int cc = c_begin; cc < c_end; cc += 2 * CHUNK) {
+        chunk(cc, sa, sb);
+        chunk(cc + CHUNK, sb, sa);
       }
       tc_fence_before();
       __syncwarp();
