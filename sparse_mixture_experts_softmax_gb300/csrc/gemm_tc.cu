@@ -401,10 +401,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 issues the operand loads.  At the start of a tile it also stages
-    // in L2 the rows that tile's epilogue will read about one tile's MMA
-    // time later (H / H1, H3 of the backward epilogues, the fp32 masters of
-    // the fused SGD).
+    // Lane 0 issues the operand loads and nothing else.
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
@@ -413,21 +410,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       bool ok = p.stall == 0;   // a stalled self-test issues nothing: the MMA waits run out
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile T = map_tile<FORM>(t, p, offs, tpre);
-        {
-          const int rhi = min(T.row_hi, T.m0 + BM);
-          const int ncols = min(BN, p.N - T.n0);
-          if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
-            for (int rr = T.m0; rr < rhi && ncols > 0; ++rr) {
-              const size_t o = (size_t)rr * p.ld_aux + T.n0;
-              prefetch_l2(p.aux0 + o, (uint32_t)ncols * 2u);
-              if (EPI == EPI_SWIGLU_BWD) prefetch_l2(p.aux1 + o, (uint32_t)ncols * 2u);
-            }
-          }
-          if (EPI == EPI_SGD_F32_TAG) {
-            for (int rr = T.m0; rr < rhi && ncols > 0; ++rr)
-              prefetch_l2(p.sgd_w + (size_t)T.e * p.sCe + (size_t)rr * p.ldc + T.n0, (uint32_t)ncols * 4u);
-          }
-        }
         for (int kb = 0; kb < T.nkb; ++kb) {
           if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full_mb[s]);
@@ -542,8 +524,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const int row = lane_base + lane;
     int buf = 0;
     uint32_t aph = 0;
+    const int et = (warp - 2) * 32 + lane;   // 0 .. 255 over the epilogue warps
+    // Side inputs (H / H1, H3 of the backward epilogues, the fp32 masters of
+    // the fused SGD) of the NEXT tile are staged in L2 while this tile's MMAs
+    // run: one bulk prefetch of one row segment per epilogue thread.
+    auto prefetch_side = [&](int tn) {
+      if (tn >= total) return;
+      const Tile N = map_tile<FORM>(tn, p, offs, tpre);
+      const int ncols = min(BN, p.N - N.n0);
+      const int rr = N.m0 + (et & (BM - 1));
+      if (ncols <= 0 || rr >= N.row_hi || N.nkb == 0) return;
+      if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
+        const bf16* src = (EPI == EPI_SWIGLU_BWD && et >= BM) ? p.aux1 : p.aux0;
+        if (EPI == EPI_SWIGLU_BWD || et < BM)
+          prefetch_l2(src + (size_t)rr * p.ld_aux + N.n0, (uint32_t)ncols * 2u);
+      }
+      if (EPI == EPI_SGD_F32_TAG && et < BM)
+        prefetch_l2(p.sgd_w + (size_t)N.e * p.sCe + (size_t)rr * p.ldc + N.n0, (uint32_t)ncols * 4u);
+    };
+    if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD || EPI == EPI_SGD_F32_TAG) prefetch_side(blockIdx.x);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
+      if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD || EPI == EPI_SGD_F32_TAG) prefetch_side(t + gridDim.x);
       const int r = T.m0 + row;
       const bool rok = r < T.row_hi;
       if (T.nkb == 0) {
