@@ -38,6 +38,27 @@ GB300_SMS = 152
 FFMA_PER_SM_PER_CLK = 128
 
 
+# DRAM bytes of the expert GEMM family per training step of the large layer,
+# from an ncu capture of the same per-expert shapes at 8 experts scaled by 16
+# (profiles/tc_gemm_large_e8_traffic.md).  Valid only for the GEMM source it
+# was taken from: reported as null once gemm_tc.cu changes.
+GEMM_TRAFFIC = {"bytes_per_step": 152.8e9, "workload": "large",
+                "gemm_source_sha256_prefix": "bcc7e6cc0f8be19b"}
+
+
+def gemm_traffic(wl: W.Workload):
+    import hashlib
+    src = os.path.join(ROOT, "sparse_mixture_experts_softmax_gb300", "csrc", "gemm_tc.cu")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if wl.name != GEMM_TRAFFIC["workload"] or not sha.startswith(GEMM_TRAFFIC["gemm_source_sha256_prefix"]):
+        return None
+    return GEMM_TRAFFIC["bytes_per_step"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -350,7 +371,8 @@ def main():
         peak = GB300_SMS * FFMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
         bound, unit = "alu", "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": gemm_traffic(wl),
+                "traffic_unit": "DRAM bytes per step of the GEMM family (ncu, scaled)",
                 "kernel": "grouped expert GEMMs (all launches of one step)",
                 "peak_source": f"{peaks['source']} ({'bf16_tflops_sustained' if lp else 'FFMA at max clock'})"}
     hb = hbm_bytes(wl)
