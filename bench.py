@@ -93,6 +93,9 @@ def hbm_bytes(wl: W.Workload) -> dict:
         "gather": T * D * es + R * D * es,                 # X once, Xe written
         "combine_loss": R * D * es + 2 * T * D * 4,       # Ye, target read; dY written
         "combine_bwd": T * D * 4 + 2 * R * D * es,        # dY, Ye read; dYe written
+        # training step (k <= 8): combine, MSE seed and combine backward in one
+        # pass: Ye and the target read, dYe written
+        "combine_fused": 2 * R * D * es + T * D * 4,
         # the stand-alone SGD launches: master and gradient read, master
         # written.  bf16 layers update the expert weights inside the dW GEMM
         # epilogues, so only the router weight and biases remain here.
@@ -378,7 +381,8 @@ def main():
     hb = hbm_bytes(wl)
     hbm = {}
     for name, key in (("gather", "gather"), ("combine_loss", "combine_loss"),
-                      ("combine_bwd", "combine_bwd")) + ((("sgd", "sgd"),) if not lp else ()):
+                      ("combine_bwd", "combine_bwd"), ("combine_fused", "combine_fused")) + \
+            ((("sgd", "sgd"),) if not lp else ()):
         if name in per_kernel and per_kernel[name] > 0:
             gbs = hb[key] / (per_kernel[name] / 1e3) / 1e9
             hbm[name] = {"ms": per_kernel[name], "GB/s": gbs, "frac": gbs / float(peaks["hbm_gbs"])}

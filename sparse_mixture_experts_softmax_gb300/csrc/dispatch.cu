@@ -123,7 +123,7 @@ gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, 
 
 // ------------------------------------------------------------------ combine --
 
-constexpr int CB_TOK = 32;   // tokens per block (4 per warp)
+constexpr int CB_TOK = 8;    // tokens per block (one per warp)
 
 // Y[t] = sum_j g_tj Ye[slot(t, j)] in j order (fp32).  With a target it also
 // forms dY = 2 (Y - target) / (T D) and a per-block sum of squared errors.
@@ -180,6 +180,98 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       for (int w = 0; w < 8; ++w) s += (double)wpart[w];
       sq_partial[blockIdx.x] = s;
     }
+  }
+}
+
+// Training-step combine with its backward fused (k <= 8): for each token,
+// with its k expert rows held in registers,
+//   Y[t]  = sum_j g_tj Ye[slot(t, j)]            (j order, as combine_kernel)
+//   dY[t] = 2 (Y[t] - target[t]) / (T D)          (MSE seed, never stored)
+//   dYe[slot(t, j)] = g_tj dY[t],  dg_tj = <dY[t], Ye[slot(t, j)]>
+// with the same arithmetic and order as combine_kernel followed by
+// combine_bwd_kernel, so dYe and dg are bit-identical to that pair; one pass
+// moves Ye and the target in and dYe out (dY never goes to HBM).  Two tokens
+// per warp and one squared-error partial per block of CB_TOK tokens (the
+// partial groups its warps' sums differently from combine_kernel, so the MSE
+// value may differ from that path in the last bits).
+// 128-thread blocks: with the k rows held in registers (~150 per thread), four
+// warps per block let three blocks share an SM.
+constexpr int CT_WARPS = 4;
+template <typename T>
+__global__ void __launch_bounds__(32 * CT_WARPS)
+combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
+                     const int* __restrict__ slot_of, int Tn, int D, int k,
+                     const float* __restrict__ target, float inv_n,
+                     double* __restrict__ sq_partial, T* __restrict__ dye,
+                     float* __restrict__ dgate) {
+  constexpr int VN = Vec<T>::N;
+  constexpr int MAXK = 8;
+  __shared__ float wpart[CT_WARPS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float sq = 0.f;
+  for (int tt = 0; tt < CB_TOK / CT_WARPS; ++tt) {
+    const int t = blockIdx.x * CB_TOK + warp * (CB_TOK / CT_WARPS) + tt;
+    if (t >= Tn) break;
+    int slot[MAXK];
+    float g[MAXK], dot[MAXK];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      slot[j] = (j < k) ? slot_of[(size_t)t * k + j] : 0;
+      g[j] = (j < k) ? gate[(size_t)t * k + j] : 0.f;
+      dot[j] = 0.f;
+    }
+    for (int d = lane * VN; d < D; d += 32 * VN) {
+      Vec<T> v[MAXK];
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j)
+        if (j < k) v[j].load(ye + (size_t)slot[j] * D + d);
+      float acc[VN];
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j)
+        if (j < k) {
+#pragma unroll
+          for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], v[j].get(i), acc[i]);
+        }
+      float dv[VN];
+#pragma unroll
+      for (int i = 0; i < VN; i += 4) {
+        const float4 tg = *reinterpret_cast<const float4*>(target + (size_t)t * D + d + i);
+        const float d0 = acc[i] - tg.x, d1 = acc[i + 1] - tg.y, d2 = acc[i + 2] - tg.z,
+                    d3 = acc[i + 3] - tg.w;
+        sq += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+        dv[i] = 2.f * d0 * inv_n;
+        dv[i + 1] = 2.f * d1 * inv_n;
+        dv[i + 2] = 2.f * d2 * inv_n;
+        dv[i + 3] = 2.f * d3 * inv_n;
+      }
+#pragma unroll
+      for (int j = 0; j < MAXK; ++j)
+        if (j < k) {
+          Vec<T> o;
+#pragma unroll
+          for (int i = 0; i < VN; ++i) {
+            dot[j] = fmaf(dv[i], v[j].get(i), dot[j]);
+            o.set(i, g[j] * dv[i]);
+          }
+          o.store(dye + (size_t)slot[j] * D + d);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j)
+      if (j < k) {
+        const float s2 = warp_sum(dot[j]);
+        if (lane == 0) dgate[(size_t)t * k + j] = s2;
+      }
+  }
+  sq = warp_sum(sq);
+  if (lane == 0) wpart[warp] = sq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int w = 0; w < CT_WARPS; ++w) s += (double)wpart[w];
+    sq_partial[blockIdx.x] = s;
   }
 }
 
@@ -417,6 +509,24 @@ cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const i
   else
     combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(ye), gate, slot_of, T, D,
                                                 k, y, target, dy, inv_n, sq_partial);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
+                                 int T, int D, int k, const float* target, double* sq_partial,
+                                 void* dye, float* dgate, cudaStream_t st) {
+  if (k > 8) return cudaErrorInvalidValue;
+  if (T == 0) return cudaSuccess;
+  const float inv_n = 1.0f / ((float)T * (float)D);
+  const int grid = combine_blocks(T);
+  if (dtype == 1)
+    combine_train_kernel<bf16><<<grid, 32 * CT_WARPS, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T,
+                                                     D, k, target, inv_n, sq_partial,
+                                                     static_cast<bf16*>(dye), dgate);
+  else
+    combine_train_kernel<float><<<grid, 32 * CT_WARPS, 0, st>>>(static_cast<const float*>(ye), gate, slot_of,
+                                                      T, D, k, target, inv_n, sq_partial,
+                                                      static_cast<float*>(dye), dgate);
   return cudaGetLastError();
 }
 

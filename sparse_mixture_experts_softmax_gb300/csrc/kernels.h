@@ -45,6 +45,10 @@ cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const i
 cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
                                    int n_ps, const int* counts, int T, int D, int E, int k,
                                    float alpha, float* d_loss, float* aux_row, cudaStream_t st);
+// Training-step combine + MSE seed + combine backward in one pass (k <= 8).
+cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
+                                 int T, int D, int k, const float* target, double* sq_partial,
+                                 void* dye, float* dgate, cudaStream_t st);
 cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
                                const int* slot_of, int T, int D, int k, void* dye, float* dgate,
                                cudaStream_t st);

@@ -308,9 +308,17 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   KL("gemm_down", run_gemm(c, d, st));
 
   const bool train = target != nullptr;
-  KL("combine_loss", launch_combine(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of), c.T,
-                    c.D, c.k, y, target, train ? P.at<float>(L.dy) : nullptr,
-                    train ? P.at<double>(L.sq) : nullptr, st));
+  if (train && y == nullptr && c.k <= 8) {
+    // training step: the combine backward runs in the same pass (dYe, dgate)
+    KL("combine_fused", launch_combine_train(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate),
+                                             P.at<int>(L.slot_of), c.T, c.D, c.k, target,
+                                             P.at<double>(L.sq), P.at<void>(L.dye),
+                                             P.at<float>(L.dgate), st));
+  } else {
+    KL("combine_loss", launch_combine(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of), c.T,
+                      c.D, c.k, y, target, train ? P.at<float>(L.dy) : nullptr,
+                      train ? P.at<double>(L.sq) : nullptr, st));
+  }
   if (train)
     KL("finalize_losses", launch_finalize_losses(P.at<double>(L.sq), combine_blocks(c.T), P.at<float>(L.psum),
                               router_fwd_blocks(c.T), P.at<int>(L.counts), c.T, c.D, c.E, c.k,
@@ -328,6 +336,7 @@ struct SgdFuse {
 };
 
 // Backward of L = L_task + alpha aux given dY (course Parts 4-6).
+// dy == nullptr: the forward's fused combine already wrote dYe and dgate.
 moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, const float* dy,
                         const moe_grads& gr, float* dx, bool aux_ready, const Ptrs& P,
                         cudaStream_t st, const SgdFuse* sgd = nullptr) {
@@ -338,8 +347,9 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
     KL("finalize_losses", launch_finalize_losses(P.at<double>(L.sq), 0, P.at<float>(L.psum), router_fwd_blocks(c.T),
                               P.at<int>(L.counts), c.T, c.D, c.E, c.k, c.aux_alpha, nullptr,
                               P.at<float>(L.aux_row), st));
-  KL("combine_bwd", launch_combine_bwd(c.dtype, dy, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of),
-                        c.T, c.D, c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st));
+  if (dy != nullptr)
+    KL("combine_bwd", launch_combine_bwd(c.dtype, dy, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of),
+                          c.T, c.D, c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st));
   // dA = dYe W2_e with the activation backward in the epilogue
   GemmArgs g = gemm_base(c, P);
   g.ragged_k = false;
@@ -642,7 +652,8 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   // bf16 layers: the expert weights' SGD runs inside the dW GEMM epilogues
   const bool fused = c.dtype == MOE_BF16;
   const SgdFuse sf{lr, p->w1, p->w3, p->w2, p->w1_lp, p->w3_lp, p->w2_lp};
-  RET_IF(run_backward(c, w, x, P.at<float>(L.dy), p->grads, dxp, true, P, st,
+  // k <= 8: the forward's combine pass already produced dYe and dgate
+  RET_IF(run_backward(c, w, x, c.k <= 8 ? nullptr : P.at<float>(L.dy), p->grads, dxp, true, P, st,
                       fused ? &sf : nullptr));
   // SGD on the fp32 masters; bf16 working copies rewritten from the result
   const long long E = c.E, D = c.D, F = c.F;
