@@ -16,7 +16,8 @@ order the course "Trainable MoE in CUDA" layers the method (Parts 1-7):
   gate weights.  The sigmoid, group-limited variant follows "AI Infra Kernel
   Lab", section "Project status" (grouped Top-K gate) and the notes under
   "DeepSeek whole-layer MoE forward": exact score ties go to the smaller group
-  or expert id.
+  or expert id; an optional correction bias changes which experts are chosen
+  but not the routing weights or their gradients.
 * Part 4, "Token Dispatch and Combine": per-expert counts, slot offsets,
   gather into per-expert buffers, scatter of gradients back, gate-weighted
   combine and its backward.
@@ -237,12 +238,26 @@ def router_scores(cfg: OracleConfig, logits: np.ndarray) -> np.ndarray:
     raise ValueError(cfg.score)
 
 
-def route(cfg: OracleConfig, scores: np.ndarray) -> np.ndarray:
-    """Top-k (or group-limited top-k) selection on the score tensor."""
+def selection_keys(scores: np.ndarray, corr_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """Keys the selection ranks: the scores, plus a per-expert correction bias
+    when one is given ("AI Infra Kernel Lab": the DeepSeek gate's correction
+    bias chooses experts only; the routing weights and their gradients come
+    from the unbiased scores).  The sum is taken in the dtype of ``scores``, so
+    float32 scores give the float32 keys a float32 kernel forms."""
+    if corr_bias is None:
+        return scores
+    return scores + np.asarray(corr_bias).astype(scores.dtype)[None, :]
+
+
+def route(cfg: OracleConfig, scores: np.ndarray,
+          corr_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """Top-k (or group-limited top-k) selection on the score tensor, or on
+    score + correction bias (group scores then come from the biased keys)."""
+    keys = selection_keys(scores, corr_bias)
     if cfg.n_groups > 1:
-        return select_grouped_topk(scores, cfg.k, cfg.n_groups, cfg.topk_groups,
+        return select_grouped_topk(keys, cfg.k, cfg.n_groups, cfg.topk_groups,
                                    cfg.group_score)
-    return select_topk(scores, cfg.k)
+    return select_topk(keys, cfg.k)
 
 
 # ---------------------------------------------------------------- Part 4 ---
@@ -405,8 +420,8 @@ def forward(cfg: OracleConfig, w: dict, x: np.ndarray,
     logits = router_logits(x, w["w_gate"], w.get("logit_bias"))
     scores = router_scores(cfg, logits)
     if idx is None:
-        idx = route(cfg, scores)
-    gate = renormalize(scores, idx)
+        idx = route(cfg, scores, w.get("corr_bias"))
+    gate = renormalize(scores, idx)      # unbiased scores, with or without a correction bias
     counts, offsets, src_tok, src_j, slot_of = dispatch(idx, cfg.E)
     xe = gather_rows(x, src_tok)
     R = xe.shape[0]

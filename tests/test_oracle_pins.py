@@ -461,3 +461,112 @@ def test_empty_expert_gets_exact_zero_grads():
     for e in (1, 2, 3):
         assert np.all(g["dw1"][e] == 0) and np.all(g["dw2"][e] == 0)
         assert np.all(g["db1"][e] == 0) and np.all(g["db2"][e] == 0)
+
+
+# -------------------------------------------------- correction-bias routing ---
+# "AI Infra Kernel Lab": the DeepSeek gate's correction bias chooses the experts
+# only; the routing weights (and their gradients) come from the unbiased scores.
+
+def test_corr_bias_zero_and_uniform_shift_change_nothing():
+    rng = np.random.default_rng(41)
+    s = rng.random((50, 12))
+    cfg = O.OracleConfig(T=50, D=1, F=1, E=12, k=3)
+    plain = O.route(cfg, s)
+    np.testing.assert_array_equal(O.route(cfg, s, np.zeros(12)), plain)
+    np.testing.assert_array_equal(O.route(cfg, s, np.full(12, 0.5)), plain)
+    cfg_g = O.OracleConfig(T=50, D=1, F=1, E=12, k=3, n_groups=4, topk_groups=2)
+    np.testing.assert_array_equal(O.route(cfg_g, s, np.full(12, 0.5)), O.route(cfg_g, s))
+
+
+def test_corr_bias_brute_force_keys_select_scores_weigh():
+    rng = np.random.default_rng(42)
+    E, k = 6, 2
+    cfg = O.OracleConfig(T=40, D=1, F=1, E=E, k=k)
+    s = rng.integers(1, 5, size=(40, E)).astype(np.float64) / 8.0     # ties in s
+    b = np.array([0.0, 0.25, -0.125, 0.125, 0.0, 0.375])              # ties in s + b
+    idx = O.route(cfg, s, b)
+    gate = O.renormalize(s, idx)
+    for t in range(40):
+        key = s[t] + b
+        assert set(idx[t].tolist()) == _brute_topk_set(key, k)
+        for a, c in zip(idx[t][:-1], idx[t][1:]):
+            assert _dominates(key[a], a, key[c], c)
+        sel = idx[t]
+        np.testing.assert_allclose(gate[t], s[t, sel] / s[t, sel].sum(), rtol=0, atol=1e-15)
+
+
+def test_corr_bias_forces_and_forbids_experts():
+    rng = np.random.default_rng(43)
+    s = rng.random((30, 8))
+    cfg = O.OracleConfig(T=30, D=1, F=1, E=8, k=2)
+    b = np.zeros(8)
+    b[5] = 10.0            # always chosen, first
+    b[2] = -10.0           # never chosen
+    idx = O.route(cfg, s, b)
+    assert np.all(idx[:, 0] == 5) and not np.any(idx == 2)
+    # the second choice is the best unbiased score among the rest
+    rest = [e for e in range(8) if e not in (2, 5)]
+    np.testing.assert_array_equal(idx[:, 1], np.array(rest)[np.argmax(s[:, rest], axis=1)])
+    g = O.renormalize(s, idx)
+    np.testing.assert_allclose(g[:, 0], s[:, 5] / (s[:, 5] + s[np.arange(30), idx[:, 1]]))
+
+
+def test_grouped_corr_bias_brute_force():
+    rng = np.random.default_rng(44)
+    E, G, kg, k = 8, 4, 2, 3
+    cfg = O.OracleConfig(T=60, D=1, F=1, E=E, k=k, n_groups=G, topk_groups=kg)
+    s = rng.integers(0, 4, size=(60, E)).astype(np.float64) / 4.0
+    b = np.array([0.0, 0.5, 0.25, -0.25, 0.0, 0.0, 0.75, -0.5])
+    idx = O.route(cfg, s, b)
+    for t in range(60):
+        key = s[t] + b
+        assert set(idx[t].tolist()) == _brute_grouped(key, k, G, kg, "top2_sum")
+
+
+def test_corr_bias_keys_summed_in_float32():
+    # 0.1f + 0.2f rounds to 0.3f in float32 (a tie: the smaller id wins), while
+    # in float64 it stays below 0.3f (expert 1 wins)
+    s32 = np.array([[0.1, 0.3]], dtype=np.float32)
+    b = np.array([0.2, 0.0], dtype=np.float32)
+    cfg = O.OracleConfig(T=1, D=1, F=1, E=2, k=1)
+    assert O.route(cfg, s32, b).tolist() == [[0]]
+    assert O.route(cfg, s32.astype(np.float64), b.astype(np.float64)).tolist() == [[1]]
+
+
+@pytest.mark.parametrize("case", [dict(act="relu", score="softmax", has_bias=True, aux_alpha=0.1),
+                                  dict(act="swiglu", score="sigmoid", has_bias=False, aux_alpha=0.05,
+                                       E=8, n_groups=4, topk_groups=2)])
+def test_corr_bias_gradients_central_differences(case):
+    """With a bias that changes the routing, the oracle's analytic gradients
+    still match central differences of its own loss (routing held by a margin
+    on the biased keys)."""
+    c = dict(T=8, D=4, F=6, E=4, k=2)
+    c.update(case)
+    cfg = O.OracleConfig(**c)
+    found = None
+    for seed in range(500, 900):
+        w, x, tgt = _weights(cfg, seed, scale=1.5)
+        w["corr_bias"] = np.random.default_rng(seed + 7).uniform(-0.3, 0.3, cfg.E)
+        st = O.forward(cfg, w, x)
+        keys = O.selection_keys(st["scores"], w["corr_bias"])
+        if not np.array_equal(st["idx"], O.route(cfg, st["scores"])) and \
+                np.min(np.abs(np.diff(np.sort(keys, axis=1), axis=1))) > 1e-3 and \
+                (cfg.n_groups == 1 or np.min(np.abs(np.diff(np.sort(
+                    O.group_scores(keys, cfg.n_groups), axis=1), axis=1))) > 1e-3) and \
+                all(np.min(np.abs(fe[kk])) > 1e-3 for fe in st["experts"] for kk in ("h", "h1")
+                    if kk in fe and fe[kk].size):
+            found = (w, x, tgt, st)
+            break
+    assert found is not None
+    w, x, tgt, st = found
+    _, _, dy = O.losses(cfg, st, tgt)
+    g = O.backward(cfg, w, x, st, dy)
+    h = 1e-6
+    for key in ("w_gate", "w1"):
+        fd = np.zeros_like(w[key])
+        for i in np.ndindex(w[key].shape):
+            wp = dict(w); wp[key] = w[key].copy(); wp[key][i] += h
+            wm = dict(w); wm[key] = w[key].copy(); wm[key][i] -= h
+            fd[i] = (O.total_loss(cfg, wp, x, tgt) - O.total_loss(cfg, wm, x, tgt)) / (2 * h)
+        err = np.max(np.abs(fd - g["d" + key])) / np.max(np.abs(fd))
+        assert err <= 1e-6, (key, err)
