@@ -98,6 +98,13 @@ typedef struct {
   const float* b2;          /* [E,D] fp32 or NULL                                  */
   const float* logit_bias;  /* [E] fixed, non-trainable bias added to the logits
                                before the score, or NULL; -INFINITY never routes  */
+  const float* corr_bias;   /* [E] selection-only correction bias, or NULL: the
+                               experts are chosen by score + corr_bias (fp32 sum;
+                               grouped routing ranks groups on these keys too),
+                               while the gates, the aux loss and every gradient
+                               use the unbiased scores ("AI Infra Kernel Lab",
+                               grouped Top-K gate with correction bias).  Not
+                               updated by the library.                            */
 } moe_weights;
 
 /* fp32 gradient buffers, overwritten (never accumulated into) by each call:
@@ -127,6 +134,8 @@ typedef struct {
   void* w3_lp;              /* [E,F,D] bf16 copy or NULL                 */
   void* w2_lp;              /* [E,D,F] bf16 copy or NULL                 */
   const float* logit_bias;  /* [E] or NULL                               */
+  const float* corr_bias;   /* [E] selection-only correction bias or NULL
+                               (as in moe_weights; never updated)         */
   moe_grads grads;          /* gradient buffers, written by the step     */
 } moe_params;
 

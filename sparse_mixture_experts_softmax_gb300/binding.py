@@ -41,7 +41,8 @@ class moe_config(ctypes.Structure):
 
 
 class moe_weights(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2", "logit_bias")]
+    _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2", "logit_bias",
+                                        "corr_bias")]
 
 
 class moe_grads(ctypes.Structure):
@@ -50,7 +51,7 @@ class moe_grads(ctypes.Structure):
 
 class moe_params(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2",
-                                        "w1_lp", "w3_lp", "w2_lp", "logit_bias")] + \
+                                        "w1_lp", "w3_lp", "w2_lp", "logit_bias", "corr_bias")] + \
                [("grads", moe_grads)]
 
 
@@ -140,9 +141,10 @@ def make_config(T, D, F, E, k, act="relu", score="softmax", n_groups=1, topk_gro
                       SCORE[score], DTYPE[dtype], int(bool(has_bias)), float(aux_alpha))
 
 
-def make_weights(w_gate, w1, w2, w3=None, b1=None, b2=None, logit_bias=None) -> moe_weights:
+def make_weights(w_gate, w1, w2, w3=None, b1=None, b2=None, logit_bias=None,
+                 corr_bias=None) -> moe_weights:
     return moe_weights(_ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(b1), _ptr(b2),
-                       _ptr(logit_bias))
+                       _ptr(logit_bias), _ptr(corr_bias))
 
 
 def make_grads(dw_gate, dw1, dw2, dw3=None, db1=None, db2=None) -> moe_grads:
@@ -150,9 +152,10 @@ def make_grads(dw_gate, dw1, dw2, dw3=None, db1=None, db2=None) -> moe_grads:
 
 
 def make_params(w_gate, w1, w2, grads: moe_grads, w3=None, b1=None, b2=None, w1_lp=None,
-                w3_lp=None, w2_lp=None, logit_bias=None) -> moe_params:
+                w3_lp=None, w2_lp=None, logit_bias=None, corr_bias=None) -> moe_params:
     return moe_params(_ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(b1), _ptr(b2),
-                      _ptr(w1_lp), _ptr(w3_lp), _ptr(w2_lp), _ptr(logit_bias), grads)
+                      _ptr(w1_lp), _ptr(w3_lp), _ptr(w2_lp), _ptr(logit_bias), _ptr(corr_bias),
+                      grads)
 
 
 def moe_workspace_size(cfg: moe_config) -> int:

@@ -11,6 +11,7 @@ struct RouterArgs {
   int T, D, E, k;
   int score;         // 0 softmax, 1 sigmoid
   int n_groups, topk_groups, group_score;
+  const float* corr_bias;   // [E] selection-only correction bias, or nullptr
 };
 
 // ---- router (router.cu)

@@ -175,12 +175,14 @@ struct ExpertW {
   const float* b1;
   const float* b2;
   const float* logit_bias;
+  const float* corr_bias;   // selection-only correction bias [E] or nullptr
 };
 
-RouterArgs router_args(const moe_config& c) {
+RouterArgs router_args(const moe_config& c, const float* corr_bias = nullptr) {
   RouterArgs a;
   a.T = c.T; a.D = c.D; a.E = c.E; a.k = c.k; a.score = c.score;
   a.n_groups = c.n_groups; a.topk_groups = c.topk_groups; a.group_score = c.group_score;
+  a.corr_bias = corr_bias;
   return a;
 }
 
@@ -207,7 +209,7 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
                        const float* target, float* d_loss, const Ptrs& P, cudaStream_t st) {
   const Layout& L = *P.L;
   const long long R = (long long)c.T * c.k;
-  const RouterArgs ra = router_args(c);
+  const RouterArgs ra = router_args(c, w.corr_bias);
   CK(cudaMemsetAsync(P.at<void>(L.status), 0, 16, st));
   if (c.dtype == MOE_BF16) {
     // logits = x W_g^T (+ logit bias) on the tensor cores, then selection
@@ -579,7 +581,7 @@ moe_status check_weights(const moe_config& c, const ExpertW& w) {
   if (!w.w_gate || !w.w1 || !w.w2) return MOE_ERR_INVALID_ARG;
   if (c.act == MOE_ACT_SWIGLU && !w.w3) return MOE_ERR_INVALID_ARG;
   if (c.has_bias && (!w.b1 || !w.b2)) return MOE_ERR_INVALID_ARG;
-  const void* ps[] = {w.w_gate, w.w1, w.w3, w.w2, w.b1, w.b2, w.logit_bias};
+  const void* ps[] = {w.w_gate, w.w1, w.w3, w.w2, w.b1, w.b2, w.logit_bias, w.corr_bias};
   for (const void* p : ps)
     if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
   return MOE_OK;
@@ -626,7 +628,7 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
     return MOE_ERR_INVALID_ARG;
   RET_IF(check_grads(c, p->grads));
   const void* ps[] = {p->w_gate, p->w1, p->w3, p->w2, p->b1, p->b2, p->w1_lp, p->w3_lp, p->w2_lp,
-                      p->logit_bias, x, y_target, d_loss, dx};
+                      p->logit_bias, p->corr_bias, x, y_target, d_loss, dx};
   for (const void* q : ps)
     if (q && !aligned16(q)) return MOE_ERR_ALIGNMENT;
   if (c.T > 0 && (!x || !y_target)) return MOE_ERR_INVALID_ARG;
@@ -647,6 +649,7 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   w.b1 = p->b1;
   w.b2 = p->b2;
   w.logit_bias = p->logit_bias;
+  w.corr_bias = p->corr_bias;
   RET_IF(run_forward(c, w, x, nullptr, y_target, d_loss, P, st));
   float* dxp = dx ? dx : P.at<float>(L.dx);
   // bf16 layers: the expert weights' SGD runs inside the dW GEMM epilogues
@@ -686,7 +689,7 @@ moe_status moe_forward(const moe_config* cfg, const moe_weights* w, const void* 
   RET_IF(validate_config(cfg));
   const moe_config& c = *cfg;
   if (w == nullptr) return MOE_ERR_INVALID_ARG;
-  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias};
+  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias, w->corr_bias};
   RET_IF(check_weights(c, ew));
   RET_IF(check_ws(c, workspace, workspace_bytes));
   if (c.T > 0 && (!x || !y)) return MOE_ERR_INVALID_ARG;
@@ -705,7 +708,7 @@ moe_status moe_backward(const moe_config* cfg, const moe_weights* w, const void*
   RET_IF(validate_config(cfg));
   const moe_config& c = *cfg;
   if (w == nullptr || g == nullptr) return MOE_ERR_INVALID_ARG;
-  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias};
+  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias, w->corr_bias};
   RET_IF(check_weights(c, ew));
   RET_IF(check_grads(c, *g));
   RET_IF(check_ws(c, workspace, workspace_bytes));

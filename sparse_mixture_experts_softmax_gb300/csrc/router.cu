@@ -34,6 +34,28 @@ __device__ __forceinline__ bool better(float v, int id, float v2, int id2) {
   return v > v2 || (v == v2 && id < id2);
 }
 
+// Selection keys: the scores, plus the correction bias when there is one
+// ("AI Infra Kernel Lab": the bias chooses experts only; gates and their
+// gradients use the unbiased scores).  Without a bias the keys are the scores.
+template <int NC>
+__device__ __forceinline__ void selection_keys(const float (&s)[NC], const float* cb, int lane,
+                                               int E, float (&key)[NC]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int e = lane + 32 * c;
+    key[c] = (cb != nullptr && e < E) ? s[c] + cb[e] : s[c];
+  }
+}
+// v[c] held by lane (id % 32) for id = lane + 32 c, broadcast to the warp.
+template <int NC>
+__device__ __forceinline__ float lane_value(const float (&v)[NC], int lane, int id) {
+  float mine = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c)
+    if (lane + 32 * c == id) mine = v[c];
+  return __shfl_sync(0xffffffffu, mine, id & 31);
+}
+
 __device__ __forceinline__ Cand warp_best(Cand c) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -147,12 +169,14 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
         s[c] = (e < E) ? sigmoidf_(ls[tk][e]) : 0.f;
       }
     }
+    float key[NC];
+    selection_keys(s, a.corr_bias, lane, E, key);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       int e = lane + 32 * c;
       if (e < E) {
         scores[(size_t)t * E + e] = s[c];
-        ls[tk][e] = s[c];   // the warp's own row now holds the scores
+        ls[tk][e] = key[c];   // the warp's own row now holds the selection keys
         colsum[c] += s[c];
       }
     }
@@ -202,7 +226,7 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         int e = lane + 32 * c;
-        if (allowed[c] && better(s[c], e, best.v, best.id)) { best.v = s[c]; best.id = e; }
+        if (allowed[c] && better(key[c], e, best.v, best.id)) { best.v = key[c]; best.id = e; }
       }
       best = warp_best(best);
       if (best.id >= E) {
@@ -214,17 +238,13 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
         best.id = (cand < E) ? cand : 0;
-        best.v = __shfl_sync(0xffffffffu, s[0], 0);
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (lane + 32 * c == best.id) best.v = s[c];
-        best.v = __shfl_sync(0xffffffffu, best.v, best.id & 31);
       }
+      const float sv = lane_value(s, lane, best.id);   // unbiased score of the pick
 #pragma unroll
       for (int c = 0; c < NC; ++c)
         if (lane + 32 * c == best.id) allowed[c] = false;
-      if (lane == j) { selv = best.v; selid = best.id; }
-      ssum += best.v;   // j order, identical on every lane
+      if (lane == j) { selv = sv; selid = best.id; }
+      ssum += sv;   // j order, identical on every lane
     }
     if (lane < a.k) {
       idx[(size_t)t * a.k + lane] = selid;
@@ -295,12 +315,14 @@ router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __re
         s[c] = (e < E) ? sigmoidf_(logits[(size_t)t * E + e]) : 0.f;
       }
     }
+    float key[NC];
+    selection_keys(s, a.corr_bias, lane, E, key);
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       int e = lane + 32 * c;
       if (e < E) {
         scores[(size_t)t * E + e] = s[c];
-        rows[warp][e] = s[c];
+        rows[warp][e] = key[c];
         colsum[c] += s[c];
       }
     }
@@ -346,7 +368,7 @@ router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __re
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         int e = lane + 32 * c;
-        if (allowed[c] && better(s[c], e, best.v, best.id)) { best.v = s[c]; best.id = e; }
+        if (allowed[c] && better(key[c], e, best.v, best.id)) { best.v = key[c]; best.id = e; }
       }
       best = warp_best(best);
       if (best.id >= E) {
@@ -357,13 +379,13 @@ router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __re
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
         best.id = (cand < E) ? cand : 0;
-        best.v = rows[warp][best.id];
       }
+      const float sv = lane_value(s, lane, best.id);   // unbiased score of the pick
 #pragma unroll
       for (int c = 0; c < NC; ++c)
         if (lane + 32 * c == best.id) allowed[c] = false;
-      if (lane == j) { selv = best.v; selid = best.id; }
-      ssum += best.v;
+      if (lane == j) { selv = sv; selid = best.id; }
+      ssum += sv;
     }
     if (lane < a.k) {
       idx[(size_t)t * a.k + lane] = selid;

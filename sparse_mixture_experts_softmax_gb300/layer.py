@@ -17,7 +17,8 @@ from . import binding as B
 class MoELayer:
     def __init__(self, T, D, F, E, k, act, score, dtype, has_bias, aux_alpha, w_gate, w1, w2,
                  w3=None, b1=None, b2=None, logit_bias=None, n_groups=1, topk_groups=1,
-                 group_score="top2_sum", w1_lp=None, w3_lp=None, w2_lp=None, device="cuda"):
+                 group_score="top2_sum", w1_lp=None, w3_lp=None, w2_lp=None, device="cuda",
+                 corr_bias=None):
         self.device = torch.device(device)
         self.dtype = dtype
         self.cfg = B.make_config(T, D, F, E, k, act=act, score=score, n_groups=n_groups,
@@ -30,6 +31,7 @@ class MoELayer:
 
         self.w_gate, self.w1, self.w2, self.w3 = f32(w_gate), f32(w1), f32(w2), f32(w3)
         self.b1, self.b2, self.logit_bias = f32(b1), f32(b2), f32(logit_bias)
+        self.corr_bias = f32(corr_bias)   # selection-only routing bias (never trained)
         if dtype == "bf16":
             def lp(given, master):
                 if master is None:
@@ -54,12 +56,12 @@ class MoELayer:
         lp = self.dtype == "bf16"
         return B.make_weights(self.w_gate, self.w1_lp if lp else self.w1,
                               self.w2_lp if lp else self.w2, self.w3_lp if lp else self.w3,
-                              self.b1, self.b2, self.logit_bias)
+                              self.b1, self.b2, self.logit_bias, self.corr_bias)
 
     def params(self) -> B.moe_params:
         return B.make_params(self.w_gate, self.w1, self.w2, self.grads, w3=self.w3, b1=self.b1,
                              b2=self.b2, w1_lp=self.w1_lp, w3_lp=self.w3_lp, w2_lp=self.w2_lp,
-                             logit_bias=self.logit_bias)
+                             logit_bias=self.logit_bias, corr_bias=self.corr_bias)
 
     def forward(self, x: torch.Tensor, y: Optional[torch.Tensor] = None) -> torch.Tensor:
         if y is None:

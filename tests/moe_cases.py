@@ -41,7 +41,8 @@ def oracle_inputs(wl: W.Workload, inp: dict):
                  w1=np64(inp["w1_bf16"] if lp else inp["w1"]),
                  w2=np64(inp["w2_bf16"] if lp else inp["w2"]),
                  w3=np64(inp["w3_bf16"] if lp else inp["w3"]) if inp["w3"] is not None else None,
-                 b1=np64(inp["b1"]), b2=np64(inp["b2"]), logit_bias=np64(inp["logit_bias"]))
+                 b1=np64(inp["b1"]), b2=np64(inp["b2"]), logit_bias=np64(inp["logit_bias"]),
+                 corr_bias=np64(inp.get("corr_bias")))
     master = dict(w_gate=np64(inp["w_gate"]), w1=np64(inp["w1"]), w2=np64(inp["w2"]),
                   w3=np64(inp["w3"]), b1=np64(inp["b1"]), b2=np64(inp["b2"]))
     x = np64(inp["x_bf16"] if lp else inp["x"])
@@ -57,7 +58,8 @@ def make_layer(wl: W.Workload, inp: dict, device="cuda", group_score="top2_sum")
                     n_groups=wl.n_groups, topk_groups=wl.topk_groups, group_score=group_score,
                     w1_lp=inp.get("w1_bf16") if lp else None,
                     w3_lp=inp.get("w3_bf16") if lp else None,
-                    w2_lp=inp.get("w2_bf16") if lp else None, device=device)
+                    w2_lp=inp.get("w2_bf16") if lp else None, device=device,
+                    corr_bias=inp.get("corr_bias"))
 
 
 def device_x(wl: W.Workload, inp: dict, device="cuda"):
@@ -81,12 +83,14 @@ def assert_close(name, got, want, tol):
     return err
 
 
-def check_routing_exact(cfg: O.OracleConfig, r: dict):
+def check_routing_exact(cfg: O.OracleConfig, r: dict, corr_bias=None):
     """Given the GPU's own fp32 scores, the oracle's selection and dispatch must
-    reproduce idx, counts, offsets and both slot maps bit for bit."""
+    reproduce idx, counts, offsets and both slot maps bit for bit.  A
+    correction bias enters the keys as float32, the kernel's precision."""
     scores = r["scores"].cpu().numpy()            # float32, the kernel's precision
     idx_gpu = r["idx"].cpu().numpy()
-    idx_o = O.route(cfg, scores)
+    cb = None if corr_bias is None else corr_bias.detach().float().cpu().numpy()
+    idx_o = O.route(cfg, scores, cb)
     np.testing.assert_array_equal(idx_gpu, idx_o)
     counts, offsets, src_tok, _, slot_of = O.dispatch(idx_gpu, cfg.E)
     np.testing.assert_array_equal(r["counts"].cpu().numpy(), counts)
@@ -100,17 +104,19 @@ def check_routing_exact(cfg: O.OracleConfig, r: dict):
 
 
 def validated_routing(cfg: O.OracleConfig, scores64: np.ndarray, idx_gpu: np.ndarray,
-                      margin_tol: float = 1e-5) -> np.ndarray:
+                      margin_tol: float = 1e-5, corr_bias=None) -> np.ndarray:
     """Routing for the oracle's float values: its own fp64 selection, except on
-    tokens where fp64 and the GPU's fp32 disagree AND the fp64 scores of the two
-    choices lie within ``margin_tol`` of each other (a near-tie that rounding may
-    legitimately flip).  Any other disagreement fails."""
-    idx_o = O.route(cfg, scores64)
+    tokens where fp64 and the GPU's fp32 disagree AND the fp64 selection keys
+    (scores, plus the correction bias if any) of the two choices lie within
+    ``margin_tol`` of each other (a near-tie that rounding may legitimately
+    flip).  Any other disagreement fails."""
+    idx_o = O.route(cfg, scores64, corr_bias)
+    keys = O.selection_keys(scores64, corr_bias)
     bad = np.nonzero(np.any(idx_o != idx_gpu, axis=1))[0]
     for t in bad:
-        a = np.sort(scores64[t, idx_o[t]])
-        b = np.sort(scores64[t, idx_gpu[t]])
-        assert np.max(np.abs(a - b)) <= margin_tol * max(1.0, np.max(np.abs(scores64[t]))), \
+        a = np.sort(keys[t, idx_o[t]])
+        b = np.sort(keys[t, idx_gpu[t]])
+        assert np.max(np.abs(a - b)) <= margin_tol * max(1.0, np.max(np.abs(keys[t]))), \
             f"token {t}: GPU routing {idx_gpu[t]} vs oracle {idx_o[t]} is not a near-tie"
     out = idx_o.copy()
     out[bad] = idx_gpu[bad]

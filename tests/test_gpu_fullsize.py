@@ -43,6 +43,7 @@ class LazyExperts:
 
 def _oracle_weights(inp, lb):
     return dict(w_gate=np64(inp["w_gate"].to(torch.bfloat16)), w1=LazyExperts(inp["w1_bf16"]),
+                corr_bias=np64(inp.get("corr_bias")),
                 w2=LazyExperts(inp["w2_bf16"]),
                 w3=LazyExperts(inp["w3_bf16"]) if inp["w3_bf16"] is not None else None,
                 b1=None, b2=None, logit_bias=lb)
@@ -91,12 +92,13 @@ def _run_full(name):
     return wl, inp, cfg, layer, y, dx, r
 
 
-@pytest.mark.parametrize("name,n_sample", [("grouped", 8), ("skewed", 6), ("large", 4)])
+@pytest.mark.parametrize("name,n_sample", [("grouped", 8), ("skewed", 6), ("large", 4),
+                                           ("grouped_cb", 8)])
 def test_full_size_layer(name, n_sample):
     wl, inp, cfg, layer, y, dx, r = _run_full(name)
     T, D, E, k = wl.T, wl.D, wl.E, wl.k
     # 1. routing over all tokens, bit-exact given the GPU's scores
-    check_routing_exact(cfg, r)
+    check_routing_exact(cfg, r, inp.get("corr_bias"))
     idx = r["idx"].cpu().numpy()
     counts = r["counts"].cpu().numpy().astype(np.int64)
     offsets = r["offsets"].cpu().numpy()
@@ -116,7 +118,8 @@ def test_full_size_layer(name, n_sample):
     assert_close("mse", loss[0], mse_of_y, 1e-4)
     # 4. sampled tokens: y and dX
     tokens = W.sample_tokens(T, n_sample).tolist()
-    idx_v = validated_routing(cfg, scores64[tokens], idx[tokens])
+    cb64 = np64(inp.get("corr_bias"))
+    idx_v = validated_routing(cfg, scores64[tokens], idx[tokens], corr_bias=cb64)
     idx_s = idx.copy()
     idx_s[tokens] = idx_v
     ys, fw, gate = _tokens_y(cfg, w, x64, scores64, idx_s, tokens)
@@ -155,7 +158,7 @@ def test_full_size_layer(name, n_sample):
           f"{'checked' if checked_dw else 'skipped (too costly for the oracle)'}")
     if checked_dw:
         rows_tok = src_tok[offsets[e_min]:offsets[e_min + 1]].tolist()
-        idx_v = validated_routing(cfg, scores64[rows_tok], idx[rows_tok])
+        idx_v = validated_routing(cfg, scores64[rows_tok], idx[rows_tok], corr_bias=cb64)
         idx_m = idx.copy()
         idx_m[rows_tok] = idx_v
         ys_m, fw_m, gate_m = _tokens_y(cfg, w, x64, scores64, idx_m, rows_tok)

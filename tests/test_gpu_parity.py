@@ -39,11 +39,12 @@ def _one_step_parity(wl, seed=0, check_dx=True):
     layer.train_step(x, tgt, wl.lr, dx=dx)
     torch.cuda.synchronize()
     r = layer.routing()
-    check_routing_exact(cfg, r)
+    check_routing_exact(cfg, r, inp.get("corr_bias"))
 
     w_fwd, master, x64, t64 = oracle_inputs(wl, inp)
     st0 = O.forward(cfg, w_fwd, x64)
-    idx = validated_routing(cfg, st0["scores"], r["idx"].cpu().numpy())
+    idx = validated_routing(cfg, st0["scores"], r["idx"].cpu().numpy(),
+                            corr_bias=w_fwd.get("corr_bias"))
     st = O.forward(cfg, w_fwd, x64, idx)
     l_mse, aux, dy = O.losses(cfg, st, t64)
     g = O.backward(cfg, w_fwd, x64, st, dy)
@@ -128,6 +129,35 @@ def test_dense_f32_step():
 def test_dense_bf16_step():
     errs, _, _ = _one_step_parity(W.WORKLOADS["dense_bf16"])
     assert max(errs.values()) <= 2e-2
+
+
+def test_correction_bias_f32_step():
+    """fp32 fused router with a selection-only correction bias: the bias moves
+    routing decisions (checked), gates and all gradients from unbiased scores."""
+    wl = W.WORKLOADS["dense_f32_cb"]
+    errs, layer, inp = _one_step_parity(wl)
+    assert max(errs.values()) <= 1e-4
+    _assert_bias_changes_routing(wl, inp, layer)
+
+
+def test_correction_bias_grouped_bf16_step():
+    """Grouped sigmoid routing with a correction bias on the tensor-core router
+    (group scores from the biased keys), at the layer's full width, 2048 tokens."""
+    wl = W.WORKLOADS["grouped_cb"].with_tokens(2048)
+    errs, layer, inp = _one_step_parity(wl, check_dx=True)
+    assert max(errs.values()) <= 2e-2
+    _assert_bias_changes_routing(wl, inp, layer)
+
+
+def _assert_bias_changes_routing(wl, inp, layer):
+    """The bias must matter for this input: the oracle's routing of the GPU's
+    scores without the bias differs on a good share of tokens."""
+    cfg = oracle_config(wl)
+    r = layer.routing()
+    scores = r["scores"].cpu().numpy()
+    plain = O.route(cfg, scores)
+    changed = np.mean(np.any(plain != r["idx"].cpu().numpy(), axis=1))
+    assert changed > 0.05, changed
 
 
 @pytest.mark.parametrize("name,T", [("grouped", 2048), ("skewed", 768), ("large", 256)])

@@ -57,6 +57,7 @@ class Workload:
     router_init: str = "normal"      # "normal" -> N(0,1/D); "uniform" -> U(-1/sqrt(D), 1/sqrt(D))
     zipf_skew: Optional[float] = None  # Zipf exponent of the fixed logit bias
     zipf_empty: int = 0                # experts that get a -inf logit bias (never selected)
+    corr_bias_scale: Optional[float] = None  # selection-only correction bias ~ U(-s, s)
 
     @property
     def R(self) -> int:
@@ -86,6 +87,13 @@ WORKLOADS = {
     "large": Workload("large", T=65536, D=4096, F=2048, E=128, k=8, act="swiglu",
                       score="softmax", n_groups=1, topk_groups=1, has_bias=False,
                       dtype="bf16", aux_alpha=0.01, lr=1e-3, router_init="uniform"),
+    # correction-bias routing (selection on score + bias, gates from the scores)
+    "grouped_cb": Workload("grouped_cb", T=16384, D=1024, F=704, E=64, k=6, act="swiglu",
+                           score="sigmoid", n_groups=8, topk_groups=4, has_bias=False,
+                           dtype="bf16", aux_alpha=0.0, lr=1e-3, corr_bias_scale=0.1),
+    "dense_f32_cb": Workload("dense_f32_cb", T=4096, D=512, F=1024, E=8, k=2, act="gelu_tanh",
+                             score="softmax", n_groups=1, topk_groups=1, has_bias=True,
+                             dtype="f32", aux_alpha=0.01, lr=0.01, corr_bias_scale=0.05),
 }
 
 
@@ -117,13 +125,24 @@ def zipf_logit_bias(wl: Workload, seed: int = 0) -> Optional[torch.Tensor]:
     return bias
 
 
+def correction_bias(wl: Workload, seed: int = 0) -> Optional[torch.Tensor]:
+    """Per-expert selection-only routing bias ~ U(-s, s), from its own seeded
+    generator (so the other draws do not move), or None."""
+    if wl.corr_bias_scale is None:
+        return None
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 2)
+    return (torch.rand(wl.E, generator=g) * 2.0 - 1.0) * wl.corr_bias_scale
+
+
 def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
                 with_target: bool = True) -> dict:
     """Draw one seeded workload.  Returns fp32 tensors plus bf16 copies.
 
     Keys: ``w_gate [E,D]``, ``w1 [E,F,D]``, ``w3 [E,F,D]`` (SwiGLU only, else
     None), ``w2 [E,D,F]``, ``b1 [E,F]`` / ``b2 [E,D]`` (zeros, or None without
-    bias), ``logit_bias [E]`` or None, ``x [T,D]`` fp32 draws, ``target [T,D]``.
+    bias), ``logit_bias [E]`` or None, ``corr_bias [E]`` or None, ``x [T,D]`` fp32
+    draws, ``target [T,D]``.
     For bf16 workloads ``x_bf16``, ``w1_bf16``, ``w3_bf16``, ``w2_bf16`` are the
     round-to-nearest-even casts; the fp32 expert weights are the master copy.
     """
@@ -149,6 +168,8 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
         out["target"] = x @ a_teacher + eps
     lb = zipf_logit_bias(wl, seed)
     out["logit_bias"] = lb.to(device) if lb is not None else None
+    cb = correction_bias(wl, seed)
+    out["corr_bias"] = cb.to(device) if cb is not None else None
     if wl.dtype == "bf16":
         out["x_bf16"] = x.to(torch.bfloat16)
         out["w1_bf16"] = w1.to(torch.bfloat16)
