@@ -29,6 +29,9 @@ order the course "Trainable MoE in CUDA" layers the method (Parts 1-7):
   probabilities, the aux loss and its gradient to router probabilities.
 * Part 7, "Loss, Optimizer, and Training Loop": MSE, zero-grad, SGD, and the
   forward / backward / one-step orchestration.
+* Shared experts ("AI Infra Kernel Lab", notes on the distributed validator):
+  one SwiGLU branch of hidden width n_shared x F that every token passes
+  through, added to the routed output without a gate.
 
 The pages lost their typeset formulas, so each step is the textbook
 definition; every reading taken where the pages are silent is marked READING
@@ -383,6 +386,28 @@ def expert_backward(cfg: OracleConfig, e: int, xe: np.ndarray, fwd: dict,
     return out
 
 
+def shared_forward(x: np.ndarray, w: dict) -> dict:
+    """Shared experts: one SwiGLU MLP that every token passes through, added to
+    the routed output without a gate ("AI Infra Kernel Lab": the replicated
+    shared branch is one SwiGLU whose hidden width is n_shared times the
+    expert hidden width).  H1 = x Ws1^T, H3 = x Ws3^T, A = SiLU(H1) * H3,
+    Ys = A Ws2^T."""
+    h1 = x @ w["ws1"].T
+    h3 = x @ w["ws3"].T
+    a = silu(h1) * h3
+    return dict(h1=h1, h3=h3, a=a, ys=a @ w["ws2"].T)
+
+
+def shared_backward(x: np.ndarray, fwd: dict, dy: np.ndarray, w: dict) -> dict:
+    """The shared branch receives the whole dY: dWs2 = dY^T A, dA = dY Ws2,
+    the SwiGLU backward, dWs1 = dH1^T x, dWs3 = dH3^T x, and its dX term."""
+    da = dy @ w["ws2"]
+    dh1 = da * fwd["h3"] * silu_derivative(fwd["h1"])
+    dh3 = da * silu(fwd["h1"])
+    return dict(dws1=dh1.T @ x, dws3=dh3.T @ x, dws2=dy.T @ fwd["a"],
+                dx=dh1 @ w["ws1"] + dh3 @ w["ws3"])
+
+
 # ---------------------------------------------------------------- Part 6 ---
 
 def aux_loss(counts: np.ndarray, scores: np.ndarray, k: int):
@@ -433,9 +458,13 @@ def forward(cfg: OracleConfig, w: dict, x: np.ndarray,
         ye[lo:hi] = fe["ye"]
         experts.append(fe)
     y = combine(ye, gate, slot_of)
+    shared = None
+    if w.get("ws1") is not None:
+        shared = shared_forward(x, w)
+        y = y + shared["ys"]
     return dict(logits=logits, scores=scores, idx=idx, gate=gate, counts=counts,
                 offsets=offsets, src_tok=src_tok, src_j=src_j, slot_of=slot_of,
-                xe=xe, ye=ye, experts=experts, y=y)
+                xe=xe, ye=ye, experts=experts, y=y, shared=shared)
 
 
 def backward(cfg: OracleConfig, w: dict, x: np.ndarray, st: dict,
@@ -457,6 +486,10 @@ def backward(cfg: OracleConfig, w: dict, x: np.ndarray, st: dict,
         for key in ("dw1", "dw2", "db1", "db2") + (("dw3",) if cfg.act == "swiglu" else ()):
             g[key][e] = be[key]
     dx = scatter_back(dxe, st["slot_of"])
+    if st.get("shared") is not None:
+        sb = shared_backward(x, st["shared"], dy, w)
+        dx = dx + sb["dx"]
+        g.update(dws1=sb["dws1"], dws3=sb["dws3"], dws2=sb["dws2"])
     # router: renormalisation backward, aux gradient, score backward
     ds = renormalize_backward(st["scores"], st["idx"], st["gate"], dgate)
     if cfg.aux_alpha != 0.0:
@@ -490,7 +523,7 @@ def total_loss(cfg: OracleConfig, w: dict, x: np.ndarray, target: np.ndarray,
     return l_mse + cfg.aux_alpha * aux
 
 
-PARAM_KEYS = ("w_gate", "w1", "w3", "w2", "b1", "b2")
+PARAM_KEYS = ("w_gate", "w1", "w3", "w2", "b1", "b2", "ws1", "ws3", "ws2")
 
 
 def sgd(w: dict, grads: dict, lr: float) -> dict:

@@ -570,3 +570,96 @@ def test_corr_bias_gradients_central_differences(case):
             fd[i] = (O.total_loss(cfg, wp, x, tgt) - O.total_loss(cfg, wm, x, tgt)) / (2 * h)
         err = np.max(np.abs(fd - g["d" + key])) / np.max(np.abs(fd))
         assert err <= 1e-6, (key, err)
+
+
+# ----------------------------------------------------------- shared experts ---
+# "AI Infra Kernel Lab": the shared branch is one SwiGLU of hidden width
+# n_shared x F that every token passes through, added without a gate.
+
+def _shared_case(seed, n_shared=2, case=None):
+    c = dict(T=8, D=4, F=6, E=4, k=2, act="swiglu", score="softmax", has_bias=False,
+             aux_alpha=0.01)
+    if case:
+        c.update(case)
+    cfg = O.OracleConfig(**c)
+    for s in range(seed, seed + 400):
+        w, x, tgt = _weights(cfg, s, scale=1.5)
+        if not _margin_ok(cfg, w, x):
+            continue
+        rng = np.random.default_rng(s + 1000)
+        Fs = n_shared * cfg.F
+        w["ws1"] = rng.normal(size=(Fs, cfg.D)) / math.sqrt(cfg.D)
+        w["ws3"] = rng.normal(size=(Fs, cfg.D)) / math.sqrt(cfg.D)
+        w["ws2"] = rng.normal(size=(cfg.D, Fs)) / math.sqrt(Fs)
+        h1 = x @ w["ws1"].T
+        if np.min(np.abs(h1)) > 1e-3:
+            return cfg, w, x, tgt
+    raise RuntimeError("no input found")
+
+
+def test_shared_branch_vs_dense_autograd():
+    cfg, w, x, tgt = _shared_case(700)
+    st = O.forward(cfg, w, x)
+    _, _, dy = O.losses(cfg, st, tgt)
+    g = O.backward(cfg, w, x, st, dy)
+    tw = {k_: torch.from_numpy(v.copy()).requires_grad_(True)
+          for k_, v in w.items() if isinstance(v, np.ndarray)}
+    xt = torch.from_numpy(x.copy()).requires_grad_(True)
+    mask = torch.zeros(cfg.T, cfg.E, dtype=torch.float64)
+    for t in range(cfg.T):
+        mask[t, st["idx"][t]] = 1.0
+    p = torch.softmax(xt @ tw["w_gate"].T, 1)
+    gate = mask * p / (mask * p).sum(1, keepdim=True)
+    F_ = torch.nn.functional
+    y = F_.linear(F_.silu(F_.linear(xt, tw["ws1"])) * F_.linear(xt, tw["ws3"]), tw["ws2"])
+    for e in range(cfg.E):
+        hh = F_.silu(xt @ tw["w1"][e].T) * (xt @ tw["w3"][e].T)
+        y = y + gate[:, e:e + 1] * (hh @ tw["w2"][e].T)
+    np.testing.assert_allclose(st["y"], y.detach().numpy(), rtol=1e-12, atol=1e-14)
+    mse = ((y - torch.from_numpy(tgt)) ** 2).mean()
+    counts = torch.from_numpy(st["counts"].astype(np.float64))
+    aux = cfg.E * (counts / (cfg.T * cfg.k) * p.mean(0)).sum()
+    (mse + cfg.aux_alpha * aux).backward()
+    for key in tw:
+        np.testing.assert_allclose(g["d" + key], tw[key].grad.numpy(), rtol=1e-10,
+                                   atol=1e-13, err_msg=key)
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+@pytest.mark.parametrize("case", [None, dict(score="sigmoid", E=8, n_groups=4, topk_groups=2,
+                                             aux_alpha=0.0)])
+def test_shared_gradients_central_differences(case):
+    cfg, w, x, tgt = _shared_case(800, n_shared=1, case=case)
+    st = O.forward(cfg, w, x)
+    _, _, dy = O.losses(cfg, st, tgt)
+    g = O.backward(cfg, w, x, st, dy)
+    h = 1e-6
+    for key in ("ws1", "ws3", "ws2"):
+        fd = np.zeros_like(w[key])
+        for i in np.ndindex(w[key].shape):
+            wp = dict(w); wp[key] = w[key].copy(); wp[key][i] += h
+            wm = dict(w); wm[key] = w[key].copy(); wm[key][i] -= h
+            fd[i] = (O.total_loss(cfg, wp, x, tgt) - O.total_loss(cfg, wm, x, tgt)) / (2 * h)
+        err = np.max(np.abs(fd - g["d" + key])) / np.max(np.abs(fd))
+        assert err <= 1e-6, (key, err)
+    fd = np.zeros_like(x)
+    for i in np.ndindex(x.shape):
+        xp = x.copy(); xp[i] += h
+        xm = x.copy(); xm[i] -= h
+        fd[i] = (O.total_loss(cfg, w, xp, tgt) - O.total_loss(cfg, w, xm, tgt)) / (2 * h)
+    assert np.max(np.abs(fd - g["dx"])) / np.max(np.abs(fd)) <= 1e-6
+
+
+def test_shared_zero_down_projection_is_identity():
+    cfg, w, x, tgt = _shared_case(900)
+    w0 = {k_: v for k_, v in w.items() if not k_.startswith("ws")}
+    w["ws2"] = np.zeros_like(w["ws2"])
+    st, st0 = O.forward(cfg, w, x), O.forward(cfg, w0, x)
+    np.testing.assert_array_equal(st["y"], st0["y"])
+    _, _, dy = O.losses(cfg, st, tgt)
+    g = O.backward(cfg, w, x, st, dy)
+    g0 = O.backward(cfg, w0, x, st0, dy)
+    assert not np.any(g["dws1"]) and not np.any(g["dws3"])
+    np.testing.assert_array_equal(g["dx"], g0["dx"])
+    a = O.silu(x @ w["ws1"].T) * (x @ w["ws3"].T)
+    np.testing.assert_allclose(g["dws2"], dy.T @ a, rtol=1e-12)
