@@ -86,6 +86,10 @@ typedef struct {
   int32_t dtype;      /* MOE_F32 | MOE_BF16: element type of x and expert W  */
   int32_t has_bias;   /* expert biases b1, b2 (not with SwiGLU)              */
   float aux_alpha;    /* L = L_mse + aux_alpha * aux                         */
+  int32_t n_shared;   /* shared experts: 0 = none; n > 0 adds one SwiGLU
+                         branch of hidden width n * F that every token passes
+                         through, added to the output without a gate ("AI
+                         Infra Kernel Lab").  Requires SwiGLU and MOE_BF16.  */
 } moe_config;
 
 /* Read-only weights for moe_forward / moe_backward. */
@@ -105,6 +109,10 @@ typedef struct {
                                use the unbiased scores ("AI Infra Kernel Lab",
                                grouped Top-K gate with correction bias).  Not
                                updated by the library.                            */
+  const void* ws1;          /* shared branch (n_shared > 0, bf16), else NULL:
+                               [n_shared*F, D]                                    */
+  const void* ws3;          /* [n_shared*F, D]                                    */
+  const void* ws2;          /* [D, n_shared*F]                                    */
 } moe_weights;
 
 /* fp32 gradient buffers, overwritten (never accumulated into) by each call:
@@ -117,6 +125,9 @@ typedef struct {
   float* dw2;       /* [E,D,F]            */
   float* db1;       /* [E,F] or NULL      */
   float* db2;       /* [E,D] or NULL      */
+  float* dws1;      /* shared branch [n_shared*F, D] or NULL (n_shared = 0) */
+  float* dws3;      /* [n_shared*F, D] or NULL                              */
+  float* dws2;      /* [D, n_shared*F] or NULL                              */
 } moe_grads;
 
 /* Trainable parameters for moe_train_step.  The fp32 masters are updated in
@@ -136,6 +147,13 @@ typedef struct {
   const float* logit_bias;  /* [E] or NULL                               */
   const float* corr_bias;   /* [E] selection-only correction bias or NULL
                                (as in moe_weights; never updated)         */
+  float* ws1;               /* shared branch fp32 masters (n_shared > 0)
+                               [n_shared*F, D], or NULL                   */
+  float* ws3;               /* [n_shared*F, D]                            */
+  float* ws2;               /* [D, n_shared*F]                            */
+  void* ws1_lp;             /* their bf16 copies, rewritten by the step   */
+  void* ws3_lp;
+  void* ws2_lp;
   moe_grads grads;          /* gradient buffers, written by the step     */
 } moe_params;
 

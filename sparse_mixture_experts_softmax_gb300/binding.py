@@ -37,21 +37,23 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", c_int32), ("D", c_int32), ("F", c_int32), ("E", c_int32), ("k", c_int32),
                 ("n_groups", c_int32), ("topk_groups", c_int32), ("group_score", c_int32),
                 ("act", c_int32), ("score", c_int32), ("dtype", c_int32), ("has_bias", c_int32),
-                ("aux_alpha", c_float)]
+                ("aux_alpha", c_float), ("n_shared", c_int32)]
 
 
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2", "logit_bias",
-                                        "corr_bias")]
+                                        "corr_bias", "ws1", "ws3", "ws2")]
 
 
 class moe_grads(ctypes.Structure):
-    _fields_ = [(n, c_void_p) for n in ("dw_gate", "dw1", "dw3", "dw2", "db1", "db2")]
+    _fields_ = [(n, c_void_p) for n in ("dw_gate", "dw1", "dw3", "dw2", "db1", "db2",
+                                        "dws1", "dws3", "dws2")]
 
 
 class moe_params(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("w_gate", "w1", "w3", "w2", "b1", "b2",
-                                        "w1_lp", "w3_lp", "w2_lp", "logit_bias", "corr_bias")] + \
+                                        "w1_lp", "w3_lp", "w2_lp", "logit_bias", "corr_bias",
+                                        "ws1", "ws3", "ws2", "ws1_lp", "ws3_lp", "ws2_lp")] + \
                [("grads", moe_grads)]
 
 
@@ -136,25 +138,31 @@ def _check(fn: str, status: int):
 
 
 def make_config(T, D, F, E, k, act="relu", score="softmax", n_groups=1, topk_groups=1,
-                group_score="top2_sum", dtype="f32", has_bias=True, aux_alpha=0.0) -> moe_config:
+                group_score="top2_sum", dtype="f32", has_bias=True, aux_alpha=0.0,
+                n_shared=0) -> moe_config:
     return moe_config(T, D, F, E, k, n_groups, topk_groups, GROUP_SCORE[group_score], ACT[act],
-                      SCORE[score], DTYPE[dtype], int(bool(has_bias)), float(aux_alpha))
+                      SCORE[score], DTYPE[dtype], int(bool(has_bias)), float(aux_alpha),
+                      int(n_shared))
 
 
 def make_weights(w_gate, w1, w2, w3=None, b1=None, b2=None, logit_bias=None,
-                 corr_bias=None) -> moe_weights:
+                 corr_bias=None, ws1=None, ws3=None, ws2=None) -> moe_weights:
     return moe_weights(_ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(b1), _ptr(b2),
-                       _ptr(logit_bias), _ptr(corr_bias))
+                       _ptr(logit_bias), _ptr(corr_bias), _ptr(ws1), _ptr(ws3), _ptr(ws2))
 
 
-def make_grads(dw_gate, dw1, dw2, dw3=None, db1=None, db2=None) -> moe_grads:
-    return moe_grads(_ptr(dw_gate), _ptr(dw1), _ptr(dw3), _ptr(dw2), _ptr(db1), _ptr(db2))
+def make_grads(dw_gate, dw1, dw2, dw3=None, db1=None, db2=None, dws1=None, dws3=None,
+               dws2=None) -> moe_grads:
+    return moe_grads(_ptr(dw_gate), _ptr(dw1), _ptr(dw3), _ptr(dw2), _ptr(db1), _ptr(db2),
+                     _ptr(dws1), _ptr(dws3), _ptr(dws2))
 
 
 def make_params(w_gate, w1, w2, grads: moe_grads, w3=None, b1=None, b2=None, w1_lp=None,
-                w3_lp=None, w2_lp=None, logit_bias=None, corr_bias=None) -> moe_params:
+                w3_lp=None, w2_lp=None, logit_bias=None, corr_bias=None, ws1=None, ws3=None,
+                ws2=None, ws1_lp=None, ws3_lp=None, ws2_lp=None) -> moe_params:
     return moe_params(_ptr(w_gate), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(b1), _ptr(b2),
                       _ptr(w1_lp), _ptr(w3_lp), _ptr(w2_lp), _ptr(logit_bias), _ptr(corr_bias),
+                      _ptr(ws1), _ptr(ws3), _ptr(ws2), _ptr(ws1_lp), _ptr(ws3_lp), _ptr(ws2_lp),
                       grads)
 
 

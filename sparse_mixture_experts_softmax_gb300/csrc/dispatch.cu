@@ -125,12 +125,14 @@ gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, 
 
 constexpr int CB_TOK = 8;    // tokens per block (one per warp)
 
-// Y[t] = sum_j g_tj Ye[slot(t, j)] in j order (fp32).  With a target it also
-// forms dY = 2 (Y - target) / (T D) and a per-block sum of squared errors.
+// Y[t] = sum_j g_tj Ye[slot(t, j)] in j order (fp32), + Ys[t] (the shared-
+// expert branch) when given.  With a target it also forms dY = 2 (Y - target)
+// / (T D) and a per-block sum of squared errors.
 template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
-               const int* __restrict__ slot_of, int Tn, int D, int k, float* __restrict__ y,
+               const int* __restrict__ slot_of, int Tn, int D, int k, const T* __restrict__ ys,
+               float* __restrict__ y,
                const float* __restrict__ target, float* __restrict__ dy, float inv_n,
                double* __restrict__ sq_partial) {
   constexpr int VN = Vec<T>::N;
@@ -151,6 +153,12 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
         v.load(ye + (size_t)s * D + d);
 #pragma unroll
         for (int i = 0; i < VN; ++i) acc[i] = fmaf(g, v.get(i), acc[i]);
+      }
+      if (ys != nullptr) {   // shared-expert branch, added after the routed sum
+        Vec<T> v;
+        v.load(ys + (size_t)t * D + d);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += v.get(i);
       }
       if (y != nullptr) {
 #pragma unroll
@@ -185,7 +193,7 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
 
 // Training-step combine with its backward fused (k <= 8): for each token,
 // with its k expert rows held in registers,
-//   Y[t]  = sum_j g_tj Ye[slot(t, j)]            (j order, as combine_kernel)
+//   Y[t]  = sum_j g_tj Ye[slot(t, j)] (+ Ys[t])  (j order, as combine_kernel)
 //   dY[t] = 2 (Y[t] - target[t]) / (T D)          (MSE seed, never stored)
 //   dYe[slot(t, j)] = g_tj dY[t],  dg_tj = <dY[t], Ye[slot(t, j)]>
 // with the same arithmetic and order as combine_kernel followed by
@@ -201,9 +209,9 @@ template <typename T>
 __global__ void __launch_bounds__(32 * CT_WARPS)
 combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
                      const int* __restrict__ slot_of, int Tn, int D, int k,
-                     const float* __restrict__ target, float inv_n,
+                     const T* __restrict__ ys, const float* __restrict__ target, float inv_n,
                      double* __restrict__ sq_partial, T* __restrict__ dye,
-                     float* __restrict__ dgate) {
+                     float* __restrict__ dgate, bf16* __restrict__ dy_lp) {
   constexpr int VN = Vec<T>::N;
   constexpr int MAXK = 8;
   __shared__ float wpart[CT_WARPS];
@@ -234,6 +242,12 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
 #pragma unroll
           for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], v[j].get(i), acc[i]);
         }
+      if (ys != nullptr) {   // shared-expert branch, added after the routed sum
+        Vec<T> u;
+        u.load(ys + (size_t)t * D + d);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += u.get(i);
+      }
       float dv[VN];
 #pragma unroll
       for (int i = 0; i < VN; i += 4) {
@@ -245,6 +259,14 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
         dv[i + 1] = 2.f * d1 * inv_n;
         dv[i + 2] = 2.f * d2 * inv_n;
         dv[i + 3] = 2.f * d3 * inv_n;
+      }
+      if constexpr (VN == 8) {   // bf16 rows: dY copy for the shared branch's GEMMs
+        if (dy_lp != nullptr) {
+          Vec<bf16> q;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) q.set(i, dv[i]);
+          q.store(dy_lp + (size_t)t * D + d);
+        }
       }
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
@@ -364,11 +386,13 @@ combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
 }
 
 // dX[t] += sum_j dXe[slot(t, j)] in j order (scatter-back of the expert rows
-// onto the router's dX term); one warp per token, 16-byte vectors along D.
+// onto the router's dX term), then + extra[t] (the shared-expert branch's dX)
+// when given; one warp per token, 16-byte vectors along D.
 template <typename T>
 __global__ void __launch_bounds__(256)
 scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
-                        const int* __restrict__ slot_of, int Tn, int D, int k) {
+                        const int* __restrict__ slot_of, int Tn, int D, int k,
+                        const T* __restrict__ extra) {
   constexpr int VN = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -383,6 +407,12 @@ scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
     for (int j = 0; j < k; ++j) {
       Vec<T> v;
       v.load(dxe + (size_t)slot_of[(size_t)t * k + j] * D + d);
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] += v.get(i);
+    }
+    if (extra != nullptr) {   // the shared branch's dX row, added last
+      Vec<T> v;
+      v.load(extra + (size_t)t * D + d);
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] += v.get(i);
     }
@@ -498,35 +528,38 @@ cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, i
 int combine_blocks(int T) { return (T + CB_TOK - 1) / CB_TOK; }
 
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of, int T,
-                           int D, int k, float* y, const float* target, float* dy,
+                           int D, int k, const void* ys, float* y, const float* target, float* dy,
                            double* sq_partial, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   float inv_n = 1.0f / ((float)T * (float)D);
   int grid = combine_blocks(T);
   if (dtype == 1)
     combine_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T, D, k,
-                                               y, target, dy, inv_n, sq_partial);
+                                               static_cast<const bf16*>(ys), y, target, dy, inv_n,
+                                               sq_partial);
   else
     combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(ye), gate, slot_of, T, D,
-                                                k, y, target, dy, inv_n, sq_partial);
+                                                k, static_cast<const float*>(ys), y, target, dy,
+                                                inv_n, sq_partial);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
-                                 int T, int D, int k, const float* target, double* sq_partial,
-                                 void* dye, float* dgate, cudaStream_t st) {
-  if (k > 8) return cudaErrorInvalidValue;
+                                 int T, int D, int k, const void* ys, const float* target,
+                                 double* sq_partial, void* dye, float* dgate, void* dy_lp,
+                                 cudaStream_t st) {
+  if (k > 8 || (dy_lp != nullptr && dtype != 1)) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
   const float inv_n = 1.0f / ((float)T * (float)D);
   const int grid = combine_blocks(T);
   if (dtype == 1)
-    combine_train_kernel<bf16><<<grid, 32 * CT_WARPS, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T,
-                                                     D, k, target, inv_n, sq_partial,
-                                                     static_cast<bf16*>(dye), dgate);
+    combine_train_kernel<bf16><<<grid, 32 * CT_WARPS, 0, st>>>(
+        static_cast<const bf16*>(ye), gate, slot_of, T, D, k, static_cast<const bf16*>(ys), target,
+        inv_n, sq_partial, static_cast<bf16*>(dye), dgate, static_cast<bf16*>(dy_lp));
   else
-    combine_train_kernel<float><<<grid, 32 * CT_WARPS, 0, st>>>(static_cast<const float*>(ye), gate, slot_of,
-                                                      T, D, k, target, inv_n, sq_partial,
-                                                      static_cast<float*>(dye), dgate);
+    combine_train_kernel<float><<<grid, 32 * CT_WARPS, 0, st>>>(
+        static_cast<const float*>(ye), gate, slot_of, T, D, k, static_cast<const float*>(ys),
+        target, inv_n, sq_partial, static_cast<float*>(dye), dgate, nullptr);
   return cudaGetLastError();
 }
 
@@ -566,15 +599,16 @@ cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const
 }
 
 cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const int* slot_of,
-                                    int T, int D, int k, cudaStream_t st) {
+                                    int T, int D, int k, const void* extra, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int grid = (T + 7) / 8;
   if (dtype == 1)
     scatter_back_add_kernel<bf16><<<grid, 256, 0, st>>>(dx, static_cast<const bf16*>(dxe), slot_of,
-                                                         T, D, k);
+                                                         T, D, k, static_cast<const bf16*>(extra));
   else
     scatter_back_add_kernel<float><<<grid, 256, 0, st>>>(dx, static_cast<const float*>(dxe),
-                                                          slot_of, T, D, k);
+                                                          slot_of, T, D, k,
+                                                          static_cast<const float*>(extra));
   return cudaGetLastError();
 }
 

@@ -40,21 +40,25 @@ cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E,
 cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, int k, int D,
                           void* xe, cudaStream_t st);
 int combine_blocks(int T);
+// ys: the shared-expert branch's output [T, D] added to Y, or nullptr.
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of,
-                           int T, int D, int k, float* y, const float* target, float* dy,
-                           double* sq_partial, cudaStream_t st);
+                           int T, int D, int k, const void* ys, float* y, const float* target,
+                           float* dy, double* sq_partial, cudaStream_t st);
 cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
                                    int n_ps, const int* counts, int T, int D, int E, int k,
                                    float alpha, float* d_loss, float* aux_row, cudaStream_t st);
 // Training-step combine + MSE seed + combine backward in one pass (k <= 8).
+// ys as in launch_combine; dy_lp (bf16 layers): also store dY in bf16, or nullptr.
 cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
-                                 int T, int D, int k, const float* target, double* sq_partial,
-                                 void* dye, float* dgate, cudaStream_t st);
+                                 int T, int D, int k, const void* ys, const float* target,
+                                 double* sq_partial, void* dye, float* dgate, void* dy_lp,
+                                 cudaStream_t st);
 cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
                                const int* slot_of, int T, int D, int k, void* dye, float* dgate,
                                cudaStream_t st);
+// extra: a [T, D] row block (cfg dtype) added to dX after the expert rows, or nullptr.
 cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const int* slot_of,
-                                    int T, int D, int k, cudaStream_t st);
+                                    int T, int D, int k, const void* extra, cudaStream_t st);
 cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets, int E, int N,
                                   float* out, cudaStream_t st);
 cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,

@@ -60,6 +60,9 @@ struct Layout {
   size_t status, scores, idx, gate, counts, offsets, chunk, src_tok, slot_of, psum, sq, aux_row;
   size_t xe, h1, h3, a, ye, dy, dye, dgate, dh1, dh3, dxe, dlogits, dwg_part, dx;
   size_t logits, wg_lp, dl_lp;   // bf16 layers: router logits, bf16 W_g, bf16 dlogits
+  // shared-expert branch (n_shared > 0): H1s, H3s, As [T, Fs]; Ys [T, D]; bf16
+  // dY [T, D]; dH1s, dH3s [T, Fs]; dXs [T, D] (all bf16)
+  size_t hs1, hs3, as, ys, dy_lp, dhs1, dhs3, dxs;
   size_t total;
 };
 
@@ -105,6 +108,17 @@ Layout make_layout(const moe_config& c) {
   L.logits = lp ? take(T * E * 4) : 0;
   L.wg_lp = lp ? take(E * D * 2) : 0;
   L.dl_lp = lp ? take(T * E * 2) : 0;
+  if (c.n_shared > 0) {
+    const size_t Fs = (size_t)c.n_shared * F;
+    L.hs1 = take(T * Fs * 2);
+    L.hs3 = take(T * Fs * 2);
+    L.as = take(T * Fs * 2);
+    L.ys = take(T * D * 2);
+    L.dy_lp = take(T * D * 2);
+    L.dhs1 = take(T * Fs * 2);
+    L.dhs3 = take(T * Fs * 2);
+    L.dxs = take(T * D * 2);
+  }
   L.total = o;
   return L;
 }
@@ -125,6 +139,10 @@ moe_status validate_config(const moe_config* c) {
   if (c->dtype == MOE_BF16 && c->E % 8 != 0) return MOE_ERR_UNSUPPORTED;   // TMA row alignment
   if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if ((long long)c->T * c->D >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
+  if (c->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared > 0 && (c->act != MOE_ACT_SWIGLU || c->dtype != MOE_BF16 ||
+                          (long long)c->n_shared * c->F > (1LL << 20)))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -176,6 +194,9 @@ struct ExpertW {
   const float* b2;
   const float* logit_bias;
   const float* corr_bias;   // selection-only correction bias [E] or nullptr
+  const void* ws1;          // shared branch (bf16), or nullptr
+  const void* ws3;
+  const void* ws2;
 };
 
 RouterArgs router_args(const moe_config& c, const float* corr_bias = nullptr) {
@@ -309,16 +330,66 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   d.C = P.at<void>(L.ye);
   KL("gemm_down", run_gemm(c, d, st));
 
+  const bool shared = c.n_shared > 0;
+  if (shared) {
+    // shared experts: one SwiGLU branch over all T tokens (a single segment)
+    const int Fs = c.n_shared * c.F;
+    GemmArgs su = gemm_base(c, P);
+    su.offsets = nullptr;
+    su.E = 1;
+    su.seg_len = c.T;
+    su.ragged_k = false;
+    su.a_kcontig = true;
+    su.b_kcontig = true;
+    su.M = c.T;
+    su.N = Fs;
+    su.A0 = x;
+    su.lda = c.D;
+    su.K0 = c.D;
+    su.B0 = w.ws1;
+    su.B0x = w.ws3;
+    su.ldb = c.D;
+    su.sBe = (long long)Fs * c.D;
+    su.ldc = Fs;
+    su.ld_aux = Fs;
+    su.epi = EPI_SWIGLU_UP;
+    su.out1 = P.at<void>(L.hs1);
+    su.out2 = P.at<void>(L.hs3);
+    su.C = P.at<void>(L.as);
+    KL("gemm_shared_up", run_gemm(c, su, st));
+    GemmArgs sd = gemm_base(c, P);
+    sd.offsets = nullptr;
+    sd.E = 1;
+    sd.seg_len = c.T;
+    sd.ragged_k = false;
+    sd.a_kcontig = true;
+    sd.b_kcontig = true;
+    sd.M = c.T;
+    sd.N = c.D;
+    sd.A0 = P.at<void>(L.as);
+    sd.lda = Fs;
+    sd.K0 = Fs;
+    sd.B0 = w.ws2;
+    sd.ldb = Fs;
+    sd.sBe = (long long)c.D * Fs;
+    sd.ldc = c.D;
+    sd.epi = EPI_STORE;
+    sd.C = P.at<void>(L.ys);
+    KL("gemm_shared_down", run_gemm(c, sd, st));
+  }
+  const void* ys = shared ? P.at<void>(L.ys) : nullptr;
+
   const bool train = target != nullptr;
   if (train && y == nullptr && c.k <= 8) {
     // training step: the combine backward runs in the same pass (dYe, dgate)
     KL("combine_fused", launch_combine_train(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate),
-                                             P.at<int>(L.slot_of), c.T, c.D, c.k, target,
+                                             P.at<int>(L.slot_of), c.T, c.D, c.k, ys, target,
                                              P.at<double>(L.sq), P.at<void>(L.dye),
-                                             P.at<float>(L.dgate), st));
+                                             P.at<float>(L.dgate),
+                                             shared ? P.at<void>(L.dy_lp) : nullptr, st));
   } else {
     KL("combine_loss", launch_combine(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of), c.T,
-                      c.D, c.k, y, target, train ? P.at<float>(L.dy) : nullptr,
+                      c.D, c.k, ys, y, target, train ? P.at<float>(L.dy) : nullptr,
                       train ? P.at<double>(L.sq) : nullptr, st));
   }
   if (train)
@@ -335,6 +406,8 @@ struct SgdFuse {
   float lr;
   float *w1, *w3, *w2;
   void *w1_lp, *w3_lp, *w2_lp;
+  float *ws1, *ws3, *ws2;        // shared branch
+  void *ws1_lp, *ws3_lp, *ws2_lp;
 };
 
 // Backward of L = L_task + alpha aux given dY (course Parts 4-6).
@@ -457,6 +530,116 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
   }
   if (gr.db1) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dh1), P.at<int>(L.offsets), c.E, c.F, gr.db1, st));
 
+  if (c.n_shared > 0) {
+    // shared branch: it receives the whole dY (bf16 copy for the tensor cores)
+    const int Fs = c.n_shared * c.F;
+    void* dyl = P.at<void>(L.dy_lp);
+    if (dy != nullptr) KL("cast_dy", launch_cast_bf16(dy, dyl, (long long)c.T * c.D, st));
+    auto one_segment = [&](GemmArgs& q) {
+      q.offsets = nullptr;
+      q.E = 1;
+      q.seg_len = c.T;
+    };
+    // dA_s = dY Ws2 with the SwiGLU backward in the epilogue
+    GemmArgs sa = gemm_base(c, P);
+    one_segment(sa);
+    sa.ragged_k = false;
+    sa.a_kcontig = true;
+    sa.b_kcontig = false;
+    sa.M = c.T;
+    sa.N = Fs;
+    sa.A0 = dyl;
+    sa.lda = c.D;
+    sa.K0 = c.D;
+    sa.B0 = w.ws2;
+    sa.ldb = Fs;
+    sa.sBe = (long long)c.D * Fs;
+    sa.ldc = Fs;
+    sa.ld_aux = Fs;
+    sa.aux0 = P.at<void>(L.hs1);
+    sa.aux1 = P.at<void>(L.hs3);
+    sa.C = P.at<void>(L.dhs1);
+    sa.out1 = P.at<void>(L.dhs3);
+    sa.epi = EPI_SWIGLU_BWD;
+    KL("gemm_shared_dA", run_gemm(c, sa, st));
+    // dWs2 = dY^T As over the T rows (SGD fused in a training step)
+    GemmArgs s2 = gemm_base(c, P);
+    one_segment(s2);
+    s2.ragged_k = true;
+    s2.a_kcontig = false;
+    s2.b_kcontig = false;
+    s2.c_type = MOE_F32;
+    s2.M = c.D;
+    s2.N = Fs;
+    s2.A0 = dyl;
+    s2.lda = c.D;
+    s2.B0 = P.at<void>(L.as);
+    s2.ldb = Fs;
+    s2.K0 = c.T;
+    s2.C = gr.dws2;
+    s2.ldc = Fs;
+    s2.sCe = (long long)c.D * Fs;
+    s2.epi = EPI_STORE;
+    if (sgd) {
+      s2.sgd_w = sgd->ws2;
+      s2.sgd_wlp = sgd->ws2_lp;
+      s2.sgd_lr = sgd->lr;
+    }
+    KL("gemm_shared_dw2", run_gemm(c, s2, st));
+    // dXs = dH1s Ws1 + dH3s Ws3 (added to dX by the scatter-back)
+    GemmArgs sx = gemm_base(c, P);
+    one_segment(sx);
+    sx.ragged_k = false;
+    sx.a_kcontig = true;
+    sx.b_kcontig = false;
+    sx.M = c.T;
+    sx.N = c.D;
+    sx.A0 = P.at<void>(L.dhs1);
+    sx.lda = Fs;
+    sx.K0 = Fs;
+    sx.B0 = w.ws1;
+    sx.ldb = c.D;
+    sx.sBe = (long long)Fs * c.D;
+    sx.A1 = P.at<void>(L.dhs3);
+    sx.B1 = w.ws3;
+    sx.K1 = Fs;
+    sx.ldc = c.D;
+    sx.epi = EPI_STORE;
+    sx.C = P.at<void>(L.dxs);
+    KL("gemm_shared_dx", run_gemm(c, sx, st));
+    // dWs1 = dH1s^T x, dWs3 = dH3s^T x (SGD fused in a training step)
+    GemmArgs s1 = gemm_base(c, P);
+    one_segment(s1);
+    s1.ragged_k = true;
+    s1.a_kcontig = false;
+    s1.b_kcontig = false;
+    s1.c_type = MOE_F32;
+    s1.M = Fs;
+    s1.N = c.D;
+    s1.A0 = P.at<void>(L.dhs1);
+    s1.lda = Fs;
+    s1.B0 = x;
+    s1.ldb = c.D;
+    s1.K0 = c.T;
+    s1.C = gr.dws1;
+    s1.ldc = c.D;
+    s1.sCe = (long long)Fs * c.D;
+    s1.epi = EPI_STORE;
+    if (sgd) {
+      s1.sgd_w = sgd->ws1;
+      s1.sgd_wlp = sgd->ws1_lp;
+      s1.sgd_lr = sgd->lr;
+    }
+    KL("gemm_shared_dw1", run_gemm(c, s1, st));
+    s1.A0 = P.at<void>(L.dhs3);
+    s1.C = gr.dws3;
+    if (sgd) {
+      s1.sgd_w = sgd->ws3;
+      s1.sgd_wlp = sgd->ws3_lp;
+    }
+    KL("gemm_shared_dw3", run_gemm(c, s1, st));
+  }
+
   // router: renormalisation + aux + score backward
   const RouterArgs ra = router_args(c);
   const bool lp = c.dtype == MOE_BF16;
@@ -512,7 +695,8 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
     dg.epi = EPI_STORE;
     KL("gemm_router_dx", launch_gemm_tc(dg, st));
     KL("scatter_back", launch_scatter_back_add(c.dtype, dx, P.at<void>(L.dxe), P.at<int>(L.slot_of),
-                                               c.T, c.D, c.k, st));
+                                               c.T, c.D, c.k,
+                                               c.n_shared > 0 ? P.at<void>(L.dxs) : nullptr, st));
     return MOE_OK;
   }
   // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
@@ -581,7 +765,9 @@ moe_status check_weights(const moe_config& c, const ExpertW& w) {
   if (!w.w_gate || !w.w1 || !w.w2) return MOE_ERR_INVALID_ARG;
   if (c.act == MOE_ACT_SWIGLU && !w.w3) return MOE_ERR_INVALID_ARG;
   if (c.has_bias && (!w.b1 || !w.b2)) return MOE_ERR_INVALID_ARG;
-  const void* ps[] = {w.w_gate, w.w1, w.w3, w.w2, w.b1, w.b2, w.logit_bias, w.corr_bias};
+  if (c.n_shared > 0 && (!w.ws1 || !w.ws3 || !w.ws2)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {w.w_gate, w.w1, w.w3, w.w2, w.b1, w.b2, w.logit_bias, w.corr_bias,
+                      w.ws1, w.ws3, w.ws2};
   for (const void* p : ps)
     if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
   return MOE_OK;
@@ -591,7 +777,8 @@ moe_status check_grads(const moe_config& c, const moe_grads& g) {
   if (!g.dw_gate || !g.dw1 || !g.dw2) return MOE_ERR_INVALID_ARG;
   if (c.act == MOE_ACT_SWIGLU && !g.dw3) return MOE_ERR_INVALID_ARG;
   if (c.has_bias && (!g.db1 || !g.db2)) return MOE_ERR_INVALID_ARG;
-  const void* ps[] = {g.dw_gate, g.dw1, g.dw3, g.dw2, g.db1, g.db2};
+  if (c.n_shared > 0 && (!g.dws1 || !g.dws3 || !g.dws2)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {g.dw_gate, g.dw1, g.dw3, g.dw2, g.db1, g.db2, g.dws1, g.dws3, g.dws2};
   for (const void* p : ps)
     if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
   return MOE_OK;
@@ -611,6 +798,12 @@ moe_status zero_grads(const moe_config& c, const moe_grads& g, cudaStream_t st) 
   CK(launch_fill_zero(g.dw2, E * D * F * 4, st));
   if (g.db1) CK(launch_fill_zero(g.db1, E * F * 4, st));
   if (g.db2) CK(launch_fill_zero(g.db2, E * D * 4, st));
+  if (c.n_shared > 0) {
+    const size_t Fs = (size_t)c.n_shared * F;
+    CK(launch_fill_zero(g.dws1, Fs * D * 4, st));
+    CK(launch_fill_zero(g.dws3, Fs * D * 4, st));
+    CK(launch_fill_zero(g.dws2, D * Fs * 4, st));
+  }
   return MOE_OK;
 }
 
@@ -626,9 +819,12 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   if (c.has_bias && (!p->b1 || !p->b2)) return MOE_ERR_INVALID_ARG;
   if (c.dtype == MOE_BF16 && (!p->w1_lp || !p->w2_lp || (c.act == MOE_ACT_SWIGLU && !p->w3_lp)))
     return MOE_ERR_INVALID_ARG;
+  if (c.n_shared > 0 && (!p->ws1 || !p->ws3 || !p->ws2 || !p->ws1_lp || !p->ws3_lp || !p->ws2_lp))
+    return MOE_ERR_INVALID_ARG;
   RET_IF(check_grads(c, p->grads));
   const void* ps[] = {p->w_gate, p->w1, p->w3, p->w2, p->b1, p->b2, p->w1_lp, p->w3_lp, p->w2_lp,
-                      p->logit_bias, p->corr_bias, x, y_target, d_loss, dx};
+                      p->logit_bias, p->corr_bias, p->ws1, p->ws3, p->ws2, p->ws1_lp,
+                      p->ws3_lp, p->ws2_lp, x, y_target, d_loss, dx};
   for (const void* q : ps)
     if (q && !aligned16(q)) return MOE_ERR_ALIGNMENT;
   if (c.T > 0 && (!x || !y_target)) return MOE_ERR_INVALID_ARG;
@@ -650,11 +846,15 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   w.b2 = p->b2;
   w.logit_bias = p->logit_bias;
   w.corr_bias = p->corr_bias;
+  w.ws1 = p->ws1_lp;   // the shared branch exists only for bf16 layers
+  w.ws3 = p->ws3_lp;
+  w.ws2 = p->ws2_lp;
   RET_IF(run_forward(c, w, x, nullptr, y_target, d_loss, P, st));
   float* dxp = dx ? dx : P.at<float>(L.dx);
   // bf16 layers: the expert weights' SGD runs inside the dW GEMM epilogues
   const bool fused = c.dtype == MOE_BF16;
-  const SgdFuse sf{lr, p->w1, p->w3, p->w2, p->w1_lp, p->w3_lp, p->w2_lp};
+  const SgdFuse sf{lr, p->w1, p->w3, p->w2, p->w1_lp, p->w3_lp, p->w2_lp,
+                   p->ws1, p->ws3, p->ws2, p->ws1_lp, p->ws3_lp, p->ws2_lp};
   // k <= 8: the forward's combine pass already produced dYe and dgate
   RET_IF(run_backward(c, w, x, c.k <= 8 ? nullptr : P.at<float>(L.dy), p->grads, dxp, true, P, st,
                       fused ? &sf : nullptr));
@@ -689,7 +889,8 @@ moe_status moe_forward(const moe_config* cfg, const moe_weights* w, const void* 
   RET_IF(validate_config(cfg));
   const moe_config& c = *cfg;
   if (w == nullptr) return MOE_ERR_INVALID_ARG;
-  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias, w->corr_bias};
+  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias, w->corr_bias,
+             w->ws1, w->ws3, w->ws2};
   RET_IF(check_weights(c, ew));
   RET_IF(check_ws(c, workspace, workspace_bytes));
   if (c.T > 0 && (!x || !y)) return MOE_ERR_INVALID_ARG;
@@ -708,7 +909,8 @@ moe_status moe_backward(const moe_config* cfg, const moe_weights* w, const void*
   RET_IF(validate_config(cfg));
   const moe_config& c = *cfg;
   if (w == nullptr || g == nullptr) return MOE_ERR_INVALID_ARG;
-  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias, w->corr_bias};
+  ExpertW ew{w->w_gate, w->w1, w->w3, w->w2, w->b1, w->b2, w->logit_bias, w->corr_bias,
+             w->ws1, w->ws3, w->ws2};
   RET_IF(check_weights(c, ew));
   RET_IF(check_grads(c, *g));
   RET_IF(check_ws(c, workspace, workspace_bytes));

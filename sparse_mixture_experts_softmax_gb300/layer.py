@@ -18,12 +18,12 @@ class MoELayer:
     def __init__(self, T, D, F, E, k, act, score, dtype, has_bias, aux_alpha, w_gate, w1, w2,
                  w3=None, b1=None, b2=None, logit_bias=None, n_groups=1, topk_groups=1,
                  group_score="top2_sum", w1_lp=None, w3_lp=None, w2_lp=None, device="cuda",
-                 corr_bias=None):
+                 corr_bias=None, n_shared=0, ws1=None, ws3=None, ws2=None):
         self.device = torch.device(device)
         self.dtype = dtype
         self.cfg = B.make_config(T, D, F, E, k, act=act, score=score, n_groups=n_groups,
                                  topk_groups=topk_groups, group_score=group_score, dtype=dtype,
-                                 has_bias=has_bias, aux_alpha=aux_alpha)
+                                 has_bias=has_bias, aux_alpha=aux_alpha, n_shared=n_shared)
         dev = self.device
 
         def f32(t):
@@ -32,6 +32,8 @@ class MoELayer:
         self.w_gate, self.w1, self.w2, self.w3 = f32(w_gate), f32(w1), f32(w2), f32(w3)
         self.b1, self.b2, self.logit_bias = f32(b1), f32(b2), f32(logit_bias)
         self.corr_bias = f32(corr_bias)   # selection-only routing bias (never trained)
+        # shared-expert branch: fp32 masters and (bf16 layers) working copies
+        self.ws1, self.ws3, self.ws2 = f32(ws1), f32(ws3), f32(ws2)
         if dtype == "bf16":
             def lp(given, master):
                 if master is None:
@@ -39,12 +41,17 @@ class MoELayer:
                 src = given if given is not None else master
                 return src.detach().to(dev, torch.bfloat16).contiguous().clone()
             self.w1_lp, self.w2_lp, self.w3_lp = lp(w1_lp, self.w1), lp(w2_lp, self.w2), lp(w3_lp, self.w3)
+            self.ws1_lp, self.ws3_lp, self.ws2_lp = (lp(None, self.ws1), lp(None, self.ws3),
+                                                     lp(None, self.ws2))
         else:
             self.w1_lp = self.w2_lp = self.w3_lp = None
+            self.ws1_lp = self.ws3_lp = self.ws2_lp = None
         z = lambda t: None if t is None else torch.zeros_like(t)  # noqa: E731
         self.dw_gate, self.dw1, self.dw2, self.dw3 = z(self.w_gate), z(self.w1), z(self.w2), z(self.w3)
         self.db1, self.db2 = z(self.b1), z(self.b2)
-        self.grads = B.make_grads(self.dw_gate, self.dw1, self.dw2, self.dw3, self.db1, self.db2)
+        self.dws1, self.dws3, self.dws2 = z(self.ws1), z(self.ws3), z(self.ws2)
+        self.grads = B.make_grads(self.dw_gate, self.dw1, self.dw2, self.dw3, self.db1, self.db2,
+                                  self.dws1, self.dws3, self.dws2)
         self.ws_bytes = B.moe_workspace_size(self.cfg)
         if self.ws_bytes == 0:
             raise B.MoEError("moe_workspace_size", B.MOE_ERR_INVALID_ARG, "invalid configuration")
@@ -56,12 +63,16 @@ class MoELayer:
         lp = self.dtype == "bf16"
         return B.make_weights(self.w_gate, self.w1_lp if lp else self.w1,
                               self.w2_lp if lp else self.w2, self.w3_lp if lp else self.w3,
-                              self.b1, self.b2, self.logit_bias, self.corr_bias)
+                              self.b1, self.b2, self.logit_bias, self.corr_bias,
+                              self.ws1_lp if lp else self.ws1, self.ws3_lp if lp else self.ws3,
+                              self.ws2_lp if lp else self.ws2)
 
     def params(self) -> B.moe_params:
         return B.make_params(self.w_gate, self.w1, self.w2, self.grads, w3=self.w3, b1=self.b1,
                              b2=self.b2, w1_lp=self.w1_lp, w3_lp=self.w3_lp, w2_lp=self.w2_lp,
-                             logit_bias=self.logit_bias, corr_bias=self.corr_bias)
+                             logit_bias=self.logit_bias, corr_bias=self.corr_bias,
+                             ws1=self.ws1, ws3=self.ws3, ws2=self.ws2, ws1_lp=self.ws1_lp,
+                             ws3_lp=self.ws3_lp, ws2_lp=self.ws2_lp)
 
     def forward(self, x: torch.Tensor, y: Optional[torch.Tensor] = None) -> torch.Tensor:
         if y is None:
@@ -79,11 +90,11 @@ class MoELayer:
 
     def grad_dict(self) -> dict:
         return dict(dw_gate=self.dw_gate, dw1=self.dw1, dw2=self.dw2, dw3=self.dw3,
-                    db1=self.db1, db2=self.db2)
+                    db1=self.db1, db2=self.db2, dws1=self.dws1, dws3=self.dws3, dws2=self.dws2)
 
     def param_dict(self) -> dict:
         return dict(w_gate=self.w_gate, w1=self.w1, w2=self.w2, w3=self.w3, b1=self.b1,
-                    b2=self.b2)
+                    b2=self.b2, ws1=self.ws1, ws3=self.ws3, ws2=self.ws2)
 
     def routing(self) -> dict:
         c = self.cfg

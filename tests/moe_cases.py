@@ -45,6 +45,10 @@ def oracle_inputs(wl: W.Workload, inp: dict):
                  corr_bias=np64(inp.get("corr_bias")))
     master = dict(w_gate=np64(inp["w_gate"]), w1=np64(inp["w1"]), w2=np64(inp["w2"]),
                   w3=np64(inp["w3"]), b1=np64(inp["b1"]), b2=np64(inp["b2"]))
+    if inp.get("ws1") is not None:   # shared-expert branch
+        for key in ("ws1", "ws3", "ws2"):
+            w_fwd[key] = np64(inp[key + "_bf16"] if lp else inp[key])
+            master[key] = np64(inp[key])
     x = np64(inp["x_bf16"] if lp else inp["x"])
     return w_fwd, master, x, np64(inp["target"])
 
@@ -59,7 +63,8 @@ def make_layer(wl: W.Workload, inp: dict, device="cuda", group_score="top2_sum")
                     w1_lp=inp.get("w1_bf16") if lp else None,
                     w3_lp=inp.get("w3_bf16") if lp else None,
                     w2_lp=inp.get("w2_bf16") if lp else None, device=device,
-                    corr_bias=inp.get("corr_bias"))
+                    corr_bias=inp.get("corr_bias"), n_shared=wl.n_shared, ws1=inp.get("ws1"),
+                    ws3=inp.get("ws3"), ws2=inp.get("ws2"))
 
 
 def device_x(wl: W.Workload, inp: dict, device="cuda"):

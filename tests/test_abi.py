@@ -52,6 +52,12 @@ def test_workspace_size_valid_and_invalid(L):
     assert B.moe_workspace_size(_cfg(act="swiglu", has_bias=True)) == 0
     assert B.moe_workspace_size(_cfg(E=8, n_groups=3, topk_groups=1)) == 0
     assert B.moe_workspace_size(_cfg(E=8, k=4, n_groups=4, topk_groups=1)) == 0  # k > kept
+    # shared experts: SwiGLU and bf16 only
+    assert B.moe_workspace_size(_cfg(n_shared=1)) == 0
+    assert B.moe_workspace_size(_cfg(E=8, act="swiglu", has_bias=False, dtype="bf16",
+                                     n_shared=2)) > \
+        B.moe_workspace_size(_cfg(E=8, act="swiglu", has_bias=False, dtype="bf16"))
+    assert B.moe_workspace_size(_cfg(n_shared=-1)) == 0
     assert B.moe_host_staging_size(_cfg()) >= 64 * 32 * 8
 
 

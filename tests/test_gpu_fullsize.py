@@ -44,6 +44,8 @@ class LazyExperts:
 def _oracle_weights(inp, lb):
     return dict(w_gate=np64(inp["w_gate"].to(torch.bfloat16)), w1=LazyExperts(inp["w1_bf16"]),
                 corr_bias=np64(inp.get("corr_bias")),
+                ws1=np64(inp.get("ws1_bf16")), ws3=np64(inp.get("ws3_bf16")),
+                ws2=np64(inp.get("ws2_bf16")),
                 w2=LazyExperts(inp["w2_bf16"]),
                 w3=LazyExperts(inp["w3_bf16"]) if inp["w3_bf16"] is not None else None,
                 b1=None, b2=None, logit_bias=lb)
@@ -64,15 +66,19 @@ def _rows_forward(cfg, w, x64, pairs):
 
 
 def _tokens_y(cfg, w, x64, scores64, idx, tokens):
-    """y[t] for the given tokens (oracle gates from its own scores)."""
+    """y[t] for the given tokens (oracle gates from its own scores), with the
+    shared-expert branch when the layer has one."""
     pairs = [(t, idx[t, j]) for t in tokens for j in range(cfg.k)]
     fw = _rows_forward(cfg, w, x64, pairs)
     gate = O.renormalize(scores64[tokens], idx[tokens])
+    sh = O.shared_forward(x64[tokens], w) if w.get("ws1") is not None else None
     ys = {}
     for i, t in enumerate(tokens):
         y = np.zeros(cfg.D)
         for j in range(cfg.k):
             y = y + gate[i, j] * fw[(t, int(idx[t, j]))]["ye"][0]
+        if sh is not None:
+            y = y + sh["ys"][i]
         ys[t] = y
     return ys, fw, gate
 
@@ -93,7 +99,7 @@ def _run_full(name):
 
 
 @pytest.mark.parametrize("name,n_sample", [("grouped", 8), ("skewed", 6), ("large", 4),
-                                           ("grouped_cb", 8)])
+                                           ("grouped_cb", 8), ("grouped_shared", 8)])
 def test_full_size_layer(name, n_sample):
     wl, inp, cfg, layer, y, dx, r = _run_full(name)
     T, D, E, k = wl.T, wl.D, wl.E, wl.k
@@ -136,6 +142,9 @@ def test_full_size_layer(name, n_sample):
             be = O.expert_backward(cfg, e, x64[t:t + 1], fe, (gate[i, j] * dy)[None], w)
             dxt = dxt + be["dxe"][0]
             dgate[j] = float(np.dot(dy, fe["ye"][0]))
+        if w.get("ws1") is not None:
+            dxt = dxt + O.shared_backward(x64[t:t + 1], O.shared_forward(x64[t:t + 1], w),
+                                          dy[None], w)["dx"][0]
         ds = O.renormalize_backward(scores64[t:t + 1], idx_s[t:t + 1], gate[i:i + 1], dgate[None])
         ds = ds + aux_row[None, :]
         if cfg.score == "softmax":
@@ -183,7 +192,7 @@ def test_full_size_layer(name, n_sample):
                          TOL + 2.0 ** -24 * np.max(np.abs(w0)) / scale)
     # 7. every expert's bf16 working copy is the round-to-nearest image of its
     #    updated fp32 master
-    for key in ("w1", "w3", "w2"):
+    for key in ("w1", "w3", "w2") + (("ws1", "ws3", "ws2") if wl.n_shared else ()):
         assert torch.equal(getattr(layer, key + "_lp"), getattr(layer, key).to(torch.bfloat16)), key
     del layer, inp
     torch.cuda.empty_cache()

@@ -23,6 +23,8 @@ def _grad_keys(wl):
         keys.append("dw3")
     if wl.has_bias:
         keys += ["db1", "db2"]
+    if wl.n_shared:
+        keys += ["dws1", "dws3", "dws2"]
     return keys
 
 
@@ -59,7 +61,7 @@ def _one_step_parity(wl, seed=0, check_dx=True):
         errs["dx"] = assert_close("dx", np64(dx), g["dx"], tol)
     # SGD: theta_1 = theta_0 - lr * grad on the fp32 masters
     new = layer.param_dict()
-    for key in ("w_gate", "w1", "w2", "w3", "b1", "b2"):
+    for key in ("w_gate", "w1", "w2", "w3", "b1", "b2", "ws1", "ws3", "ws2"):
         if master.get(key) is None:
             continue
         want = master[key] - wl.lr * g["d" + key]
@@ -74,7 +76,7 @@ def _one_step_parity(wl, seed=0, check_dx=True):
         assert_close("step " + key, step, want_step, step_tol)
     if wl.dtype == "bf16":
         # the bf16 working copies are the round-to-nearest images of the masters
-        for key in ("w1", "w2", "w3"):
+        for key in ("w1", "w2", "w3", "ws1", "ws3", "ws2"):
             lp = getattr(layer, key + "_lp")
             if lp is not None:
                 assert torch.equal(lp, new[key].to(torch.bfloat16)), key
@@ -147,6 +149,40 @@ def test_correction_bias_grouped_bf16_step():
     errs, layer, inp = _one_step_parity(wl, check_dx=True)
     assert max(errs.values()) <= 2e-2
     _assert_bias_changes_routing(wl, inp, layer)
+
+
+@pytest.mark.parametrize("T", [2048, 777])
+def test_shared_experts_step(T):
+    """Shared-expert SwiGLU branch (width 2F, every token, no gate) on the
+    grouped layer: forward through combine, its dA / dX / dW GEMMs, the scatter
+    of its dX, and its fused SGD step (a ragged token count included)."""
+    wl = W.WORKLOADS["grouped_shared"].with_tokens(T)
+    errs, layer, _ = _one_step_parity(wl)
+    assert max(errs.values()) <= 2e-2
+    assert layer.dws1.abs().max().item() > 0 and layer.dws2.abs().max().item() > 0
+
+
+def test_shared_experts_forward_backward_entry_points():
+    """moe_forward / moe_backward (external dY, fp32) with the shared branch."""
+    wl = W.WORKLOADS["grouped_shared"].with_tokens(1024)
+    inp = W.make_inputs(wl, seed=5)
+    cfg = oracle_config(wl)
+    layer = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    y = layer.forward(x)
+    w_fwd, _, x64, t64 = oracle_inputs(wl, inp)
+    st0 = O.forward(cfg, w_fwd, x64)
+    idx = validated_routing(cfg, st0["scores"], layer.routing()["idx"].cpu().numpy())
+    st = O.forward(cfg, w_fwd, x64, idx)
+    assert_close("y", np64(y), st["y"], 2e-2)
+    _, _, dy = O.losses(cfg, st, t64)
+    dyt = torch.from_numpy(dy.astype(np.float32)).cuda()
+    dx = torch.empty_like(dyt)
+    layer.backward(x, dyt, dx)
+    g = O.backward(cfg, w_fwd, x64, st, dy)
+    for key in _grad_keys(wl):
+        assert_close(key, np64(layer.grad_dict()[key]), g[key], 2e-2)
+    assert_close("dx", np64(dx), g["dx"], 2e-2)
 
 
 def _assert_bias_changes_routing(wl, inp, layer):

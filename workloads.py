@@ -58,6 +58,7 @@ class Workload:
     zipf_skew: Optional[float] = None  # Zipf exponent of the fixed logit bias
     zipf_empty: int = 0                # experts that get a -inf logit bias (never selected)
     corr_bias_scale: Optional[float] = None  # selection-only correction bias ~ U(-s, s)
+    n_shared: int = 0                  # shared-expert SwiGLU branch of width n_shared * F
 
     @property
     def R(self) -> int:
@@ -91,6 +92,14 @@ WORKLOADS = {
     "grouped_cb": Workload("grouped_cb", T=16384, D=1024, F=704, E=64, k=6, act="swiglu",
                            score="sigmoid", n_groups=8, topk_groups=4, has_bias=False,
                            dtype="bf16", aux_alpha=0.0, lr=1e-3, corr_bias_scale=0.1),
+    # shared experts (one SwiGLU branch of width n_shared * F on every token)
+    "grouped_shared": Workload("grouped_shared", T=16384, D=1024, F=704, E=64, k=6,
+                               act="swiglu", score="sigmoid", n_groups=8, topk_groups=4,
+                               has_bias=False, dtype="bf16", aux_alpha=0.0, lr=1e-3, n_shared=2),
+    "large_shared": Workload("large_shared", T=65536, D=4096, F=2048, E=128, k=8, act="swiglu",
+                             score="softmax", n_groups=1, topk_groups=1, has_bias=False,
+                             dtype="bf16", aux_alpha=0.01, lr=1e-3, router_init="uniform",
+                             n_shared=1),
     "dense_f32_cb": Workload("dense_f32_cb", T=4096, D=512, F=1024, E=8, k=2, act="gelu_tanh",
                              score="softmax", n_groups=1, topk_groups=1, has_bias=True,
                              dtype="f32", aux_alpha=0.01, lr=0.01, corr_bias_scale=0.05),
@@ -135,6 +144,27 @@ def correction_bias(wl: Workload, seed: int = 0) -> Optional[torch.Tensor]:
     return (torch.rand(wl.E, generator=g) * 2.0 - 1.0) * wl.corr_bias_scale
 
 
+def shared_weights(wl: Workload, seed: int = 0, device: str = "cpu") -> dict:
+    """Shared-expert weights ws1, ws3 [n_shared F, D] ~ N(0, 1/D) and ws2
+    [D, n_shared F] ~ N(0, 1/(n_shared F)) from their own seeded generator (so
+    the other draws do not move), with bf16 copies for bf16 workloads; all
+    None without shared experts."""
+    keys = ("ws1", "ws3", "ws2", "ws1_bf16", "ws3_bf16", "ws2_bf16")
+    if wl.n_shared <= 0:
+        return {k_: None for k_ in keys}
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 3)
+    Fs = wl.n_shared * wl.F
+    ws1 = _normal((Fs, wl.D), 1.0 / math.sqrt(wl.D), g, device)
+    ws3 = _normal((Fs, wl.D), 1.0 / math.sqrt(wl.D), g, device)
+    ws2 = _normal((wl.D, Fs), 1.0 / math.sqrt(Fs), g, device)
+    out = dict(ws1=ws1, ws3=ws3, ws2=ws2)
+    lp = wl.dtype == "bf16"
+    for k_ in ("ws1", "ws3", "ws2"):
+        out[k_ + "_bf16"] = out[k_].to(torch.bfloat16) if lp else None
+    return out
+
+
 def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
                 with_target: bool = True) -> dict:
     """Draw one seeded workload.  Returns fp32 tensors plus bf16 copies.
@@ -170,6 +200,7 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu",
     out["logit_bias"] = lb.to(device) if lb is not None else None
     cb = correction_bias(wl, seed)
     out["corr_bias"] = cb.to(device) if cb is not None else None
+    out.update(shared_weights(wl, seed, device))
     if wl.dtype == "bf16":
         out["x_bf16"] = x.to(torch.bfloat16)
         out["w1_bf16"] = w1.to(torch.bfloat16)
