@@ -79,6 +79,13 @@ def expert_flops_per_step(wl: W.Workload) -> float:
     return 3.0 * proj * 2.0 * wl.D * wl.F * wl.R
 
 
+def shared_flops_per_step(wl: W.Workload) -> float:
+    """The shared-expert branch (reported separately from the routed experts):
+    three projections of 2*T*D*(n_shared*F) FLOPs, forward and twice that in
+    backward."""
+    return 3.0 * 3.0 * 2.0 * wl.T * wl.D * wl.n_shared * wl.F
+
+
 def router_flops_per_step(wl: W.Workload) -> float:
     return 3.0 * 2.0 * wl.T * wl.D * wl.E
 
@@ -197,7 +204,8 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
     sub = W.Workload(wl.name + "_sample", T=T_s, D=wl.D, F=wl.F, E=E_s, k=wl.k, act=wl.act,
                      score=wl.score, n_groups=n_groups, topk_groups=topk_groups,
                      has_bias=wl.has_bias, dtype=wl.dtype, aux_alpha=wl.aux_alpha, lr=wl.lr,
-                     router_init=wl.router_init)
+                     router_init=wl.router_init, corr_bias_scale=wl.corr_bias_scale,
+                     n_shared=wl.n_shared)
     inp = W.make_inputs(sub, seed=seed)
     f64 = lambda t: None if t is None else t.detach().double().numpy()  # noqa: E731
     lp = wl.dtype == "bf16"
@@ -205,7 +213,11 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
              w1=f64(inp["w1_bf16"] if lp else inp["w1"]),
              w2=f64(inp["w2_bf16"] if lp else inp["w2"]),
              w3=f64(inp["w3_bf16"] if lp and inp["w3"] is not None else inp["w3"]),
-             b1=f64(inp["b1"]), b2=f64(inp["b2"]), logit_bias=None)
+             b1=f64(inp["b1"]), b2=f64(inp["b2"]), logit_bias=None,
+             corr_bias=f64(inp.get("corr_bias")))
+    if wl.n_shared > 0:
+        for key in ("ws1", "ws3", "ws2"):
+            w[key] = f64(inp[key + "_bf16"] if lp else inp[key])
     x = f64(inp["x_bf16"] if lp else inp["x"])
     tgt = f64(inp["target"])
     cfg = O.OracleConfig(T=T_s, D=wl.D, F=wl.F, E=E_s, k=wl.k, act=wl.act, score=wl.score,
@@ -222,6 +234,7 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
 def sample_size(wl: W.Workload):
     """Tokens / experts of the CPU sample: about 10-30 s of float64 work."""
     per_tok = 3 * (3 if wl.act == "swiglu" else 2) * 2 * wl.D * wl.F * wl.k
+    per_tok += 3 * 3 * 2 * wl.D * wl.n_shared * wl.F      # shared-expert branch
     T_s = int(max(16, min(wl.T, 2.0e11 / per_tok)))
     E_s = min(wl.E, 16)
     return T_s, E_s
@@ -264,6 +277,7 @@ def workload_config(wl: W.Workload) -> dict:
             "top_k": wl.k, "activation": wl.act, "scores": wl.score, "n_groups": wl.n_groups,
             "topk_groups": wl.topk_groups, "expert_dtype": wl.dtype, "aux_alpha": wl.aux_alpha,
             "lr": wl.lr, "global_batch": wl.T, "parallelism": "replicas",
+            "n_shared": wl.n_shared, "corr_bias": wl.corr_bias_scale is not None,
             "l2": "inputs larger than L2 (weights and expert-major activations >> 129 MB)"}
 
 
@@ -316,11 +330,14 @@ def main():
                      b1=inp["b1"], b2=inp["b2"], logit_bias=inp["logit_bias"],
                      n_groups=wl.n_groups, topk_groups=wl.topk_groups,
                      w1_lp=inp.get("w1_bf16"), w3_lp=inp.get("w3_bf16"),
-                     w2_lp=inp.get("w2_bf16"), device=str(dev))
+                     w2_lp=inp.get("w2_bf16"), device=str(dev), corr_bias=inp.get("corr_bias"),
+                     n_shared=wl.n_shared, ws1=inp.get("ws1"), ws3=inp.get("ws3"),
+                     ws2=inp.get("ws2"))
     x = (inp["x_bf16"] if lp else inp["x"]).contiguous()
     tgt = inp["target"].contiguous()
     dx = torch.empty(wl.T, wl.D, device=dev)
-    for k_ in ("w1", "w2", "w3", "w1_bf16", "w2_bf16", "w3_bf16"):
+    for k_ in ("w1", "w2", "w3", "w1_bf16", "w2_bf16", "w3_bf16", "ws1", "ws3", "ws2",
+               "ws1_bf16", "ws3_bf16", "ws2_bf16"):
         inp.pop(k_, None)
     torch.cuda.empty_cache()
 
@@ -361,7 +378,8 @@ def main():
     for k_ in per_kernel:
         per_kernel[k_] /= args.steps
     gemm_ms = sum(v for k_, v in per_kernel.items()
-                  if k_.startswith("gemm_") and not k_.startswith("gemm_router"))
+                  if k_.startswith("gemm_") and not k_.startswith(("gemm_router", "gemm_shared")))
+    shared_ms = sum(v for k_, v in per_kernel.items() if k_.startswith("gemm_shared"))
     peaks = load_peaks()
     eflops = expert_flops_per_step(wl)
     if lp:
@@ -396,6 +414,10 @@ def main():
             "gpu_launches": launches * args.steps, "clocks": clk,
             "loss": {"mse": loss[0], "aux": loss[1]},
             "kernels_ms_per_step": {k_: round(v, 4) for k_, v in sorted(per_kernel.items())}}
+    if wl.n_shared > 0 and shared_ms > 0:
+        sf = shared_flops_per_step(wl)
+        line["shared_experts"] = {"n_shared": wl.n_shared, "gflop_per_step": sf / 1e9,
+                                  "ms_per_step": shared_ms, "tflops": sf / (shared_ms / 1e3) / 1e12}
 
     # end to end through the host-buffer entry point
     if not args.no_e2e:
