@@ -341,9 +341,16 @@ def main():
         inp.pop(k_, None)
     torch.cuda.empty_cache()
 
+    # warm-up steps, each timed on its own (the first one includes the
+    # one-time costs: module load, tensor-map encoding, attribute setup)
+    warm_ms = []
     for _ in range(args.warmup):
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record()
         layer.train_step(x, tgt, wl.lr, dx=dx)
-    torch.cuda.synchronize()
+        b_ev.record()
+        torch.cuda.synchronize()
+        warm_ms.append(a_ev.elapsed_time(b_ev))
     launches = B.moe_last_launch_count()
 
     stream = torch.cuda.current_stream()
@@ -355,11 +362,16 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps - 1)]
     start.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         layer.train_step(x, tgt, wl.lr, dx=dx)
+        if i < args.steps - 1:
+            step_ev[i].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
+    marks = [start] + step_ev + [end]
+    step_ms = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps))
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -412,6 +424,10 @@ def main():
             "expert_gemm_tflops": achieved, "router_gflop_per_step": router_flops_per_step(wl) / 1e9,
             "expert_gflop_per_step": eflops / 1e9, "roofline": roofline, "hbm_passes": hbm,
             "gpu_launches": launches * args.steps, "clocks": clk,
+            "step_ms": {"p50": step_ms[len(step_ms) // 2],
+                        "p90": step_ms[min(len(step_ms) - 1, int(0.9 * len(step_ms)))],
+                        "min": step_ms[0], "max": step_ms[-1]},
+            "warmup_ms": [round(v, 3) for v in warm_ms],
             "loss": {"mse": loss[0], "aux": loss[1]},
             "kernels_ms_per_step": {k_: round(v, 4) for k_, v in sorted(per_kernel.items())}}
     if wl.n_shared > 0 and shared_ms > 0:

@@ -6,10 +6,12 @@ compute exactly or one token at a time:
   * routing over ALL tokens, bit-exact given the GPU's own fp32 scores;
   * the scores and the aux loss against the oracle's fp64 router (cheap);
   * the MSE loss against the mean of (y - target)^2 of the GPU's own y;
-  * y and dX on sampled tokens, each token's k expert rows run by the oracle;
-  * the weight gradients and SGD step of the smallest non-empty expert (every
-    token routed to it runs through the oracle), and exact zeros for experts
-    with no rows;
+  * y, dX and the router gradient dlogits on sampled tokens, each token's k
+    expert rows run by the oracle;
+  * dW_g in full, as the GPU's (sample-checked) dlogits times x in float64;
+  * the weight gradients and SGD step of the smallest, median and largest
+    non-empty experts when the oracle can afford every token routed to them,
+    and exact zeros for experts with no rows;
   * every bf16 working copy equal to the bf16 rounding of its updated master.
 Expert weights are pulled to float64 one expert at a time.
 """
@@ -20,6 +22,7 @@ import torch
 
 import workloads as W
 from oracle import moe_oracle as O
+from sparse_mixture_experts_softmax_gb300 import binding as B
 from tests.moe_cases import (assert_close, check_routing_exact, make_layer, np64, oracle_config,
                              validated_routing)
 
@@ -93,8 +96,11 @@ def _run_full(name):
     y = layer.forward(x).clone()
     dx = torch.empty(wl.T, wl.D, device="cuda")
     layer.train_step(x, tgt, wl.lr, dx=dx)
+    dlogits = torch.empty(wl.T, wl.E, device="cuda")
+    B.moe_get_intermediates(layer.cfg, layer.workspace, dlogits=dlogits)
     torch.cuda.synchronize()
     r = layer.routing()
+    r["dlogits"] = dlogits
     return wl, inp, cfg, layer, y, dx, r
 
 
@@ -152,20 +158,31 @@ def test_full_size_layer(name, n_sample):
         else:
             dl = O.sigmoid_backward(scores64[t:t + 1], ds)
         dxt = dxt + (dl @ w["w_gate"])[0]
+        assert_close(f"dlogits[{t}]", r["dlogits"][t].double().cpu().numpy(), dl[0], TOL)
         assert_close(f"dx[{t}]", dx[t].double().cpu().numpy(), dxt, TOL)
+    # dW_g in full: the GPU's dlogits (checked on the samples above) times x,
+    # summed in float64, must give the GPU's router weight gradient
+    dwg_want = (r["dlogits"].double().T @ inp["x_bf16"].double()).cpu().numpy()
+    assert_close("dW_g", np64(layer.dw_gate), dwg_want, TOL)
     # 5. empty experts: exact zero gradients
     for e in np.nonzero(counts == 0)[0]:
         assert torch.all(layer.dw1[e] == 0) and torch.all(layer.dw2[e] == 0)
         assert torch.all(layer.dw3[e] == 0)
-    # 6. the smallest non-empty expert's weight gradients (when cheap enough)
+    # 6. weight gradients and SGD step of the smallest, median and largest
+    #    non-empty experts, each when the oracle can afford all its tokens
     nonzero = np.nonzero(counts)[0]
-    e_min = int(nonzero[np.argmin(counts[nonzero])])
-    n_rows = int(counts[e_min])
-    checked_dw = n_rows * k * 6 * D * wl.F <= 4e11
-    print(f"\n{name}: T={T} R={T * k} routed rows checked bit-exact; sampled tokens {tokens}; "
-          f"{int((counts == 0).sum())} empty experts; smallest expert {e_min} with {n_rows} rows "
-          f"{'checked' if checked_dw else 'skipped (too costly for the oracle)'}")
-    if checked_dw:
+    order = nonzero[np.argsort(counts[nonzero], kind="stable")]
+    picks = []
+    for e_sel in (order[0], order[len(order) // 2], order[-1]):
+        if int(e_sel) not in picks:
+            picks.append(int(e_sel))
+    report = []
+    for e_min in picks:
+        n_rows = int(counts[e_min])
+        checked_dw = n_rows * k * 6 * D * wl.F <= 4e11
+        report.append(f"expert {e_min} ({n_rows} rows) {'checked' if checked_dw else 'skipped'}")
+        if not checked_dw:
+            continue
         rows_tok = src_tok[offsets[e_min]:offsets[e_min + 1]].tolist()
         idx_v = validated_routing(cfg, scores64[rows_tok], idx[rows_tok], corr_bias=cb64)
         idx_m = idx.copy()
@@ -190,6 +207,8 @@ def test_full_size_layer(name, n_sample):
             scale = np.max(np.abs(want))
             assert_close(f"step {key}[{e_min}]", step, want,
                          TOL + 2.0 ** -24 * np.max(np.abs(w0)) / scale)
+    print(f"\n{name}: T={T} R={T * k} routed rows checked bit-exact; sampled tokens {tokens}; "
+          f"{int((counts == 0).sum())} empty experts; dW of " + ", ".join(report))
     # 7. every expert's bf16 working copy is the round-to-nearest image of its
     #    updated fp32 master
     for key in ("w1", "w3", "w2") + (("ws1", "ws3", "ws2") if wl.n_shared else ()):
