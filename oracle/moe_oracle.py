@@ -51,6 +51,7 @@ is "parity unpinned".
 from __future__ import annotations
 
 import dataclasses
+import math
 from typing import Optional
 
 import numpy as np
@@ -73,6 +74,7 @@ class OracleConfig:
     group_score: str = "top2_sum"   # or "max"  (parity unpinned choice)
     has_bias: bool = True
     aux_alpha: float = 0.0
+    capacity_factor: float = 0.0    # 0: no expert capacity (nothing dropped)
 
 
 # ---------------------------------------------------------------- Part 1 ---
@@ -265,36 +267,56 @@ def route(cfg: OracleConfig, scores: np.ndarray,
 
 # ---------------------------------------------------------------- Part 4 ---
 
-def dispatch(idx: np.ndarray, E: int):
+def expert_capacity(cfg: "OracleConfig") -> Optional[int]:
+    """Rows an expert may process, or None without a capacity factor.
+
+    READING: the pages name a capacity factor that "models drop/padding"
+    ("AI Infra Kernel Lab", the distributed validator) but give no formula;
+    the plainest reading is the usual one, C = ceil(cf * T * k / E)."""
+    if cfg.capacity_factor <= 0:
+        return None
+    return int(math.ceil(cfg.capacity_factor * cfg.T * cfg.k / cfg.E))
+
+
+def dispatch(idx: np.ndarray, E: int, capacity: Optional[int] = None):
     """Per-expert counts, exclusive-scan offsets and the stable slot map.
 
-    slot(t, j) = off_e + #{(t', j') before (t, j) in token order routed to e};
+    rank(t, j) = #{(t', j') before (t, j) in token order routed to e};
     READING: rows of one expert keep ascending token order (the pages' own
-    packing order is atomic and unspecified).  Returns ``counts [E]``,
-    ``offsets [E+1]``, ``src_tok [R]`` (slot -> token), ``src_j [R]`` (slot ->
-    position in the token's top-k list) and ``slot_of [T, k]``.
+    packing order is atomic and unspecified).  With a capacity C an expert
+    keeps the assignments of rank < C (the first C in token order) and drops
+    the rest (READING: drop rather than pad, no re-routing).  Returns
+    ``counts [E]`` (routed assignments, before any drop), ``offsets [E+1]``
+    (exclusive scan of the kept counts), ``src_tok`` / ``src_j`` (slot ->
+    token / position in its top-k list, kept slots only) and ``slot_of [T, k]``
+    (-1 for a dropped assignment).
     """
     T, k = idx.shape
     counts = np.zeros(E, dtype=np.int64)
     for t in range(T):
         for j in range(k):
             counts[idx[t, j]] += 1
+    kept = counts if capacity is None else np.minimum(counts, capacity)
     offsets = np.zeros(E + 1, dtype=np.int64)
     for e in range(E):
-        offsets[e + 1] = offsets[e] + counts[e]
-    R = T * k
+        offsets[e + 1] = offsets[e] + kept[e]
+    R = int(offsets[E])
     src_tok = np.empty(R, dtype=np.int64)
     src_j = np.empty(R, dtype=np.int64)
     slot_of = np.empty((T, k), dtype=np.int64)
-    cursor = offsets[:E].copy()
+    rank = np.zeros(E, dtype=np.int64)
     for t in range(T):
         for j in range(k):
             e = idx[t, j]
-            s = cursor[e]
-            cursor[e] += 1
-            src_tok[s] = t
-            src_j[s] = j
-            slot_of[t, j] = s
+            r = rank[e]
+            rank[e] += 1
+            if r < kept[e]:
+                s = offsets[e] + r
+                src_tok[s] = t
+                src_j[s] = j
+                slot_of[t, j] = s
+            else:
+                slot_of[t, j] = -1
     return counts, offsets, src_tok, src_j, slot_of
 
 
@@ -304,33 +326,39 @@ def gather_rows(x: np.ndarray, src_tok: np.ndarray) -> np.ndarray:
 
 
 def combine(ye: np.ndarray, gate: np.ndarray, slot_of: np.ndarray) -> np.ndarray:
-    """Y[t] = sum_j g_tj Ye[slot(t, j)], summed in j order."""
+    """Y[t] = sum_j g_tj Ye[slot(t, j)], summed in j order; a dropped
+    assignment (slot -1) contributes nothing (READING: the gates are not
+    renormalised over the kept experts)."""
     T, k = gate.shape
     y = np.zeros((T, ye.shape[1]), dtype=np.float64)
     for j in range(k):
-        y += gate[:, j:j + 1] * ye[slot_of[:, j]]
+        kept = slot_of[:, j] >= 0
+        y[kept] += gate[kept, j:j + 1] * ye[slot_of[kept, j]]
     return y
 
 
 def combine_backward(dy: np.ndarray, ye: np.ndarray, gate: np.ndarray,
                      slot_of: np.ndarray):
-    """dYe[slot(t,j)] = g_tj dY[t];  dg_tj = <dY[t], Ye[slot(t,j)]>."""
+    """dYe[slot(t,j)] = g_tj dY[t];  dg_tj = <dY[t], Ye[slot(t,j)]> (0 for a
+    dropped assignment)."""
     T, k = gate.shape
     dye = np.zeros_like(ye, dtype=np.float64)
     dgate = np.zeros((T, k), dtype=np.float64)
     for j in range(k):
-        rows = slot_of[:, j]
-        dye[rows] = gate[:, j:j + 1] * dy
-        dgate[:, j] = np.sum(dy * ye[rows], axis=1)
+        kept = slot_of[:, j] >= 0
+        rows = slot_of[kept, j]
+        dye[rows] = gate[kept, j:j + 1] * dy[kept]
+        dgate[kept, j] = np.sum(dy[kept] * ye[rows], axis=1)
     return dye, dgate
 
 
 def scatter_back(dxe: np.ndarray, slot_of: np.ndarray) -> np.ndarray:
-    """dX[t] = sum_j dXe[slot(t, j)] (j order)."""
+    """dX[t] = sum_j dXe[slot(t, j)] (j order, kept assignments only)."""
     T, k = slot_of.shape
     dx = np.zeros((T, dxe.shape[1]), dtype=np.float64)
     for j in range(k):
-        dx += dxe[slot_of[:, j]]
+        kept = slot_of[:, j] >= 0
+        dx[kept] += dxe[slot_of[kept, j]]
     return dx
 
 
@@ -447,7 +475,7 @@ def forward(cfg: OracleConfig, w: dict, x: np.ndarray,
     if idx is None:
         idx = route(cfg, scores, w.get("corr_bias"))
     gate = renormalize(scores, idx)      # unbiased scores, with or without a correction bias
-    counts, offsets, src_tok, src_j, slot_of = dispatch(idx, cfg.E)
+    counts, offsets, src_tok, src_j, slot_of = dispatch(idx, cfg.E, expert_capacity(cfg))
     xe = gather_rows(x, src_tok)
     R = xe.shape[0]
     ye = np.zeros((R, cfg.D), dtype=np.float64)

@@ -663,3 +663,94 @@ def test_shared_zero_down_projection_is_identity():
     np.testing.assert_array_equal(g["dx"], g0["dx"])
     a = O.silu(x @ w["ws1"].T) * (x @ w["ws3"].T)
     np.testing.assert_allclose(g["dws2"], dy.T @ a, rtol=1e-12)
+
+
+# ----------------------------------------------------- capacity / dropping ---
+# Reading of the capacity factor ("AI Infra Kernel Lab" names it as modelling
+# drop/padding): C = ceil(cf T k / E); an expert keeps its first C assignments
+# in token order, the rest contribute nothing and get no gradient.
+
+def test_capacity_formula_and_no_drop_limit():
+    cfg = O.OracleConfig(T=10, D=1, F=1, E=4, k=2, capacity_factor=1.25)
+    assert O.expert_capacity(cfg) == 7                      # ceil(1.25 * 20 / 4) = ceil(6.25)
+    assert O.expert_capacity(O.OracleConfig(T=10, D=1, F=1, E=4, k=2)) is None
+    rng = np.random.default_rng(51)
+    idx = np.stack([rng.permutation(6)[:3] for _ in range(40)]).astype(np.int32)
+    plain = O.dispatch(idx, 6)
+    big = O.dispatch(idx, 6, capacity=int(plain[0].max()))  # nothing above the cap
+    for a, b in zip(plain, big):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_capacity_dispatch_brute_force():
+    rng = np.random.default_rng(52)
+    T, E, k, C = 30, 5, 2, 4
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts, offsets, src_tok, src_j, slot_of = O.dispatch(idx, E, capacity=C)
+    for e in range(E):
+        order = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        assert counts[e] == len(order)
+        kept = order[:C]
+        assert offsets[e + 1] - offsets[e] == len(kept)
+        for r, (t, j) in enumerate(kept):
+            s = offsets[e] + r
+            assert slot_of[t, j] == s and src_tok[s] == t and src_j[s] == j
+        for (t, j) in order[C:]:
+            assert slot_of[t, j] == -1
+    assert len(src_tok) == offsets[E] == sum(min(c, C) for c in counts)
+
+
+def _capacity_case(seed):
+    cfg = O.OracleConfig(T=12, D=4, F=6, E=4, k=2, act="gelu_tanh", score="softmax",
+                         has_bias=True, aux_alpha=0.05, capacity_factor=0.5)
+    for s in range(seed, seed + 400):
+        w, x, tgt = _weights(cfg, s, scale=1.5)
+        if _margin_ok(cfg, w, x):
+            st = O.forward(cfg, w, x)
+            if np.any(st["slot_of"] < 0) and np.any(np.all(st["slot_of"] < 0, axis=1)):
+                return cfg, w, x, tgt, st
+    raise RuntimeError("no input with drops found")
+
+
+def test_capacity_forward_by_hand_and_zero_gate_gradients():
+    cfg, w, x, tgt, st = _capacity_case(1100)
+    assert O.expert_capacity(cfg) == 3
+    for t in range(cfg.T):
+        y = np.zeros(cfg.D)
+        for j in range(cfg.k):
+            if st["slot_of"][t, j] < 0:
+                continue
+            e = st["idx"][t, j]
+            h = x[t] @ w["w1"][e].T + w["b1"][e]
+            a = 0.5 * h * (1 + np.tanh(math.sqrt(2 / math.pi) * (h + 0.044715 * h ** 3)))
+            y += st["gate"][t, j] * (a @ w["w2"][e].T + w["b2"][e])
+        if np.all(st["slot_of"][t] < 0):
+            assert not np.any(st["y"][t])                   # fully dropped: exactly 0
+        np.testing.assert_allclose(st["y"][t], y, rtol=1e-12, atol=1e-15)
+    _, _, dy = O.losses(cfg, st, tgt)
+    g = O.backward(cfg, w, x, st, dy)
+    assert np.all(g["dgate"][st["slot_of"] < 0] == 0)
+    # the aux loss counts the router's assignments before any drop
+    aux, f, _ = O.aux_loss(st["counts"], st["scores"], cfg.k)
+    assert st["counts"].sum() == cfg.T * cfg.k and st["offsets"][-1] < cfg.T * cfg.k
+
+
+def test_capacity_gradients_central_differences():
+    cfg, w, x, tgt, st = _capacity_case(1200)
+    _, _, dy = O.losses(cfg, st, tgt)
+    g = O.backward(cfg, w, x, st, dy)
+    h = 1e-6
+    for key in ("w_gate", "w1", "b2"):
+        fd = np.zeros_like(w[key])
+        for i in np.ndindex(w[key].shape):
+            wp = dict(w); wp[key] = w[key].copy(); wp[key][i] += h
+            wm = dict(w); wm[key] = w[key].copy(); wm[key][i] -= h
+            fd[i] = (O.total_loss(cfg, wp, x, tgt) - O.total_loss(cfg, wm, x, tgt)) / (2 * h)
+        err = np.max(np.abs(fd - g["d" + key])) / np.max(np.abs(fd))
+        assert err <= 1e-6, (key, err)
+    fd = np.zeros_like(x)
+    for i in np.ndindex(x.shape):
+        xp = x.copy(); xp[i] += h
+        xm = x.copy(); xm[i] -= h
+        fd[i] = (O.total_loss(cfg, w, xp, tgt) - O.total_loss(cfg, w, xm, tgt)) / (2 * h)
+    assert np.max(np.abs(fd - g["dx"])) / np.max(np.abs(fd)) <= 1e-6
