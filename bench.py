@@ -205,7 +205,7 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
                      score=wl.score, n_groups=n_groups, topk_groups=topk_groups,
                      has_bias=wl.has_bias, dtype=wl.dtype, aux_alpha=wl.aux_alpha, lr=wl.lr,
                      router_init=wl.router_init, corr_bias_scale=wl.corr_bias_scale,
-                     n_shared=wl.n_shared)
+                     n_shared=wl.n_shared, capacity_factor=wl.capacity_factor)
     inp = W.make_inputs(sub, seed=seed)
     f64 = lambda t: None if t is None else t.detach().double().numpy()  # noqa: E731
     lp = wl.dtype == "bf16"
@@ -222,7 +222,7 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
     tgt = f64(inp["target"])
     cfg = O.OracleConfig(T=T_s, D=wl.D, F=wl.F, E=E_s, k=wl.k, act=wl.act, score=wl.score,
                          n_groups=n_groups, topk_groups=topk_groups, has_bias=wl.has_bias,
-                         aux_alpha=wl.aux_alpha)
+                         aux_alpha=wl.aux_alpha, capacity_factor=wl.capacity_factor)
     t0 = time.perf_counter()
     O.train_step(cfg, w, x, tgt, wl.lr)
     dt = time.perf_counter() - t0
@@ -278,6 +278,7 @@ def workload_config(wl: W.Workload) -> dict:
             "topk_groups": wl.topk_groups, "expert_dtype": wl.dtype, "aux_alpha": wl.aux_alpha,
             "lr": wl.lr, "global_batch": wl.T, "parallelism": "replicas",
             "n_shared": wl.n_shared, "corr_bias": wl.corr_bias_scale is not None,
+            "capacity_factor": wl.capacity_factor,
             "l2": "inputs larger than L2 (weights and expert-major activations >> 129 MB)"}
 
 
@@ -332,7 +333,7 @@ def main():
                      w1_lp=inp.get("w1_bf16"), w3_lp=inp.get("w3_bf16"),
                      w2_lp=inp.get("w2_bf16"), device=str(dev), corr_bias=inp.get("corr_bias"),
                      n_shared=wl.n_shared, ws1=inp.get("ws1"), ws3=inp.get("ws3"),
-                     ws2=inp.get("ws2"))
+                     ws2=inp.get("ws2"), capacity_factor=wl.capacity_factor)
     x = (inp["x_bf16"] if lp else inp["x"]).contiguous()
     tgt = inp["target"].contiguous()
     dx = torch.empty(wl.T, wl.D, device=dev)

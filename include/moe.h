@@ -90,6 +90,13 @@ typedef struct {
                          branch of hidden width n * F that every token passes
                          through, added to the output without a gate ("AI
                          Infra Kernel Lab").  Requires SwiGLU and MOE_BF16.  */
+  float capacity_factor; /* 0: no expert capacity.  cf > 0: each expert keeps
+                         its first C = ceil(cf * T * k / E) assignments in token
+                         order and drops the rest (no output, zero gate
+                         gradient, gates not renormalised); moe_get_routing then
+                         reports slot_of = -1 for a dropped assignment, counts
+                         before the drop (they also feed the aux loss) and
+                         offsets over the kept rows.                          */
 } moe_config;
 
 /* Read-only weights for moe_forward / moe_backward. */

@@ -37,7 +37,7 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", c_int32), ("D", c_int32), ("F", c_int32), ("E", c_int32), ("k", c_int32),
                 ("n_groups", c_int32), ("topk_groups", c_int32), ("group_score", c_int32),
                 ("act", c_int32), ("score", c_int32), ("dtype", c_int32), ("has_bias", c_int32),
-                ("aux_alpha", c_float), ("n_shared", c_int32)]
+                ("aux_alpha", c_float), ("n_shared", c_int32), ("capacity_factor", c_float)]
 
 
 class moe_weights(ctypes.Structure):
@@ -139,10 +139,10 @@ def _check(fn: str, status: int):
 
 def make_config(T, D, F, E, k, act="relu", score="softmax", n_groups=1, topk_groups=1,
                 group_score="top2_sum", dtype="f32", has_bias=True, aux_alpha=0.0,
-                n_shared=0) -> moe_config:
+                n_shared=0, capacity_factor=0.0) -> moe_config:
     return moe_config(T, D, F, E, k, n_groups, topk_groups, GROUP_SCORE[group_score], ACT[act],
                       SCORE[score], DTYPE[dtype], int(bool(has_bias)), float(aux_alpha),
-                      int(n_shared))
+                      int(n_shared), float(capacity_factor))
 
 
 def make_weights(w_gate, w1, w2, w3=None, b1=None, b2=None, logit_bias=None,

@@ -27,10 +27,12 @@ route_count_kernel(const int* __restrict__ idx, long long R, int E, int* __restr
     chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
 }
 
-// counts[e] = sum over chunks; offsets = exclusive scan of counts (offsets[E] = R);
-// chunk_counts[c][e] becomes the first slot of chunk c's rows for expert e.
+// counts[e] = sum over chunks (the routed assignments); with an expert
+// capacity `cap` an expert keeps min(counts[e], cap) rows; offsets = exclusive
+// scan of the kept counts; chunk_counts[c][e] becomes the rank of chunk c's
+// first assignment to expert e among all of e's assignments (token order).
 __global__ void __launch_bounds__(256)
-route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int* __restrict__ counts,
+route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int cap, int* __restrict__ counts,
                   int* __restrict__ offsets) {
   __shared__ int tot[256];
   __shared__ int scan[257];
@@ -40,7 +42,7 @@ route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int* __restrict__ co
 #pragma unroll 8
     for (int c = 0; c < nchunks; ++c) total += cc[(size_t)c * E + e];
   }
-  tot[e] = (e < E) ? total : 0;
+  tot[e] = (e < E) ? min(total, cap) : 0;
   __syncthreads();
   if (threadIdx.x == 0) {
     int run = 0;
@@ -51,7 +53,7 @@ route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int* __restrict__ co
   if (e < E) {
     counts[e] = total;
     offsets[e] = scan[e];
-    int run = scan[e];
+    int run = 0;
     for (int c = 0; c < nchunks; ++c) {
       int v = cc[(size_t)c * E + e];
       cc[(size_t)c * E + e] = run;
@@ -63,13 +65,18 @@ route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int* __restrict__ co
 
 // Stable scatter: one warp walks its chunk in token order; lanes holding the
 // same expert are ranked by lane id (match_any), so slots keep token order.
+// An assignment of rank >= cap within its expert is dropped (slot -1).
 __global__ void __launch_bounds__(32)
-route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E,
-                     const int* __restrict__ chunk_base, int* __restrict__ src_tok,
-                     int* __restrict__ slot_of) {
+route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E, int cap,
+                     const int* __restrict__ chunk_base, const int* __restrict__ offsets,
+                     int* __restrict__ src_tok, int* __restrict__ slot_of) {
   __shared__ int cursor[256];
+  __shared__ int off[256];
   const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[(size_t)blockIdx.x * E + e];
+  for (int e = lane; e < E; e += 32) {
+    cursor[e] = chunk_base[(size_t)blockIdx.x * E + e];
+    off[e] = offsets[e];
+  }
   __syncwarp();
   const long long lo = (long long)blockIdx.x * ROUTE_CHUNK;
   const long long hi = min(lo + ROUTE_CHUNK, R);
@@ -81,10 +88,13 @@ route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E,
     if ((unsigned)e >= (unsigned)E) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
-    int slot = 0;
     if (e >= 0) {
-      slot = cursor[e] + rank;
-      src_tok[slot] = (int)(f / k);
+      const int r = cursor[e] + rank;
+      int slot = -1;
+      if (r < cap) {
+        slot = off[e] + r;
+        src_tok[slot] = (int)(f / k);
+      }
       slot_of[f] = slot;
     }
     __syncwarp();
@@ -110,13 +120,15 @@ gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, 
     for (; v + 96 < nv; v += 128) {
       const uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
       for (int j = 0; j < k; ++j) {
+        if (so[j] < 0) continue;   // dropped by the expert capacity
         uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)so[j] * D);
         dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
       }
     }
     for (; v < nv; v += 32) {
       const uint4 a = src[v];
-      for (int j = 0; j < k; ++j) reinterpret_cast<uint4*>(xe + (size_t)so[j] * D)[v] = a;
+      for (int j = 0; j < k; ++j)
+        if (so[j] >= 0) reinterpret_cast<uint4*>(xe + (size_t)so[j] * D)[v] = a;
     }
   }
 }
@@ -148,6 +160,7 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
       for (int j = 0; j < k; ++j) {
         const int s = slot_of[(size_t)t * k + j];
+        if (s < 0) continue;   // dropped by the expert capacity: no output
         const float g = gate[(size_t)t * k + j];
         Vec<T> v;
         v.load(ye + (size_t)s * D + d);
@@ -232,13 +245,13 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       Vec<T> v[MAXK];
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
-        if (j < k) v[j].load(ye + (size_t)slot[j] * D + d);
+        if (j < k && slot[j] >= 0) v[j].load(ye + (size_t)slot[j] * D + d);
       float acc[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
-        if (j < k) {
+        if (j < k && slot[j] >= 0) {
 #pragma unroll
           for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], v[j].get(i), acc[i]);
         }
@@ -270,7 +283,7 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       }
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
-        if (j < k) {
+        if (j < k && slot[j] >= 0) {   // a dropped assignment keeps dg = 0
           Vec<T> o;
 #pragma unroll
           for (int i = 0; i < VN; ++i) {
@@ -364,7 +377,7 @@ combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
     }
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
-      if (j < k) {
+      if (j < k && slot[j] >= 0) {   // dropped by the expert capacity: dg = 0
         Vec<T> v, o;
         v.load(ye + (size_t)slot[j] * D + d);
 #pragma unroll
@@ -405,8 +418,10 @@ scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
       acc[i] = q.x; acc[i + 1] = q.y; acc[i + 2] = q.z; acc[i + 3] = q.w;
     }
     for (int j = 0; j < k; ++j) {
+      const int s = slot_of[(size_t)t * k + j];
+      if (s < 0) continue;   // dropped by the expert capacity
       Vec<T> v;
-      v.load(dxe + (size_t)slot_of[(size_t)t * k + j] * D + d);
+      v.load(dxe + (size_t)s * D + d);
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] += v.get(i);
     }
@@ -498,17 +513,19 @@ cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_co
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int* counts, int* offsets,
-                              cudaStream_t st) {
-  route_scan_kernel<<<1, 256, 0, st>>>(chunk_counts, nchunks, E, counts, offsets);
+cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int cap, int* counts,
+                              int* offsets, cudaStream_t st) {
+  route_scan_kernel<<<1, 256, 0, st>>>(chunk_counts, nchunks, E, cap, counts, offsets);
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, const int* chunk_base,
-                                 int* src_tok, int* slot_of, cudaStream_t st) {
+cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, int cap,
+                                 const int* chunk_base, const int* offsets, int* src_tok,
+                                 int* slot_of, cudaStream_t st) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
-  route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, k, E, chunk_base, src_tok, slot_of);
+  route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, k, E, cap, chunk_base, offsets, src_tok,
+                                          slot_of);
   return cudaGetLastError();
 }
 

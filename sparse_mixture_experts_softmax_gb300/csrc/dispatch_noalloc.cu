@@ -81,9 +81,11 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int nchunks = moe::route_chunks(R);
   if (moe::launch_route_count(idx, R, c.E, scratch, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_route_scan(scratch, nchunks, c.E, counts, offsets, s) != cudaSuccess)
+  const int cap = moe::expert_capacity_rows(c.capacity_factor, c.T, c.k, c.E);
+  if (moe::launch_route_scan(scratch, nchunks, c.E, cap, counts, offsets, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (moe::launch_route_scatter(idx, R, c.k, c.E, scratch, src_tok, slot_of, s) != cudaSuccess)
+  if (moe::launch_route_scatter(idx, R, c.k, c.E, cap, scratch, offsets, src_tok, slot_of, s) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
           float s = v;
           for (int jj = 0; jj < g.k; ++jj) {
             const int slot = g.slot_of[(size_t)r * g.k + jj];
+            if (slot < 0) continue;   // dropped by the expert capacity
             s += ld_rt(g.src, (size_t)slot * g.N + c, g.src_type);
           }
           static_cast<float*>(g.C)[ci] = s;

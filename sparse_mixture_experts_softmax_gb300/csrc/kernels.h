@@ -1,6 +1,7 @@
 // Host-side launchers of the MoE kernels (internal to the library).
 #pragma once
 
+#include <cmath>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -32,11 +33,21 @@ constexpr int ROUTE_CHUNK = 1024;   // routed assignments per scatter chunk
 int route_chunks(long long R);
 cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
                                cudaStream_t st);
-cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int* counts, int* offsets,
-                              cudaStream_t st);
-cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E,
-                                 const int* chunk_base, int* src_tok, int* slot_of,
-                                 cudaStream_t st);
+// Rows an expert may keep under a capacity factor cf > 0: ceil(cf * T * k / E)
+// (computed in double), else INT_MAX (no limit).
+inline int expert_capacity_rows(float cf, int T, int k, int E) {
+  if (!(cf > 0.f)) return 0x7fffffff;
+  const double c = std::ceil((double)cf * (double)T * (double)k / (double)E);
+  return c >= 2147483647.0 ? 0x7fffffff : (int)c;
+}
+// cap: rows an expert may keep (an expert capacity), INT_MAX for no limit;
+// counts stay the routed (pre-drop) counts, offsets scan the kept counts and a
+// dropped assignment gets slot_of = -1.
+cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int cap, int* counts,
+                              int* offsets, cudaStream_t st);
+cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, int cap,
+                                 const int* chunk_base, const int* offsets, int* src_tok,
+                                 int* slot_of, cudaStream_t st);
 cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, int k, int D,
                           void* xe, cudaStream_t st);
 int combine_blocks(int T);

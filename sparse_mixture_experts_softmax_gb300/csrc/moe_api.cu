@@ -140,6 +140,7 @@ moe_status validate_config(const moe_config* c) {
   if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if ((long long)c->T * c->D >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
   if (c->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (!(c->capacity_factor >= 0.f) || c->capacity_factor > 1e6f) return MOE_ERR_INVALID_ARG;
   if (c->n_shared > 0 && (c->act != MOE_ACT_SWIGLU || c->dtype != MOE_BF16 ||
                           (long long)c->n_shared * c->F > (1LL << 20)))
     return MOE_ERR_UNSUPPORTED;
@@ -265,10 +266,14 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
                                        P.at<int>(L.idx), P.at<float>(L.gate), P.at<float>(L.psum), st));
   }
   KL("route_count", launch_route_count(P.at<int>(L.idx), R, c.E, P.at<int>(L.chunk), st));
-  KL("route_scan", launch_route_scan(P.at<int>(L.chunk), route_chunks(R), c.E, P.at<int>(L.counts),
-                       P.at<int>(L.offsets), st));
-  KL("route_scatter", launch_route_scatter(P.at<int>(L.idx), R, c.k, c.E, P.at<int>(L.chunk),
-                          P.at<int>(L.src_tok), P.at<int>(L.slot_of), st));
+  // with a capacity factor each expert keeps its first `cap` assignments in
+  // token order; dropped ones get slot -1 and are skipped downstream
+  const int cap = expert_capacity_rows(c.capacity_factor, c.T, c.k, c.E);
+  KL("route_scan", launch_route_scan(P.at<int>(L.chunk), route_chunks(R), c.E, cap,
+                                     P.at<int>(L.counts), P.at<int>(L.offsets), st));
+  KL("route_scatter", launch_route_scatter(P.at<int>(L.idx), R, c.k, c.E, cap, P.at<int>(L.chunk),
+                                           P.at<int>(L.offsets), P.at<int>(L.src_tok),
+                                           P.at<int>(L.slot_of), st));
   KL("gather", launch_gather(c.dtype, x, P.at<int>(L.slot_of), c.T, c.k, c.D, P.at<void>(L.xe), st));
 
   // expert up-projection (+ activation)

@@ -18,12 +18,13 @@ class MoELayer:
     def __init__(self, T, D, F, E, k, act, score, dtype, has_bias, aux_alpha, w_gate, w1, w2,
                  w3=None, b1=None, b2=None, logit_bias=None, n_groups=1, topk_groups=1,
                  group_score="top2_sum", w1_lp=None, w3_lp=None, w2_lp=None, device="cuda",
-                 corr_bias=None, n_shared=0, ws1=None, ws3=None, ws2=None):
+                 corr_bias=None, n_shared=0, ws1=None, ws3=None, ws2=None, capacity_factor=0.0):
         self.device = torch.device(device)
         self.dtype = dtype
         self.cfg = B.make_config(T, D, F, E, k, act=act, score=score, n_groups=n_groups,
                                  topk_groups=topk_groups, group_score=group_score, dtype=dtype,
-                                 has_bias=has_bias, aux_alpha=aux_alpha, n_shared=n_shared)
+                                 has_bias=has_bias, aux_alpha=aux_alpha, n_shared=n_shared,
+                                 capacity_factor=capacity_factor)
         dev = self.device
 
         def f32(t):

@@ -24,7 +24,7 @@ def oracle_config(wl: W.Workload, group_score="top2_sum") -> O.OracleConfig:
     return O.OracleConfig(T=wl.T, D=wl.D, F=wl.F, E=wl.E, k=wl.k, act=wl.act, score=wl.score,
                           n_groups=wl.n_groups, topk_groups=wl.topk_groups,
                           group_score=group_score, has_bias=wl.has_bias,
-                          aux_alpha=wl.aux_alpha)
+                          aux_alpha=wl.aux_alpha, capacity_factor=wl.capacity_factor)
 
 
 def np64(t):
@@ -64,7 +64,7 @@ def make_layer(wl: W.Workload, inp: dict, device="cuda", group_score="top2_sum")
                     w3_lp=inp.get("w3_bf16") if lp else None,
                     w2_lp=inp.get("w2_bf16") if lp else None, device=device,
                     corr_bias=inp.get("corr_bias"), n_shared=wl.n_shared, ws1=inp.get("ws1"),
-                    ws3=inp.get("ws3"), ws2=inp.get("ws2"))
+                    ws3=inp.get("ws3"), ws2=inp.get("ws2"), capacity_factor=wl.capacity_factor)
 
 
 def device_x(wl: W.Workload, inp: dict, device="cuda"):
@@ -97,10 +97,10 @@ def check_routing_exact(cfg: O.OracleConfig, r: dict, corr_bias=None):
     cb = None if corr_bias is None else corr_bias.detach().float().cpu().numpy()
     idx_o = O.route(cfg, scores, cb)
     np.testing.assert_array_equal(idx_gpu, idx_o)
-    counts, offsets, src_tok, _, slot_of = O.dispatch(idx_gpu, cfg.E)
+    counts, offsets, src_tok, _, slot_of = O.dispatch(idx_gpu, cfg.E, O.expert_capacity(cfg))
     np.testing.assert_array_equal(r["counts"].cpu().numpy(), counts)
     np.testing.assert_array_equal(r["offsets"].cpu().numpy(), offsets)
-    R = cfg.T * cfg.k
+    R = int(offsets[-1])   # kept rows (all T k of them without a capacity)
     np.testing.assert_array_equal(r["src_tok"].cpu().numpy()[:R], src_tok)
     np.testing.assert_array_equal(r["slot_of"].cpu().numpy(), slot_of)
     # gates: renormalised selected scores, in the kernel's fp32

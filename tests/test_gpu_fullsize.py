@@ -68,10 +68,13 @@ def _rows_forward(cfg, w, x64, pairs):
     return out
 
 
-def _tokens_y(cfg, w, x64, scores64, idx, tokens):
+def _tokens_y(cfg, w, x64, scores64, idx, tokens, kept=None):
     """y[t] for the given tokens (oracle gates from its own scores), with the
-    shared-expert branch when the layer has one."""
-    pairs = [(t, idx[t, j]) for t in tokens for j in range(cfg.k)]
+    shared-expert branch when the layer has one; ``kept[t, j]`` False marks an
+    assignment dropped by the expert capacity (no output)."""
+    if kept is None:
+        kept = np.ones(idx.shape, dtype=bool)
+    pairs = [(t, idx[t, j]) for t in tokens for j in range(cfg.k) if kept[t, j]]
     fw = _rows_forward(cfg, w, x64, pairs)
     gate = O.renormalize(scores64[tokens], idx[tokens])
     sh = O.shared_forward(x64[tokens], w) if w.get("ws1") is not None else None
@@ -79,7 +82,8 @@ def _tokens_y(cfg, w, x64, scores64, idx, tokens):
     for i, t in enumerate(tokens):
         y = np.zeros(cfg.D)
         for j in range(cfg.k):
-            y = y + gate[i, j] * fw[(t, int(idx[t, j]))]["ye"][0]
+            if kept[t, j]:
+                y = y + gate[i, j] * fw[(t, int(idx[t, j]))]["ye"][0]
         if sh is not None:
             y = y + sh["ys"][i]
         ys[t] = y
@@ -105,7 +109,8 @@ def _run_full(name):
 
 
 @pytest.mark.parametrize("name,n_sample", [("grouped", 8), ("skewed", 6), ("large", 4),
-                                           ("grouped_cb", 8), ("grouped_shared", 8)])
+                                           ("grouped_cb", 8), ("grouped_shared", 8),
+                                           ("skewed_cap", 12)])
 def test_full_size_layer(name, n_sample):
     wl, inp, cfg, layer, y, dx, r = _run_full(name)
     T, D, E, k = wl.T, wl.D, wl.E, wl.k
@@ -115,6 +120,7 @@ def test_full_size_layer(name, n_sample):
     counts = r["counts"].cpu().numpy().astype(np.int64)
     offsets = r["offsets"].cpu().numpy()
     src_tok = r["src_tok"].cpu().numpy()
+    kept = r["slot_of"].cpu().numpy() >= 0     # checked against the oracle's dispatch above
     # 2. scores and aux against the oracle's fp64 router on all tokens
     lb = np64(inp["logit_bias"])
     w = _oracle_weights(inp, lb)
@@ -134,7 +140,7 @@ def test_full_size_layer(name, n_sample):
     idx_v = validated_routing(cfg, scores64[tokens], idx[tokens], corr_bias=cb64)
     idx_s = idx.copy()
     idx_s[tokens] = idx_v
-    ys, fw, gate = _tokens_y(cfg, w, x64, scores64, idx_s, tokens)
+    ys, fw, gate = _tokens_y(cfg, w, x64, scores64, idx_s, tokens, kept)
     t64 = inp["target"][tokens].double().cpu().numpy()
     aux_row = cfg.aux_alpha * O.aux_loss_score_grad(counts / float(T * k), T)
     for i, t in enumerate(tokens):
@@ -143,6 +149,8 @@ def test_full_size_layer(name, n_sample):
         dxt = np.zeros(D)
         dgate = np.zeros(k)
         for j in range(k):
+            if not kept[t, j]:
+                continue
             e = int(idx_s[t, j])
             fe = fw[(t, e)]
             be = O.expert_backward(cfg, e, x64[t:t + 1], fe, (gate[i, j] * dy)[None], w)
@@ -170,15 +178,16 @@ def test_full_size_layer(name, n_sample):
         assert torch.all(layer.dw3[e] == 0)
     # 6. weight gradients and SGD step of the smallest, median and largest
     #    non-empty experts, each when the oracle can afford all its tokens
-    nonzero = np.nonzero(counts)[0]
-    order = nonzero[np.argsort(counts[nonzero], kind="stable")]
+    rows_kept = np.diff(offsets)              # rows each expert processed (after any drop)
+    nonzero = np.nonzero(rows_kept)[0]
+    order = nonzero[np.argsort(rows_kept[nonzero], kind="stable")]
     picks = []
     for e_sel in (order[0], order[len(order) // 2], order[-1]):
         if int(e_sel) not in picks:
             picks.append(int(e_sel))
     report = []
     for e_min in picks:
-        n_rows = int(counts[e_min])
+        n_rows = int(rows_kept[e_min])
         checked_dw = n_rows * k * 6 * D * wl.F <= 4e11
         report.append(f"expert {e_min} ({n_rows} rows) {'checked' if checked_dw else 'skipped'}")
         if not checked_dw:
@@ -187,11 +196,12 @@ def test_full_size_layer(name, n_sample):
         idx_v = validated_routing(cfg, scores64[rows_tok], idx[rows_tok], corr_bias=cb64)
         idx_m = idx.copy()
         idx_m[rows_tok] = idx_v
-        ys_m, fw_m, gate_m = _tokens_y(cfg, w, x64, scores64, idx_m, rows_tok)
+        ys_m, fw_m, gate_m = _tokens_y(cfg, w, x64, scores64, idx_m, rows_tok, kept)
         t_rows = inp["target"][rows_tok].double().cpu().numpy()
         dye = np.zeros((n_rows, D))
         for i, t in enumerate(rows_tok):
             j = int(np.nonzero(idx_m[t] == e_min)[0][0])
+            assert kept[t, j]
             dye[i] = gate_m[i, j] * 2.0 * (ys_m[t] - t_rows[i]) / float(T * D)
         xe = x64[rows_tok]
         fe = O.expert_forward(cfg, e_min, xe, w)

@@ -185,6 +185,20 @@ def test_shared_experts_forward_backward_entry_points():
     assert_close("dx", np64(dx), g["dx"], 2e-2)
 
 
+@pytest.mark.parametrize("name,T", [("dense_f32_cap", 4096), ("skewed_cap", 1536)])
+def test_capacity_factor_step(name, T):
+    """Expert capacity: each expert keeps its first C assignments in token
+    order; dropped ones contribute nothing and their gates get zero gradient.
+    Checks that drops occur, then full one-step parity."""
+    wl = W.WORKLOADS[name].with_tokens(T)
+    errs, layer, inp = _one_step_parity(wl)
+    assert max(errs.values()) <= TOL[wl.dtype]
+    r = layer.routing()
+    dropped = int((r["slot_of"] < 0).sum().item())
+    kept_rows = int(r["offsets"][-1].item())
+    assert dropped > 0 and kept_rows + dropped == wl.T * wl.k
+
+
 def _assert_bias_changes_routing(wl, inp, layer):
     """The bias must matter for this input: the oracle's routing of the GPU's
     scores without the bias differs on a good share of tokens."""

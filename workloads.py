@@ -59,6 +59,7 @@ class Workload:
     zipf_empty: int = 0                # experts that get a -inf logit bias (never selected)
     corr_bias_scale: Optional[float] = None  # selection-only correction bias ~ U(-s, s)
     n_shared: int = 0                  # shared-expert SwiGLU branch of width n_shared * F
+    capacity_factor: float = 0.0       # expert capacity ceil(cf T k / E); 0 = none
 
     @property
     def R(self) -> int:
@@ -100,6 +101,15 @@ WORKLOADS = {
                              score="softmax", n_groups=1, topk_groups=1, has_bias=False,
                              dtype="bf16", aux_alpha=0.01, lr=1e-3, router_init="uniform",
                              n_shared=1),
+    # expert capacity (token dropping); factors exact in float32
+    "skewed_cap": Workload("skewed_cap", T=32768, D=2048, F=1408, E=64, k=8, act="swiglu",
+                           score="softmax", n_groups=1, topk_groups=1, has_bias=False,
+                           dtype="bf16", aux_alpha=0.01, lr=1e-3, zipf_skew=1.2, zipf_empty=4,
+                           capacity_factor=1.25),
+    "dense_f32_cap": Workload("dense_f32_cap", T=4096, D=512, F=1024, E=8, k=2,
+                              act="gelu_tanh", score="softmax", n_groups=1, topk_groups=1,
+                              has_bias=True, dtype="f32", aux_alpha=0.01, lr=0.01,
+                              capacity_factor=0.75),
     "dense_f32_cb": Workload("dense_f32_cb", T=4096, D=512, F=1024, E=8, k=2, act="gelu_tanh",
                              score="softmax", n_groups=1, topk_groups=1, has_bias=True,
                              dtype="f32", aux_alpha=0.01, lr=0.01, corr_bias_scale=0.05),
