@@ -211,6 +211,21 @@ MOE_API moe_status moe_train_step_host(const moe_config* cfg, const moe_params* 
                                void* staging, size_t staging_bytes,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* n_steps training steps from HOST batches, pipelined for a data loader:
+ * while step i runs on `stream`, the inputs of step i+1 are copied on an
+ * internal side stream into the other half of `staging` (two input slots:
+ * 2 * moe_host_staging_size(cfg) bytes).  x_hosts[i] -> [T,D] in cfg.dtype and
+ * y_target_hosts[i] -> [T,D] fp32 are step i's batch (the same pointer may
+ * repeat); the losses of step i land in loss_host[2 i], loss_host[2 i + 1].
+ * Every step is exactly moe_train_step on its batch, in order.  Returns after
+ * the last step's losses have been copied back.  Host batches should be
+ * pinned and must stay valid until the call returns. */
+MOE_API moe_status moe_train_steps_host(const moe_config* cfg, const moe_params* p,
+                                        int32_t n_steps, const void* const* x_hosts,
+                                        const float* const* y_target_hosts, float lr,
+                                        float* loss_host, void* staging, size_t staging_bytes,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Copies the routing the last forward left in `workspace` into caller buffers
  * (device, any may be NULL): scores [T,E] fp32, idx [T,k], gate [T,k] fp32,
  * counts [E], offsets [E+1], src_tok [R] (slot -> token), slot_of [T,k]

@@ -88,6 +88,9 @@ def lib() -> ctypes.CDLL:
         L.moe_train_step_host.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p,
                                           c_float, c_void_p, c_void_p, c_size_t, c_void_p,
                                           c_size_t, c_void_p]
+        L.moe_train_steps_host.argtypes = [P(moe_config), P(moe_params), c_int32, c_void_p,
+                                           c_void_p, c_float, c_void_p, c_void_p, c_size_t,
+                                           c_void_p, c_size_t, c_void_p]
         L.moe_get_routing.argtypes = [P(moe_config), c_void_p, c_size_t] + [c_void_p] * 8
         L.moe_get_intermediates.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
                                             c_void_p, c_void_p]
@@ -109,6 +112,7 @@ def lib() -> ctypes.CDLL:
         L.moe_selftest_wait_timeout.argtypes = [c_int32] * 5 + [c_void_p] * 5 + [ctypes.c_int64,
                                                                                 c_void_p]
         for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
+                   "moe_train_steps_host",
                    "moe_get_routing", "moe_get_intermediates", "moe_dispatch_noalloc",
                    "moe_device_status", "moe_grouped_gemm", "moe_selftest_wait_timeout"):
             getattr(L, fn).restype = c_int32
@@ -201,6 +205,22 @@ def moe_train_step_host(cfg, params, x_host, y_target_host, lr, loss_host, stagi
                                      _ptr(y_target_host), float(lr), _ptr(loss_host),
                                      _ptr(staging), staging.numel(), _ptr(workspace),
                                      workspace.numel(), _stream(stream)))
+
+
+def moe_train_steps_host(cfg, params, x_hosts, y_target_hosts, lr, loss_host, staging, workspace,
+                         stream=None):
+    """Pipelined steps over host batches (lists of CPU tensors, pinned for full
+    speed); loss_host is a CPU float32 tensor of 2 * len(x_hosts) values and
+    staging a device buffer of 2 * moe_host_staging_size(cfg) bytes."""
+    n = len(x_hosts)
+    if len(y_target_hosts) != n:
+        raise ValueError("one target batch per input batch")
+    xs = (c_void_p * max(n, 1))(*[_ptr(t) for t in x_hosts])
+    ts = (c_void_p * max(n, 1))(*[_ptr(t) for t in y_target_hosts])
+    _check("moe_train_steps_host",
+           lib().moe_train_steps_host(ctypes.byref(cfg), ctypes.byref(params), int(n), xs, ts,
+                                      float(lr), _ptr(loss_host), _ptr(staging), staging.numel(),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def moe_get_routing(cfg, workspace, scores=None, idx=None, gate=None, counts=None, offsets=None,

@@ -227,8 +227,11 @@ cudaError_t run_gemm(const moe_config& c, const GemmArgs& g, cudaStream_t st) {
 
 // Forward: router -> dispatch -> experts -> combine.  With a target, combine
 // also forms dY and the squared-error partials, and the losses are finalised.
+// target_ready: recorded when `target` has landed (its copy may still be in
+// flight on another stream while the router and experts run), or nullptr.
 moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, float* y,
-                       const float* target, float* d_loss, const Ptrs& P, cudaStream_t st) {
+                       const float* target, float* d_loss, const Ptrs& P, cudaStream_t st,
+                       cudaEvent_t target_ready = nullptr) {
   const Layout& L = *P.L;
   const long long R = (long long)c.T * c.k;
   const RouterArgs ra = router_args(c, w.corr_bias);
@@ -385,6 +388,7 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   const void* ys = shared ? P.at<void>(L.ys) : nullptr;
 
   const bool train = target != nullptr;
+  if (target_ready != nullptr) CK(cudaStreamWaitEvent(st, target_ready, 0));
   if (train && y == nullptr && c.k <= 8) {
     // training step: the combine backward runs in the same pass (dYe, dgate)
     KL("combine_fused", launch_combine_train(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate),
@@ -814,7 +818,8 @@ moe_status zero_grads(const moe_config& c, const moe_grads& g, cudaStream_t st) 
 
 moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const void* x,
                            const float* y_target, float lr, float* d_loss, float* dx,
-                           void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                           void* workspace, size_t workspace_bytes, cudaStream_t st,
+                           cudaEvent_t target_ready = nullptr) {
   RET_IF(validate_config(cfg));
   const moe_config& c = *cfg;
   if (p == nullptr) return MOE_ERR_INVALID_ARG;
@@ -854,7 +859,7 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   w.ws1 = p->ws1_lp;   // the shared branch exists only for bf16 layers
   w.ws3 = p->ws3_lp;
   w.ws2 = p->ws2_lp;
-  RET_IF(run_forward(c, w, x, nullptr, y_target, d_loss, P, st));
+  RET_IF(run_forward(c, w, x, nullptr, y_target, d_loss, P, st, target_ready));
   float* dxp = dx ? dx : P.at<float>(L.dx);
   // bf16 layers: the expert weights' SGD runs inside the dW GEMM epilogues
   const bool fused = c.dtype == MOE_BF16;
@@ -945,6 +950,35 @@ size_t moe_host_staging_size(const moe_config* cfg) {
   return align_up(n * esize(cfg->dtype)) + align_up(n * 4) + kAlign;
 }
 
+// Per device: a side stream for the target's host-to-device copy and two
+// events (the copy may start / the copy is done), created on first use.
+struct HostCopyLane {
+  cudaStream_t side = nullptr;
+  cudaEvent_t go = nullptr, done = nullptr;
+  cudaEvent_t copied[2] = {nullptr, nullptr};     // inputs of a slot have landed
+  cudaEvent_t consumed[2] = {nullptr, nullptr};   // the step using a slot is done
+};
+moe_status host_copy_lane(HostCopyLane** out) {
+  static std::mutex mu;
+  static HostCopyLane lanes[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  HostCopyLane& l = lanes[dev];
+  if (l.side == nullptr) {
+    if (cudaStreamCreateWithFlags(&l.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.go, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    for (int q = 0; q < 2; ++q)
+      if (cudaEventCreateWithFlags(&l.copied[q], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&l.consumed[q], cudaEventDisableTiming) != cudaSuccess)
+        return MOE_ERR_CUDA;
+  }
+  *out = &l;
+  return MOE_OK;
+}
+
 moe_status moe_train_step_host(const moe_config* cfg, const moe_params* p, const void* x_host,
                                const float* y_target_host, float lr, float* loss_host,
                                void* staging, size_t staging_bytes, void* workspace,
@@ -962,18 +996,96 @@ moe_status moe_train_step_host(const moe_config* cfg, const moe_params* p, const
   void* xd = sbase;
   float* td = reinterpret_cast<float*>(sbase + align_up(n * esize(c.dtype)));
   float* ld = reinterpret_cast<float*>(sbase + align_up(n * esize(c.dtype)) + align_up(n * 4));
+  // x goes first on the step's stream; the target (needed only from the
+  // combine on) is copied on a side stream while the router and the expert
+  // GEMMs run, and the step's stream waits for it just before the combine
+  cudaEvent_t target_ready = nullptr;
   if (n > 0) {
-    if (cudaMemcpyAsync(xd, x_host, n * esize(c.dtype), cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    if (cudaMemcpyAsync(td, y_target_host, n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    RET_IF(check_device());
+    HostCopyLane* lane = nullptr;
+    RET_IF(host_copy_lane(&lane));
+    CK(cudaEventRecord(lane->go, st));   // earlier work on `st` is done with the staging
+    CK(cudaStreamWaitEvent(lane->side, lane->go, 0));
+    CK(cudaMemcpyAsync(xd, x_host, n * esize(c.dtype), cudaMemcpyHostToDevice, st));
+    CK(cudaMemcpyAsync(td, y_target_host, n * 4, cudaMemcpyHostToDevice, lane->side));
+    CK(cudaEventRecord(lane->done, lane->side));
+    target_ready = lane->done;
   }
-  moe_status s = train_step_impl(cfg, p, xd, td, lr, ld, nullptr, workspace, workspace_bytes, st);
-  if (s != MOE_OK) return s;
+  moe_status s = train_step_impl(cfg, p, xd, td, lr, ld, nullptr, workspace, workspace_bytes, st,
+                                 target_ready);
+  if (s != MOE_OK) {
+    // the caller's host buffer must outlive the copy even on an early return
+    if (target_ready != nullptr) cudaEventSynchronize(target_ready);
+    return s;
+  }
   if (cudaMemcpyAsync(loss_host, ld, 2 * sizeof(float), cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status moe_train_steps_host(const moe_config* cfg, const moe_params* p, int32_t n_steps,
+                                const void* const* x_hosts, const float* const* y_target_hosts,
+                                float lr, float* loss_host, void* staging, size_t staging_bytes,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  g_launches = 0;
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  if (n_steps < 0 || !staging || !loss_host || (n_steps > 0 && (!x_hosts || !y_target_hosts)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(staging)) return MOE_ERR_ALIGNMENT;
+  const size_t slot_bytes = moe_host_staging_size(cfg);
+  if (staging_bytes < 2 * slot_bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const size_t n = (size_t)c.T * c.D;
+  for (int i = 0; i < n_steps; ++i)
+    if (n > 0 && (!x_hosts[i] || !y_target_hosts[i])) return MOE_ERR_INVALID_ARG;
+  if (n_steps == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RET_IF(check_device());
+  HostCopyLane* lane = nullptr;
+  RET_IF(host_copy_lane(&lane));
+  char* sbase = static_cast<char*>(staging);
+  auto slot_x = [&](int q) -> void* { return sbase + q * slot_bytes; };
+  auto slot_t = [&](int q) {
+    return reinterpret_cast<float*>(sbase + q * slot_bytes + align_up(n * esize(c.dtype)));
+  };
+  auto slot_l = [&](int q) {
+    return reinterpret_cast<float*>(sbase + q * slot_bytes + align_up(n * esize(c.dtype)) +
+                                    align_up(n * 4));
+  };
+  auto upload = [&](int i) -> moe_status {   // step i's batch into slot i % 2 (side stream)
+    const int q = i & 1;
+    CK(cudaStreamWaitEvent(lane->side, lane->consumed[q], 0));
+    if (n > 0) {
+      CK(cudaMemcpyAsync(slot_x(q), x_hosts[i], n * esize(c.dtype), cudaMemcpyHostToDevice,
+                         lane->side));
+      CK(cudaMemcpyAsync(slot_t(q), y_target_hosts[i], n * 4, cudaMemcpyHostToDevice,
+                         lane->side));
+    }
+    CK(cudaEventRecord(lane->copied[q], lane->side));
+    return MOE_OK;
+  };
+  // both slots are free once the work already queued on `stream` is done
+  CK(cudaEventRecord(lane->consumed[0], st));
+  CK(cudaEventRecord(lane->consumed[1], st));
+  moe_status s = upload(0);
+  for (int i = 0; i < n_steps && s == MOE_OK; ++i) {
+    const int q = i & 1;
+    if (i + 1 < n_steps) s = upload(i + 1);     // overlaps step i below
+    if (s != MOE_OK) break;
+    if (cudaStreamWaitEvent(st, lane->copied[q], 0) != cudaSuccess) { s = MOE_ERR_CUDA; break; }
+    s = train_step_impl(cfg, p, slot_x(q), slot_t(q), lr, slot_l(q), nullptr, workspace,
+                        workspace_bytes, st);   // launches accumulate over the steps
+    if (s != MOE_OK) break;
+    if (cudaMemcpyAsync(loss_host + 2 * (size_t)i, slot_l(q), 2 * sizeof(float),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaEventRecord(lane->consumed[q], st) != cudaSuccess)
+      s = MOE_ERR_CUDA;
+  }
+  // the caller's host batches must outlive every copy, also on an early return
+  cudaStreamSynchronize(lane->side);
+  if (cudaStreamSynchronize(st) != cudaSuccess && s == MOE_OK) s = MOE_ERR_CUDA;
+  return s;
 }
 
 moe_status moe_get_routing(const moe_config* cfg, const void* workspace, size_t workspace_bytes,

@@ -128,6 +128,18 @@ def test_selftest_rejects_unbounded_wait_limit(L):
                        good(4), good(5), bad) == B.MOE_ERR_INVALID_ARG
 
 
+def test_pipelined_host_steps_validation(L):
+    good = lambda i: _Fake(0x10000 * (i + 1))  # noqa: E731
+    g = B.make_grads(good(8), good(9), good(10), db1=good(11), db2=good(12))
+    p = B.make_params(good(1), good(2), good(3), g, b1=good(4), b2=good(5))
+    ws = _Fake(0x900000, 1 << 40)
+    small = _Fake(0xA00000, B.moe_host_staging_size(_cfg()))   # one slot, two needed
+    assert _status(B.moe_train_steps_host, _cfg(), p, [good(6)], [good(7)], 0.1, good(13),
+                   small, ws) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert _status(B.moe_train_steps_host, _cfg(), p, [good(6)], [good(7)], 0.1, good(13),
+                   _Fake(0xA00008, 1 << 30), ws) == B.MOE_ERR_ALIGNMENT
+
+
 def test_status_strings(L):
     for s in range(7):
         assert B.moe_status_string(s)

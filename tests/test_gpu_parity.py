@@ -293,6 +293,34 @@ def test_host_entry_point_matches_device():
             assert torch.equal(v, b.param_dict()[k]), k
 
 
+def test_pipelined_host_steps_match_sequential_steps():
+    """moe_train_steps_host over three different host batches (inputs of step
+    i+1 uploaded while step i runs) gives bit-identical losses and weights to
+    three moe_train_step calls in order."""
+    from sparse_mixture_experts_softmax_gb300 import binding as B
+    wl = W.WORKLOADS["dense_bf16"].with_tokens(777)
+    batches = [W.make_inputs(wl, seed=s) for s in (21, 22, 23)]
+    inp = batches[0]
+    a = make_layer(wl, inp)
+    b = make_layer(wl, inp)
+    losses_a = []
+    for bt in batches:
+        a.train_step(device_x(wl, bt), bt["target"].cuda(), wl.lr)
+        losses_a.append(a.d_loss.cpu().clone())
+    xs = [bt["x_bf16"].contiguous().pin_memory() for bt in batches]
+    ts = [bt["target"].contiguous().pin_memory() for bt in batches]
+    staging = torch.empty(2 * B.moe_host_staging_size(b.cfg), dtype=torch.uint8, device="cuda")
+    loss_host = torch.zeros(2 * len(batches), dtype=torch.float32).pin_memory()
+    B.moe_train_steps_host(b.cfg, b.params(), xs, ts, wl.lr, loss_host, staging, b.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(losses_a), loss_host)
+    for k, v in a.param_dict().items():
+        if v is not None:
+            assert torch.equal(v, b.param_dict()[k]), k
+    for k in ("w1", "w2"):
+        assert torch.equal(getattr(a, k + "_lp"), getattr(b, k + "_lp")), k
+
+
 def test_empty_tokens():
     wl = W.WORKLOADS["tiny"]
     inp = W.make_inputs(wl, seed=0)
