@@ -321,6 +321,47 @@ def test_pipelined_host_steps_match_sequential_steps():
         assert torch.equal(getattr(a, k + "_lp"), getattr(b, k + "_lp")), k
 
 
+def test_all_routing_options_together():
+    """Correction bias + shared experts + expert capacity on the grouped layer
+    at once (full width, 1024 tokens): the options compose."""
+    import dataclasses
+    wl = dataclasses.replace(W.WORKLOADS["grouped"], name="grouped_all", T=1024,
+                             corr_bias_scale=0.1, n_shared=1, capacity_factor=1.0)
+    errs, layer, _ = _one_step_parity(wl)
+    assert max(errs.values()) <= 2e-2
+    assert int((layer.routing()["slot_of"] < 0).sum().item()) > 0
+
+
+def test_cuda_graph_replay_matches_eager():
+    """After one eager call, a training step captures into a CUDA graph (no
+    host synchronisation or allocation inside); three replays give the same
+    bits as three eager steps."""
+    wl = W.WORKLOADS["dense_bf16"].with_tokens(1000)
+    inp = W.make_inputs(wl, seed=8)
+    a = make_layer(wl, inp)
+    b = make_layer(wl, inp)
+    x = device_x(wl, inp)
+    tgt = inp["target"].cuda()
+    for _ in range(4):
+        a.train_step(x, tgt, wl.lr)
+    b.train_step(x, tgt, wl.lr)                  # eager first call (one-time setup)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            b.train_step(x, tgt, wl.lr)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a.d_loss, b.d_loss)
+    for k, v in a.param_dict().items():
+        if v is not None:
+            assert torch.equal(v, b.param_dict()[k]), k
+
+
 def test_empty_tokens():
     wl = W.WORKLOADS["tiny"]
     inp = W.make_inputs(wl, seed=0)
