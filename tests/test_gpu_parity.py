@@ -362,6 +362,20 @@ def test_cuda_graph_replay_matches_eager():
             assert torch.equal(v, b.param_dict()[k]), k
 
 
+@pytest.mark.parametrize("E,k,T", [(256, 8, 1536), (64, 12, 700), (16, 16, 300)])
+def test_wide_routing_bf16(E, k, T):
+    """The largest expert count (256: eight score registers per lane, the
+    GEMM's segment table at its limit) and k > 8 (the training step then runs
+    the separate combine and combine-backward kernels) on a bf16 SwiGLU layer;
+    k = E = 16 routes every token to every expert."""
+    import dataclasses
+    wl = dataclasses.replace(W.WORKLOADS["grouped"], name=f"wide_{E}_{k}", T=T, D=256, F=128,
+                             E=E, k=k, n_groups=1, topk_groups=1, score="softmax",
+                             aux_alpha=0.01)
+    errs, _, _ = _one_step_parity(wl, seed=13)
+    assert max(errs.values()) <= 2e-2
+
+
 def test_empty_tokens():
     wl = W.WORKLOADS["tiny"]
     inp = W.make_inputs(wl, seed=0)
