@@ -26,6 +26,7 @@ import subprocess
 import sys
 import threading
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -71,12 +72,13 @@ def load_peaks():
     return d
 
 
-def expert_flops_per_step(wl: W.Workload) -> float:
+def expert_flops_per_step(wl: W.Workload, rows: Optional[int] = None) -> float:
     """Algorithmic active-row FLOPs of the expert GEMMs in one training step:
     per routed row 2*D*F per projection, SwiGLU has 3 projections (W1, W3, W2),
-    the two-layer MLP 2; backward is twice the forward."""
+    the two-layer MLP 2; backward is twice the forward.  ``rows``: the rows
+    the experts process (fewer than T k when a capacity drops some)."""
     proj = 3 if wl.act == "swiglu" else 2
-    return 3.0 * proj * 2.0 * wl.D * wl.F * wl.R
+    return 3.0 * proj * 2.0 * wl.D * wl.F * (wl.R if rows is None else rows)
 
 
 def shared_flops_per_step(wl: W.Workload) -> float:
@@ -90,10 +92,11 @@ def router_flops_per_step(wl: W.Workload) -> float:
     return 3.0 * 2.0 * wl.T * wl.D * wl.E
 
 
-def hbm_bytes(wl: W.Workload) -> dict:
-    """Algorithmic bytes per launch of the HBM-bound passes."""
+def hbm_bytes(wl: W.Workload, rows: Optional[int] = None) -> dict:
+    """Algorithmic bytes per launch of the HBM-bound passes (``rows``: expert
+    rows kept, T k without a capacity)."""
     es = 2 if wl.dtype == "bf16" else 4
-    T, D, R = wl.T, wl.D, wl.R
+    T, D, R = wl.T, wl.D, (wl.R if rows is None else rows)
     n_exp = (3 if wl.act == "swiglu" else 2) * wl.E * wl.D * wl.F
     n_bias = wl.E * (wl.F + wl.D) if wl.has_bias else 0
     return {
@@ -394,7 +397,8 @@ def main():
                   if k_.startswith("gemm_") and not k_.startswith(("gemm_router", "gemm_shared")))
     shared_ms = sum(v for k_, v in per_kernel.items() if k_.startswith("gemm_shared"))
     peaks = load_peaks()
-    eflops = expert_flops_per_step(wl)
+    rows_kept = int(layer.routing()["offsets"][-1].item())   # T k unless a capacity drops
+    eflops = expert_flops_per_step(wl, rows_kept)
     if lp:
         achieved = eflops / (gemm_ms / 1e3) / 1e12
         peak = float(peaks["bf16_tflops_sustained"])
@@ -409,7 +413,7 @@ def main():
                 "traffic_unit": "DRAM bytes per step of the GEMM family (ncu, scaled)",
                 "kernel": "grouped expert GEMMs (all launches of one step)",
                 "peak_source": f"{peaks['source']} ({'bf16_tflops_sustained' if lp else 'FFMA at max clock'})"}
-    hb = hbm_bytes(wl)
+    hb = hbm_bytes(wl, rows_kept)
     hbm = {}
     for name, key in (("gather", "gather"), ("combine_loss", "combine_loss"),
                       ("combine_bwd", "combine_bwd"), ("combine_fused", "combine_fused")) + \
@@ -423,7 +427,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if lp else "f32", "data": "synthetic", "config": workload_config(wl),
             "expert_gemm_tflops": achieved, "router_gflop_per_step": router_flops_per_step(wl) / 1e9,
-            "expert_gflop_per_step": eflops / 1e9, "roofline": roofline, "hbm_passes": hbm,
+            "expert_gflop_per_step": eflops / 1e9, "expert_rows_per_step": rows_kept,
+            "roofline": roofline, "hbm_passes": hbm,
             "gpu_launches": launches * args.steps, "clocks": clk,
             "step_ms": {"p50": step_ms[len(step_ms) // 2],
                         "p90": step_ms[min(len(step_ms) - 1, int(0.9 * len(step_ms)))],

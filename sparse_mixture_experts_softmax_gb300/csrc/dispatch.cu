@@ -217,8 +217,10 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
 // value may differ from that path in the last bits).
 // 128-thread blocks: with the k rows held in registers (~150 per thread), four
 // warps per block let three blocks share an SM.
+// SHARED: the layer has a shared-expert branch (Ys added, bf16 dY written);
+// a separate instantiation keeps the plain kernel's registers down.
 constexpr int CT_WARPS = 4;
-template <typename T>
+template <typename T, bool SHARED>
 __global__ void __launch_bounds__(32 * CT_WARPS)
 combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
                      const int* __restrict__ slot_of, int Tn, int D, int k,
@@ -255,7 +257,7 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
 #pragma unroll
           for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], v[j].get(i), acc[i]);
         }
-      if (ys != nullptr) {   // shared-expert branch, added after the routed sum
+      if constexpr (SHARED) {   // shared-expert branch, added after the routed sum
         Vec<T> u;
         u.load(ys + (size_t)t * D + d);
 #pragma unroll
@@ -273,13 +275,11 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
         dv[i + 2] = 2.f * d2 * inv_n;
         dv[i + 3] = 2.f * d3 * inv_n;
       }
-      if constexpr (VN == 8) {   // bf16 rows: dY copy for the shared branch's GEMMs
-        if (dy_lp != nullptr) {
-          Vec<bf16> q;
+      if constexpr (SHARED && VN == 8) {   // bf16 dY for the shared branch's GEMMs
+        Vec<bf16> q;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) q.set(i, dv[i]);
-          q.store(dy_lp + (size_t)t * D + d);
-        }
+        for (int i = 0; i < 8; ++i) q.set(i, dv[i]);
+        q.store(dy_lp + (size_t)t * D + d);
       }
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
@@ -565,18 +565,24 @@ cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, c
                                  int T, int D, int k, const void* ys, const float* target,
                                  double* sq_partial, void* dye, float* dgate, void* dy_lp,
                                  cudaStream_t st) {
-  if (k > 8 || (dy_lp != nullptr && dtype != 1)) return cudaErrorInvalidValue;
+  // the shared branch exists only for bf16 layers and comes with both Ys and dY
+  const bool shared = ys != nullptr;
+  if (k > 8 || (shared && (dy_lp == nullptr || dtype != 1))) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
   const float inv_n = 1.0f / ((float)T * (float)D);
   const int grid = combine_blocks(T);
-  if (dtype == 1)
-    combine_train_kernel<bf16><<<grid, 32 * CT_WARPS, 0, st>>>(
+  if (dtype == 1 && shared)
+    combine_train_kernel<bf16, true><<<grid, 32 * CT_WARPS, 0, st>>>(
         static_cast<const bf16*>(ye), gate, slot_of, T, D, k, static_cast<const bf16*>(ys), target,
         inv_n, sq_partial, static_cast<bf16*>(dye), dgate, static_cast<bf16*>(dy_lp));
+  else if (dtype == 1)
+    combine_train_kernel<bf16, false><<<grid, 32 * CT_WARPS, 0, st>>>(
+        static_cast<const bf16*>(ye), gate, slot_of, T, D, k, nullptr, target, inv_n, sq_partial,
+        static_cast<bf16*>(dye), dgate, nullptr);
   else
-    combine_train_kernel<float><<<grid, 32 * CT_WARPS, 0, st>>>(
-        static_cast<const float*>(ye), gate, slot_of, T, D, k, static_cast<const float*>(ys),
-        target, inv_n, sq_partial, static_cast<float*>(dye), dgate, nullptr);
+    combine_train_kernel<float, false><<<grid, 32 * CT_WARPS, 0, st>>>(
+        static_cast<const float*>(ye), gate, slot_of, T, D, k, nullptr, target, inv_n,
+        sq_partial, static_cast<float*>(dye), dgate, nullptr);
   return cudaGetLastError();
 }
 
