@@ -9,6 +9,9 @@
  * two-layer MLP (ReLU / GELU-tanh with biases, or SwiGLU W2(SiLU(W1 x) * W3 x),
  * "AI Infra Kernel Lab", "Numerical contracts") -> gate-weighted combine ->
  * MSE task loss + load-balancing aux loss -> the full backward -> SGD.
+ * Optional, per moe_config / moe_weights: a selection-only correction bias
+ * (the DeepSeek gate of "AI Infra Kernel Lab"), a shared-expert SwiGLU branch
+ * on every token, and an expert capacity that drops assignments beyond it.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -22,7 +25,10 @@
  *   allocates or frees.  Pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT).
  * - Streams: all work is enqueued on `stream` (a cudaStream_t; NULL = the
  *   legacy default stream).  No entry point synchronises the host except
- *   moe_train_step_host, which waits for its own loss read-back.
+ *   moe_train_step_host / moe_train_steps_host, which wait for their own loss
+ *   read-back (and use one internal side stream per device for uploads).
+ *   After its first call on a device, moe_train_step neither synchronises
+ *   nor allocates, so it can be captured into a CUDA graph.
  * - Validation: every call checks its arguments on the host before the first
  *   launch and returns a status; an unsupported request fails, it never falls
  *   back to another code path.
@@ -40,8 +46,9 @@
  *
  * Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= E <= 256, 1 <= k <= 32,
  * k <= E; n_groups divides E and is <= 32; D and F are multiples of 8;
- * for MOE_BF16 also E; T*k < 2^31.  SwiGLU experts carry no biases.  T = 0 is accepted and does no
- * work (train step losses read 0).  The device must be sm_103.
+ * for MOE_BF16 also E; T*k < 2^31.  SwiGLU experts carry no biases; shared
+ * experts need SwiGLU and MOE_BF16.  T = 0 is accepted and does no work
+ * (train step losses read 0).  The device must be sm_103.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
