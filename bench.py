@@ -43,8 +43,8 @@ FFMA_PER_SM_PER_CLK = 128
 # from an ncu capture of the same per-expert shapes at 8 experts scaled by 16
 # (profiles/tc_gemm_large_e8_traffic.md).  Valid only for the GEMM source it
 # was taken from: reported as null once gemm_tc.cu changes.
-GEMM_TRAFFIC = {"bytes_per_step": 152.8e9, "workload": "large",
-                "gemm_source_sha256_prefix": "bcc7e6cc0f8be19b"}
+GEMM_TRAFFIC = {"bytes_per_step": 146.1e9, "workload": "large",
+                "gemm_source_sha256_prefix": "11a44030c4b22d55"}
 
 
 def gemm_traffic(wl: W.Workload):

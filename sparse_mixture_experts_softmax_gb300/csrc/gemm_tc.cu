@@ -69,6 +69,7 @@ struct TcParams {
   int M, N, E;          // ragged-M: M = total rows; TN: output rows per expert
   int K0, K1;           // reduction lengths of pair 0 / pair 1 (ragged-M)
   int nM, nN;           // tiles along M (TN) and N
+  int m_fast;           // TN: tiles of an expert ordered M-fastest (else N-fastest)
   int ntile_n;          // columns of one N tile in output space (128 for SwiGLU up)
   const int* offsets;   // [E+1]
   void* C;
@@ -343,8 +344,13 @@ __device__ __forceinline__ Tile map_tile(int t, const TcParams& p, const int* of
     const int per = p.nM * p.nN;
     T.e = t / per;
     const int rem = t % per;
-    T.m0 = (rem / p.nN) * BM;
-    T.n0 = (rem % p.nN) * BN;
+    if (p.m_fast) {
+      T.m0 = (rem % p.nM) * BM;
+      T.n0 = (rem / p.nM) * BN;
+    } else {
+      T.m0 = (rem / p.nN) * BM;
+      T.n0 = (rem % p.nN) * BN;
+    }
     T.row_hi = p.M;
     T.kbeg = offs[T.e];
     T.kend = offs[T.e + 1];
@@ -875,6 +881,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   p.nM = (g.M + BM - 1) / BM;
   p.nN = (g.N + BN - 1) / BN;
   p.K1 = 0;
+  // An expert's tiles span more than one wave of CTAs, and the operand indexed
+  // by the slower tile coordinate is re-read from DRAM by every wave that
+  // touches it; step fastest along the smaller operand's dimension (M: the
+  // A operand [rows, M]; N: B [rows, N]) so that the larger one is read once.
+  p.m_fast = g.M < g.N ? 1 : 0;
   tiles_upper = g.E * p.nM * p.nN;
   if (g.sgd_w != nullptr) return launch_inst<FORM_TN, EPI_SGD_F32_TAG>(maps, p, tiles_upper, st);
   return launch_inst<FORM_TN, EPI_STORE_F32_TAG>(maps, p, tiles_upper, st);
