@@ -754,3 +754,39 @@ def test_capacity_gradients_central_differences():
         xm = x.copy(); xm[i] -= h
         fd[i] = (O.total_loss(cfg, w, xp, tgt) - O.total_loss(cfg, w, xm, tgt)) / (2 * h)
     assert np.max(np.abs(fd - g["dx"])) / np.max(np.abs(fd)) <= 1e-6
+
+
+# -------------------------------------------------------- hand-worked case ---
+
+def _golden(name):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    out = {}
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, rest = line.split(None, 1)
+        out[key] = [[float(v) for v in part.split()] for part in rest.split("|")]
+    return out
+
+
+def test_hand_worked_router_dispatch_aux():
+    g = _golden("hand_worked_router_dispatch.txt")
+    m = np.array(g["multipliers"])
+    logits = np.log(m)
+    cfg = O.OracleConfig(T=3, D=1, F=1, E=4, k=2)
+    p = O.softmax_rows(logits)
+    np.testing.assert_allclose(p, np.array(g["scores"]), rtol=0, atol=1e-15)
+    idx = O.route(cfg, p)
+    np.testing.assert_array_equal(idx, np.array(g["idx"]).astype(int))
+    gate = O.renormalize(p, idx)
+    want = np.array(g["gate_num"]) / np.array(g["gate_den"])
+    np.testing.assert_allclose(gate, want, rtol=0, atol=1e-15)
+    counts, offsets, src_tok, _, slot_of = O.dispatch(idx, 4)
+    np.testing.assert_array_equal(counts, np.array(g["counts"][0]).astype(int))
+    np.testing.assert_array_equal(offsets, np.array(g["offsets"][0]).astype(int))
+    np.testing.assert_array_equal(src_tok, np.array(g["src_tok"][0]).astype(int))
+    np.testing.assert_array_equal(slot_of, np.array(g["slot_of"]).astype(int))
+    aux, _, _ = O.aux_loss(counts, p, 2)
+    assert abs(aux - g["aux_num"][0][0] / g["aux_den"][0][0]) <= 1e-15
