@@ -40,11 +40,11 @@ FFMA_PER_SM_PER_CLK = 128
 
 
 # DRAM bytes of the expert GEMM family per training step of the large layer,
-# from an ncu capture of the same per-expert shapes at 8 experts scaled by 16
-# (profiles/tc_gemm_large_e8_traffic.md).  Valid only for the GEMM source it
-# was taken from: reported as null once gemm_tc.cu changes.
-GEMM_TRAFFIC = {"bytes_per_step": 146.1e9, "workload": "large",
-                "gemm_source_sha256_prefix": "11a44030c4b22d55"}
+# from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# same per-expert shapes at 8 experts, scaled by 16.  Valid only for the GEMM
+# source it was taken from: reported as null once gemm_tc.cu changes.
+GEMM_TRAFFIC = {"bytes_per_step": 127.9e9, "workload": "large",
+                "gemm_source_sha256_prefix": "042ec496f411df6a"}
 
 
 def gemm_traffic(wl: W.Workload):

@@ -163,11 +163,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Bulk prefetch of a 16-byte aligned range (a multiple of 16 bytes) into L2.
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
@@ -530,28 +525,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const int row = lane_base + lane;
     int buf = 0;
     uint32_t aph = 0;
-    const int et = (warp - 2) * 32 + lane;   // 0 .. 255 over the epilogue warps
-    // Side inputs (H / H1, H3 of the backward epilogues, the fp32 masters of
-    // the fused SGD) of the NEXT tile are staged in L2 while this tile's MMAs
-    // run: one bulk prefetch of one row segment per epilogue thread.
-    auto prefetch_side = [&](int tn) {
-      if (tn >= total) return;
-      const Tile N = map_tile<FORM>(tn, p, offs, tpre);
-      const int ncols = min(BN, p.N - N.n0);
-      const int rr = N.m0 + (et & (BM - 1));
-      if (ncols <= 0 || rr >= N.row_hi || N.nkb == 0) return;
-      if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
-        const bf16* src = (EPI == EPI_SWIGLU_BWD && et >= BM) ? p.aux1 : p.aux0;
-        if (EPI == EPI_SWIGLU_BWD || et < BM)
-          prefetch_l2(src + (size_t)rr * p.ld_aux + N.n0, (uint32_t)ncols * 2u);
-      }
-      if (EPI == EPI_SGD_F32_TAG && et < BM)
-        prefetch_l2(p.sgd_w + (size_t)N.e * p.sCe + (size_t)rr * p.ldc + N.n0, (uint32_t)ncols * 4u);
-    };
-    if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD || EPI == EPI_SGD_F32_TAG) prefetch_side(blockIdx.x);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
-      if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD || EPI == EPI_SGD_F32_TAG) prefetch_side(t + gridDim.x);
       const int r = T.m0 + row;
       const bool rok = r < T.row_hi;
       if (T.nkb == 0) {
