@@ -27,6 +27,9 @@
  *   legacy default stream).  No entry point synchronises the host except
  *   moe_train_step_host / moe_train_steps_host, which wait for their own loss
  *   read-back (and use one internal side stream per device for uploads).
+ *   Those two run one call at a time per device when called from several
+ *   host threads, and every return, an error included, comes after their
+ *   copies from the caller's host buffers have finished.
  *   After its first call on a device, moe_train_step neither synchronises
  *   nor allocates, so it can be captured into a CUDA graph.
  * - Validation: every call checks its arguments on the host before the first

@@ -31,36 +31,61 @@ route_count_kernel(const int* __restrict__ idx, long long R, int E, int* __restr
 // capacity `cap` an expert keeps min(counts[e], cap) rows; offsets = exclusive
 // scan of the kept counts; chunk_counts[c][e] becomes the rank of chunk c's
 // first assignment to expert e among all of e's assignments (token order).
-__global__ void __launch_bounds__(256)
+// G = SCAN_THREADS / E groups of E threads: group g owns a contiguous range of
+// chunks, sums it, and after the ranges' bases are known (a scan over the
+// groups, in order) writes the running ranks of its range.  Integer sums:
+// exact in any grouping.
+constexpr int SCAN_THREADS = 1024;
+__global__ void __launch_bounds__(SCAN_THREADS)
 route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int cap, int* __restrict__ counts,
                   int* __restrict__ offsets) {
+  __shared__ int part[SCAN_THREADS];   // (group, expert): the range's sum, then its base
   __shared__ int tot[256];
   __shared__ int scan[257];
-  const int e = threadIdx.x;
-  int total = 0;
-  if (e < E) {
+  const int G = SCAN_THREADS / E;      // E <= 256, so G >= 4
+  const int g = threadIdx.x / E, e = threadIdx.x - g * E;
+  const bool active = g < G;
+  const int per = (nchunks + G - 1) / G;
+  const int c0 = active ? min(g * per, nchunks) : 0;
+  const int c1 = active ? min(c0 + per, nchunks) : 0;
+  int sum = 0;
 #pragma unroll 8
-    for (int c = 0; c < nchunks; ++c) total += cc[(size_t)c * E + e];
+  for (int c = c0; c < c1; ++c) sum += cc[(size_t)c * E + e];
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x < E) {
+    int run = 0;
+    for (int q = 0; q < G; ++q) {
+      const int v = part[q * E + threadIdx.x];
+      part[q * E + threadIdx.x] = run;
+      run += v;
+    }
+    tot[threadIdx.x] = run;
   }
-  tot[e] = (e < E) ? min(total, cap) : 0;
   __syncthreads();
   if (threadIdx.x == 0) {
     int run = 0;
-    for (int i = 0; i < E; ++i) { scan[i] = run; run += tot[i]; }
+    for (int i = 0; i < E; ++i) {
+      scan[i] = run;
+      run += min(tot[i], cap);
+    }
     scan[E] = run;
   }
   __syncthreads();
-  if (e < E) {
-    counts[e] = total;
-    offsets[e] = scan[e];
-    int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      int v = cc[(size_t)c * E + e];
+  if (threadIdx.x < E) {
+    counts[threadIdx.x] = tot[threadIdx.x];
+    offsets[threadIdx.x] = scan[threadIdx.x];
+  }
+  if (threadIdx.x == 0) offsets[E] = scan[E];
+  if (active) {
+    int run = part[threadIdx.x];
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) {
+      const int v = cc[(size_t)c * E + e];
       cc[(size_t)c * E + e] = run;
       run += v;
     }
   }
-  if (threadIdx.x == 0) offsets[E] = scan[E];
 }
 
 // Stable scatter: one warp walks its chunk in token order; lanes holding the
@@ -312,35 +337,60 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
 
 // L_mse = sum(sq_partial) / (T D);  P_e = sum_b psum[b][e] / T;  f_e = c_e / (T k);
 // aux = E sum_e f_e P_e;  aux_row[e] = alpha E f_e / T (d aux / d s_te, f constant).
-__global__ void __launch_bounds__(256)
+// One block, every sum in a fixed order (deterministic).  The column sums of
+// psum use G = FL_THREADS / E groups of E threads: group g takes partial rows
+// g, g + G, ... into four fp32 accumulators (this GPU's fp64 rate is a small
+// fraction of its fp32 rate), which are then combined, and the groups added in
+// order, in double.
+constexpr int FL_THREADS = 1024;
+__global__ void __launch_bounds__(FL_THREADS)
 finalize_losses_kernel(const double* __restrict__ sq_partial, int n_sq,
                        const float* __restrict__ psum, int n_ps, const int* __restrict__ counts,
                        int T, int D, int E, int k, float alpha, float* __restrict__ d_loss,
                        float* __restrict__ aux_row) {
-  __shared__ double red[256];
+  __shared__ double red[FL_THREADS];
   const int tid = threadIdx.x;
   double s = 0.0;
-  for (int i = tid; i < n_sq; i += 256) s += sq_partial[i];
+#pragma unroll 4
+  for (int i = tid; i < n_sq; i += FL_THREADS) s += sq_partial[i];
   red[tid] = s;
   __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
+  for (int w = FL_THREADS / 2; w > 0; w >>= 1) {
     if (tid < w) red[tid] += red[tid + w];
     __syncthreads();
   }
   const double mse = red[0] / ((double)T * (double)D);
   __syncthreads();
-  double term = 0.0;
-  for (int e = tid; e < E; e += 256) {
-    double P = 0.0;
-    for (int b = 0; b < n_ps; ++b) P += (double)psum[(size_t)b * E + e];
-    P /= (double)T;
-    const double f = (double)counts[e] / ((double)T * (double)k);
-    term += f * P;
-    if (aux_row != nullptr) aux_row[e] = (float)((double)alpha * (double)E * f / (double)T);
+  const int G = FL_THREADS / E;   // E <= 256, so G >= 4
+  const int g = tid / E, e = tid - g * E;
+  double P = 0.0;
+  if (g < G) {
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+    int b = g;
+    for (; b + 3 * G < n_ps; b += 4 * G) {
+      p0 += psum[(size_t)b * E + e];
+      p1 += psum[(size_t)(b + G) * E + e];
+      p2 += psum[(size_t)(b + 2 * G) * E + e];
+      p3 += psum[(size_t)(b + 3 * G) * E + e];
+    }
+    for (; b < n_ps; b += G) p0 += psum[(size_t)b * E + e];
+    P = ((double)p0 + (double)p1) + ((double)p2 + (double)p3);
   }
+  red[tid] = P;
+  __syncthreads();
+  double term = 0.0;
+  if (tid < E) {
+    double Pe = 0.0;
+    for (int q = 0; q < G; ++q) Pe += red[q * E + tid];
+    Pe /= (double)T;
+    const double f = (double)counts[tid] / ((double)T * (double)k);
+    term = f * Pe;
+    if (aux_row != nullptr) aux_row[tid] = (float)((double)alpha * (double)E * f / (double)T);
+  }
+  __syncthreads();
   red[tid] = term;
   __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
+  for (int w = FL_THREADS / 2; w > 0; w >>= 1) {
     if (tid < w) red[tid] += red[tid + w];
     __syncthreads();
   }
@@ -515,7 +565,7 @@ cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_co
 
 cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int cap, int* counts,
                               int* offsets, cudaStream_t st) {
-  route_scan_kernel<<<1, 256, 0, st>>>(chunk_counts, nchunks, E, cap, counts, offsets);
+  route_scan_kernel<<<1, SCAN_THREADS, 0, st>>>(chunk_counts, nchunks, E, cap, counts, offsets);
   return cudaGetLastError();
 }
 
@@ -589,8 +639,8 @@ cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, c
 cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
                                    int n_ps, const int* counts, int T, int D, int E, int k,
                                    float alpha, float* d_loss, float* aux_row, cudaStream_t st) {
-  finalize_losses_kernel<<<1, 256, 0, st>>>(sq_partial, n_sq, psum_partial, n_ps, counts, T, D, E,
-                                            k, alpha, d_loss, aux_row);
+  finalize_losses_kernel<<<1, FL_THREADS, 0, st>>>(sq_partial, n_sq, psum_partial, n_ps, counts, T,
+                                                   D, E, k, alpha, d_loss, aux_row);
   return cudaGetLastError();
 }
 

@@ -702,28 +702,30 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
+// SMs of the current device (cached per device ordinal): the persistent grid.
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const bool slot = dev >= 0 && dev < 64;
+  if (slot) {
+    const int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
   }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    return 152;   // any grid is correct (tiles are strided over the grid); this one fits a GB300
+  if (slot) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
 template <int FORM, int EPI>
 cudaError_t launch_inst(const CUtensorMap* maps, const TcParams& p, int tiles_upper,
                         cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<FORM, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_dynamic_smem(tc_gemm_kernel<FORM, EPI>, (int)SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
   int grid = sm_count();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) return cudaSuccess;

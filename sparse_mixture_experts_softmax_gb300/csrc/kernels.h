@@ -1,12 +1,31 @@
 // Host-side launchers of the MoE kernels (internal to the library).
 #pragma once
 
+#include <atomic>
 #include <cmath>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace moe {
+
+// Raises a kernel's dynamic shared-memory limit once per device: the
+// attribute belongs to the current device's context, so a process that drives
+// several devices sets it on each.  `done` holds one bit per device ordinal
+// (ordinals from 64 on set it on every call).  Safe to call from several host
+// threads: a race only repeats the idempotent setting.
+template <typename Kernel>
+inline cudaError_t ensure_dynamic_smem(Kernel* kernel, int bytes,
+                                       std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 struct RouterArgs {
   int T, D, E, k;

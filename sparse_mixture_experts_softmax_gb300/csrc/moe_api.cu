@@ -950,9 +950,13 @@ size_t moe_host_staging_size(const moe_config* cfg) {
   return align_up(n * esize(cfg->dtype)) + align_up(n * 4) + kAlign;
 }
 
-// Per device: a side stream for the target's host-to-device copy and two
-// events (the copy may start / the copy is done), created on first use.
+// Per device: a side stream for host-to-device copies and its events (the
+// copy may start / the copy is done; per input slot: landed / consumed),
+// created on first use.  `busy` serialises the host entry points of one
+// device, which share these.
 struct HostCopyLane {
+  bool ready = false;
+  std::mutex busy;
   cudaStream_t side = nullptr;
   cudaEvent_t go = nullptr, done = nullptr;
   cudaEvent_t copied[2] = {nullptr, nullptr};     // inputs of a slot have landed
@@ -965,15 +969,27 @@ moe_status host_copy_lane(HostCopyLane** out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   HostCopyLane& l = lanes[dev];
-  if (l.side == nullptr) {
-    if (cudaStreamCreateWithFlags(&l.side, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.go, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.done, cudaEventDisableTiming) != cudaSuccess)
+  if (!l.ready) {
+    // create everything, and publish the lane only when all of it exists
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    bool ok = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < 6 && ok; ++i)
+      ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      for (cudaEvent_t e : ev)
+        if (e) cudaEventDestroy(e);
+      if (side) cudaStreamDestroy(side);
       return MOE_ERR_CUDA;
-    for (int q = 0; q < 2; ++q)
-      if (cudaEventCreateWithFlags(&l.copied[q], cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&l.consumed[q], cudaEventDisableTiming) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    }
+    l.side = side;
+    l.go = ev[0];
+    l.done = ev[1];
+    l.copied[0] = ev[2];
+    l.copied[1] = ev[3];
+    l.consumed[0] = ev[4];
+    l.consumed[1] = ev[5];
+    l.ready = true;
   }
   *out = &l;
   return MOE_OK;
@@ -996,32 +1012,38 @@ moe_status moe_train_step_host(const moe_config* cfg, const moe_params* p, const
   void* xd = sbase;
   float* td = reinterpret_cast<float*>(sbase + align_up(n * esize(c.dtype)));
   float* ld = reinterpret_cast<float*>(sbase + align_up(n * esize(c.dtype)) + align_up(n * 4));
+  RET_IF(check_device());
+  HostCopyLane* lane = nullptr;
+  RET_IF(host_copy_lane(&lane));
+  std::lock_guard<std::mutex> hold(lane->busy);
+  // every return from here on waits for the copies issued so far: the
+  // caller's host buffers must outlive them, also on an error
+  auto finish = [&](moe_status s) {
+    cudaStreamSynchronize(lane->side);
+    if (cudaStreamSynchronize(st) != cudaSuccess && s == MOE_OK) s = MOE_ERR_CUDA;
+    return s;
+  };
   // x goes first on the step's stream; the target (needed only from the
   // combine on) is copied on a side stream while the router and the expert
   // GEMMs run, and the step's stream waits for it just before the combine
   cudaEvent_t target_ready = nullptr;
   if (n > 0) {
-    RET_IF(check_device());
-    HostCopyLane* lane = nullptr;
-    RET_IF(host_copy_lane(&lane));
-    CK(cudaEventRecord(lane->go, st));   // earlier work on `st` is done with the staging
-    CK(cudaStreamWaitEvent(lane->side, lane->go, 0));
-    CK(cudaMemcpyAsync(xd, x_host, n * esize(c.dtype), cudaMemcpyHostToDevice, st));
-    CK(cudaMemcpyAsync(td, y_target_host, n * 4, cudaMemcpyHostToDevice, lane->side));
-    CK(cudaEventRecord(lane->done, lane->side));
+    // earlier work on `st` is done with the staging before the side copy starts
+    if (cudaEventRecord(lane->go, st) != cudaSuccess ||
+        cudaStreamWaitEvent(lane->side, lane->go, 0) != cudaSuccess ||
+        cudaMemcpyAsync(xd, x_host, n * esize(c.dtype), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(td, y_target_host, n * 4, cudaMemcpyHostToDevice, lane->side) !=
+            cudaSuccess ||
+        cudaEventRecord(lane->done, lane->side) != cudaSuccess)
+      return finish(MOE_ERR_CUDA);
     target_ready = lane->done;
   }
   moe_status s = train_step_impl(cfg, p, xd, td, lr, ld, nullptr, workspace, workspace_bytes, st,
                                  target_ready);
-  if (s != MOE_OK) {
-    // the caller's host buffer must outlive the copy even on an early return
-    if (target_ready != nullptr) cudaEventSynchronize(target_ready);
-    return s;
-  }
+  if (s != MOE_OK) return finish(s);
   if (cudaMemcpyAsync(loss_host, ld, 2 * sizeof(float), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
-  return MOE_OK;
+    return finish(MOE_ERR_CUDA);
+  return finish(MOE_OK);
 }
 
 moe_status moe_train_steps_host(const moe_config* cfg, const moe_params* p, int32_t n_steps,
@@ -1044,6 +1066,7 @@ moe_status moe_train_steps_host(const moe_config* cfg, const moe_params* p, int3
   RET_IF(check_device());
   HostCopyLane* lane = nullptr;
   RET_IF(host_copy_lane(&lane));
+  std::lock_guard<std::mutex> hold(lane->busy);
   char* sbase = static_cast<char*>(staging);
   auto slot_x = [&](int q) -> void* { return sbase + q * slot_bytes; };
   auto slot_t = [&](int q) {

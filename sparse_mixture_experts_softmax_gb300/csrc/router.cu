@@ -490,13 +490,9 @@ static cudaError_t launch_fwd_nj(const void* x, const float* wg, const float* lb
                                  float* psum, cudaStream_t st) {
   dim3 grid(router_fwd_blocks(a.T));
   const size_t smem = RouterSmem<NJ>::bytes;
-  static bool attr_set = false;   // per instantiation; benign race (idempotent)
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(router_fwd_kernel<XT, NJ>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};   // per instantiation and device
+  cudaError_t e = ensure_dynamic_smem(router_fwd_kernel<XT, NJ>, (int)smem, attr_done);
+  if (e != cudaSuccess) return e;
   router_fwd_kernel<XT, NJ><<<grid, RT_THREADS, smem, st>>>(
       static_cast<const XT*>(x), wg, lb, a, scores, idx, gate, psum);
   return cudaGetLastError();
