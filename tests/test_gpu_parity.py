@@ -321,6 +321,71 @@ def test_pipelined_host_steps_match_sequential_steps():
         assert torch.equal(getattr(a, k + "_lp"), getattr(b, k + "_lp")), k
 
 
+def test_host_entry_points_from_two_threads():
+    """Two host threads drive moe_train_steps_host and moe_train_step_host on
+    one device at once, each with its own layer, stream, staging and batches
+    (the library serialises these calls per device).  Each thread's losses and
+    weights are bit-identical to the same call sequence made alone."""
+    import threading
+    from sparse_mixture_experts_softmax_gb300 import binding as B
+    wl = W.WORKLOADS["dense_bf16"].with_tokens(640)
+    seeds = {0: (31, 32, 33), 1: (41, 42, 43)}
+    batches = {w: [W.make_inputs(wl, seed=s) for s in seeds[w]] for w in seeds}
+    host = {w: ([bt["x_bf16"].contiguous().pin_memory() for bt in batches[w]],
+                [bt["target"].contiguous().pin_memory() for bt in batches[w]]) for w in seeds}
+
+    def sequence(layer, w, stream, out):
+        xs, ts = host[w]
+        with torch.cuda.stream(stream):
+            staging = torch.empty(2 * B.moe_host_staging_size(layer.cfg), dtype=torch.uint8,
+                                  device="cuda")
+            losses = torch.zeros(2 * len(xs), dtype=torch.float32).pin_memory()
+            loss1 = torch.zeros(2, dtype=torch.float32).pin_memory()
+            for _ in range(3):
+                B.moe_train_steps_host(layer.cfg, layer.params(), xs, ts, wl.lr, losses, staging,
+                                       layer.workspace, stream=stream)
+                out.append(losses.clone())
+                B.moe_train_step_host(layer.cfg, layer.params(), xs[1], ts[1], wl.lr, loss1,
+                                      staging, layer.workspace, stream=stream)
+                out.append(loss1.clone())
+            stream.synchronize()
+
+    alone, together = {}, {}
+    for w in seeds:   # each sequence alone, one after the other
+        layer = make_layer(wl, batches[w][0])
+        torch.cuda.synchronize()   # the layer's set-up ran on the default stream
+        out = []
+        sequence(layer, w, torch.cuda.Stream(), out)
+        alone[w] = (out, {k: v.clone() for k, v in layer.param_dict().items() if v is not None})
+    layers = {w: make_layer(wl, batches[w][0]) for w in seeds}
+    streams = {w: torch.cuda.Stream() for w in seeds}
+    torch.cuda.synchronize()
+    outs = {w: [] for w in seeds}
+    errors = []
+
+    def worker(w):
+        try:
+            sequence(layers[w], w, streams[w], outs[w])
+        except Exception as e:   # surfaced on the main thread below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(w,)) for w in seeds]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for w in seeds:
+        ref_losses, ref_params = alone[w]
+        assert len(outs[w]) == len(ref_losses)
+        for a, b in zip(ref_losses, outs[w]):
+            assert torch.equal(a, b), w
+        for k, v in layers[w].param_dict().items():
+            if v is not None:
+                assert torch.equal(ref_params[k], v), (w, k)
+
+
 def test_all_routing_options_together():
     """Correction bias + shared experts + expert capacity on the grouped layer
     at once (full width, 1024 tokens): the options compose."""
