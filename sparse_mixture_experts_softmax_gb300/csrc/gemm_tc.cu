@@ -267,6 +267,26 @@ struct Side {
   float4 w[4];
 };
 
+
+// Epilogue outputs are stored with an L2 evict-first policy: no later launch
+// re-reads them soon, and the operand tiles that neighbouring CTAs and the
+// next wave re-read then stay in L2 (fewer DRAM re-reads of the weights).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_ef(void* ptr, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(ptr), "r"(v.x),
+               "r"(v.y), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_ef(void* ptr, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 // Four bf16 at column n of rows row0 + 8 j (j = 0..3) of a row-major matrix
 // with leading dimension ld; zeros for rows >= row_hi or n >= N.
 __device__ __forceinline__ void load_bf16x4_rows(const bf16* base, long long ld, int row0,
@@ -523,6 +543,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const int lane_base = (warp & 3) * 32;
     const int half = (warp - 2) >> 2;
     const int row = lane_base + lane;
+    const uint64_t pol = policy_evict_first();
     int buf = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -596,33 +617,33 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           }
           const size_t o = (size_t)g * p.ldc + n;
           if (EPI == EPI_STORE) {
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(x);
+            st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(x), pol);
           } else if (EPI == EPI_ROWS_F32_TAG) {
-            *reinterpret_cast<float4*>(static_cast<float*>(p.C) + o) = make_float4(x[0], x[1], x[2], x[3]);
+            st_ef(static_cast<float*>(p.C) + o, make_float4(x[0], x[1], x[2], x[3]), pol);
           } else if (EPI == EPI_STORE_F32_TAG) {
-            *reinterpret_cast<float4*>(static_cast<float*>(p.C) + wbase + o) = acc[j];
+            st_ef(static_cast<float*>(p.C) + wbase + o, acc[j], pol);
           } else if (EPI == EPI_SGD_F32_TAG) {
             // dW stored as is; the update uses the same fused multiply-add and
             // round-to-nearest bf16 conversion as the stand-alone SGD kernel
-            *reinterpret_cast<float4*>(static_cast<float*>(p.C) + wbase + o) = acc[j];
+            st_ef(static_cast<float*>(p.C) + wbase + o, acc[j], pol);
             float w[4] = {use.w[j].x, use.w[j].y, use.w[j].z, use.w[j].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) w[i] = fmaf(-p.sgd_lr, x[i], w[i]);
-            *reinterpret_cast<float4*>(p.sgd_w + wbase + o) = make_float4(w[0], w[1], w[2], w[3]);
-            if (p.sgd_wlp) *reinterpret_cast<uint2*>(p.sgd_wlp + wbase + o) = pack4_bf16(w);
+            st_ef(p.sgd_w + wbase + o, make_float4(w[0], w[1], w[2], w[3]), pol);
+            if (p.sgd_wlp) st_ef(p.sgd_wlp + wbase + o, pack4_bf16(w), pol);
           } else if (EPI == EPI_ACT_FWD) {
             float a[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) a[i] = p.act == 0 ? fmaxf(x[i], 0.f) : gelu_tanh_f(x[i]);
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out1) + o) = pack4_bf16(x);
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(a);
+            st_ef(static_cast<bf16*>(p.out1) + o, pack4_bf16(x), pol);
+            st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(a), pol);
           } else if (EPI == EPI_ACT_BWD) {
             float h[4], dh[4];
             unpack4_bf16(use.h1[j], h);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_tanh_grad_f(h[i]);
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(dh);
+            st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(dh), pol);
           } else if (EPI == EPI_SWIGLU_BWD) {
             float h1[4], h3[4], d1[4], d3[4];
             unpack4_bf16(use.h1[j], h1);
@@ -632,16 +653,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
               d1[i] = x[i] * h3[i] * silu_grad_f(h1[i]);
               d3[i] = x[i] * silu_f(h1[i]);
             }
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(d1);
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out1) + o) = pack4_bf16(d3);
+            st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(d1), pol);
+            st_ef(static_cast<bf16*>(p.out1) + o, pack4_bf16(d3), pol);
           } else if (EPI == EPI_SWIGLU_UP) {
             const float h3[4] = {acc3[j].x, acc3[j].y, acc3[j].z, acc3[j].w};
             float a[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) a[i] = silu_f(x[i]) * h3[i];
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out1) + o) = pack4_bf16(x);
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out2) + o) = pack4_bf16(h3);
-            *reinterpret_cast<uint2*>(static_cast<bf16*>(p.C) + o) = pack4_bf16(a);
+            st_ef(static_cast<bf16*>(p.out1) + o, pack4_bf16(x), pol);
+            st_ef(static_cast<bf16*>(p.out2) + o, pack4_bf16(h3), pol);
+            st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(a), pol);
           }
         }
       };
