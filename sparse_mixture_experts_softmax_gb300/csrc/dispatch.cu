@@ -337,33 +337,31 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
 
 // L_mse = sum(sq_partial) / (T D);  P_e = sum_b psum[b][e] / T;  f_e = c_e / (T k);
 // aux = E sum_e f_e P_e;  aux_row[e] = alpha E f_e / T (d aux / d s_te, f constant).
-// One block, every sum in a fixed order (deterministic).  The column sums of
-// psum use G = FL_THREADS / E groups of E threads: group g takes partial rows
-// g, g + G, ... into four fp32 accumulators (this GPU's fp64 rate is a small
-// fraction of its fp32 rate), which are then combined, and the groups added in
-// order, in double.
+// One block, every sum in a fixed order (deterministic).  This GPU's fp64 rate
+// is a small fraction of its fp32 rate, so double is kept only for the sum of
+// the squared-error partials (which are double already): the score column sums
+// use G = FL_THREADS / E groups of E threads (group g takes partial rows g,
+// g + G, ... into four fp32 accumulators), folded pairwise over the groups;
+// the per-expert terms and their sum are fp32 as well.
 constexpr int FL_THREADS = 1024;
 __global__ void __launch_bounds__(FL_THREADS)
 finalize_losses_kernel(const double* __restrict__ sq_partial, int n_sq,
                        const float* __restrict__ psum, int n_ps, const int* __restrict__ counts,
                        int T, int D, int E, int k, float alpha, float* __restrict__ d_loss,
                        float* __restrict__ aux_row) {
-  __shared__ double red[FL_THREADS];
-  const int tid = threadIdx.x;
+  __shared__ double sq_warp[FL_THREADS / 32];
+  __shared__ float col[FL_THREADS];
+  __shared__ float term_warp[FL_THREADS / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // squared error: a double per thread, a shuffle tree per warp, warps in order
   double s = 0.0;
-#pragma unroll 4
   for (int i = tid; i < n_sq; i += FL_THREADS) s += sq_partial[i];
-  red[tid] = s;
-  __syncthreads();
-  for (int w = FL_THREADS / 2; w > 0; w >>= 1) {
-    if (tid < w) red[tid] += red[tid + w];
-    __syncthreads();
-  }
-  const double mse = red[0] / ((double)T * (double)D);
-  __syncthreads();
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+  if (lane == 0) sq_warp[warp] = s;
+  // score column sums
   const int G = FL_THREADS / E;   // E <= 256, so G >= 4
   const int g = tid / E, e = tid - g * E;
-  double P = 0.0;
+  float P = 0.f;
   if (g < G) {
     float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
     int b = g;
@@ -374,29 +372,38 @@ finalize_losses_kernel(const double* __restrict__ sq_partial, int n_sq,
       p3 += psum[(size_t)(b + 3 * G) * E + e];
     }
     for (; b < n_ps; b += G) p0 += psum[(size_t)b * E + e];
-    P = ((double)p0 + (double)p1) + ((double)p2 + (double)p3);
+    P = (p0 + p1) + (p2 + p3);
   }
-  red[tid] = P;
+  col[tid] = P;
   __syncthreads();
-  double term = 0.0;
-  if (tid < E) {
-    double Pe = 0.0;
-    for (int q = 0; q < G; ++q) Pe += red[q * E + tid];
-    Pe /= (double)T;
-    const double f = (double)counts[tid] / ((double)T * (double)k);
-    term = f * Pe;
-    if (aux_row != nullptr) aux_row[tid] = (float)((double)alpha * (double)E * f / (double)T);
-  }
+  // fold the groups: those from Gp on (Gp = largest power of two <= G) onto
+  // the first ones, then halve Gp until group 0 holds the column sums
+  int Gp = 1;
+  while (2 * Gp <= G) Gp *= 2;
+  if (g >= Gp && g < G) col[tid - Gp * E] += col[tid];
   __syncthreads();
-  red[tid] = term;
-  __syncthreads();
-  for (int w = FL_THREADS / 2; w > 0; w >>= 1) {
-    if (tid < w) red[tid] += red[tid + w];
+  for (int w = Gp / 2; w > 0; w >>= 1) {
+    if (g < w) col[tid] += col[tid + w * E];
     __syncthreads();
   }
+  float term = 0.f;
+  if (tid < E) {
+    const float f = (float)counts[tid] / ((float)T * (float)k);
+    term = f * (col[tid] / (float)T);
+    if (aux_row != nullptr) aux_row[tid] = alpha * (float)E * f / (float)T;
+  }
+  for (int o = 16; o > 0; o >>= 1) term += __shfl_down_sync(0xffffffffu, term, o);
+  if (lane == 0) term_warp[warp] = term;
+  __syncthreads();
   if (tid == 0 && d_loss != nullptr) {
-    d_loss[0] = (float)mse;
-    d_loss[1] = (float)((double)E * red[0]);
+    double sq = 0.0;
+    float aux = 0.f;
+    for (int w = 0; w < FL_THREADS / 32; ++w) {
+      sq += sq_warp[w];
+      aux += term_warp[w];
+    }
+    d_loss[0] = (float)(sq / ((double)T * (double)D));
+    d_loss[1] = (float)E * aux;
   }
 }
 
