@@ -12,12 +12,13 @@ namespace {
 
 // Per-chunk expert histogram of the routed assignments (t, j) in token order.
 __global__ void __launch_bounds__(256)
-route_count_kernel(const int* __restrict__ idx, long long R, int E, int* __restrict__ chunk_counts) {
+route_count_kernel(const int* __restrict__ idx, long long R, int chunk, int E,
+                   int* __restrict__ chunk_counts) {
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const long long lo = (long long)blockIdx.x * ROUTE_CHUNK;
-  const long long hi = min(lo + ROUTE_CHUNK, R);
+  const long long lo = (long long)blockIdx.x * chunk;
+  const long long hi = min(lo + chunk, R);
   for (long long f = lo + threadIdx.x; f < hi; f += blockDim.x) {
     int e = idx[f];
     if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);   // integer: order-independent
@@ -92,7 +93,7 @@ route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int cap, int* __rest
 // same expert are ranked by lane id (match_any), so slots keep token order.
 // An assignment of rank >= cap within its expert is dropped (slot -1).
 __global__ void __launch_bounds__(32)
-route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E, int cap,
+route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k, int E, int cap,
                      const int* __restrict__ chunk_base, const int* __restrict__ offsets,
                      int* __restrict__ src_tok, int* __restrict__ slot_of) {
   __shared__ int cursor[256];
@@ -103,8 +104,8 @@ route_scatter_kernel(const int* __restrict__ idx, long long R, int k, int E, int
     off[e] = offsets[e];
   }
   __syncwarp();
-  const long long lo = (long long)blockIdx.x * ROUTE_CHUNK;
-  const long long hi = min(lo + ROUTE_CHUNK, R);
+  const long long lo = (long long)blockIdx.x * chunk;
+  const long long hi = min(lo + chunk, R);
   const unsigned lt_mask = (1u << lane) - 1u;
   for (long long base = lo; base < hi; base += 32) {
     const long long f = base + lane;
@@ -560,13 +561,21 @@ inline int grid_for(long long n, int per_block, int cap) {
 
 }  // namespace
 
-int route_chunks(long long R) { return (int)((R + ROUTE_CHUNK - 1) / ROUTE_CHUNK); }
+int route_chunk(long long R) {
+  long long c = (R + ROUTE_TARGET_CHUNKS - 1) / ROUTE_TARGET_CHUNKS;
+  c = (c + 31) / 32 * 32;
+  return (int)(c < ROUTE_CHUNK_MIN ? ROUTE_CHUNK_MIN : c > ROUTE_CHUNK_MAX ? ROUTE_CHUNK_MAX : c);
+}
+int route_chunks(long long R) {
+  const int c = route_chunk(R);
+  return (int)((R + c - 1) / c);
+}
 
 cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
                                cudaStream_t st) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
-  route_count_kernel<<<nc, 256, 0, st>>>(idx, R, E, chunk_counts);
+  route_count_kernel<<<nc, 256, 0, st>>>(idx, R, route_chunk(R), E, chunk_counts);
   return cudaGetLastError();
 }
 
@@ -581,8 +590,8 @@ cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, int 
                                  int* slot_of, cudaStream_t st) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
-  route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, k, E, cap, chunk_base, offsets, src_tok,
-                                          slot_of);
+  route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, route_chunk(R), k, E, cap, chunk_base, offsets,
+                                          src_tok, slot_of);
   return cudaGetLastError();
 }
 

@@ -10,8 +10,9 @@
 // held in a fixed, file-scope device array instead of a caller workspace.
 //
 // The array is sized for MOE_NOALLOC_MAX_ROUTED routed assignments (T*k) and
-// up to 256 experts: 1024 chunks x 256 experts x 4 bytes = 1 MiB, which every
-// GPU that loads this library keeps until the process exits.
+// up to 256 experts: at most max(ROUTE_TARGET_CHUNKS, R / ROUTE_CHUNK_MAX) =
+// 1024 chunks x 256 experts x 4 bytes = 1 MiB, which every GPU that loads this
+// library keeps until the process exits.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -21,8 +22,10 @@
 
 namespace {
 
-constexpr int kMaxChunks = MOE_NOALLOC_MAX_ROUTED / moe::ROUTE_CHUNK;
-static_assert(MOE_NOALLOC_MAX_ROUTED % moe::ROUTE_CHUNK == 0, "whole chunks");
+constexpr int kMaxChunks = MOE_NOALLOC_MAX_ROUTED / moe::ROUTE_CHUNK_MAX > moe::ROUTE_TARGET_CHUNKS
+                               ? MOE_NOALLOC_MAX_ROUTED / moe::ROUTE_CHUNK_MAX
+                               : moe::ROUTE_TARGET_CHUNKS;
+static_assert(MOE_NOALLOC_MAX_ROUTED % moe::ROUTE_CHUNK_MAX == 0, "whole chunks");
 
 // Per-chunk expert counts, then per-chunk first slots.  Shared by every call:
 // each call overwrites the entries it reads before reading them, so nothing
@@ -80,6 +83,7 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t*
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int nchunks = moe::route_chunks(R);
+  if (nchunks > kMaxChunks) return MOE_ERR_UNSUPPORTED;   // cannot happen within the limit
   if (moe::launch_route_count(idx, R, c.E, scratch, s) != cudaSuccess) return MOE_ERR_CUDA;
   const int cap = moe::expert_capacity_rows(c.capacity_factor, c.T, c.k, c.E);
   if (moe::launch_route_scan(scratch, nchunks, c.E, cap, counts, offsets, s) != cudaSuccess)

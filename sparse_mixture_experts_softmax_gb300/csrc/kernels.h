@@ -48,7 +48,14 @@ cudaError_t launch_router_select(const float* logits, const RouterArgs& a, float
 cudaError_t launch_cast_bf16(const float* src, void* dst, long long n, cudaStream_t st);
 
 // ---- dispatch, combine, losses, optimizer (dispatch.cu)
-constexpr int ROUTE_CHUNK = 1024;   // routed assignments per scatter chunk
+// Routed assignments per dispatch chunk (one warp walks a chunk in the
+// scatter): about ROUTE_TARGET_CHUNKS chunks, a multiple of 32 assignments
+// between ROUTE_CHUNK_MIN and ROUTE_CHUNK_MAX.  Any chunking gives the same
+// result; so at most max(ROUTE_TARGET_CHUNKS, ceil(R / ROUTE_CHUNK_MAX)) chunks.
+constexpr int ROUTE_CHUNK_MIN = 256;
+constexpr int ROUTE_CHUNK_MAX = 1024;
+constexpr int ROUTE_TARGET_CHUNKS = 608;   // four per SM
+int route_chunk(long long R);
 int route_chunks(long long R);
 cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
                                cudaStream_t st);
