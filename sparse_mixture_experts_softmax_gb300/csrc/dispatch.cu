@@ -530,25 +530,36 @@ sum_partials_kernel(const float* __restrict__ p, int nparts, long long n, float*
 }
 
 // theta <- theta - lr * grad (fp32 master); optional bf16 working copy (RNE).
-__global__ void __launch_bounds__(256)
-sgd_kernel(float* __restrict__ w, const float* __restrict__ g, long long n4, float lr,
-           bf16* __restrict__ w_lp) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+// Several tensors per launch: element i of the concatenated float4 index
+// space belongs to the first tensor whose running end4 exceeds i.
+struct SgdList {
+  float* w[SGD_MAX_TENSORS];
+  const float* g[SGD_MAX_TENSORS];
+  bf16* lp[SGD_MAX_TENSORS];
+  long long end4[SGD_MAX_TENSORS];   // running sums of n / 4
+  int count;
+};
+__global__ void __launch_bounds__(256) sgd_kernel(const SgdList L, float lr) {
+  const long long total = L.end4[L.count - 1];
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
-    float4 wv = reinterpret_cast<float4*>(w)[i];
-    const float4 gv = reinterpret_cast<const float4*>(g)[i];
+    int t = 0;
+    while (i >= L.end4[t]) ++t;
+    const long long j = i - (t > 0 ? L.end4[t - 1] : 0);
+    float4 wv = reinterpret_cast<float4*>(L.w[t])[j];
+    const float4 gv = reinterpret_cast<const float4*>(L.g[t])[j];
     wv.x = fmaf(-lr, gv.x, wv.x);
     wv.y = fmaf(-lr, gv.y, wv.y);
     wv.z = fmaf(-lr, gv.z, wv.z);
     wv.w = fmaf(-lr, gv.w, wv.w);
-    reinterpret_cast<float4*>(w)[i] = wv;
-    if (w_lp != nullptr) {
+    reinterpret_cast<float4*>(L.w[t])[j] = wv;
+    if (L.lp[t] != nullptr) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(wv.x, wv.y);
       __nv_bfloat162 hi = __floats2bfloat162_rn(wv.z, wv.w);
       uint2 q;
       q.x = *reinterpret_cast<uint32_t*>(&lo);
       q.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(w_lp)[i] = q;
+      reinterpret_cast<uint2*>(L.lp[t])[j] = q;
     }
   }
 }
@@ -718,11 +729,23 @@ cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_sgd(float* w, const float* g, long long n, float lr, void* w_lp,
-                       cudaStream_t st) {
+cudaError_t launch_sgd(const SgdTensor* tensors, int count, float lr, cudaStream_t st) {
+  if (count < 1 || count > SGD_MAX_TENSORS) return cudaErrorInvalidValue;
+  SgdList L{};
+  long long total = 0;
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    if (tensors[i].n == 0) continue;
+    total += tensors[i].n / 4;   // every parameter tensor holds a multiple of 8 elements
+    L.w[n] = tensors[i].w;
+    L.g[n] = tensors[i].g;
+    L.lp[n] = static_cast<bf16*>(tensors[i].w_lp);
+    L.end4[n] = total;
+    ++n;
+  }
   if (n == 0) return cudaSuccess;
-  long long n4 = n / 4;   // every parameter tensor holds a multiple of 8 elements
-  sgd_kernel<<<grid_for(n4, 256, 152 * 16), 256, 0, st>>>(w, g, n4, lr, static_cast<bf16*>(w_lp));
+  L.count = n;
+  sgd_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, st>>>(L, lr);
   return cudaGetLastError();
 }
 

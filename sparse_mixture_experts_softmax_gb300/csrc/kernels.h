@@ -100,8 +100,17 @@ cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets
                                   float* out, cudaStream_t st);
 cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,
                                 cudaStream_t st);
-cudaError_t launch_sgd(float* w, const float* g, long long n, float lr, void* w_lp,
-                       cudaStream_t st);
+// SGD on up to SGD_MAX_TENSORS fp32 tensors in one launch: w -= lr * g over
+// n elements (a multiple of 4) of each, and w_lp (bf16 copy, or null)
+// rewritten from the result with round-to-nearest-even.
+constexpr int SGD_MAX_TENSORS = 6;
+struct SgdTensor {
+  float* w;
+  const float* g;
+  long long n;
+  void* w_lp;
+};
+cudaError_t launch_sgd(const SgdTensor* tensors, int count, float lr, cudaStream_t st);
 cudaError_t launch_fill_zero(void* p, size_t bytes, cudaStream_t st);
 
 // ---- grouped GEMMs (gemm_simt_f32.cu for fp32; gemm_tc.cu for bf16 on tcgen05)

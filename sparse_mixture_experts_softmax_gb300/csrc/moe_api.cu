@@ -657,8 +657,10 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
                        ra, P.at<float>(L.dlogits), lp ? P.at<void>(L.dl_lp) : nullptr, st));
   if (lp) {
     // tensor-core router products: dW_g = dlogits^T x (split over token
-    // chunks, fixed-order sum) and dX = dlogits W_g + scatter-back of dXe
-    KL("cast_wg", launch_cast_bf16(w.w_gate, P.at<void>(L.wg_lp), (long long)c.E * c.D, st));
+    // chunks, fixed-order sum) and dX = dlogits W_g + scatter-back of dXe.
+    // W_g's bf16 copy is the forward's, still in the workspace: the backward
+    // runs with the forward's weights, and a training step updates W_g only
+    // after the backward.
     const int S = dwg_splits(c.T);
     GemmArgs rg{};
     rg.a_type = rg.b_type = MOE_BF16;
@@ -871,16 +873,20 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   // SGD on the fp32 masters; bf16 working copies rewritten from the result
   const long long E = c.E, D = c.D, F = c.F;
   const moe_grads& g = p->grads;
-  KL("sgd", launch_sgd(p->w_gate, g.dw_gate, E * D, lr, nullptr, st));
+  // one launch for every tensor the GEMM epilogues did not update
+  SgdTensor ts[SGD_MAX_TENSORS];
+  int nt = 0;
+  ts[nt++] = {p->w_gate, g.dw_gate, E * D, nullptr};
   if (!fused) {
-    KL("sgd", launch_sgd(p->w1, g.dw1, E * F * D, lr, nullptr, st));
-    if (c.act == MOE_ACT_SWIGLU) KL("sgd", launch_sgd(p->w3, g.dw3, E * F * D, lr, nullptr, st));
-    KL("sgd", launch_sgd(p->w2, g.dw2, E * D * F, lr, nullptr, st));
+    ts[nt++] = {p->w1, g.dw1, E * F * D, nullptr};
+    if (c.act == MOE_ACT_SWIGLU) ts[nt++] = {p->w3, g.dw3, E * F * D, nullptr};
+    ts[nt++] = {p->w2, g.dw2, E * D * F, nullptr};
   }
   if (c.has_bias) {
-    KL("sgd", launch_sgd(p->b1, g.db1, E * F, lr, nullptr, st));
-    KL("sgd", launch_sgd(p->b2, g.db2, E * D, lr, nullptr, st));
+    ts[nt++] = {p->b1, g.db1, E * F, nullptr};
+    ts[nt++] = {p->b2, g.db2, E * D, nullptr};
   }
+  KL("sgd", launch_sgd(ts, nt, lr, st));
   return MOE_OK;
 }
 
