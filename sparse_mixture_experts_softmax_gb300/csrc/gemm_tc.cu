@@ -499,9 +499,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         if (FORM == FORM_TN && kb == T.nkb - 1) {
           const int valid = T.kend - (T.kbeg + kb * BK);
           if (valid < BK) {
-            // rows past the expert's last row: zero them in both A boxes
+            // rows past the expert's last row: zero them in both operands
+            // (the two A and the four B boxes, each BK rows of 128 bytes;
+            // whole rows are invariant under the 128-byte swizzle).  Zeroing
+            // A alone is not enough: rows past the last kept row of an
+            // expert capacity are never written, and 0 * NaN is NaN.
             const int nchunk = (BK - valid) * 8;   // 16-byte chunks per box
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < 6; ++j) {
               uint4* dst = reinterpret_cast<uint4*>(smem + s * STAGE_BYTES + j * (64 * BK * 2) + valid * 128);
               for (int c = lane; c < nchunk; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
             }
