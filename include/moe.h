@@ -251,6 +251,16 @@ MOE_API moe_status moe_get_intermediates(const moe_config* cfg, const void* work
                                  size_t workspace_bytes, void* ye, void* dxe, float* dlogits,
                                  void* stream);
 
+/* Copies the expert pre-activations of the last forward out of `workspace`
+ * for inspection (device, either may be NULL), [R,F] each in cfg.dtype with
+ * rows in the expert-major slot order of moe_get_routing: h1 = X_e W1^T (+ b1)
+ * for ReLU / GELU experts (the backward's activation derivative reads it) or
+ * H1 = X_e W1^T for SwiGLU; h3 = X_e W3^T (SwiGLU only, else
+ * MOE_ERR_INVALID_ARG).  Rows past the last kept row of an expert capacity
+ * are unspecified.  Device-to-device copies on `stream`. */
+MOE_API moe_status moe_get_hidden(const moe_config* cfg, const void* workspace,
+                                  size_t workspace_bytes, void* h1, void* h3, void* stream);
+
 /* Reads the device status word of the last call that used `workspace`: 0, or
  * MOE_ERR_TIMEOUT when a bounded device-side wait of a tensor-core kernel
  * expired (that kernel then stopped early and its outputs are invalid).

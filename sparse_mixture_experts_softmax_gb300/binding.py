@@ -108,12 +108,15 @@ def lib() -> ctypes.CDLL:
         L.moe_profile_ms.restype = c_float
         L.moe_dispatch_noalloc.argtypes = [P(moe_config)] + [c_void_p] * 6
         L.moe_device_status.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p]
+        L.moe_get_hidden.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
+                                     c_void_p]
         L.moe_grouped_gemm.argtypes = [c_int32] * 5 + [c_void_p] * 6
         L.moe_selftest_wait_timeout.argtypes = [c_int32] * 5 + [c_void_p] * 5 + [ctypes.c_int64,
                                                                                 c_void_p]
         for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
                    "moe_train_steps_host",
-                   "moe_get_routing", "moe_get_intermediates", "moe_dispatch_noalloc",
+                   "moe_get_routing", "moe_get_intermediates", "moe_get_hidden",
+                   "moe_dispatch_noalloc",
                    "moe_device_status", "moe_grouped_gemm", "moe_selftest_wait_timeout"):
             getattr(L, fn).restype = c_int32
         _lib = L
@@ -235,6 +238,12 @@ def moe_get_intermediates(cfg, workspace, ye=None, dxe=None, dlogits=None, strea
     _check("moe_get_intermediates",
            lib().moe_get_intermediates(ctypes.byref(cfg), _ptr(workspace), workspace.numel(),
                                        _ptr(ye), _ptr(dxe), _ptr(dlogits), _stream(stream)))
+
+
+def moe_get_hidden(cfg, workspace, h1=None, h3=None, stream=None):
+    _check("moe_get_hidden",
+           lib().moe_get_hidden(ctypes.byref(cfg), _ptr(workspace), workspace.numel(),
+                                _ptr(h1), _ptr(h3), _stream(stream)))
 
 
 def moe_status_string(status: int) -> str:

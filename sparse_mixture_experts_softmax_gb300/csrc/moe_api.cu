@@ -1157,6 +1157,23 @@ moe_status moe_get_intermediates(const moe_config* cfg, const void* workspace,
   return MOE_OK;
 }
 
+moe_status moe_get_hidden(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
+                          void* h1, void* h3, void* stream) {
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  if (h3 != nullptr && c.act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  Layout L = make_layout(c);
+  const char* b = static_cast<const char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)c.T * c.k * c.F * esize(c.dtype);
+  if (h1 != nullptr && bytes > 0)
+    CK(cudaMemcpyAsync(h1, b + L.h1, bytes, cudaMemcpyDeviceToDevice, st));
+  if (h3 != nullptr && bytes > 0)
+    CK(cudaMemcpyAsync(h3, b + L.h3, bytes, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
 moe_status moe_device_status(const moe_config* cfg, const void* workspace, size_t workspace_bytes,
                              int32_t* status_host, void* stream) {
   RET_IF(validate_config(cfg));

@@ -110,3 +110,14 @@ class MoELayer:
                    slot_of=torch.empty(c.T, c.k, dtype=torch.int32, device=dev))
         B.moe_get_routing(c, self.workspace, **out)
         return out
+
+    def hidden(self) -> dict:
+        """The last forward's expert pre-activations [R, F] in the layer dtype:
+        h1 (H, or H1 for SwiGLU) and h3 (SwiGLU only)."""
+        c = self.cfg
+        R = max(c.T * c.k, 1)
+        dt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        h1 = torch.empty(R, c.F, dtype=dt, device=self.device)
+        h3 = torch.empty(R, c.F, dtype=dt, device=self.device) if c.act == 2 else None
+        B.moe_get_hidden(c, self.workspace, h1=h1, h3=h3)
+        return dict(h1=h1, h3=h3)

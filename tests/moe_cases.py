@@ -5,8 +5,11 @@ The oracle side receives exactly the values the CUDA side computes with:
 fp32 draws for fp32 layers; for bf16 layers the bf16-rounded x and expert
 weights (widened to float64), the bf16 copy of the router weight that the
 router GEMM multiplies with, and the fp32 masters for the SGD update.  Nothing
-the oracle consumes comes out of the CUDA library, except a routing that has
-first been validated against the oracle's own (see ``validated_routing``).
+the oracle consumes comes out of the CUDA library, except two kinds of
+decision that floating point takes and that both sides must take in the
+kernel's precision, each first validated against the oracle's own: a routing
+(``validated_routing``: near-ties of the selection keys) and ReLU derivatives
+at pre-activations within rounding of zero (``validated_relu_decisions``).
 """
 
 from __future__ import annotations
@@ -86,6 +89,41 @@ def assert_close(name, got, want, tol):
     err = rel_err(got, want)
     assert err <= tol, f"{name}: max-norm relative error {err:.3e} > {tol:.1e}"
     return err
+
+
+def validated_relu_decisions(cfg: O.OracleConfig, st: dict, w: dict, h_kernel) -> int:
+    """The ReLU derivative 1[h > 0] is a decision taken in floating point: a
+    pre-activation within accumulation error of zero can fall on the kernel's
+    side of zero differently from the float64 one.  Where the signs of the
+    kernel's stored H (expert-major rows, the layer dtype) and the oracle's
+    differ, check that the oracle's value is within a bound far above fp32
+    accumulation error of zero (2^-14 * sum |x w| (+ |b|)), then let the
+    oracle's backward take the kernel's decision (h set to a signed tiny value
+    there; the forward values already computed are unchanged).  Returns the
+    number of decisions taken from the kernel."""
+    if cfg.act != "relu":
+        return 0
+    hk = np.asarray(h_kernel, dtype=np.float64)
+    taken = 0
+    for e in range(cfg.E):
+        lo, hi = int(st["offsets"][e]), int(st["offsets"][e + 1])
+        if hi == lo:
+            continue
+        fe = st["experts"][e]
+        h64 = fe["h"]
+        differ = (hk[lo:hi] > 0.0) != (h64 > 0.0)
+        if not differ.any():
+            continue
+        scale = np.abs(st["xe"][lo:hi]) @ np.abs(w["w1"][e]).T
+        if cfg.has_bias:
+            scale = scale + np.abs(w["b1"][e])
+        assert np.all(np.abs(h64[differ]) <= 2.0 ** -14 * scale[differ]), \
+            f"expert {e}: ReLU decisions differ beyond rounding of a zero pre-activation"
+        h_new = h64.copy()
+        h_new[differ] = np.where(hk[lo:hi][differ] > 0.0, 1e-300, -1e-300)
+        fe["h"] = h_new
+        taken += int(differ.sum())
+    return taken
 
 
 def check_routing_exact(cfg: O.OracleConfig, r: dict, corr_bias=None):

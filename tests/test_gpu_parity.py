@@ -12,7 +12,8 @@ import torch
 import workloads as W
 from oracle import moe_oracle as O
 from tests.moe_cases import (TOL, assert_close, check_routing_exact, device_x, make_layer, np64,
-                             oracle_config, oracle_inputs, rel_err, validated_routing)
+                             oracle_config, oracle_inputs, rel_err, validated_relu_decisions,
+                             validated_routing)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,6 +49,10 @@ def _one_step_parity(wl, seed=0, check_dx=True):
     idx = validated_routing(cfg, st0["scores"], r["idx"].cpu().numpy(),
                             corr_bias=w_fwd.get("corr_bias"))
     st = O.forward(cfg, w_fwd, x64, idx)
+    if wl.act == "relu":
+        # kept rows only: rows past the last kept row of a capacity are unspecified
+        h_kept = layer.hidden()["h1"][: int(r["offsets"][-1].item())]
+        validated_relu_decisions(cfg, st, w_fwd, np64(h_kept))
     l_mse, aux, dy = O.losses(cfg, st, t64)
     g = O.backward(cfg, w_fwd, x64, st, dy)
     errs = {}

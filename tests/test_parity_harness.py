@@ -1,0 +1,71 @@
+"""The parity harness's validated ReLU decisions, checked on the CPU against
+planted kernel pre-activations: a sign flip at a pre-activation within
+rounding of zero is taken from the kernel (and changes the oracle's dH there
+only), and a flip anywhere else fails."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from tests.moe_cases import validated_relu_decisions
+
+
+def _case():
+    cfg = O.OracleConfig(T=24, D=16, F=8, E=3, k=2, act="relu", score="softmax",
+                         has_bias=True, aux_alpha=0.0)
+    rng = np.random.default_rng(5)
+    w = dict(w_gate=rng.normal(0, 0.3, (3, 16)), w1=rng.normal(0, 0.3, (3, 8, 16)),
+             w2=rng.normal(0, 0.3, (3, 16, 8)), w3=None, b1=rng.normal(0, 0.1, (3, 8)),
+             b2=np.zeros((3, 16)))
+    x = rng.normal(0, 1, (24, 16))
+    return cfg, w, x
+
+
+def _kernel_h(st):
+    """The oracle's own H in expert-major rows: what an exact kernel would store."""
+    R = int(st["offsets"][-1])
+    h = np.zeros((R, 8))
+    for e in range(3):
+        lo, hi = int(st["offsets"][e]), int(st["offsets"][e + 1])
+        h[lo:hi] = st["experts"][e]["h"]
+    return h
+
+
+def test_no_flip_takes_nothing():
+    cfg, w, x = _case()
+    st = O.forward(cfg, w, x)
+    assert validated_relu_decisions(cfg, st, w, _kernel_h(st)) == 0
+
+
+def test_flip_within_rounding_is_taken_from_the_kernel():
+    cfg, w, x = _case()
+    st = O.forward(cfg, w, x)
+    lo = int(st["offsets"][1])
+    # plant an exactly representable near-zero pre-activation in the oracle's
+    # H of expert 1 (row 0, column 3), negative in float64 ...
+    st["experts"][1]["h"][0, 3] = -1e-9
+    hk = _kernel_h(st)
+    hk[lo, 3] = 1e-9          # ... and positive in the kernel's
+    dy = np.random.default_rng(6).normal(0, 1, (24, 16))
+    g_before = O.backward(cfg, w, x, st, dy)
+    assert validated_relu_decisions(cfg, st, w, hk) == 1
+    assert st["experts"][1]["h"][0, 3] > 0
+    g_after = O.backward(cfg, w, x, st, dy)
+    # dW1 of expert 1 changes in row 3 only; the other experts are untouched
+    diff = np.abs(g_after["dw1"] - g_before["dw1"]) > 0
+    assert diff[1, 3].any() and not diff[1, :3].any() and not diff[1, 4:].any()
+    assert not diff[0].any() and not diff[2].any()
+
+
+def test_flip_beyond_rounding_fails():
+    cfg, w, x = _case()
+    st = O.forward(cfg, w, x)
+    hk = _kernel_h(st)
+    e = next(e for e in range(3) if st["offsets"][e + 1] > st["offsets"][e])
+    lo = int(st["offsets"][e])
+    j = int(np.argmax(np.abs(st["experts"][e]["h"][0])))
+    hk[lo, j] = -st["experts"][e]["h"][0, j]     # a clear sign error in the kernel
+    with pytest.raises(AssertionError):
+        validated_relu_decisions(cfg, st, w, hk)
