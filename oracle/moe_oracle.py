@@ -270,7 +270,7 @@ def route(cfg: OracleConfig, scores: np.ndarray,
 def expert_capacity(cfg: "OracleConfig") -> Optional[int]:
     """Rows an expert may process, or None without a capacity factor.
 
-    READING: the pages name a capacity factor that "models drop/padding"
+    READING: the pages name a capacity factor for dropping or padding tokens
     ("AI Infra Kernel Lab", the distributed validator) but give no formula;
     the plainest reading is the usual one, C = ceil(cf * T * k / E)."""
     if cfg.capacity_factor <= 0:
