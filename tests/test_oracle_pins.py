@@ -666,8 +666,8 @@ def test_shared_zero_down_projection_is_identity():
 
 
 # ----------------------------------------------------- capacity / dropping ---
-# Reading of the capacity factor ("AI Infra Kernel Lab" names it as modelling
-# drop/padding): C = ceil(cf T k / E); an expert keeps its first C assignments
+# Reading of the capacity factor ("AI Infra Kernel Lab" names it for dropping
+# or padding tokens): C = ceil(cf T k / E); an expert keeps its first C assignments
 # in token order, the rest contribute nothing and get no gradient.
 
 def test_capacity_formula_and_no_drop_limit():
