@@ -1,0 +1,119 @@
+"""The synthetic input recipe (workloads.py), checked on the CPU against the
+configurations it stands for: each named layer has the shapes and options of
+its configuration, and the seeded draws have the stated distributions (weights
+N(0, 1/fan_in), zero biases, x ~ N(0, 1), teacher targets with N(0, 0.01)
+noise, the skewed layer's Zipf logit bias with its excluded experts, the large
+layer's uniform router init).  Draws are deterministic per seed, and the bf16
+copies are round-to-nearest casts of the fp32 draws."""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+import workloads as W
+
+# (T, D, F, E, k, act, score, n_groups, topk_groups, has_bias, dtype, aux_alpha, lr)
+CONFIGS = {
+    "tiny": (64, 32, 64, 4, 2, "relu", "softmax", 1, 1, True, "f32", 0.01, 0.05),
+    "dense_f32": (4096, 512, 1024, 8, 2, "gelu_tanh", "softmax", 1, 1, True, "f32", 0.01, 0.01),
+    "dense_bf16": (4096, 512, 1024, 8, 2, "gelu_tanh", "softmax", 1, 1, True, "bf16", 0.01,
+                   0.01),
+    "grouped": (16384, 1024, 704, 64, 6, "swiglu", "sigmoid", 8, 4, False, "bf16", 0.0, 1e-3),
+    "skewed": (32768, 2048, 1408, 64, 8, "swiglu", "softmax", 1, 1, False, "bf16", 0.01, 1e-3),
+    "large": (65536, 4096, 2048, 128, 8, "swiglu", "softmax", 1, 1, False, "bf16", 0.01, 1e-3),
+}
+
+
+def test_named_layers_have_their_configurations():
+    for name, want in CONFIGS.items():
+        wl = W.WORKLOADS[name]
+        got = (wl.T, wl.D, wl.F, wl.E, wl.k, wl.act, wl.score, wl.n_groups, wl.topk_groups,
+               wl.has_bias, wl.dtype, wl.aux_alpha, wl.lr)
+        assert got == want, name
+    assert W.WORKLOADS["tiny"].steps == 20
+    assert W.WORKLOADS["large"].router_init == "uniform"
+    assert W.WORKLOADS["skewed"].zipf_skew == 1.2 and W.WORKLOADS["skewed"].zipf_empty == 4
+
+
+def _std_close(t, std, rel=0.02):
+    s = float(t.float().std())
+    assert abs(s - std) <= rel * std, (s, std)
+
+
+def test_weight_and_input_distributions():
+    # the dense layer at its full width (a few million draws), fewer tokens
+    wl = W.WORKLOADS["dense_f32"].with_tokens(2048)
+    inp = W.make_inputs(wl, seed=0)
+    _std_close(inp["w_gate"], 1.0 / math.sqrt(wl.D))
+    _std_close(inp["w1"], 1.0 / math.sqrt(wl.D))
+    _std_close(inp["w2"], 1.0 / math.sqrt(wl.F))
+    assert inp["w3"] is None
+    assert torch.count_nonzero(inp["b1"]) == 0 and torch.count_nonzero(inp["b2"]) == 0
+    x = inp["x"]
+    assert abs(float(x.mean())) < 0.01
+    _std_close(x, 1.0)
+    # y = x A + eps with A ~ N(0, 1/D), eps ~ N(0, 0.01): var(y) = 1 + 0.01
+    _std_close(inp["target"], math.sqrt(1.01))
+
+
+def test_swiglu_layers_draw_w3_and_no_biases():
+    wl = dataclasses.replace(W.WORKLOADS["grouped"], T=256)
+    inp = W.make_inputs(wl, seed=0)
+    _std_close(inp["w3"], 1.0 / math.sqrt(wl.D))
+    assert inp["b1"] is None and inp["b2"] is None
+
+
+def test_large_layer_router_init_is_uniform():
+    # the large layer's options at reduced widths (the init law depends on D only)
+    wl = dataclasses.replace(W.WORKLOADS["large"], T=64, D=1024, F=64, E=128)
+    w = W.make_inputs(wl, seed=0, with_target=False)["w_gate"]
+    a = 1.0 / math.sqrt(wl.D)
+    assert float(w.abs().max()) <= a
+    _std_close(w, a / math.sqrt(3.0))   # U(-a, a) has std a / sqrt(3)
+
+
+def test_skewed_layer_logit_bias():
+    wl = W.WORKLOADS["skewed"]
+    lb = W.zipf_logit_bias(wl, seed=0).numpy()
+    dead = np.isneginf(lb)
+    assert int(dead.sum()) == 4   # four experts receive no tokens
+    live = np.sort(lb[~dead])[::-1]
+    ranks = np.arange(1, wl.E - wl.zipf_empty + 1)
+    np.testing.assert_allclose(live, -1.2 * np.log(ranks), rtol=1e-6, atol=1e-6)
+    # the dead experts do not all sit at one end of the id range
+    ids = np.nonzero(dead)[0]
+    assert not (np.all(ids >= wl.E - 4) or np.all(ids < 4))
+
+
+def test_draws_are_seeded_and_bf16_copies_round_to_nearest():
+    wl = W.WORKLOADS["dense_bf16"].with_tokens(128)
+    a = W.make_inputs(wl, seed=3)
+    b = W.make_inputs(wl, seed=3)
+    c = W.make_inputs(wl, seed=4)
+    for key in ("w_gate", "w1", "w2", "x", "target"):
+        assert torch.equal(a[key], b[key]), key
+        assert not torch.equal(a[key], c[key]), key
+    for key in ("x", "w1", "w2"):
+        assert torch.equal(a[key + "_bf16"], a[key].to(torch.bfloat16)), key
+        # round to nearest: the bf16 value is within half a bf16 ulp of the draw
+        v = a[key].double()
+        r = a[key + "_bf16"].double()
+        ulp = torch.where(v != 0, 2.0 ** (torch.floor(torch.log2(v.abs())) - 7),
+                          torch.zeros_like(v))
+        assert bool(torch.all((r - v).abs() <= ulp / 2 + 1e-30)), key
+
+
+def test_side_draws_do_not_move_the_main_draws():
+    # the correction bias and the shared weights come from their own generators
+    base = dataclasses.replace(W.WORKLOADS["grouped"], T=64)
+    plain = W.make_inputs(base, seed=0)
+    extra = W.make_inputs(dataclasses.replace(base, corr_bias_scale=0.1, n_shared=1), seed=0)
+    for key in ("w_gate", "w1", "w3", "w2", "x", "target"):
+        assert torch.equal(plain[key], extra[key]), key
+    cb = extra["corr_bias"]
+    assert cb.shape == (base.E,) and float(cb.abs().max()) <= 0.1
+    assert extra["ws1"].shape == (base.F, base.D) and extra["ws2"].shape == (base.D, base.F)
