@@ -140,6 +140,22 @@ def test_pipelined_host_steps_validation(L):
                    _Fake(0xA00008, 1 << 30), ws) == B.MOE_ERR_ALIGNMENT
 
 
+def test_inspection_accessors_validation(L):
+    good = lambda i: _Fake(0x10000 * (i + 1))  # noqa: E731
+    ws = _Fake(0x900000, 1 << 40)
+    small = _Fake(0x900000, 1024)
+    # workspace checks before any copy
+    assert _status(B.moe_get_hidden, _cfg(), small, good(1)) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert _status(B.moe_get_hidden, _cfg(), _Fake(0x900008, 1 << 40), good(1)) \
+        == B.MOE_ERR_ALIGNMENT
+    assert _status(B.moe_get_intermediates, _cfg(), small, good(1)) \
+        == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    # H3 exists only for SwiGLU experts
+    assert _status(B.moe_get_hidden, _cfg(), ws, good(1), good(2)) == B.MOE_ERR_INVALID_ARG
+    # an invalid configuration is refused first
+    assert _status(B.moe_get_hidden, _cfg(k=0), ws, good(1)) == B.MOE_ERR_INVALID_ARG
+
+
 def test_status_strings(L):
     for s in range(7):
         assert B.moe_status_string(s)
