@@ -118,6 +118,7 @@ class MoELayer:
         R = max(c.T * c.k, 1)
         dt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
         h1 = torch.empty(R, c.F, dtype=dt, device=self.device)
-        h3 = torch.empty(R, c.F, dtype=dt, device=self.device) if c.act == 2 else None
+        h3 = (torch.empty(R, c.F, dtype=dt, device=self.device)
+              if c.act == B.ACT["swiglu"] else None)
         B.moe_get_hidden(c, self.workspace, h1=h1, h3=h3)
         return dict(h1=h1, h3=h3)
