@@ -790,3 +790,30 @@ def test_hand_worked_router_dispatch_aux():
     np.testing.assert_array_equal(slot_of, np.array(g["slot_of"]).astype(int))
     aux, _, _ = O.aux_loss(counts, p, 2)
     assert abs(aux - g["aux_num"][0][0] / g["aux_den"][0][0]) <= 1e-15
+
+
+def test_hand_worked_grouped_router():
+    """The group-limited router on a hand-derived case: group scores by top-2
+    sums (not whole-group sums), group ties to the smaller group id, expert
+    ties to the smaller id, renormalised sigmoid gates, stable dispatch and
+    the aux value 53/16."""
+    g = _golden("hand_worked_grouped_router.txt")
+    m = np.array(g["m"])
+    s = m / 32.0
+    cfg = O.OracleConfig(T=3, D=1, F=1, E=9, k=3, score="sigmoid", n_groups=3, topk_groups=2,
+                         group_score="top2_sum")
+    # the logits ln(m / (32 - m)) give the scores back through the sigmoid
+    np.testing.assert_allclose(O.router_scores(cfg, np.log(m / (32.0 - m))), s,
+                               rtol=0, atol=1e-15)
+    idx = O.route(cfg, s)
+    np.testing.assert_array_equal(idx, np.array(g["idx"]).astype(int))
+    gate = O.renormalize(s, idx)
+    want = np.array(g["gate_num"]) / np.array(g["gate_den"])
+    np.testing.assert_allclose(gate, want, rtol=0, atol=1e-15)
+    counts, offsets, src_tok, _, slot_of = O.dispatch(idx, 9)
+    np.testing.assert_array_equal(counts, np.array(g["counts"][0]).astype(int))
+    np.testing.assert_array_equal(offsets, np.array(g["offsets"][0]).astype(int))
+    np.testing.assert_array_equal(src_tok, np.array(g["src_tok"][0]).astype(int))
+    np.testing.assert_array_equal(slot_of, np.array(g["slot_of"]).astype(int))
+    aux, _, _ = O.aux_loss(counts, s, 3)
+    assert abs(aux - g["aux_num"][0][0] / g["aux_den"][0][0]) <= 1e-15
