@@ -817,3 +817,25 @@ def test_hand_worked_grouped_router():
     np.testing.assert_array_equal(slot_of, np.array(g["slot_of"]).astype(int))
     aux, _, _ = O.aux_loss(counts, s, 3)
     assert abs(aux - g["aux_num"][0][0] / g["aux_den"][0][0]) <= 1e-15
+
+
+def test_hand_worked_expert_mlp():
+    """One token through one ReLU expert with biases, every value by hand."""
+    g = _golden("hand_worked_expert_mlp.txt")
+    arr = lambda key: np.array(g[key])  # noqa: E731
+    cfg = O.OracleConfig(T=1, D=2, F=2, E=1, k=1, act="relu", score="softmax",
+                         has_bias=True, aux_alpha=0.0)
+    w = dict(w_gate=np.zeros((1, 2)), w1=arr("w1")[None], w2=arr("w2")[None],
+             b1=arr("b1"), b2=arr("b2"))
+    x = arr("x")
+    st = O.forward(cfg, w, x)
+    np.testing.assert_array_equal(st["experts"][0]["h"], arr("h"))
+    np.testing.assert_array_equal(st["y"], arr("y"))
+    l_mse, aux, dy = O.losses(cfg, st, arr("target"))
+    assert l_mse == g["mse"][0][0] and aux == g["aux"][0][0]
+    gr = O.backward(cfg, w, x, st, dy)
+    np.testing.assert_array_equal(gr["dw2"][0], arr("dw2"))
+    np.testing.assert_array_equal(gr["db2"][0], arr("db2")[0])
+    np.testing.assert_array_equal(gr["dw1"][0], arr("dw1"))
+    np.testing.assert_array_equal(gr["db1"][0], arr("db1")[0])
+    np.testing.assert_array_equal(gr["dx"], arr("dx"))
