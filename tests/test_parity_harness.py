@@ -1,7 +1,12 @@
-"""The parity harness's validated ReLU decisions, checked on the CPU against
-planted kernel pre-activations: a sign flip at a pre-activation within
-rounding of zero is taken from the kernel (and changes the oracle's dH there
-only), and a flip anywhere else fails."""
+"""The parity harness's two validated floating-point decisions, checked on
+the CPU against planted kernel outputs.
+
+- ReLU derivatives: a sign flip at a pre-activation within rounding of zero
+  is taken from the kernel, and changes the oracle's dH there only. A flip
+  anywhere else fails.
+- Routing: a selection that differs from the oracle's own only on near-tied
+  (or exactly tied) keys is taken from the kernel. Any other difference fails.
+"""
 
 from __future__ import annotations
 
@@ -9,7 +14,7 @@ import numpy as np
 import pytest
 
 from oracle import moe_oracle as O
-from tests.moe_cases import validated_relu_decisions
+from tests.moe_cases import validated_relu_decisions, validated_routing
 
 
 def _case():
@@ -69,3 +74,47 @@ def test_flip_beyond_rounding_fails():
     hk[lo, j] = -st["experts"][e]["h"][0, j]     # a clear sign error in the kernel
     with pytest.raises(AssertionError):
         validated_relu_decisions(cfg, st, w, hk)
+
+
+# ------------------------------------------------------- validated routing ---
+# The other floating-point decision the harness takes from the kernel: a
+# routing that differs from the oracle's own only on near-ties of the keys.
+
+def _route_case():
+    cfg = O.OracleConfig(T=4, D=1, F=1, E=6, k=2, score="softmax")
+    scores = np.array([[0.30, 0.25, 0.20, 0.10, 0.10, 0.05],
+                       [0.20, 0.20, 0.20, 0.20, 0.10, 0.10],
+                       [0.05, 0.40, 0.40 - 1e-9, 0.05, 0.05, 0.05],
+                       [0.10, 0.10, 0.10, 0.10, 0.30, 0.30]])
+    return cfg, scores
+
+
+def test_identical_routing_is_the_oracles():
+    cfg, s = _route_case()
+    idx = O.route(cfg, s)
+    np.testing.assert_array_equal(validated_routing(cfg, s, idx.copy()), idx)
+
+
+def test_near_tie_flip_is_taken_from_the_kernel():
+    cfg, s = _route_case()
+    idx = O.route(cfg, s)
+    assert list(idx[2]) == [1, 2]   # 0.40 ahead of 0.40 - 1e-9
+    kernel = idx.copy()
+    kernel[2] = [2, 1]              # rounding put the near-tied pair the other way round
+    out = validated_routing(cfg, s, kernel)
+    np.testing.assert_array_equal(out[2], [2, 1])
+    np.testing.assert_array_equal(np.delete(out, 2, axis=0), np.delete(idx, 2, axis=0))
+    # an exact tie broken the other way round is a near-tie too (distance 0)
+    kernel = idx.copy()
+    kernel[1] = [2, 3]              # 0.20 x 4: the oracle keeps 0, 1 (smaller ids)
+    out = validated_routing(cfg, s, kernel)
+    np.testing.assert_array_equal(out[1], [2, 3])
+
+
+def test_routing_flip_beyond_rounding_fails():
+    cfg, s = _route_case()
+    idx = O.route(cfg, s)
+    kernel = idx.copy()
+    kernel[0] = [0, 3]              # 0.10 instead of 0.25: not a near-tie
+    with pytest.raises(AssertionError):
+        validated_routing(cfg, s, kernel)
