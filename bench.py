@@ -81,6 +81,23 @@ def expert_flops_per_step(wl: W.Workload, rows: Optional[int] = None) -> float:
     return 3.0 * proj * 2.0 * wl.D * wl.F * (wl.R if rows is None else rows)
 
 
+def gemm_launch_flops(wl: W.Workload, rows: Optional[int] = None) -> dict:
+    """Algorithmic FLOPs per training step of each named expert-GEMM launch
+    (2 flops per multiply-add over the rows the experts process).  The SwiGLU
+    up-projection multiplies by W1 and W3 in one launch; the dX launch sums
+    dH1 W1 + dH3 W3.  Summed, they give ``expert_flops_per_step``."""
+    R = wl.R if rows is None else rows
+    one = 2.0 * R * wl.D * wl.F
+    if wl.act == "swiglu" and wl.dtype == "bf16":
+        return {"gemm_up": 2 * one, "gemm_down": one, "gemm_dA": one, "gemm_dw2": one,
+                "gemm_dxe": 2 * one, "gemm_dw1": one, "gemm_dw3": one}
+    if wl.act == "swiglu":
+        return {"gemm_up": one, "gemm_up_w3": one, "gemm_down": one, "gemm_dA": one,
+                "gemm_dw2": one, "gemm_dxe": 2 * one, "gemm_dw1": one, "gemm_dw3": one}
+    return {"gemm_up": one, "gemm_down": one, "gemm_dA": one, "gemm_dw2": one,
+            "gemm_dxe": one, "gemm_dw1": one}
+
+
 def shared_flops_per_step(wl: W.Workload) -> float:
     """The shared-expert branch (reported separately from the routed experts):
     three projections of 2*T*D*(n_shared*F) FLOPs, forward and twice that in
@@ -106,6 +123,8 @@ def hbm_bytes(wl: W.Workload, rows: Optional[int] = None) -> dict:
         # training step (k <= 8): combine, MSE seed and combine backward in one
         # pass: Ye and the target read, dYe written
         "combine_fused": 2 * R * D * es + T * D * 4,
+        # dX = router term + sum_j dXe[slot(t, j)]: dXe read, dX read and written
+        "scatter_back": R * D * es + 2 * T * D * 4,
         # the stand-alone SGD launches: master and gradient read, master
         # written.  bf16 layers update the expert weights inside the dW GEMM
         # epilogues, so only the router weight and biases remain here.
@@ -226,12 +245,26 @@ def oracle_sample_step(wl: W.Workload, T_s: int, E_s: int, seed: int = 0):
     cfg = O.OracleConfig(T=T_s, D=wl.D, F=wl.F, E=E_s, k=wl.k, act=wl.act, score=wl.score,
                          n_groups=n_groups, topk_groups=topk_groups, has_bias=wl.has_bias,
                          aux_alpha=wl.aux_alpha, capacity_factor=wl.capacity_factor)
+    # the oracle's train step, its SGD timed apart: the same calls as
+    # O.train_step, in its order
     t0 = time.perf_counter()
-    O.train_step(cfg, w, x, tgt, wl.lr)
-    dt = time.perf_counter() - t0
+    st = O.forward(cfg, w, x)
+    _, _, dy = O.losses(cfg, st, tgt)
+    grads = O.backward(cfg, w, x, st, dy)
+    t1 = time.perf_counter()
+    O.sgd(w, grads, wl.lr)
+    t2 = time.perf_counter()
     desc = (f"oracle train step (fwd+bwd+SGD, float64 numpy) on {T_s} tokens of the "
             f"{wl.name} layer (D={wl.D}, F={wl.F}, k={wl.k}) over {E_s} of its {wl.E} experts")
-    return dt, desc
+    return t1 - t0, t2 - t1, desc
+
+
+def extrapolated_rate(wl: W.Workload, T_s: int, E_s: int, t_tok: float, t_sgd: float) -> float:
+    """Tokens/s of a whole step of the workload from a sample: the per-token
+    part (router, dispatch, experts, combine, losses, backward) scales with T
+    / T_s; the SGD part updates every parameter once per step and scales with
+    the E / E_s experts (router and biases included in that share)."""
+    return wl.T / (t_tok * wl.T / T_s + t_sgd * wl.E / E_s)
 
 
 def sample_size(wl: W.Workload):
@@ -255,24 +288,31 @@ def run_reference(args, wl):
     if rank != 0:
         return
     T_s, E_s = sample_size(wl)
-    times = []
+    tok, sgd = [], []
     desc = ""
     for i in range(args.warmup + args.steps):
-        dt, desc = oracle_sample_step(wl, T_s, E_s)
+        t_tok, t_sgd, desc = oracle_sample_step(wl, T_s, E_s)
         if i >= args.warmup:
-            times.append(dt)
-    total = sum(times)
-    value = T_s * len(times) / total
+            tok.append(t_tok)
+            sgd.append(t_sgd)
+    t_tok, t_sgd = sum(tok) / len(tok), sum(sgd) / len(sgd)
+    value = extrapolated_rate(wl, T_s, E_s, t_tok, t_sgd)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "ms_per_step": 1e3 * wl.T / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
-                             "kind": "oracle", "sample": desc},
+                             "kind": "oracle", "sample": desc,
+                             "extrapolated": extrapolation_note(wl, T_s, E_s, t_tok, t_sgd)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def extrapolation_note(wl, T_s, E_s, t_tok, t_sgd) -> str:
+    return (f"extrapolated from a sample: whole-step time = {t_tok:.3f} s x {wl.T}/{T_s} tokens "
+            f"+ SGD {t_sgd:.3f} s x {wl.E}/{E_s} experts")
 
 
 def workload_config(wl: W.Workload) -> dict:
@@ -283,6 +323,16 @@ def workload_config(wl: W.Workload) -> dict:
             "n_shared": wl.n_shared, "corr_bias": wl.corr_bias_scale is not None,
             "capacity_factor": wl.capacity_factor,
             "l2": "inputs larger than L2 (weights and expert-major activations >> 129 MB)"}
+
+
+def routing_summary(layer, wl: W.Workload) -> dict:
+    """Realised load of the step's routing: the share of the T k assignments
+    taken by the three busiest experts, the largest and smallest expert
+    loads, and the experts that received none."""
+    counts = sorted((int(c) for c in layer.routing()["counts"].cpu().tolist()), reverse=True)
+    R = max(wl.T * wl.k, 1)
+    return {"top3_share": round(sum(counts[:3]) / R, 4), "max_rows": counts[0],
+            "min_rows": counts[-1], "empty_experts": sum(1 for c in counts if c == 0)}
 
 
 def main():
@@ -299,6 +349,9 @@ def main():
                     help="override T (profiling a smaller case of the same layer)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (profiling a smaller case of the same layer)")
+    ap.add_argument("--store-grads", action="store_true",
+                    help="hand out every fp32 gradient (default: the step applies them "
+                         "in the fused SGD without storing them)")
     args = ap.parse_args()
     wl = W.WORKLOADS[args.workload]
     if args.tokens is not None or args.experts is not None:
@@ -336,7 +389,8 @@ def main():
                      w1_lp=inp.get("w1_bf16"), w3_lp=inp.get("w3_bf16"),
                      w2_lp=inp.get("w2_bf16"), device=str(dev), corr_bias=inp.get("corr_bias"),
                      n_shared=wl.n_shared, ws1=inp.get("ws1"), ws3=inp.get("ws3"),
-                     ws2=inp.get("ws2"), capacity_factor=wl.capacity_factor)
+                     ws2=inp.get("ws2"), capacity_factor=wl.capacity_factor,
+                     store_grads=args.store_grads)
     x = (inp["x_bf16"] if lp else inp["x"]).contiguous()
     tgt = inp["target"].contiguous()
     dx = torch.empty(wl.T, wl.D, device=dev)
@@ -410,13 +464,33 @@ def main():
         bound, unit = "alu", "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": gemm_traffic(wl),
-                "traffic_unit": "DRAM bytes per step of the GEMM family (ncu, scaled)",
+                "traffic_unit": "DRAM bytes per step of the GEMM family",
+                "traffic_measured_in_this_run": False,
+                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of every "
+                                   "expert-GEMM launch at 8 experts, scaled by 16 "
+                                   "(profiles/tc_gemm_large_e8_traffic.md); null when the GEMM "
+                                   "source differs from the one captured"),
                 "kernel": "grouped expert GEMMs (all launches of one step)",
                 "peak_source": f"{peaks['source']} ({'bf16_tflops_sustained' if lp else 'FFMA at max clock'})"}
+    if lp:
+        burst = float(peaks["bf16_tflops"])
+        roofline["peak_burst"] = burst
+        roofline["frac_of_burst"] = achieved / burst
+    # each expert-GEMM launch on its own (FLOPs per step / its time per step)
+    launches_tc = {}
+    for name, fl in gemm_launch_flops(wl, rows_kept).items():
+        ms = per_kernel.get(name, 0.0)
+        if ms > 0:
+            tf = fl / (ms / 1e3) / 1e12
+            launches_tc[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                 "frac": round(tf / peak, 4)}
+            if lp:
+                launches_tc[name]["frac_of_burst"] = round(tf / float(peaks["bf16_tflops"]), 4)
     hb = hbm_bytes(wl, rows_kept)
     hbm = {}
     for name, key in (("gather", "gather"), ("combine_loss", "combine_loss"),
-                      ("combine_bwd", "combine_bwd"), ("combine_fused", "combine_fused")) + \
+                      ("combine_bwd", "combine_bwd"), ("combine_fused", "combine_fused"),
+                      ("scatter_back", "scatter_back")) + \
             ((("sgd", "sgd"),) if not lp else ()):
         if name in per_kernel and per_kernel[name] > 0:
             gbs = hb[key] / (per_kernel[name] / 1e3) / 1e9
@@ -428,7 +502,8 @@ def main():
             "dtype": "bf16" if lp else "f32", "data": "synthetic", "config": workload_config(wl),
             "expert_gemm_tflops": achieved, "router_gflop_per_step": router_flops_per_step(wl) / 1e9,
             "expert_gflop_per_step": eflops / 1e9, "expert_rows_per_step": rows_kept,
-            "roofline": roofline, "hbm_passes": hbm,
+            "roofline": roofline, "gemm_launches": launches_tc, "hbm_passes": hbm,
+            "routing": routing_summary(layer, wl),
             "gpu_launches": launches * args.steps, "clocks": clk,
             "step_ms": {"p50": step_ms[len(step_ms) // 2],
                         "p90": step_ms[min(len(step_ms) - 1, int(0.9 * len(step_ms)))],
@@ -436,6 +511,10 @@ def main():
             "warmup_ms": [round(v, 3) for v in warm_ms],
             "loss": {"mse": loss[0], "aux": loss[1]},
             "kernels_ms_per_step": {k_: round(v, 4) for k_, v in sorted(per_kernel.items())}}
+    line["config"]["gradients"] = (
+        "every fp32 gradient stored" if args.store_grads else
+        "applied by SGD, not handed out (NULL gradient buffers): bf16 layers update the "
+        "expert weights inside the weight-gradient GEMMs and store no fp32 gradient")
     if wl.n_shared > 0 and shared_ms > 0:
         sf = shared_flops_per_step(wl)
         line["shared_experts"] = {"n_shared": wl.n_shared, "gflop_per_step": sf / 1e9,
@@ -466,9 +545,11 @@ def main():
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         T_s, E_s = sample_size(wl)
-        dt, desc = oracle_sample_step(wl, T_s, E_s)
-        line["cpu_baseline"] = {"value": T_s / dt, "unit": "tokens/s", "cores": cpu_cores(),
-                                "kind": "oracle", "sample": desc}
+        t_tok, t_sgd, desc = oracle_sample_step(wl, T_s, E_s)
+        line["cpu_baseline"] = {"value": extrapolated_rate(wl, T_s, E_s, t_tok, t_sgd),
+                                "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc,
+                                "extrapolated": extrapolation_note(wl, T_s, E_s, t_tok, t_sgd)}
     if args.kernels and rank == 0:
         for k_, v in sorted(per_kernel.items(), key=lambda kv: -kv[1]):
             print(f"{k_:20s} {v:9.3f} ms", file=sys.stderr)

@@ -171,7 +171,17 @@ typedef struct {
   void* ws1_lp;             /* their bf16 copies, rewritten by the step   */
   void* ws3_lp;
   void* ws2_lp;
-  moe_grads grads;          /* gradient buffers, written by the step     */
+  moe_grads grads;          /* gradient buffers, written by the step.
+                               Any member may be NULL: the step still
+                               computes that gradient and applies it to
+                               its parameter, but does not hand it out.
+                               For MOE_BF16 layers a NULL dw1 / dw3 / dw2
+                               (dws1 / dws3 / dws2) also saves the HBM
+                               traffic of storing it: the SGD update runs
+                               inside the weight-gradient GEMM, which then
+                               writes only the updated master and its
+                               bf16 copy.  The updated parameters are
+                               bit-identical either way.                */
 } moe_params;
 
 /* Bytes of device workspace the forward / backward / train step need for one
@@ -203,7 +213,8 @@ MOE_API moe_status moe_backward(const moe_config* cfg, const moe_weights* w, con
  * for W_g, W1, W3, W2, b1, b2.  x is in cfg.dtype (it must equal the bf16
  * rounding the expert weights' copies use for MOE_BF16); y_target [T,D] fp32.
  * d_loss: device float[2] receiving (L_mse, aux) of the forward, before the
- * update.  dx, when not NULL, receives dL/dx [T,D] fp32. */
+ * update.  dx, when not NULL, receives dL/dx [T,D] fp32.  p->grads members
+ * may be NULL (see moe_params). */
 MOE_API moe_status moe_train_step(const moe_config* cfg, const moe_params* p, const void* x,
                           const float* y_target, float lr, float* d_loss, float* dx,
                           void* workspace, size_t workspace_bytes, void* stream);
@@ -277,7 +288,11 @@ MOE_API moe_status moe_device_status(const moe_config* cfg, const void* workspac
  *   form 1: C[r,n] = sum_k A[r,k] B[e,k,n]    A [M,K], B [E,K,N], C [M,N] bf16
  *   form 2: C[e,m,n] = sum_{r in e} A[r,m] B[r,n]
  *                                            A [K,M], B [K,N], C [E,M,N] fp32
- * (forms 0/1: M = total rows; form 2: K = total rows).  The contiguous
+ * (forms 0/1: M = total rows; form 2: K = total rows).  Offsets that break
+ * these rules are clamped on the device to a non-decreasing sequence within
+ * [0, total rows] (each entry raised to its predecessor, then capped), so no
+ * access leaves A, B or C; rows outside the clamped segments are not
+ * written.  The contiguous
  * dimensions must be multiples of 8: N always, K for forms 0/1, M for form 2.  dev_status: device int32, set to
  * MOE_ERR_TIMEOUT if a bounded wait expired (the caller zeroes it). */
 MOE_API moe_status moe_grouped_gemm(int32_t form, int32_t M, int32_t N, int32_t K, int32_t E,
@@ -319,7 +334,10 @@ MOE_API float moe_profile_ms(int32_t i);
  * have no counterpart of this entry point: it is a deployment convenience.
  *
  * Given idx [T,k] (each entry in [0,E)), writes counts [E], offsets [E+1],
- * src_tok [T*k] and slot_of [T,k] exactly as moe_forward's dispatch does.  The
+ * src_tok [T*k] and slot_of [T,k] exactly as moe_forward's dispatch does,
+ * including the expert capacity of cfg->capacity_factor (a NaN or negative
+ * factor is MOE_ERR_INVALID_ARG, as for moe_forward).  An idx entry outside
+ * [0,E) is not counted and gets slot_of = -1.  The
  * per-chunk scratch counts live in one fixed device array inside the library
  * (1 MiB on every GPU that loads it, held until the process exits), so T*k
  * must not exceed MOE_NOALLOC_MAX_ROUTED (MOE_ERR_UNSUPPORTED otherwise).  It

@@ -57,6 +57,15 @@ class moe_params(ctypes.Structure):
                [("grads", moe_grads)]
 
 
+class moe_ep_config(ctypes.Structure):
+    _fields_ = [("n_ranks", c_int32), ("rank", c_int32), ("T_total", c_int32)]
+
+
+class moe_ep_rows(ctypes.Structure):
+    _fields_ = [("rows", c_int32)] + [(n, c_void_p) for n in (
+        "offsets", "x", "h1", "h3", "a", "y", "dy", "dh1", "dh3", "dx", "status")]
+
+
 class MoEError(RuntimeError):
     def __init__(self, fn: str, status: int, text: str):
         super().__init__(f"{fn}: {text} (status {status})")
@@ -113,6 +122,27 @@ def lib() -> ctypes.CDLL:
         L.moe_grouped_gemm.argtypes = [c_int32] * 5 + [c_void_p] * 6
         L.moe_selftest_wait_timeout.argtypes = [c_int32] * 5 + [c_void_p] * 5 + [ctypes.c_int64,
                                                                                 c_void_p]
+        L.moe_ep_workspace_size.argtypes = [P(moe_config), P(moe_ep_config)]
+        L.moe_ep_workspace_size.restype = c_size_t
+        L.moe_ep_buffer_offsets.argtypes = [P(moe_config), P(moe_ep_config), P(c_size_t)]
+        L.moe_ep_route.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights), c_void_p,
+                                   c_void_p, c_void_p, c_size_t, c_void_p]
+        L.moe_ep_expert_forward.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights),
+                                            P(moe_ep_rows), c_void_p]
+        L.moe_ep_combine.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+        L.moe_ep_expert_backward.argtypes = [P(moe_config), P(moe_ep_config), P(moe_params),
+                                             P(moe_ep_rows), c_float, c_void_p]
+        L.moe_ep_router_backward.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_void_p,
+                                             c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+        L.moe_ep_router_update.argtypes = [P(moe_config), c_void_p, c_void_p, c_float, c_void_p]
+        L.moe_ep_get_routing.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_size_t] + \
+            [c_void_p] * 8
+        for fn in ("moe_ep_buffer_offsets", "moe_ep_get_routing", "moe_ep_route",
+                   "moe_ep_expert_forward",
+                   "moe_ep_combine", "moe_ep_expert_backward", "moe_ep_router_backward",
+                   "moe_ep_router_update"):
+            getattr(L, fn).restype = c_int32
         for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
                    "moe_train_steps_host",
                    "moe_get_routing", "moe_get_intermediates", "moe_get_hidden",
@@ -298,3 +328,72 @@ def moe_selftest_wait_timeout(form, M, N, K, E, offsets, A, B, C, dev_status, li
            lib().moe_selftest_wait_timeout(int(form), int(M), int(N), int(K), int(E),
                                            _ptr(offsets), _ptr(A), _ptr(B), _ptr(C),
                                            _ptr(dev_status), int(limit_ns), _stream(stream)))
+
+
+# ---- expert-parallel phases (include/moe_ep.h)
+
+def make_ep_rows(rows: int, offsets, x=None, h1=None, h3=None, a=None, y=None, dy=None,
+                 dh1=None, dh3=None, dx=None, status=None) -> moe_ep_rows:
+    return moe_ep_rows(int(rows), _ptr(offsets), _ptr(x), _ptr(h1), _ptr(h3), _ptr(a), _ptr(y),
+                       _ptr(dy), _ptr(dh1), _ptr(dh3), _ptr(dx), _ptr(status))
+
+
+def moe_ep_workspace_size(cfg, ep) -> int:
+    return int(lib().moe_ep_workspace_size(ctypes.byref(cfg), ctypes.byref(ep)))
+
+
+def moe_ep_buffer_offsets(cfg, ep):
+    """Byte offsets of (x_e, y_e, dy_e, dx_e) inside the rank's workspace."""
+    out = (c_size_t * 4)()
+    _check("moe_ep_buffer_offsets",
+           lib().moe_ep_buffer_offsets(ctypes.byref(cfg), ctypes.byref(ep), out))
+    return [int(v) for v in out]
+
+
+def moe_ep_get_routing(cfg, ep, workspace, scores=None, idx=None, gate=None, counts=None,
+                       offsets=None, src_tok=None, slot_of=None, stream=None):
+    _check("moe_ep_get_routing",
+           lib().moe_ep_get_routing(ctypes.byref(cfg), ctypes.byref(ep), _ptr(workspace),
+                                    workspace.numel(), _ptr(scores), _ptr(idx), _ptr(gate),
+                                    _ptr(counts), _ptr(offsets), _ptr(src_tok), _ptr(slot_of),
+                                    _stream(stream)))
+
+
+def moe_ep_route(cfg, ep, weights, x, score_sum, workspace, stream=None):
+    _check("moe_ep_route",
+           lib().moe_ep_route(ctypes.byref(cfg), ctypes.byref(ep), ctypes.byref(weights), _ptr(x),
+                              _ptr(score_sum), _ptr(workspace), workspace.numel(),
+                              _stream(stream)))
+
+
+def moe_ep_expert_forward(cfg, ep, weights, rows, stream=None):
+    _check("moe_ep_expert_forward",
+           lib().moe_ep_expert_forward(ctypes.byref(cfg), ctypes.byref(ep), ctypes.byref(weights),
+                                       ctypes.byref(rows), _stream(stream)))
+
+
+def moe_ep_combine(cfg, ep, counts_total, score_sum_total, y_target, d_loss, workspace,
+                   stream=None):
+    _check("moe_ep_combine",
+           lib().moe_ep_combine(ctypes.byref(cfg), ctypes.byref(ep), _ptr(counts_total),
+                                _ptr(score_sum_total), _ptr(y_target), _ptr(d_loss),
+                                _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_ep_expert_backward(cfg, ep, params, rows, lr, stream=None):
+    _check("moe_ep_expert_backward",
+           lib().moe_ep_expert_backward(ctypes.byref(cfg), ctypes.byref(ep), ctypes.byref(params),
+                                        ctypes.byref(rows), float(lr), _stream(stream)))
+
+
+def moe_ep_router_backward(cfg, ep, w_gate, x, dw_gate_part, dx, workspace, stream=None):
+    _check("moe_ep_router_backward",
+           lib().moe_ep_router_backward(ctypes.byref(cfg), ctypes.byref(ep), _ptr(w_gate), _ptr(x),
+                                        _ptr(dw_gate_part), _ptr(dx), _ptr(workspace),
+                                        workspace.numel(), _stream(stream)))
+
+
+def moe_ep_router_update(cfg, w_gate, dw_gate, lr, stream=None):
+    _check("moe_ep_router_update",
+           lib().moe_ep_router_update(ctypes.byref(cfg), _ptr(w_gate), _ptr(dw_gate), float(lr),
+                                      _stream(stream)))

@@ -91,7 +91,8 @@ route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int cap, int* __rest
 
 // Stable scatter: one warp walks its chunk in token order; lanes holding the
 // same expert are ranked by lane id (match_any), so slots keep token order.
-// An assignment of rank >= cap within its expert is dropped (slot -1).
+// An assignment of rank >= cap within its expert is dropped (slot -1), and so
+// is one whose expert id lies outside [0, E) (the count skipped it too).
 __global__ void __launch_bounds__(32)
 route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k, int E, int cap,
                      const int* __restrict__ chunk_base, const int* __restrict__ offsets,
@@ -122,6 +123,8 @@ route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k,
         src_tok[slot] = (int)(f / k);
       }
       slot_of[f] = slot;
+    } else if (valid) {
+      slot_of[f] = -1;   // an expert id outside [0, E): no slot
     }
     __syncwarp();
     if (e >= 0 && lane == __ffs(peers) - 1) cursor[e] += __popc(peers);
@@ -623,9 +626,9 @@ int combine_blocks(int T) { return (T + CB_TOK - 1) / CB_TOK; }
 
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of, int T,
                            int D, int k, const void* ys, float* y, const float* target, float* dy,
-                           double* sq_partial, cudaStream_t st) {
+                           double* sq_partial, cudaStream_t st, float inv_n) {
   if (T == 0) return cudaSuccess;
-  float inv_n = 1.0f / ((float)T * (float)D);
+  if (inv_n == 0.f) inv_n = 1.0f / ((float)T * (float)D);
   int grid = combine_blocks(T);
   if (dtype == 1)
     combine_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T, D, k,
@@ -641,12 +644,12 @@ cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const i
 cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
                                  int T, int D, int k, const void* ys, const float* target,
                                  double* sq_partial, void* dye, float* dgate, void* dy_lp,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, float inv_n) {
   // the shared branch exists only for bf16 layers and comes with both Ys and dY
   const bool shared = ys != nullptr;
   if (k > 8 || (shared && (dy_lp == nullptr || dtype != 1))) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
-  const float inv_n = 1.0f / ((float)T * (float)D);
+  if (inv_n == 0.f) inv_n = 1.0f / ((float)T * (float)D);
   const int grid = combine_blocks(T);
   if (dtype == 1 && shared)
     combine_train_kernel<bf16, true><<<grid, 32 * CT_WARPS, 0, st>>>(

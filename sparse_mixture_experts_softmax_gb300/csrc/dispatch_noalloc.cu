@@ -65,6 +65,8 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t*
   if (cfg == nullptr) return MOE_ERR_INVALID_ARG;
   const moe_config& c = *cfg;
   if (c.T < 0 || c.k <= 0 || c.E <= 0) return MOE_ERR_INVALID_ARG;
+  // the routing fields are checked exactly as moe_forward checks them
+  if (!(c.capacity_factor >= 0.f) || c.capacity_factor > 1e6f) return MOE_ERR_INVALID_ARG;
   if (c.E > 256 || c.k > 32 || c.k > c.E) return MOE_ERR_UNSUPPORTED;
   const long long R = (long long)c.T * c.k;
   if (R > MOE_NOALLOC_MAX_ROUTED) return MOE_ERR_UNSUPPORTED;   // beyond the fixed scratch

@@ -336,6 +336,22 @@ struct Tile {
   int e, m0, n0, row_hi, kbeg, kend, nkb, nkb0;
 };
 
+// How many 16-column chunks ahead an epilogue loads its side inputs: the
+// fp32 master weights of the fused SGD step come from DRAM under a heavy
+// write stream, so they are fetched further ahead than the activation
+// backward's H1 / H3.
+#ifndef MOE_SGD_PREFETCH
+#define MOE_SGD_PREFETCH 3
+#endif
+#ifndef MOE_BWD_PREFETCH
+#define MOE_BWD_PREFETCH 3
+#endif
+template <int EPI>
+__host__ __device__ constexpr int side_prefetch() {
+  return EPI == EPI_SGD_F32_TAG ? MOE_SGD_PREFETCH
+         : (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) ? MOE_BWD_PREFETCH : 1;
+}
+
 template <int FORM>
 __device__ __forceinline__ Tile map_tile(int t, const TcParams& p, const int* offs,
                                          const int* tpre) {
@@ -412,9 +428,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (FORM != FORM_TN && tid == 0) {
-    tpre[0] = 0;
-    for (int e = 0; e < p.E; ++e) tpre[e + 1] = tpre[e] + (offs[e + 1] - offs[e] + BM - 1) / BM;
+  if (tid == 0) {
+    // Offsets given by a caller are clamped to a non-decreasing sequence
+    // within [0, total rows]: no tile then reads or stores past the row
+    // operands or C, whatever the table holds (the routing path's own
+    // offsets already satisfy this and are unchanged by it).
+    int prev = 0;
+    for (int e = 0; e <= p.E; ++e) {
+      const int v = min(max(offs[e], prev), p.seg_rows);
+      offs[e] = v;
+      prev = v;
+    }
+    if (FORM != FORM_TN) {
+      tpre[0] = 0;
+      for (int e = 0; e < p.E; ++e) tpre[e + 1] = tpre[e] + (offs[e + 1] - offs[e] + BM - 1) / BM;
+    }
   }
   __syncthreads();
   const uint32_t tmem_base = tmem_slot;
@@ -559,10 +587,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         // step leaves W as it is; its bf16 copy is still rewritten from W)
         if (FORM == FORM_TN && rok) {
           const size_t o = (size_t)T.e * p.sCe + (size_t)r * p.ldc;
-          float* c = static_cast<float*>(p.C) + o;
           const int nb = T.n0 + half * (BN / 2), ne = min(nb + BN / 2, p.N);
-          for (int n = nb; n < ne; n += 4)
-            *reinterpret_cast<float4*>(c + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.C != nullptr) {
+            float* c = static_cast<float*>(p.C) + o;
+            for (int n = nb; n < ne; n += 4)
+              *reinterpret_cast<float4*>(c + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           if (EPI == EPI_SGD_F32_TAG && p.sgd_wlp) {
             for (int n = nb; n < ne; n += 8) {
               float w[8];
@@ -584,7 +614,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       const int ncols = EPI == EPI_SWIGLU_UP ? 128 : BN;
       const int c_begin = half * (ncols / 2), c_end = c_begin + ncols / 2;
       const size_t wbase = (size_t)T.e * p.sCe;
-      // side inputs are fetched one chunk ahead, alternating two buffers
+      // side inputs are fetched PF chunks ahead into a ring of PF + 1
+      // register buffers (the first PF while the accumulator is still being
+      // produced)
+      constexpr int PF = side_prefetch<EPI>();
+      constexpr int NB = PF + 1;
       auto load_side = [&](int n, Side& d) {
         if (EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD) {
           load_bf16x4_rows(p.aux0, p.ld_aux, row0, T.row_hi, n, p.N, d.h1);
@@ -592,15 +626,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         }
         if (EPI == EPI_SGD_F32_TAG) load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, n, p.N, d.w);
       };
-      Side sa, sb;
-      load_side(T.n0 + c_begin + 4 * cq, sa);
+      Side sd[NB];
+#pragma unroll
+      for (int q = 0; q < PF; ++q)
+        if (c_begin + q * CHUNK < c_end) load_side(T.n0 + c_begin + q * CHUNK + 4 * cq, sd[q]);
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
       auto chunk = [&](int cc, const Side& use, Side& fill) {
         const int n = T.n0 + cc + 4 * cq;
-        if (cc + CHUNK < c_end) load_side(n + CHUNK, fill);
+        if (cc + PF * CHUNK < c_end) load_side(n + PF * CHUNK, fill);
         float4 acc[4], acc3[4];
         stage_chunk(stg, lane, t_row + cc, acc);
         if (EPI == EPI_SWIGLU_UP) stage_chunk(stg, lane, t_row + 128 + cc, acc3);
@@ -627,9 +663,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           } else if (EPI == EPI_STORE_F32_TAG) {
             st_ef(static_cast<float*>(p.C) + wbase + o, acc[j], pol);
           } else if (EPI == EPI_SGD_F32_TAG) {
-            // dW stored as is; the update uses the same fused multiply-add and
-            // round-to-nearest bf16 conversion as the stand-alone SGD kernel
-            st_ef(static_cast<float*>(p.C) + wbase + o, acc[j], pol);
+            // dW stored as is (unless the caller asked for no gradient); the
+            // update uses the same fused multiply-add and round-to-nearest
+            // bf16 conversion as the stand-alone SGD kernel
+            if (p.C != nullptr) st_ef(static_cast<float*>(p.C) + wbase + o, acc[j], pol);
             float w[4] = {use.w[j].x, use.w[j].y, use.w[j].z, use.w[j].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) w[i] = fmaf(-p.sgd_lr, x[i], w[i]);
@@ -670,11 +707,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           }
         }
       };
-      // an even number of chunks per warp: 8 (64 for SwiGLU-up tiles: 4)
+      // chunks per warp: 8 (SwiGLU-up tiles: 4), a multiple of NB; chunk i
+      // reads buffer i % NB and fills buffer (i + PF) % NB with chunk i + PF
+      static_assert(((EPI == EPI_SWIGLU_UP ? 64 : BN / 2) / CHUNK) % NB == 0, "whole rings");
 #pragma unroll 1
-      for (int cc = c_begin; cc < c_end; cc += 2 * CHUNK) {
-        chunk(cc, sa, sb);
-        chunk(cc + CHUNK, sb, sa);
+      for (int cc = c_begin; cc < c_end; cc += NB * CHUNK) {
+#pragma unroll
+        for (int q = 0; q < NB; ++q) chunk(cc + q * CHUNK, sd[q], sd[(q + PF) % NB]);
       }
       tc_fence_before();
       __syncwarp();
@@ -766,8 +805,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
   if (g.a_type != 1 || g.b_type != 1 || g.E > MAX_E) return cudaErrorInvalidValue;
   if (g.offsets == nullptr && g.seg_len <= 0) return cudaErrorInvalidValue;
-  // every pointer the chosen epilogue dereferences must be set
-  if (g.A0 == nullptr || g.B0 == nullptr || g.C == nullptr) return cudaErrorInvalidValue;
+  // every pointer the chosen epilogue dereferences must be set; a weight
+  // gradient with the SGD step fused may go unstored (C == nullptr)
+  const bool sgd_only = g.ragged_k && g.sgd_w != nullptr;
+  if (g.A0 == nullptr || g.B0 == nullptr || (g.C == nullptr && !sgd_only)) return cudaErrorInvalidValue;
   if ((g.epi == EPI_SWIGLU_UP && (g.B0x == nullptr || g.out1 == nullptr || g.out2 == nullptr)) ||
       (g.epi == EPI_ACT_FWD && g.out1 == nullptr) || (g.epi == EPI_ACT_BWD && g.aux0 == nullptr) ||
       (g.epi == EPI_SWIGLU_BWD && (g.aux0 == nullptr || g.aux1 == nullptr || g.out1 == nullptr)) ||

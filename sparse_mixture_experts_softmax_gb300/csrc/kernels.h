@@ -78,9 +78,11 @@ cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, i
                           void* xe, cudaStream_t st);
 int combine_blocks(int T);
 // ys: the shared-expert branch's output [T, D] added to Y, or nullptr.
+// inv_n: the MSE normaliser 1 / (tokens D); 0 takes 1 / (T D) (a single
+// device; an expert-parallel rank passes the one over all ranks' tokens).
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of,
                            int T, int D, int k, const void* ys, float* y, const float* target,
-                           float* dy, double* sq_partial, cudaStream_t st);
+                           float* dy, double* sq_partial, cudaStream_t st, float inv_n = 0.f);
 cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
                                    int n_ps, const int* counts, int T, int D, int E, int k,
                                    float alpha, float* d_loss, float* aux_row, cudaStream_t st);
@@ -89,7 +91,7 @@ cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const flo
 cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
                                  int T, int D, int k, const void* ys, const float* target,
                                  double* sq_partial, void* dye, float* dgate, void* dy_lp,
-                                 cudaStream_t st);
+                                 cudaStream_t st, float inv_n = 0.f);
 cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
                                const int* slot_of, int T, int D, int k, void* dye, float* dgate,
                                cudaStream_t st);

@@ -9,229 +9,198 @@
 #include <vector>
 
 #include "../../include/moe.h"
+#include "api_common.h"
 #include "kernels.h"
 
 using namespace moe;
+using namespace moe::api;
 
-namespace {
+namespace moe {
+namespace api {
 
-thread_local int g_launches = 0;
-
-// Optional per-kernel timing: CUDA events recorded around every kernel launch
-// of the calling thread's last entry-point call.
-struct ProfRec {
-  const char* name;
-  cudaEvent_t a, b;
-};
-thread_local bool g_prof = false;
-thread_local std::vector<ProfRec> g_prof_recs;
-thread_local int g_prof_n = 0;
-
-inline void prof_begin(const char* name, cudaStream_t st) {
-  if (!g_prof || g_prof_n >= 4096) return;
-  if (g_prof_n == (int)g_prof_recs.size()) {
-    ProfRec r{name, nullptr, nullptr};
-    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
-    g_prof_recs.push_back(r);
+// Expert MLPs over the row segments of `r` (course Part 5): up-projection
+// with bias + activation or the SwiGLU gate, then the down-projection.
+moe_status experts_forward(const moe_config& c, const ExpertW& w, const ExpertRows& r,
+                           cudaStream_t st) {
+  // expert up-projection (+ activation)
+  GemmArgs g = rows_gemm(c, r);
+  g.ragged_k = false;
+  g.a_kcontig = true;
+  g.b_kcontig = true;
+  g.M = r.M;
+  g.N = c.F;
+  g.A0 = r.xe;
+  g.lda = c.D;
+  g.K0 = c.D;
+  g.B0 = w.w1;
+  g.ldb = c.D;
+  g.sBe = (long long)c.F * c.D;
+  g.ldc = c.F;
+  g.ld_aux = c.F;
+  if (c.act == MOE_ACT_SWIGLU && c.dtype == MOE_BF16) {
+    // one launch: W1 and W3 tiles side by side in a 2 x 128-column accumulator
+    g.epi = EPI_SWIGLU_UP;
+    g.B0x = w.w3;
+    g.out1 = r.h1;
+    g.out2 = r.h3;
+    g.C = r.a;
+    KL("gemm_up", run_gemm(c, g, st));
+  } else if (c.act == MOE_ACT_SWIGLU) {
+    g.epi = EPI_STORE;
+    g.C = r.h1;
+    KL("gemm_up", run_gemm(c, g, st));
+    g.B0 = w.w3;
+    g.epi = EPI_SWIGLU_FWD;
+    g.aux0 = r.h1;
+    g.out1 = r.h3;
+    g.C = r.a;
+    KL("gemm_up_w3", run_gemm(c, g, st));
+  } else {
+    g.epi = EPI_ACT_FWD;
+    g.bias = w.b1;
+    g.out1 = r.h1;
+    g.C = r.a;
+    KL("gemm_up", run_gemm(c, g, st));
   }
-  g_prof_recs[g_prof_n].name = name;
-  cudaEventRecord(g_prof_recs[g_prof_n].a, st);
-}
-inline void prof_end(cudaStream_t st) {
-  if (!g_prof || g_prof_n >= 4096 || g_prof_n >= (int)g_prof_recs.size()) return;
-  cudaEventRecord(g_prof_recs[g_prof_n].b, st);
-  ++g_prof_n;
-}
+  // expert down-projection (+ bias)
+  GemmArgs d = rows_gemm(c, r);
+  d.ragged_k = false;
+  d.a_kcontig = true;
+  d.b_kcontig = true;
+  d.M = r.M;
+  d.N = c.D;
+  d.A0 = r.a;
+  d.lda = c.F;
+  d.K0 = c.F;
+  d.B0 = w.w2;
+  d.ldb = c.F;
+  d.sBe = (long long)c.D * c.F;
+  d.ldc = c.D;
+  d.epi = EPI_STORE;
+  d.bias = w.b2;
+  d.C = r.ye;
+  KL("gemm_down", run_gemm(c, d, st));
 
-constexpr size_t kAlign = 256;
-inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
-inline size_t esize(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// split-K factor of the router weight gradient dW_g = dlogits^T x
-inline int dwg_splits(int T) {
-  int s = T / 2048;
-  if (s < 1) s = 1;
-  if (s > 32) s = 32;
-  return s;
-}
-
-struct Layout {
-  size_t status, scores, idx, gate, counts, offsets, chunk, src_tok, slot_of, psum, sq, aux_row;
-  size_t xe, h1, h3, a, ye, dy, dye, dgate, dh1, dh3, dxe, dlogits, dwg_part, dx;
-  size_t logits, wg_lp, dl_lp;   // bf16 layers: router logits, bf16 W_g, bf16 dlogits
-  // shared-expert branch (n_shared > 0): H1s, H3s, As [T, Fs]; Ys [T, D]; bf16
-  // dY [T, D]; dH1s, dH3s [T, Fs]; dXs [T, D] (all bf16)
-  size_t hs1, hs3, as, ys, dy_lp, dhs1, dhs3, dxs;
-  size_t total;
-};
-
-Layout make_layout(const moe_config& c) {
-  Layout L{};
-  const size_t T = (size_t)c.T, D = (size_t)c.D, F = (size_t)c.F, E = (size_t)c.E;
-  const size_t R = T * (size_t)c.k;
-  const size_t es = esize(c.dtype);
-  const bool swiglu = c.act == MOE_ACT_SWIGLU;
-  size_t o = 0;
-  auto take = [&](size_t bytes) {
-    size_t at = o;
-    o += align_up(bytes > 0 ? bytes : 1);
-    return at;
-  };
-  L.status = take(16);
-  L.scores = take(T * E * 4);
-  L.idx = take(R * 4);
-  L.gate = take(R * 4);
-  L.counts = take(E * 4);
-  L.offsets = take((E + 1) * 4);
-  L.chunk = take((size_t)route_chunks((long long)R) * E * 4);
-  L.src_tok = take(R * 4);
-  L.slot_of = take(R * 4);
-  L.psum = take((size_t)router_fwd_blocks(c.T) * E * 4);
-  L.sq = take((size_t)combine_blocks(c.T) * 8);
-  L.aux_row = take(E * 4);
-  L.xe = take(R * D * es);
-  L.h1 = take(R * F * es);
-  L.h3 = swiglu ? take(R * F * es) : 0;
-  L.a = take(R * F * es);
-  L.ye = take(R * D * es);
-  L.dy = take(T * D * 4);
-  L.dye = take(R * D * es);
-  L.dgate = take(R * 4);
-  L.dh1 = take(R * F * es);
-  L.dh3 = swiglu ? take(R * F * es) : 0;
-  L.dxe = take(R * D * es);
-  L.dlogits = take(T * E * 4);
-  L.dwg_part = take((size_t)dwg_splits(c.T) * E * D * 4);
-  L.dx = take(T * D * 4);
-  const bool lp = c.dtype == MOE_BF16;
-  L.logits = lp ? take(T * E * 4) : 0;
-  L.wg_lp = lp ? take(E * D * 2) : 0;
-  L.dl_lp = lp ? take(T * E * 2) : 0;
-  if (c.n_shared > 0) {
-    const size_t Fs = (size_t)c.n_shared * F;
-    L.hs1 = take(T * Fs * 2);
-    L.hs3 = take(T * Fs * 2);
-    L.as = take(T * Fs * 2);
-    L.ys = take(T * D * 2);
-    L.dy_lp = take(T * D * 2);
-    L.dhs1 = take(T * Fs * 2);
-    L.dhs3 = take(T * Fs * 2);
-    L.dxs = take(T * D * 2);
-  }
-  L.total = o;
-  return L;
-}
-
-moe_status validate_config(const moe_config* c) {
-  if (c == nullptr) return MOE_ERR_INVALID_ARG;
-  if (c->T < 0 || c->D <= 0 || c->F <= 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
-  if (c->act < 0 || c->act > 2 || c->score < 0 || c->score > 1 || c->dtype < 0 || c->dtype > 1 ||
-      c->group_score < 0 || c->group_score > 1)
-    return MOE_ERR_INVALID_ARG;
-  if (c->n_groups <= 0 || c->topk_groups <= 0 || c->topk_groups > c->n_groups)
-    return MOE_ERR_INVALID_ARG;
-  if (c->E > 256 || c->k > 32 || c->k > c->E) return MOE_ERR_UNSUPPORTED;
-  if (c->E % c->n_groups != 0 || c->n_groups > 32) return MOE_ERR_UNSUPPORTED;
-  if ((long long)c->k > (long long)c->topk_groups * (c->E / c->n_groups)) return MOE_ERR_UNSUPPORTED;
-  if (c->D % 8 != 0 || c->F % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
-  if (c->dtype == MOE_BF16 && c->E % 8 != 0) return MOE_ERR_UNSUPPORTED;   // TMA row alignment
-  if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
-  if ((long long)c->T * c->D >= (1LL << 40)) return MOE_ERR_UNSUPPORTED;
-  if (c->n_shared < 0) return MOE_ERR_INVALID_ARG;
-  if (!(c->capacity_factor >= 0.f) || c->capacity_factor > 1e6f) return MOE_ERR_INVALID_ARG;
-  if (c->n_shared > 0 && (c->act != MOE_ACT_SWIGLU || c->dtype != MOE_BF16 ||
-                          (long long)c->n_shared * c->F > (1LL << 20)))
-    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
-// Device check, once per device: sm_103 only.
-moe_status check_device() {
-  static std::mutex mu;
-  static int checked[64] = {0};   // 0 unknown, 1 ok, 2 bad
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (checked[dev] == 0) {
-    int maj = 0, min = 0;
-    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    checked[dev] = (maj == 10 && min == 3) ? 1 : 2;
+// Backward of the expert MLPs over the row segments of `r` given dYe: dA with
+// the activation backward, dW2 (+ SGD), db2, dXe, dW1 / dW3 (+ SGD), db1.
+moe_status experts_backward(const moe_config& c, const ExpertW& w, const ExpertRows& r,
+                            const moe_grads& gr, const SgdFuse* sgd, cudaStream_t st) {
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  // dA = dYe W2_e with the activation backward in the epilogue
+  GemmArgs g = rows_gemm(c, r);
+  g.ragged_k = false;
+  g.a_kcontig = true;
+  g.b_kcontig = false;
+  g.M = r.M;
+  g.N = c.F;
+  g.A0 = r.dye;
+  g.lda = c.D;
+  g.K0 = c.D;
+  g.B0 = w.w2;
+  g.ldb = c.F;
+  g.sBe = (long long)c.D * c.F;
+  g.ldc = c.F;
+  g.ld_aux = c.F;
+  g.aux0 = r.h1;
+  g.C = r.dh1;
+  if (swiglu) {
+    g.epi = EPI_SWIGLU_BWD;
+    g.aux1 = r.h3;
+    g.out1 = r.dh3;
+  } else {
+    g.epi = EPI_ACT_BWD;
   }
-  return checked[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+  KL("gemm_dA", run_gemm(c, g, st));
+  // dW2_e = dYe_e^T A_e  (ragged K)
+  GemmArgs w2g = rows_gemm(c, r);
+  w2g.ragged_k = true;
+  w2g.a_kcontig = false;
+  w2g.b_kcontig = false;
+  w2g.c_type = MOE_F32;
+  w2g.M = c.D;
+  w2g.N = c.F;
+  w2g.A0 = r.dye;
+  w2g.lda = c.D;
+  w2g.B0 = r.a;
+  w2g.ldb = c.F;
+  w2g.K0 = r.M;
+  w2g.C = gr.dw2;
+  w2g.ldc = c.F;
+  w2g.sCe = (long long)c.D * c.F;
+  w2g.epi = EPI_STORE;
+  if (sgd) {
+    w2g.sgd_w = sgd->w2;
+    w2g.sgd_wlp = sgd->w2_lp;
+    w2g.sgd_lr = sgd->lr;
+  }
+  KL("gemm_dw2", run_gemm(c, w2g, st));
+  if (gr.db2) KL("bias_grad", launch_segment_colsum(c.dtype, r.dye, r.offsets, r.E, c.D, gr.db2, st));
+  // dXe = dH1 W1_e (+ dH3 W3_e)
+  GemmArgs xg = rows_gemm(c, r);
+  xg.ragged_k = false;
+  xg.a_kcontig = true;
+  xg.b_kcontig = false;
+  xg.M = r.M;
+  xg.N = c.D;
+  xg.A0 = r.dh1;
+  xg.lda = c.F;
+  xg.K0 = c.F;
+  xg.B0 = w.w1;
+  xg.ldb = c.D;
+  xg.sBe = (long long)c.F * c.D;
+  if (swiglu) {
+    xg.A1 = r.dh3;
+    xg.B1 = w.w3;
+    xg.K1 = c.F;
+  }
+  xg.ldc = c.D;
+  xg.epi = EPI_STORE;
+  xg.C = r.dxe;
+  KL("gemm_dxe", run_gemm(c, xg, st));
+  // dW1_e = dH1_e^T Xe_e (dW3 likewise)
+  GemmArgs w1g = rows_gemm(c, r);
+  w1g.ragged_k = true;
+  w1g.a_kcontig = false;
+  w1g.b_kcontig = false;
+  w1g.c_type = MOE_F32;
+  w1g.M = c.F;
+  w1g.N = c.D;
+  w1g.A0 = r.dh1;
+  w1g.lda = c.F;
+  w1g.B0 = r.xe;
+  w1g.ldb = c.D;
+  w1g.K0 = r.M;
+  w1g.C = gr.dw1;
+  w1g.ldc = c.D;
+  w1g.sCe = (long long)c.F * c.D;
+  w1g.epi = EPI_STORE;
+  if (sgd) {
+    w1g.sgd_w = sgd->w1;
+    w1g.sgd_wlp = sgd->w1_lp;
+    w1g.sgd_lr = sgd->lr;
+  }
+  KL("gemm_dw1", run_gemm(c, w1g, st));
+  if (swiglu) {
+    w1g.A0 = r.dh3;
+    w1g.C = gr.dw3;
+    if (sgd) {
+      w1g.sgd_w = sgd->w3;
+      w1g.sgd_wlp = sgd->w3_lp;
+    }
+    KL("gemm_dw3", run_gemm(c, w1g, st));
+  }
+  if (gr.db1) KL("bias_grad", launch_segment_colsum(c.dtype, r.dh1, r.offsets, r.E, c.F, gr.db1, st));
+  return MOE_OK;
 }
 
-// KL: a named kernel launch on stream `st` (counted, optionally timed);
-// CK: any other CUDA call.
-#define KL(name, expr)                           \
-  do {                                           \
-    prof_begin(name, st);                        \
-    cudaError_t _e = (expr);                     \
-    prof_end(st);                                \
-    ++g_launches;                                \
-    if (_e != cudaSuccess) return MOE_ERR_CUDA;  \
-  } while (0)
-#define CK(expr)                                 \
-  do {                                           \
-    cudaError_t _e = (expr);                     \
-    if (_e != cudaSuccess) return MOE_ERR_CUDA;  \
-  } while (0)
-
-struct Ptrs {
-  char* base;
-  const Layout* L;
-  template <typename T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
-};
-
-struct ExpertW {
-  const float* w_gate;
-  const void* w1;
-  const void* w3;
-  const void* w2;
-  const float* b1;
-  const float* b2;
-  const float* logit_bias;
-  const float* corr_bias;   // selection-only correction bias [E] or nullptr
-  const void* ws1;          // shared branch (bf16), or nullptr
-  const void* ws3;
-  const void* ws2;
-};
-
-RouterArgs router_args(const moe_config& c, const float* corr_bias = nullptr) {
-  RouterArgs a;
-  a.T = c.T; a.D = c.D; a.E = c.E; a.k = c.k; a.score = c.score;
-  a.n_groups = c.n_groups; a.topk_groups = c.topk_groups; a.group_score = c.group_score;
-  a.corr_bias = corr_bias;
-  return a;
-}
-
-GemmArgs gemm_base(const moe_config& c, const Ptrs& P) {
-  GemmArgs g{};
-  g.status = P.at<int>(P.L->status);
-  g.a_type = g.b_type = g.c_type = c.dtype;
-  g.offsets = P.at<int>(P.L->offsets);
-  g.E = c.E;
-  g.src_type = c.dtype;
-  g.act = c.act == MOE_ACT_GELU_TANH ? 1 : 0;
-  return g;
-}
-
-// Expert GEMMs: tcgen05 tensor cores for bf16 layers, CUDA cores for fp32.
-cudaError_t run_gemm(const moe_config& c, const GemmArgs& g, cudaStream_t st) {
-  if (c.dtype == MOE_BF16) return launch_gemm_tc(g, st);
-  return launch_gemm_simt(g, st);
-}
-
-// Forward: router -> dispatch -> experts -> combine.  With a target, combine
-// also forms dY and the squared-error partials, and the losses are finalised.
-// target_ready: recorded when `target` has landed (its copy may still be in
-// flight on another stream while the router and experts run), or nullptr.
-moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, float* y,
-                       const float* target, float* d_loss, const Ptrs& P, cudaStream_t st,
-                       cudaEvent_t target_ready = nullptr) {
+// Router and dispatch of the T tokens of `x` (course Parts 3 and 4): scores,
+// top-k and gates, counts, offsets and slot maps, and the gather into the
+// expert-major rows of the workspace.  Also clears the device status word.
+moe_status route_tokens(const moe_config& c, const ExpertW& w, const void* x, const Ptrs& P,
+                        cudaStream_t st) {
   const Layout& L = *P.L;
   const long long R = (long long)c.T * c.k;
   const RouterArgs ra = router_args(c, w.corr_bias);
@@ -278,65 +247,169 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
                                            P.at<int>(L.offsets), P.at<int>(L.src_tok),
                                            P.at<int>(L.slot_of), st));
   KL("gather", launch_gather(c.dtype, x, P.at<int>(L.slot_of), c.T, c.k, c.D, P.at<void>(L.xe), st));
+  return MOE_OK;
+}
 
-  // expert up-projection (+ activation)
-  GemmArgs g = gemm_base(c, P);
-  g.ragged_k = false;
-  g.a_kcontig = true;
-  g.b_kcontig = true;
-  g.M = (int)R;
-  g.N = c.F;
-  g.A0 = P.at<void>(L.xe);
-  g.lda = c.D;
-  g.K0 = c.D;
-  g.B0 = w.w1;
-  g.ldb = c.D;
-  g.sBe = (long long)c.F * c.D;
-  g.ldc = c.F;
-  g.ld_aux = c.F;
-  if (c.act == MOE_ACT_SWIGLU && c.dtype == MOE_BF16) {
-    // one launch: W1 and W3 tiles side by side in a 2 x 128-column accumulator
-    g.epi = EPI_SWIGLU_UP;
-    g.B0x = w.w3;
-    g.out1 = P.at<void>(L.h1);
-    g.out2 = P.at<void>(L.h3);
-    g.C = P.at<void>(L.a);
-    KL("gemm_up", run_gemm(c, g, st));
-  } else if (c.act == MOE_ACT_SWIGLU) {
-    g.epi = EPI_STORE;
-    g.C = P.at<void>(L.h1);
-    KL("gemm_up", run_gemm(c, g, st));
-    g.B0 = w.w3;
-    g.epi = EPI_SWIGLU_FWD;
-    g.aux0 = P.at<void>(L.h1);
-    g.out1 = P.at<void>(L.h3);
-    g.C = P.at<void>(L.a);
-    KL("gemm_up_w3", run_gemm(c, g, st));
-  } else {
-    g.epi = EPI_ACT_FWD;
-    g.bias = w.b1;
-    g.out1 = P.at<void>(L.h1);
-    g.C = P.at<void>(L.a);
-    KL("gemm_up", run_gemm(c, g, st));
+// Router backward (course Parts 3 and 6): renormalisation and aux gradient
+// to the scores, the score backward to dlogits, dW_g = dlogits^T x and
+// dX = dlogits W_g + the expert rows of each token scattered back (+ extra_dx,
+// a [T, D] block in the layer dtype, or nullptr).  Uses the gate gradients
+// and the aux row the combine and the loss finalisation left in the
+// workspace.
+moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x, float* dw_gate,
+                           float* dx, const void* extra_dx, const Ptrs& P, cudaStream_t st) {
+  const Layout& L = *P.L;
+  // router: renormalisation + aux + score backward
+  const RouterArgs ra = router_args(c);
+  const bool lp = c.dtype == MOE_BF16;
+  KL("router_bwd", launch_router_bwd(P.at<float>(L.scores), P.at<int>(L.idx), P.at<float>(L.gate),
+                       P.at<float>(L.dgate), c.aux_alpha != 0.f ? P.at<float>(L.aux_row) : nullptr,
+                       ra, P.at<float>(L.dlogits), lp ? P.at<void>(L.dl_lp) : nullptr, st));
+  if (lp) {
+    // tensor-core router products: dW_g = dlogits^T x (split over token
+    // chunks, fixed-order sum) and dX = dlogits W_g + scatter-back of dXe.
+    // W_g's bf16 copy is the forward's, still in the workspace: the backward
+    // runs with the forward's weights, and a training step updates W_g only
+    // after the backward.
+    const int S = dwg_splits(c.T);
+    GemmArgs rg{};
+    rg.a_type = rg.b_type = MOE_BF16;
+    rg.c_type = MOE_F32;
+    rg.status = P.at<int>(L.status);
+    rg.ragged_k = true;
+    rg.M = c.E;
+    rg.N = c.D;
+    rg.A0 = P.at<void>(L.dl_lp);
+    rg.lda = c.E;
+    rg.B0 = x;
+    rg.ldb = c.D;
+    rg.K0 = c.T;
+    rg.offsets = nullptr;
+    rg.E = S;
+    rg.seg_len = (c.T + S - 1) / S;
+    rg.C = P.at<void>(L.dwg_part);
+    rg.ldc = c.D;
+    rg.sCe = (long long)c.E * c.D;
+    rg.epi = EPI_STORE;
+    KL("gemm_router_dwg", launch_gemm_tc(rg, st));
+    KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D,
+                                             dw_gate, st));
+    GemmArgs dg{};
+    dg.a_type = dg.b_type = MOE_BF16;
+    dg.c_type = MOE_F32;
+    dg.status = P.at<int>(L.status);
+    dg.ragged_k = false;
+    dg.b_kcontig = false;
+    dg.M = c.T;
+    dg.N = c.D;
+    dg.K0 = c.E;
+    dg.A0 = P.at<void>(L.dl_lp);
+    dg.lda = c.E;
+    dg.B0 = P.at<void>(L.wg_lp);
+    dg.ldb = c.D;
+    dg.sBe = (long long)c.E * c.D;
+    dg.offsets = nullptr;
+    dg.E = 1;
+    dg.seg_len = c.T;
+    dg.C = dx;
+    dg.ldc = c.D;
+    dg.epi = EPI_STORE;
+    KL("gemm_router_dx", launch_gemm_tc(dg, st));
+    KL("scatter_back", launch_scatter_back_add(c.dtype, dx, P.at<void>(L.dxe), P.at<int>(L.slot_of),
+                                               c.T, c.D, c.k, extra_dx, st));
+    return MOE_OK;
   }
-  // expert down-projection (+ bias)
-  GemmArgs d = gemm_base(c, P);
-  d.ragged_k = false;
-  d.a_kcontig = true;
-  d.b_kcontig = true;
-  d.M = (int)R;
-  d.N = c.D;
-  d.A0 = P.at<void>(L.a);
-  d.lda = c.F;
-  d.K0 = c.F;
-  d.B0 = w.w2;
-  d.ldb = c.F;
-  d.sBe = (long long)c.D * c.F;
-  d.ldc = c.D;
-  d.epi = EPI_STORE;
-  d.bias = w.b2;
-  d.C = P.at<void>(L.ye);
-  KL("gemm_down", run_gemm(c, d, st));
+  // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
+  const int S = dwg_splits(c.T);
+  GemmArgs rg{};
+  rg.a_type = MOE_F32;
+  rg.b_type = c.dtype;
+  rg.c_type = MOE_F32;
+  rg.ragged_k = true;
+  rg.a_kcontig = false;
+  rg.b_kcontig = false;
+  rg.M = c.E;
+  rg.N = c.D;
+  rg.A0 = P.at<void>(L.dlogits);
+  rg.lda = c.E;
+  rg.B0 = x;
+  rg.ldb = c.D;
+  rg.K0 = c.T;
+  rg.offsets = nullptr;
+  rg.E = S;
+  rg.seg_len = (c.T + S - 1) / S;
+  rg.C = P.at<void>(L.dwg_part);
+  rg.ldc = c.D;
+  rg.sCe = (long long)c.E * c.D;
+  rg.epi = EPI_STORE;
+  KL("gemm_router_dwg", launch_gemm_simt(rg, st));
+  KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D, dw_gate, st));
+  // dX = dlogits W_g + sum_j dXe[slot(t, j)]
+  GemmArgs dg{};
+  dg.a_type = MOE_F32;
+  dg.b_type = MOE_F32;
+  dg.c_type = MOE_F32;
+  dg.ragged_k = false;
+  dg.a_kcontig = true;
+  dg.b_kcontig = false;
+  dg.M = c.T;
+  dg.N = c.D;
+  dg.A0 = P.at<void>(L.dlogits);
+  dg.lda = c.E;
+  dg.K0 = c.E;
+  dg.B0 = w.w_gate;
+  dg.ldb = c.D;
+  dg.sBe = 0;
+  dg.offsets = nullptr;
+  dg.E = 1;
+  dg.seg_len = c.T;
+  dg.C = dx;
+  dg.ldc = c.D;
+  dg.epi = EPI_SCATTER_ADD;
+  dg.slot_of = P.at<int>(L.slot_of);
+  dg.k = c.k;
+  dg.src = P.at<void>(L.dxe);
+  dg.src_type = c.dtype;
+  KL("gemm_router_dx", launch_gemm_simt(dg, st));
+  return MOE_OK;
+}
+
+}  // namespace api
+}  // namespace moe
+
+namespace {
+
+// The expert-major row buffers of the single-device step (all E experts).
+ExpertRows expert_rows(const moe_config& c, const Ptrs& P) {
+  const Layout& L = *P.L;
+  ExpertRows r{};
+  r.E = c.E;
+  r.M = (int)((long long)c.T * c.k);
+  r.offsets = P.at<int>(L.offsets);
+  r.status = P.at<int>(L.status);
+  r.xe = P.at<void>(L.xe);
+  r.h1 = P.at<void>(L.h1);
+  r.h3 = L.h3 ? P.at<void>(L.h3) : nullptr;
+  r.a = P.at<void>(L.a);
+  r.ye = P.at<void>(L.ye);
+  r.dye = P.at<void>(L.dye);
+  r.dh1 = P.at<void>(L.dh1);
+  r.dh3 = L.dh3 ? P.at<void>(L.dh3) : nullptr;
+  r.dxe = P.at<void>(L.dxe);
+  return r;
+}
+
+// Forward: router -> dispatch -> experts -> combine.  With a target, combine
+// also forms dY and the squared-error partials, and the losses are finalised.
+// target_ready: recorded when `target` has landed (its copy may still be in
+// flight on another stream while the router and experts run), or nullptr.
+moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, float* y,
+                       const float* target, float* d_loss, const Ptrs& P, cudaStream_t st,
+                       cudaEvent_t target_ready = nullptr) {
+  const Layout& L = *P.L;
+  RET_IF(route_tokens(c, w, x, P, st));
+
+  RET_IF(experts_forward(c, w, expert_rows(c, P), st));
 
   const bool shared = c.n_shared > 0;
   if (shared) {
@@ -408,16 +481,6 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
   return MOE_OK;
 }
 
-// SGD folded into the weight-gradient GEMMs of a bf16 training step: each
-// expert weight is updated, and its bf16 copy rewritten, as soon as its
-// gradient tile exists (every GEMM reading that copy has run by then).
-struct SgdFuse {
-  float lr;
-  float *w1, *w3, *w2;
-  void *w1_lp, *w3_lp, *w2_lp;
-  float *ws1, *ws3, *ws2;        // shared branch
-  void *ws1_lp, *ws3_lp, *ws2_lp;
-};
 
 // Backward of L = L_task + alpha aux given dY (course Parts 4-6).
 // dy == nullptr: the forward's fused combine already wrote dYe and dgate.
@@ -425,8 +488,6 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
                         const moe_grads& gr, float* dx, bool aux_ready, const Ptrs& P,
                         cudaStream_t st, const SgdFuse* sgd = nullptr) {
   const Layout& L = *P.L;
-  const long long R = (long long)c.T * c.k;
-  const bool swiglu = c.act == MOE_ACT_SWIGLU;
   if (!aux_ready)
     KL("finalize_losses", launch_finalize_losses(P.at<double>(L.sq), 0, P.at<float>(L.psum), router_fwd_blocks(c.T),
                               P.at<int>(L.counts), c.T, c.D, c.E, c.k, c.aux_alpha, nullptr,
@@ -434,110 +495,7 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
   if (dy != nullptr)
     KL("combine_bwd", launch_combine_bwd(c.dtype, dy, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of),
                           c.T, c.D, c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st));
-  // dA = dYe W2_e with the activation backward in the epilogue
-  GemmArgs g = gemm_base(c, P);
-  g.ragged_k = false;
-  g.a_kcontig = true;
-  g.b_kcontig = false;
-  g.M = (int)R;
-  g.N = c.F;
-  g.A0 = P.at<void>(L.dye);
-  g.lda = c.D;
-  g.K0 = c.D;
-  g.B0 = w.w2;
-  g.ldb = c.F;
-  g.sBe = (long long)c.D * c.F;
-  g.ldc = c.F;
-  g.ld_aux = c.F;
-  g.aux0 = P.at<void>(L.h1);
-  g.C = P.at<void>(L.dh1);
-  if (swiglu) {
-    g.epi = EPI_SWIGLU_BWD;
-    g.aux1 = P.at<void>(L.h3);
-    g.out1 = P.at<void>(L.dh3);
-  } else {
-    g.epi = EPI_ACT_BWD;
-  }
-  KL("gemm_dA", run_gemm(c, g, st));
-  // dW2_e = dYe_e^T A_e  (ragged K)
-  GemmArgs w2g = gemm_base(c, P);
-  w2g.ragged_k = true;
-  w2g.a_kcontig = false;
-  w2g.b_kcontig = false;
-  w2g.c_type = MOE_F32;
-  w2g.M = c.D;
-  w2g.N = c.F;
-  w2g.A0 = P.at<void>(L.dye);
-  w2g.lda = c.D;
-  w2g.B0 = P.at<void>(L.a);
-  w2g.ldb = c.F;
-  w2g.K0 = (int)R;
-  w2g.C = gr.dw2;
-  w2g.ldc = c.F;
-  w2g.sCe = (long long)c.D * c.F;
-  w2g.epi = EPI_STORE;
-  if (sgd) {
-    w2g.sgd_w = sgd->w2;
-    w2g.sgd_wlp = sgd->w2_lp;
-    w2g.sgd_lr = sgd->lr;
-  }
-  KL("gemm_dw2", run_gemm(c, w2g, st));
-  if (gr.db2) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dye), P.at<int>(L.offsets), c.E, c.D, gr.db2, st));
-  // dXe = dH1 W1_e (+ dH3 W3_e)
-  GemmArgs xg = gemm_base(c, P);
-  xg.ragged_k = false;
-  xg.a_kcontig = true;
-  xg.b_kcontig = false;
-  xg.M = (int)R;
-  xg.N = c.D;
-  xg.A0 = P.at<void>(L.dh1);
-  xg.lda = c.F;
-  xg.K0 = c.F;
-  xg.B0 = w.w1;
-  xg.ldb = c.D;
-  xg.sBe = (long long)c.F * c.D;
-  if (swiglu) {
-    xg.A1 = P.at<void>(L.dh3);
-    xg.B1 = w.w3;
-    xg.K1 = c.F;
-  }
-  xg.ldc = c.D;
-  xg.epi = EPI_STORE;
-  xg.C = P.at<void>(L.dxe);
-  KL("gemm_dxe", run_gemm(c, xg, st));
-  // dW1_e = dH1_e^T Xe_e (dW3 likewise)
-  GemmArgs w1g = gemm_base(c, P);
-  w1g.ragged_k = true;
-  w1g.a_kcontig = false;
-  w1g.b_kcontig = false;
-  w1g.c_type = MOE_F32;
-  w1g.M = c.F;
-  w1g.N = c.D;
-  w1g.A0 = P.at<void>(L.dh1);
-  w1g.lda = c.F;
-  w1g.B0 = P.at<void>(L.xe);
-  w1g.ldb = c.D;
-  w1g.K0 = (int)R;
-  w1g.C = gr.dw1;
-  w1g.ldc = c.D;
-  w1g.sCe = (long long)c.F * c.D;
-  w1g.epi = EPI_STORE;
-  if (sgd) {
-    w1g.sgd_w = sgd->w1;
-    w1g.sgd_wlp = sgd->w1_lp;
-    w1g.sgd_lr = sgd->lr;
-  }
-  KL("gemm_dw1", run_gemm(c, w1g, st));
-  if (swiglu) {
-    w1g.A0 = P.at<void>(L.dh3);
-    w1g.C = gr.dw3;
-    if (sgd) {
-      w1g.sgd_w = sgd->w3;
-      w1g.sgd_wlp = sgd->w3_lp;
-    }
-    KL("gemm_dw3", run_gemm(c, w1g, st));
-  }
-  if (gr.db1) KL("bias_grad", launch_segment_colsum(c.dtype, P.at<void>(L.dh1), P.at<int>(L.offsets), c.E, c.F, gr.db1, st));
+  RET_IF(experts_backward(c, w, expert_rows(c, P), gr, sgd, st));
 
   if (c.n_shared > 0) {
     // shared branch: it receives the whole dY (bf16 copy for the tensor cores)
@@ -649,120 +607,8 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
     KL("gemm_shared_dw3", run_gemm(c, s1, st));
   }
 
-  // router: renormalisation + aux + score backward
-  const RouterArgs ra = router_args(c);
-  const bool lp = c.dtype == MOE_BF16;
-  KL("router_bwd", launch_router_bwd(P.at<float>(L.scores), P.at<int>(L.idx), P.at<float>(L.gate),
-                       P.at<float>(L.dgate), c.aux_alpha != 0.f ? P.at<float>(L.aux_row) : nullptr,
-                       ra, P.at<float>(L.dlogits), lp ? P.at<void>(L.dl_lp) : nullptr, st));
-  if (lp) {
-    // tensor-core router products: dW_g = dlogits^T x (split over token
-    // chunks, fixed-order sum) and dX = dlogits W_g + scatter-back of dXe.
-    // W_g's bf16 copy is the forward's, still in the workspace: the backward
-    // runs with the forward's weights, and a training step updates W_g only
-    // after the backward.
-    const int S = dwg_splits(c.T);
-    GemmArgs rg{};
-    rg.a_type = rg.b_type = MOE_BF16;
-    rg.c_type = MOE_F32;
-    rg.status = P.at<int>(L.status);
-    rg.ragged_k = true;
-    rg.M = c.E;
-    rg.N = c.D;
-    rg.A0 = P.at<void>(L.dl_lp);
-    rg.lda = c.E;
-    rg.B0 = x;
-    rg.ldb = c.D;
-    rg.K0 = c.T;
-    rg.offsets = nullptr;
-    rg.E = S;
-    rg.seg_len = (c.T + S - 1) / S;
-    rg.C = P.at<void>(L.dwg_part);
-    rg.ldc = c.D;
-    rg.sCe = (long long)c.E * c.D;
-    rg.epi = EPI_STORE;
-    KL("gemm_router_dwg", launch_gemm_tc(rg, st));
-    KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D,
-                                             gr.dw_gate, st));
-    GemmArgs dg{};
-    dg.a_type = dg.b_type = MOE_BF16;
-    dg.c_type = MOE_F32;
-    dg.status = P.at<int>(L.status);
-    dg.ragged_k = false;
-    dg.b_kcontig = false;
-    dg.M = c.T;
-    dg.N = c.D;
-    dg.K0 = c.E;
-    dg.A0 = P.at<void>(L.dl_lp);
-    dg.lda = c.E;
-    dg.B0 = P.at<void>(L.wg_lp);
-    dg.ldb = c.D;
-    dg.sBe = (long long)c.E * c.D;
-    dg.offsets = nullptr;
-    dg.E = 1;
-    dg.seg_len = c.T;
-    dg.C = dx;
-    dg.ldc = c.D;
-    dg.epi = EPI_STORE;
-    KL("gemm_router_dx", launch_gemm_tc(dg, st));
-    KL("scatter_back", launch_scatter_back_add(c.dtype, dx, P.at<void>(L.dxe), P.at<int>(L.slot_of),
-                                               c.T, c.D, c.k,
-                                               c.n_shared > 0 ? P.at<void>(L.dxs) : nullptr, st));
-    return MOE_OK;
-  }
-  // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
-  const int S = dwg_splits(c.T);
-  GemmArgs rg{};
-  rg.a_type = MOE_F32;
-  rg.b_type = c.dtype;
-  rg.c_type = MOE_F32;
-  rg.ragged_k = true;
-  rg.a_kcontig = false;
-  rg.b_kcontig = false;
-  rg.M = c.E;
-  rg.N = c.D;
-  rg.A0 = P.at<void>(L.dlogits);
-  rg.lda = c.E;
-  rg.B0 = x;
-  rg.ldb = c.D;
-  rg.K0 = c.T;
-  rg.offsets = nullptr;
-  rg.E = S;
-  rg.seg_len = (c.T + S - 1) / S;
-  rg.C = P.at<void>(L.dwg_part);
-  rg.ldc = c.D;
-  rg.sCe = (long long)c.E * c.D;
-  rg.epi = EPI_STORE;
-  KL("gemm_router_dwg", launch_gemm_simt(rg, st));
-  KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D, gr.dw_gate, st));
-  // dX = dlogits W_g + sum_j dXe[slot(t, j)]
-  GemmArgs dg{};
-  dg.a_type = MOE_F32;
-  dg.b_type = MOE_F32;
-  dg.c_type = MOE_F32;
-  dg.ragged_k = false;
-  dg.a_kcontig = true;
-  dg.b_kcontig = false;
-  dg.M = c.T;
-  dg.N = c.D;
-  dg.A0 = P.at<void>(L.dlogits);
-  dg.lda = c.E;
-  dg.K0 = c.E;
-  dg.B0 = w.w_gate;
-  dg.ldb = c.D;
-  dg.sBe = 0;
-  dg.offsets = nullptr;
-  dg.E = 1;
-  dg.seg_len = c.T;
-  dg.C = dx;
-  dg.ldc = c.D;
-  dg.epi = EPI_SCATTER_ADD;
-  dg.slot_of = P.at<int>(L.slot_of);
-  dg.k = c.k;
-  dg.src = P.at<void>(L.dxe);
-  dg.src_type = c.dtype;
-  KL("gemm_router_dx", launch_gemm_simt(dg, st));
-  return MOE_OK;
+  return router_backward(c, w, x, gr.dw_gate, dx, c.n_shared > 0 ? P.at<void>(L.dxs) : nullptr,
+                         P, st);
 }
 
 moe_status check_ws(const moe_config& c, const void* ws, size_t bytes) {
@@ -795,27 +641,34 @@ moe_status check_grads(const moe_config& c, const moe_grads& g) {
   return MOE_OK;
 }
 
-#define RET_IF(expr)                \
-  do {                              \
-    moe_status _s = (expr);         \
-    if (_s != MOE_OK) return _s;    \
-  } while (0)
-
+// Zeroes every gradient buffer that is given (NULL ones are skipped).
 moe_status zero_grads(const moe_config& c, const moe_grads& g, cudaStream_t st) {
   const size_t E = c.E, D = c.D, F = c.F;
-  CK(launch_fill_zero(g.dw_gate, E * D * 4, st));
-  CK(launch_fill_zero(g.dw1, E * F * D * 4, st));
-  if (g.dw3) CK(launch_fill_zero(g.dw3, E * F * D * 4, st));
-  CK(launch_fill_zero(g.dw2, E * D * F * 4, st));
-  if (g.db1) CK(launch_fill_zero(g.db1, E * F * 4, st));
-  if (g.db2) CK(launch_fill_zero(g.db2, E * D * 4, st));
-  if (c.n_shared > 0) {
-    const size_t Fs = (size_t)c.n_shared * F;
-    CK(launch_fill_zero(g.dws1, Fs * D * 4, st));
-    CK(launch_fill_zero(g.dws3, Fs * D * 4, st));
-    CK(launch_fill_zero(g.dws2, D * Fs * 4, st));
-  }
+  const size_t Fs = (size_t)c.n_shared * F;
+  struct Z { float* p; size_t bytes; } zs[] = {
+      {g.dw_gate, E * D * 4}, {g.dw1, E * F * D * 4}, {g.dw3, E * F * D * 4},
+      {g.dw2, E * D * F * 4}, {g.db1, E * F * 4},     {g.db2, E * D * 4},
+      {g.dws1, Fs * D * 4},   {g.dws3, Fs * D * 4},   {g.dws2, D * Fs * 4}};
+  for (const Z& z : zs)
+    if (z.p && z.bytes) CK(launch_fill_zero(z.p, z.bytes, st));
   return MOE_OK;
+}
+
+// The gradients a training step works with: the caller's buffers, and for
+// each one left NULL a workspace stand-in, except the expert weights of bf16
+// layers, whose fused SGD then stores no gradient at all.
+moe_grads step_grads(const moe_config& c, const moe_grads& given, const Ptrs& P) {
+  moe_grads g = given;
+  const Layout& L = *P.L;
+  if (!g.dw_gate) g.dw_gate = P.at<float>(L.g_wg);
+  if (c.has_bias && !g.db1) g.db1 = P.at<float>(L.g_b1);
+  if (c.has_bias && !g.db2) g.db2 = P.at<float>(L.g_b2);
+  if (c.dtype != MOE_BF16) {
+    if (!g.dw1) g.dw1 = P.at<float>(L.g_w1);
+    if (c.act == MOE_ACT_SWIGLU && !g.dw3) g.dw3 = P.at<float>(L.g_w3);
+    if (!g.dw2) g.dw2 = P.at<float>(L.g_w2);
+  }
+  return g;
 }
 
 moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const void* x,
@@ -833,10 +686,14 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
     return MOE_ERR_INVALID_ARG;
   if (c.n_shared > 0 && (!p->ws1 || !p->ws3 || !p->ws2 || !p->ws1_lp || !p->ws3_lp || !p->ws2_lp))
     return MOE_ERR_INVALID_ARG;
-  RET_IF(check_grads(c, p->grads));
+  // gradient buffers are optional here (NULL: the step still applies that
+  // gradient, it just does not hand it out); those given must be aligned
+  const moe_grads& gv = p->grads;
   const void* ps[] = {p->w_gate, p->w1, p->w3, p->w2, p->b1, p->b2, p->w1_lp, p->w3_lp, p->w2_lp,
                       p->logit_bias, p->corr_bias, p->ws1, p->ws3, p->ws2, p->ws1_lp,
-                      p->ws3_lp, p->ws2_lp, x, y_target, d_loss, dx};
+                      p->ws3_lp, p->ws2_lp, x, y_target, d_loss, dx,
+                      gv.dw_gate, gv.dw1, gv.dw3, gv.dw2, gv.db1, gv.db2, gv.dws1, gv.dws3,
+                      gv.dws2};
   for (const void* q : ps)
     if (q && !aligned16(q)) return MOE_ERR_ALIGNMENT;
   if (c.T > 0 && (!x || !y_target)) return MOE_ERR_INVALID_ARG;
@@ -867,12 +724,12 @@ moe_status train_step_impl(const moe_config* cfg, const moe_params* p, const voi
   const bool fused = c.dtype == MOE_BF16;
   const SgdFuse sf{lr, p->w1, p->w3, p->w2, p->w1_lp, p->w3_lp, p->w2_lp,
                    p->ws1, p->ws3, p->ws2, p->ws1_lp, p->ws3_lp, p->ws2_lp};
+  const moe_grads g = step_grads(c, p->grads, P);
   // k <= 8: the forward's combine pass already produced dYe and dgate
-  RET_IF(run_backward(c, w, x, c.k <= 8 ? nullptr : P.at<float>(L.dy), p->grads, dxp, true, P, st,
+  RET_IF(run_backward(c, w, x, c.k <= 8 ? nullptr : P.at<float>(L.dy), g, dxp, true, P, st,
                       fused ? &sf : nullptr));
   // SGD on the fp32 masters; bf16 working copies rewritten from the result
   const long long E = c.E, D = c.D, F = c.F;
-  const moe_grads& g = p->grads;
   // one launch for every tensor the GEMM epilogues did not update
   SgdTensor ts[SGD_MAX_TENSORS];
   int nt = 0;

@@ -18,7 +18,12 @@ class MoELayer:
     def __init__(self, T, D, F, E, k, act, score, dtype, has_bias, aux_alpha, w_gate, w1, w2,
                  w3=None, b1=None, b2=None, logit_bias=None, n_groups=1, topk_groups=1,
                  group_score="top2_sum", w1_lp=None, w3_lp=None, w2_lp=None, device="cuda",
-                 corr_bias=None, n_shared=0, ws1=None, ws3=None, ws2=None, capacity_factor=0.0):
+                 corr_bias=None, n_shared=0, ws1=None, ws3=None, ws2=None, capacity_factor=0.0,
+                 store_grads=True):
+        """store_grads=False: training steps pass NULL gradient buffers (the
+        step still applies every gradient; bf16 layers then skip storing the
+        expert weights' fp32 gradients) and no gradient tensors are
+        allocated; ``backward`` is then unavailable."""
         self.device = torch.device(device)
         self.dtype = dtype
         self.cfg = B.make_config(T, D, F, E, k, act=act, score=score, n_groups=n_groups,
@@ -47,7 +52,7 @@ class MoELayer:
         else:
             self.w1_lp = self.w2_lp = self.w3_lp = None
             self.ws1_lp = self.ws3_lp = self.ws2_lp = None
-        z = lambda t: None if t is None else torch.zeros_like(t)  # noqa: E731
+        z = lambda t: None if t is None or not store_grads else torch.zeros_like(t)  # noqa: E731
         self.dw_gate, self.dw1, self.dw2, self.dw3 = z(self.w_gate), z(self.w1), z(self.w2), z(self.w3)
         self.db1, self.db2 = z(self.b1), z(self.b2)
         self.dws1, self.dws3, self.dws2 = z(self.ws1), z(self.ws3), z(self.ws2)
@@ -82,6 +87,8 @@ class MoELayer:
         return y
 
     def backward(self, x: torch.Tensor, dy: torch.Tensor, dx: Optional[torch.Tensor] = None):
+        if self.dw_gate is None:
+            raise ValueError("this layer was built with store_grads=False: no gradient buffers")
         B.moe_backward(self.cfg, self.weights(), x, dy, self.grads, dx, self.workspace)
         return dx
 

@@ -119,6 +119,11 @@ def test_host_validation_errors(L):
     # bf16 layers need E % 8 == 0 (16-byte rows of the bf16 router operands)
     assert _status(B.moe_train_step, _cfg(dtype="bf16", E=4), p, good(6), good(7), 0.1, good(13), ws) \
         == B.MOE_ERR_UNSUPPORTED
+    # train step: gradient buffers are optional, but those given must be aligned
+    g_odd = B.make_grads(good(8), _Fake(0x90004), None, db1=good(11), db2=good(12))
+    p_odd = B.make_params(good(1), good(2), good(3), g_odd, b1=good(4), b2=good(5))
+    assert _status(B.moe_train_step, _cfg(), p_odd, good(6), good(7), 0.1, good(13), ws) \
+        == B.MOE_ERR_ALIGNMENT
 
 
 def test_selftest_rejects_unbounded_wait_limit(L):

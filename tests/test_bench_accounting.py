@@ -96,3 +96,33 @@ def test_clock_record_parsing():
     s2.proc = _DoneProc()
     s2.lines = ["1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"]
     assert sorted(s2.stop()["reasons"]) == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_per_launch_flops_sum_to_the_step():
+    """The per-launch split the bench reports adds up to the step's expert
+    FLOPs, and each launch carries 2 M N K of its own operand shapes."""
+    for name in ("tiny", "dense_f32", "dense_bf16", "grouped", "skewed", "large"):
+        wl = W.WORKLOADS[name]
+        per = bench.gemm_launch_flops(wl, 1234)
+        assert abs(sum(per.values()) - bench.expert_flops_per_step(wl, 1234)) < 1e-6 * sum(per.values())
+    wl = W.WORKLOADS["large"]
+    per = bench.gemm_launch_flops(wl)
+    R, D, F = wl.R, wl.D, wl.F
+    assert per["gemm_up"] == 2 * R * D * (2 * F)       # [R, D] x [2F, D]^T
+    assert per["gemm_dw1"] == 2 * F * D * R            # [F, R] x [R, D]
+    assert per["gemm_dxe"] == 2 * R * (2 * F) * D      # [R, 2F] x [2F, D]
+
+
+def test_scatter_back_bytes():
+    wl = W.WORKLOADS["large"]
+    # dXe [R, D] bf16 read; dX [T, D] fp32 read (router term) and written
+    assert bench.hbm_bytes(wl)["scatter_back"] == wl.R * wl.D * 2 + 2 * wl.T * wl.D * 4
+
+
+def test_cpu_baseline_extrapolation():
+    """Per-token time scales with the tokens, SGD with the experts: a sample
+    of 100 tokens over 16 of 128 experts taking 2 s + 0.5 s of SGD stands for
+    a 65536-token step of 2 * 655.36 + 0.5 * 8 seconds."""
+    wl = W.WORKLOADS["large"]
+    rate = bench.extrapolated_rate(wl, 100, 16, 2.0, 0.5)
+    assert abs(rate - 65536 / (2.0 * 655.36 + 0.5 * 8)) < 1e-9

@@ -123,3 +123,57 @@ def test_bounded_wait_times_out_and_context_survives():
             ref = A[o[e]:o[e + 1]].float() @ Bw[e].float().T
             assert _rel(C[o[e]:o[e + 1]].float(), ref) <= 1e-2
 
+
+@pytest.mark.parametrize("form,raw", [(0, [0, 100, 50, 400]), (0, [0, 100, 50, 220]),
+                                      (1, [-7, 64, 64, 1000]), (2, [0, 900, 20, 20])])
+def test_caller_offsets_are_clamped(form, raw):
+    """Offsets from a caller that run past the total rows, go negative or
+    decrease are clamped on the device to a non-decreasing sequence within
+    [0, total rows]: the result equals the GEMM over the clamped segments and
+    nothing past the end of C is written (a guard region behind C keeps its
+    sentinel)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    E = len(raw) - 1
+    rows = 300
+    clamped, prev = [], 0
+    for v in raw:
+        prev = min(max(v, prev), rows)
+        clamped.append(prev)
+    off = torch.tensor(raw, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    guard = 4096
+    if form in (0, 1):
+        N, K = 256, 128
+        A = torch.randn(rows, K, generator=g, device="cuda").to(torch.bfloat16)
+        Bw = (torch.randn(E, N, K, generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
+        Bt = Bw if form == 0 else Bw.transpose(1, 2).contiguous()
+        buf = torch.full((rows * N + guard,), 7.0, dtype=torch.bfloat16, device="cuda")
+        C = buf[: rows * N].view(rows, N)
+        B.moe_grouped_gemm(form, rows, N, K, E, off, A, Bt, C, st)
+        torch.cuda.synchronize()
+        for e in range(E):
+            lo, hi = clamped[e], clamped[e + 1]
+            if hi > lo:
+                ref = A[lo:hi].float() @ Bw[e].float().T
+                assert _rel(C[lo:hi].float(), ref) <= 1e-2, e
+        # rows outside every clamped segment are not written
+        assert torch.all(C[clamped[-1]:] == 7.0)
+        assert torch.all(buf[rows * N:] == 7.0)
+    else:
+        Mo, N = 128, 256
+        A = torch.randn(rows, Mo, generator=g, device="cuda").to(torch.bfloat16)
+        Bm = torch.randn(rows, N, generator=g, device="cuda").to(torch.bfloat16)
+        buf = torch.full((E * Mo * N + guard,), 7.0, dtype=torch.float32, device="cuda")
+        C = buf[: E * Mo * N].view(E, Mo, N)
+        B.moe_grouped_gemm(2, Mo, N, rows, E, off, A, Bm, C, st)
+        torch.cuda.synchronize()
+        for e in range(E):
+            lo, hi = clamped[e], clamped[e + 1]
+            ref = A[lo:hi].float().T @ Bm[lo:hi].float()
+            if hi == lo:
+                assert torch.equal(C[e], torch.zeros_like(C[e])), e
+            else:
+                assert _rel(C[e], ref) <= 1e-4, e
+        assert torch.all(buf[E * Mo * N:] == 7.0)
+    assert st.item() == 0

@@ -29,8 +29,13 @@ def _grad_keys(wl):
     return keys
 
 
-def _one_step_parity(wl, seed=0, check_dx=True):
-    """One training step on both sides; returns the errors by tensor."""
+def _one_step_parity(wl, seed=0, check_dx=True, keep=None):
+    """One training step on both sides; returns the errors by tensor.  When
+    ``keep`` is a dict it receives the oracle's forward state ``st``, its
+    gradients ``g``, the fp32 masters before the step ``master``, the
+    forward weights ``w_fwd`` and ``x64``, the output ``y`` of a forward call
+    made before the step and the step's ``dx``, for further checks by the
+    caller."""
     inp = W.make_inputs(wl, seed=seed)
     cfg = oracle_config(wl)
     tol = TOL[wl.dtype]
@@ -38,15 +43,17 @@ def _one_step_parity(wl, seed=0, check_dx=True):
     x = device_x(wl, inp)
     tgt = inp["target"].cuda()
     dx = torch.empty(wl.T, wl.D, device="cuda")
-    w0 = {k: (v.clone() if v is not None else None) for k, v in layer.param_dict().items()}
+    y_fwd = layer.forward(x).clone() if keep is not None else None   # forward alone, before the step
     layer.train_step(x, tgt, wl.lr, dx=dx)
     torch.cuda.synchronize()
     r = layer.routing()
     check_routing_exact(cfg, r, inp.get("corr_bias"))
 
     w_fwd, master, x64, t64 = oracle_inputs(wl, inp)
-    st0 = O.forward(cfg, w_fwd, x64)
-    idx = validated_routing(cfg, st0["scores"], r["idx"].cpu().numpy(),
+    # the oracle's own fp64 scores (the first steps of its forward) decide
+    # which GPU routing decisions are near-ties to take from the kernel
+    scores64 = O.router_scores(cfg, O.router_logits(x64, w_fwd["w_gate"], w_fwd.get("logit_bias")))
+    idx = validated_routing(cfg, scores64, r["idx"].cpu().numpy(),
                             corr_bias=w_fwd.get("corr_bias"))
     st = O.forward(cfg, w_fwd, x64, idx)
     if wl.act == "relu":
@@ -85,6 +92,8 @@ def _one_step_parity(wl, seed=0, check_dx=True):
             lp = getattr(layer, key + "_lp")
             if lp is not None:
                 assert torch.equal(lp, new[key].to(torch.bfloat16)), key
+    if keep is not None:
+        keep.update(st=st, g=g, master=master, w_fwd=w_fwd, x64=x64, y=y_fwd, dx=dx)
     return errs, layer, inp
 
 
@@ -466,3 +475,40 @@ def test_edge_shapes(T, k, E):
     wl = dataclasses.replace(base, T=T, k=k, E=E)
     errs, _, _ = _one_step_parity(wl, seed=11)
     assert max(errs.values()) <= 1e-4
+
+
+@pytest.mark.parametrize("name,T", [("grouped_shared", 1000), ("dense_bf16", 900),
+                                    ("dense_f32", 700)])
+def test_unstored_gradients_give_identical_steps(name, T):
+    """A training step whose caller passes NULL gradient buffers still applies
+    every gradient: two steps give bit-identical losses, fp32 masters and bf16
+    copies to the same steps with every gradient stored (bf16 layers then skip
+    the expert weights' gradient store inside the fused SGD epilogue; fp32
+    layers and the router / bias gradients use workspace stand-ins)."""
+    from sparse_mixture_experts_softmax_gb300.layer import MoELayer as L_
+    wl = W.WORKLOADS[name].with_tokens(T)
+    inp = W.make_inputs(wl, seed=17)
+    a = make_layer(wl, inp)
+    lp = wl.dtype == "bf16"
+    b = L_(wl.T, wl.D, wl.F, wl.E, wl.k, wl.act, wl.score, wl.dtype, wl.has_bias, wl.aux_alpha,
+           inp["w_gate"], inp["w1"], inp["w2"], w3=inp["w3"], b1=inp["b1"], b2=inp["b2"],
+           logit_bias=inp["logit_bias"], n_groups=wl.n_groups, topk_groups=wl.topk_groups,
+           w1_lp=inp.get("w1_bf16") if lp else None, w3_lp=inp.get("w3_bf16") if lp else None,
+           w2_lp=inp.get("w2_bf16") if lp else None, corr_bias=inp.get("corr_bias"),
+           n_shared=wl.n_shared, ws1=inp.get("ws1"), ws3=inp.get("ws3"), ws2=inp.get("ws2"),
+           capacity_factor=wl.capacity_factor, store_grads=False)
+    assert b.dw1 is None and b.dw_gate is None
+    x = device_x(wl, inp)
+    tgt = inp["target"].cuda()
+    for _ in range(2):
+        a.train_step(x, tgt, wl.lr)
+        b.train_step(x, tgt, wl.lr)
+        torch.cuda.synchronize()
+        assert torch.equal(a.d_loss, b.d_loss)
+    for k_, v in a.param_dict().items():
+        if v is not None:
+            assert torch.equal(v, b.param_dict()[k_]), k_
+    for k_ in ("w1", "w2", "w3", "ws1", "ws3", "ws2"):
+        if getattr(a, k_ + "_lp") is not None:
+            assert torch.equal(getattr(a, k_ + "_lp"), getattr(b, k_ + "_lp")), k_
+    assert a.dw1.abs().max().item() > 0
