@@ -274,8 +274,10 @@ MOE_API moe_status moe_get_hidden(const moe_config* cfg, const void* workspace,
 
 /* Reads the device status word of the last call that used `workspace`: 0, or
  * MOE_ERR_TIMEOUT when a bounded device-side wait of a tensor-core kernel
- * expired (that kernel then stopped early and its outputs are invalid).
- * Synchronises `stream`. */
+ * expired (that kernel then stopped early and its outputs are invalid), or,
+ * in the MOE_DEBUG variant only, MOE_ERR_INVALID_ARG when a routing index was
+ * out of range (see moe_build_flags).  A forward clears it.  Synchronises
+ * `stream`. */
 MOE_API moe_status moe_device_status(const moe_config* cfg, const void* workspace,
                                      size_t workspace_bytes, int32_t* status_host, void* stream);
 
@@ -308,6 +310,27 @@ MOE_API moe_status moe_selftest_wait_timeout(int32_t form, int32_t M, int32_t N,
                                              int32_t E, const int32_t* offsets, const void* A,
                                              const void* B, void* C, int32_t* dev_status,
                                              int64_t limit_ns, void* stream);
+
+/* Build options of the loaded library: MOE_BUILD_DEBUG_CHECKS is set in the
+ * MOE_DEBUG variant (libmoe_gb300_debug.so), whose gather, combine, combine
+ * backward, scatter-back, route count / scatter and router backward kernels
+ * check every routing index (expert ids against [0, E), expert-major slots
+ * against [-1, T k)) before dereferencing it; an index out of range is
+ * skipped and MOE_ERR_INVALID_ARG is recorded in the workspace status word
+ * (read by moe_device_status).  The release library trusts the dispatch that
+ * wrote the indices. */
+#define MOE_BUILD_DEBUG_CHECKS 1
+MOE_API int32_t moe_build_flags(void);
+
+/* Fault injection for the MOE_DEBUG variant's tests, on the host side: writes
+ * `value` into entry `index` (0 <= index < T k) of the routing state the last
+ * forward left in `workspace`: field 0 the expert ids idx [T,k], field 1 the
+ * slot map slot_of [T,k].  Synchronises `stream`.  The release library
+ * returns MOE_ERR_UNSUPPORTED and writes nothing.  Diagnostic only; the pages
+ * have no counterpart. */
+MOE_API moe_status moe_debug_poke_routing(const moe_config* cfg, void* workspace,
+                                          size_t workspace_bytes, int32_t field, int64_t index,
+                                          int32_t value, void* stream);
 
 /* Static text for a status code. */
 MOE_API const char* moe_status_string(moe_status s);

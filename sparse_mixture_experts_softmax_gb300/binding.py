@@ -24,6 +24,7 @@ MOE_ERR_ALIGNMENT = 3
 MOE_ERR_WORKSPACE_TOO_SMALL = 4
 MOE_ERR_CUDA = 5
 MOE_ERR_TIMEOUT = 6
+MOE_BUILD_DEBUG_CHECKS = 1
 
 ACT = {"relu": 0, "gelu_tanh": 1, "swiglu": 2}
 SCORE = {"softmax": 0, "sigmoid": 1}
@@ -72,85 +73,120 @@ class MoEError(RuntimeError):
         self.status = status
 
 
-_lib = None
+_LIB_DEBUG_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                               "libmoe_gb300_debug.so")
+_lib = None          # the library every call below goes through
+_loaded = {}         # path -> loaded handle
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded library; raises if it has not been built."""
+    """The loaded library (the release build unless ``use_library`` switched
+    to the MOE_DEBUG variant); raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_LIB_PATH):
-            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
-                               "sparse_mixture_experts_softmax_gb300.build.build_library()")
-        L = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.POINTER
-        L.moe_workspace_size.argtypes = [P(moe_config)]
-        L.moe_workspace_size.restype = c_size_t
-        L.moe_host_staging_size.argtypes = [P(moe_config)]
-        L.moe_host_staging_size.restype = c_size_t
-        L.moe_forward.argtypes = [P(moe_config), P(moe_weights), c_void_p, c_void_p, c_void_p,
-                                  c_size_t, c_void_p]
-        L.moe_backward.argtypes = [P(moe_config), P(moe_weights), c_void_p, c_void_p, P(moe_grads),
-                                   c_void_p, c_void_p, c_size_t, c_void_p]
-        L.moe_train_step.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p, c_float,
-                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
-        L.moe_train_step_host.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p,
-                                          c_float, c_void_p, c_void_p, c_size_t, c_void_p,
-                                          c_size_t, c_void_p]
-        L.moe_train_steps_host.argtypes = [P(moe_config), P(moe_params), c_int32, c_void_p,
-                                           c_void_p, c_float, c_void_p, c_void_p, c_size_t,
-                                           c_void_p, c_size_t, c_void_p]
-        L.moe_get_routing.argtypes = [P(moe_config), c_void_p, c_size_t] + [c_void_p] * 8
-        L.moe_get_intermediates.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
-                                            c_void_p, c_void_p]
-        L.moe_status_string.argtypes = [c_int32]
-        L.moe_status_string.restype = ctypes.c_char_p
-        L.moe_last_launch_count.argtypes = []
-        L.moe_last_launch_count.restype = c_int32
-        L.moe_profile_enable.argtypes = [c_int32]
-        L.moe_profile_enable.restype = None
-        L.moe_profile_count.argtypes = []
-        L.moe_profile_count.restype = c_int32
-        L.moe_profile_name.argtypes = [c_int32]
-        L.moe_profile_name.restype = ctypes.c_char_p
-        L.moe_profile_ms.argtypes = [c_int32]
-        L.moe_profile_ms.restype = c_float
-        L.moe_dispatch_noalloc.argtypes = [P(moe_config)] + [c_void_p] * 6
-        L.moe_device_status.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p]
-        L.moe_get_hidden.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
-                                     c_void_p]
-        L.moe_grouped_gemm.argtypes = [c_int32] * 5 + [c_void_p] * 6
-        L.moe_selftest_wait_timeout.argtypes = [c_int32] * 5 + [c_void_p] * 5 + [ctypes.c_int64,
-                                                                                c_void_p]
-        L.moe_ep_workspace_size.argtypes = [P(moe_config), P(moe_ep_config)]
-        L.moe_ep_workspace_size.restype = c_size_t
-        L.moe_ep_buffer_offsets.argtypes = [P(moe_config), P(moe_ep_config), P(c_size_t)]
-        L.moe_ep_route.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights), c_void_p,
-                                   c_void_p, c_void_p, c_size_t, c_void_p]
-        L.moe_ep_expert_forward.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights),
-                                            P(moe_ep_rows), c_void_p]
-        L.moe_ep_combine.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_void_p,
-                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
-        L.moe_ep_expert_backward.argtypes = [P(moe_config), P(moe_ep_config), P(moe_params),
-                                             P(moe_ep_rows), c_float, c_void_p]
-        L.moe_ep_router_backward.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_void_p,
-                                             c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
-        L.moe_ep_router_update.argtypes = [P(moe_config), c_void_p, c_void_p, c_float, c_void_p]
-        L.moe_ep_get_routing.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_size_t] + \
-            [c_void_p] * 8
-        for fn in ("moe_ep_buffer_offsets", "moe_ep_get_routing", "moe_ep_route",
-                   "moe_ep_expert_forward",
-                   "moe_ep_combine", "moe_ep_expert_backward", "moe_ep_router_backward",
-                   "moe_ep_router_update"):
-            getattr(L, fn).restype = c_int32
-        for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
-                   "moe_train_steps_host",
-                   "moe_get_routing", "moe_get_intermediates", "moe_get_hidden",
-                   "moe_dispatch_noalloc",
-                   "moe_device_status", "moe_grouped_gemm", "moe_selftest_wait_timeout"):
-            getattr(L, fn).restype = c_int32
-        _lib = L
+        _lib = _load(_LIB_PATH)
     return _lib
+
+
+class use_library:
+    """``with use_library(debug=True): ...`` routes every call of this module
+    to the MOE_DEBUG variant (device-side index checks) for the block."""
+
+    def __init__(self, debug: bool):
+        self.path = _LIB_DEBUG_PATH if debug else _LIB_PATH
+
+    def __enter__(self):
+        global _lib
+        self.saved = _lib
+        _lib = _load(self.path)
+        return _lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def _load(path: str) -> ctypes.CDLL:
+    if path in _loaded:
+        return _loaded[path]
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "sparse_mixture_experts_softmax_gb300.build.build_library()")
+    L = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    L.moe_workspace_size.argtypes = [P(moe_config)]
+    L.moe_workspace_size.restype = c_size_t
+    L.moe_host_staging_size.argtypes = [P(moe_config)]
+    L.moe_host_staging_size.restype = c_size_t
+    L.moe_forward.argtypes = [P(moe_config), P(moe_weights), c_void_p, c_void_p, c_void_p,
+                              c_size_t, c_void_p]
+    L.moe_backward.argtypes = [P(moe_config), P(moe_weights), c_void_p, c_void_p, P(moe_grads),
+                               c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_train_step.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p, c_float,
+                                 c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_train_step_host.argtypes = [P(moe_config), P(moe_params), c_void_p, c_void_p,
+                                      c_float, c_void_p, c_void_p, c_size_t, c_void_p,
+                                      c_size_t, c_void_p]
+    L.moe_train_steps_host.argtypes = [P(moe_config), P(moe_params), c_int32, c_void_p,
+                                       c_void_p, c_float, c_void_p, c_void_p, c_size_t,
+                                       c_void_p, c_size_t, c_void_p]
+    L.moe_get_routing.argtypes = [P(moe_config), c_void_p, c_size_t] + [c_void_p] * 8
+    L.moe_get_intermediates.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
+                                        c_void_p, c_void_p]
+    L.moe_status_string.argtypes = [c_int32]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_last_launch_count.argtypes = []
+    L.moe_last_launch_count.restype = c_int32
+    L.moe_profile_enable.argtypes = [c_int32]
+    L.moe_profile_enable.restype = None
+    L.moe_profile_count.argtypes = []
+    L.moe_profile_count.restype = c_int32
+    L.moe_profile_name.argtypes = [c_int32]
+    L.moe_profile_name.restype = ctypes.c_char_p
+    L.moe_profile_ms.argtypes = [c_int32]
+    L.moe_profile_ms.restype = c_float
+    L.moe_dispatch_noalloc.argtypes = [P(moe_config)] + [c_void_p] * 6
+    L.moe_device_status.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p]
+    L.moe_get_hidden.argtypes = [P(moe_config), c_void_p, c_size_t, c_void_p, c_void_p,
+                                 c_void_p]
+    L.moe_grouped_gemm.argtypes = [c_int32] * 5 + [c_void_p] * 6
+    L.moe_selftest_wait_timeout.argtypes = [c_int32] * 5 + [c_void_p] * 5 + [ctypes.c_int64,
+                                                                            c_void_p]
+    L.moe_ep_workspace_size.argtypes = [P(moe_config), P(moe_ep_config)]
+    L.moe_ep_workspace_size.restype = c_size_t
+    L.moe_ep_buffer_offsets.argtypes = [P(moe_config), P(moe_ep_config), P(c_size_t)]
+    L.moe_ep_route.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights), c_void_p,
+                               c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_ep_expert_forward.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights),
+                                        P(moe_ep_rows), c_void_p]
+    L.moe_ep_combine.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_ep_expert_backward.argtypes = [P(moe_config), P(moe_ep_config), P(moe_params),
+                                         P(moe_ep_rows), c_float, c_void_p]
+    L.moe_ep_router_backward.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.moe_ep_router_update.argtypes = [P(moe_config), c_void_p, c_void_p, c_float, c_void_p]
+    L.moe_ep_get_routing.argtypes = [P(moe_config), P(moe_ep_config), c_void_p, c_size_t] + \
+        [c_void_p] * 8
+    for fn in ("moe_ep_buffer_offsets", "moe_ep_get_routing", "moe_ep_route",
+               "moe_ep_expert_forward",
+               "moe_ep_combine", "moe_ep_expert_backward", "moe_ep_router_backward",
+               "moe_ep_router_update"):
+        getattr(L, fn).restype = c_int32
+    for fn in ("moe_forward", "moe_backward", "moe_train_step", "moe_train_step_host",
+               "moe_train_steps_host",
+               "moe_get_routing", "moe_get_intermediates", "moe_get_hidden",
+               "moe_dispatch_noalloc",
+               "moe_device_status", "moe_grouped_gemm", "moe_selftest_wait_timeout"):
+        getattr(L, fn).restype = c_int32
+    L.moe_build_flags.argtypes = []
+    L.moe_build_flags.restype = c_int32
+    L.moe_debug_poke_routing.argtypes = [P(moe_config), c_void_p, c_size_t, c_int32,
+                                         ctypes.c_int64, c_int32, c_void_p]
+    L.moe_debug_poke_routing.restype = c_int32
+    _loaded[path] = L
+    return L
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -397,3 +433,16 @@ def moe_ep_router_update(cfg, w_gate, dw_gate, lr, stream=None):
     _check("moe_ep_router_update",
            lib().moe_ep_router_update(ctypes.byref(cfg), _ptr(w_gate), _ptr(dw_gate), float(lr),
                                       _stream(stream)))
+
+
+def moe_build_flags() -> int:
+    return int(lib().moe_build_flags())
+
+
+def moe_debug_poke_routing(cfg, workspace, field: int, index: int, value: int, stream=None):
+    """Write one routing entry (field 0 idx, 1 slot_of) of the last forward's
+    state: the MOE_DEBUG variant's fault injection (the release library
+    refuses)."""
+    _check("moe_debug_poke_routing",
+           lib().moe_debug_poke_routing(ctypes.byref(cfg), _ptr(workspace), workspace.numel(),
+                                        int(field), int(index), int(value), _stream(stream)))

@@ -46,36 +46,54 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_library(verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link the library; returns its path."""
+LIB_DEBUG = os.path.join(PKG, "libmoe_gb300_debug.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+
+
+def _variant(debug: bool):
+    """(object directory, library path, extra nvcc flags) of the release or
+    the MOE_DEBUG build (device-side index checks; see csrc/common.cuh)."""
+    if debug:
+        return BUILD_DEBUG, LIB_DEBUG, ["-DMOE_DEBUG"]
+    return BUILD, LIB, []
+
+
+def _run(cmd, verbose):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    if verbose and (r.stdout or r.stderr):
+        print(r.stdout + r.stderr)
+    return cmd
+
+
+def build_library(verbose: bool = False, extra_flags=None, debug: bool = False,
+                  also_debug: bool = False) -> str:
+    """Compile and link the library (or, with debug=True, its MOE_DEBUG
+    variant); also_debug builds both, their files compiled in one pool.
+    Returns the path of the (first) library."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    flags = NVCC_FLAGS + list(extra_flags or [])
     headers = _headers()
-    jobs = []
-    objs = []
-    for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        objs.append(obj)
-        if _stale(obj, [src] + headers):
-            cmd = [nvcc] + ARCH + flags + ["-I", INCLUDE, "-c", src, "-o", obj]
-            jobs.append(cmd)
-
-    def run(cmd):
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-        if verbose and (r.stdout or r.stderr):
-            print(r.stdout + r.stderr)
-        return cmd
-
-    if jobs:
-        with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
-            list(ex.map(run, jobs))
-    if jobs or _stale(LIB, objs):
-        cmd = [nvcc] + ARCH + ["-shared", "-o", LIB] + objs
-        run(cmd)
-    return LIB
+    variants = [debug] + ([not debug] if also_debug else [])
+    compile_jobs, links = [], []
+    for dbg in variants:
+        bdir, lib, vflags = _variant(dbg)
+        os.makedirs(bdir, exist_ok=True)
+        flags = NVCC_FLAGS + vflags + list(extra_flags or [])
+        objs = []
+        for src in _sources():
+            obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+            objs.append(obj)
+            if _stale(obj, [src] + headers):
+                compile_jobs.append([nvcc] + ARCH + flags + ["-I", INCLUDE, "-c", src, "-o", obj])
+        links.append((lib, objs))
+    if compile_jobs:
+        with cf.ThreadPoolExecutor(max_workers=min(len(compile_jobs), os.cpu_count() or 4)) as ex:
+            list(ex.map(lambda c: _run(c, verbose), compile_jobs))
+    for lib, objs in links:
+        if _stale(lib, objs):
+            _run([nvcc] + ARCH + ["-shared", "-o", lib] + objs, verbose)
+    return links[0][0]
 
 
 if __name__ == "__main__":

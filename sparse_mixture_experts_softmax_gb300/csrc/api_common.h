@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <mutex>
 #include <vector>
@@ -27,7 +28,12 @@ inline thread_local bool g_prof = false;
 inline thread_local std::vector<ProfRec> g_prof_recs;
 inline thread_local int g_prof_n = 0;
 
+// Every kernel launch is also an NVTX range named after the step it runs
+// ("gemm_dw1", "combine_fused", ...), so that profilers can select kernels
+// by step (ncu --nvtx --nvtx-include "gemm_dw1/").  NVTX v3 is header-only:
+// with no tool attached a range costs a check of a function pointer.
 inline void prof_begin(const char* name, cudaStream_t st) {
+  nvtxRangePushA(name);
   if (!g_prof || g_prof_n >= 4096) return;
   if (g_prof_n == (int)g_prof_recs.size()) {
     ProfRec r{name, nullptr, nullptr};
@@ -38,6 +44,7 @@ inline void prof_begin(const char* name, cudaStream_t st) {
   cudaEventRecord(g_prof_recs[g_prof_n].a, st);
 }
 inline void prof_end(cudaStream_t st) {
+  nvtxRangePop();
   if (!g_prof || g_prof_n >= 4096 || g_prof_n >= (int)g_prof_recs.size()) return;
   cudaEventRecord(g_prof_recs[g_prof_n].b, st);
   ++g_prof_n;

@@ -70,6 +70,36 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Routing indices before use.  A release build trusts the dispatch that
+// wrote them: a slot s >= 0 is used, -1 (an assignment dropped by the expert
+// capacity) is skipped; an expert id outside [0, E) is skipped.  A MOE_DEBUG
+// build checks every index against its range before it is dereferenced: a
+// slot outside [-1, R) or an expert id outside [0, E) is skipped and
+// MOE_ERR_INVALID_ARG (1) is recorded in the status word (never a trap).
+#ifdef MOE_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+constexpr int DEV_STATUS_INVALID_INDEX = 1;
+__device__ __forceinline__ void debug_flag(int* status) {
+  if (status != nullptr) atomicCAS(status, 0, DEV_STATUS_INVALID_INDEX);
+}
+__device__ __forceinline__ bool use_slot(int s, long long R, int* status) {
+  if (!kDebugChecks) return s >= 0;
+  if (s == -1) return false;
+  if (s < 0 || (long long)s >= R) {
+    debug_flag(status);
+    return false;
+  }
+  return true;
+}
+__device__ __forceinline__ bool valid_expert(int e, int E, int* status) {
+  if ((unsigned)e < (unsigned)E) return true;
+  if (kDebugChecks) debug_flag(status);
+  return false;
+}
+
 // Activations (course Part 1) and their derivatives.  CUDA's own tanhf/expf
 // are called; nothing of their implementation is restated.
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }

@@ -13,7 +13,7 @@ namespace {
 // Per-chunk expert histogram of the routed assignments (t, j) in token order.
 __global__ void __launch_bounds__(256)
 route_count_kernel(const int* __restrict__ idx, long long R, int chunk, int E,
-                   int* __restrict__ chunk_counts) {
+                   int* __restrict__ chunk_counts, int* dbg) {
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -21,7 +21,7 @@ route_count_kernel(const int* __restrict__ idx, long long R, int chunk, int E,
   const long long hi = min(lo + chunk, R);
   for (long long f = lo + threadIdx.x; f < hi; f += blockDim.x) {
     int e = idx[f];
-    if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);   // integer: order-independent
+    if (valid_expert(e, E, dbg)) atomicAdd(&hist[e], 1);   // integer: order-independent
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -96,7 +96,7 @@ route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int cap, int* __rest
 __global__ void __launch_bounds__(32)
 route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k, int E, int cap,
                      const int* __restrict__ chunk_base, const int* __restrict__ offsets,
-                     int* __restrict__ src_tok, int* __restrict__ slot_of) {
+                     int* __restrict__ src_tok, int* __restrict__ slot_of, int* dbg) {
   __shared__ int cursor[256];
   __shared__ int off[256];
   const int lane = threadIdx.x;
@@ -112,7 +112,7 @@ route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k,
     const long long f = base + lane;
     const bool valid = f < hi;
     int e = valid ? idx[f] : -1;
-    if ((unsigned)e >= (unsigned)E) e = -1;
+    if (valid && !valid_expert(e, E, dbg)) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
     if (e >= 0) {
@@ -137,8 +137,9 @@ route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k,
 template <typename T>
 __global__ void __launch_bounds__(256)
 gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, int k, int D,
-              T* __restrict__ xe) {
+              T* __restrict__ xe, int* dbg) {
   constexpr int VN = 16 / sizeof(T);
+  const long long R = (long long)Tn * k;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int nv = D / VN;
@@ -149,7 +150,7 @@ gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, 
     for (; v + 96 < nv; v += 128) {
       const uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
       for (int j = 0; j < k; ++j) {
-        if (so[j] < 0) continue;   // dropped by the expert capacity
+        if (!use_slot(so[j], R, dbg)) continue;   // dropped by the expert capacity
         uint4* dst = reinterpret_cast<uint4*>(xe + (size_t)so[j] * D);
         dst[v] = a0; dst[v + 32] = a1; dst[v + 64] = a2; dst[v + 96] = a3;
       }
@@ -157,7 +158,7 @@ gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, 
     for (; v < nv; v += 32) {
       const uint4 a = src[v];
       for (int j = 0; j < k; ++j)
-        if (so[j] >= 0) reinterpret_cast<uint4*>(xe + (size_t)so[j] * D)[v] = a;
+        if (use_slot(so[j], R, dbg)) reinterpret_cast<uint4*>(xe + (size_t)so[j] * D)[v] = a;
     }
   }
 }
@@ -175,8 +176,9 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
                const int* __restrict__ slot_of, int Tn, int D, int k, const T* __restrict__ ys,
                float* __restrict__ y,
                const float* __restrict__ target, float* __restrict__ dy, float inv_n,
-               double* __restrict__ sq_partial) {
+               double* __restrict__ sq_partial, int* dbg) {
   constexpr int VN = Vec<T>::N;
+  const long long R = (long long)Tn * k;
   __shared__ float wpart[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float sq = 0.f;
@@ -189,7 +191,7 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
       for (int j = 0; j < k; ++j) {
         const int s = slot_of[(size_t)t * k + j];
-        if (s < 0) continue;   // dropped by the expert capacity: no output
+        if (!use_slot(s, R, dbg)) continue;   // dropped by the expert capacity: no output
         const float g = gate[(size_t)t * k + j];
         Vec<T> v;
         v.load(ye + (size_t)s * D + d);
@@ -255,9 +257,10 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
                      const int* __restrict__ slot_of, int Tn, int D, int k,
                      const T* __restrict__ ys, const float* __restrict__ target, float inv_n,
                      double* __restrict__ sq_partial, T* __restrict__ dye,
-                     float* __restrict__ dgate, bf16* __restrict__ dy_lp) {
+                     float* __restrict__ dgate, bf16* __restrict__ dy_lp, int* dbg) {
   constexpr int VN = Vec<T>::N;
   constexpr int MAXK = 8;
+  const long long R = (long long)Tn * k;
   __shared__ float wpart[CT_WARPS];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float sq = 0.f;
@@ -265,10 +268,12 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
     const int t = blockIdx.x * CB_TOK + warp * (CB_TOK / CT_WARPS) + tt;
     if (t >= Tn) break;
     int slot[MAXK];
+    bool use[MAXK];
     float g[MAXK], dot[MAXK];
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
       slot[j] = (j < k) ? slot_of[(size_t)t * k + j] : 0;
+      use[j] = j < k && use_slot(slot[j], R, dbg);
       g[j] = (j < k) ? gate[(size_t)t * k + j] : 0.f;
       dot[j] = 0.f;
     }
@@ -276,13 +281,13 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       Vec<T> v[MAXK];
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
-        if (j < k && slot[j] >= 0) v[j].load(ye + (size_t)slot[j] * D + d);
+        if (use[j]) v[j].load(ye + (size_t)slot[j] * D + d);
       float acc[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
-        if (j < k && slot[j] >= 0) {
+        if (use[j]) {
 #pragma unroll
           for (int i = 0; i < VN; ++i) acc[i] = fmaf(g[j], v[j].get(i), acc[i]);
         }
@@ -312,7 +317,7 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
       }
 #pragma unroll
       for (int j = 0; j < MAXK; ++j)
-        if (j < k && slot[j] >= 0) {   // a dropped assignment keeps dg = 0
+        if (use[j]) {   // a dropped assignment keeps dg = 0
           Vec<T> o;
 #pragma unroll
           for (int i = 0; i < VN; ++i) {
@@ -416,16 +421,19 @@ template <typename T, int MAXK>
 __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
                    const float* __restrict__ gate, const int* __restrict__ slot_of, int Tn, int D,
-                   int k, T* __restrict__ dye, float* __restrict__ dgate) {
+                   int k, T* __restrict__ dye, float* __restrict__ dgate, int* dbg) {
   constexpr int VN = Vec<T>::N;
+  const long long R = (long long)Tn * k;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= Tn) return;
   int slot[MAXK];
+  bool use[MAXK];
   float g[MAXK], dot[MAXK];
 #pragma unroll
   for (int j = 0; j < MAXK; ++j) {
     slot[j] = (j < k) ? slot_of[(size_t)t * k + j] : 0;
+    use[j] = j < k && use_slot(slot[j], R, dbg);
     g[j] = (j < k) ? gate[(size_t)t * k + j] : 0.f;
     dot[j] = 0.f;
   }
@@ -438,7 +446,7 @@ combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
     }
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
-      if (j < k && slot[j] >= 0) {   // dropped by the expert capacity: dg = 0
+      if (use[j]) {   // dropped by the expert capacity: dg = 0
         Vec<T> v, o;
         v.load(ye + (size_t)slot[j] * D + d);
 #pragma unroll
@@ -466,8 +474,9 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
                         const int* __restrict__ slot_of, int Tn, int D, int k,
-                        const T* __restrict__ extra) {
+                        const T* __restrict__ extra, int* dbg) {
   constexpr int VN = Vec<T>::N;
+  const long long R = (long long)Tn * k;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= Tn) return;
@@ -480,7 +489,7 @@ scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
     }
     for (int j = 0; j < k; ++j) {
       const int s = slot_of[(size_t)t * k + j];
-      if (s < 0) continue;   // dropped by the expert capacity
+      if (!use_slot(s, R, dbg)) continue;   // dropped by the expert capacity
       Vec<T> v;
       v.load(dxe + (size_t)s * D + d);
 #pragma unroll
@@ -586,10 +595,10 @@ int route_chunks(long long R) {
 }
 
 cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
-                               cudaStream_t st) {
+                               cudaStream_t st, int* dbg) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
-  route_count_kernel<<<nc, 256, 0, st>>>(idx, R, route_chunk(R), E, chunk_counts);
+  route_count_kernel<<<nc, 256, 0, st>>>(idx, R, route_chunk(R), E, chunk_counts, dbg);
   return cudaGetLastError();
 }
 
@@ -601,24 +610,24 @@ cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int cap, in
 
 cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, int cap,
                                  const int* chunk_base, const int* offsets, int* src_tok,
-                                 int* slot_of, cudaStream_t st) {
+                                 int* slot_of, cudaStream_t st, int* dbg) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
   route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, route_chunk(R), k, E, cap, chunk_base, offsets,
-                                          src_tok, slot_of);
+                                          src_tok, slot_of, dbg);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, int k, int D,
-                          void* xe, cudaStream_t st) {
+                          void* xe, cudaStream_t st, int* dbg) {
   if (T == 0) return cudaSuccess;
   int grid = grid_for(T, 8, 152 * 16);
   if (dtype == 1)
     gather_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(x), slot_of, T, k, D,
-                                              static_cast<bf16*>(xe));
+                                              static_cast<bf16*>(xe), dbg);
   else
     gather_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), slot_of, T, k, D,
-                                               static_cast<float*>(xe));
+                                               static_cast<float*>(xe), dbg);
   return cudaGetLastError();
 }
 
@@ -626,25 +635,25 @@ int combine_blocks(int T) { return (T + CB_TOK - 1) / CB_TOK; }
 
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of, int T,
                            int D, int k, const void* ys, float* y, const float* target, float* dy,
-                           double* sq_partial, cudaStream_t st, float inv_n) {
+                           double* sq_partial, cudaStream_t st, float inv_n, int* dbg) {
   if (T == 0) return cudaSuccess;
   if (inv_n == 0.f) inv_n = 1.0f / ((float)T * (float)D);
   int grid = combine_blocks(T);
   if (dtype == 1)
     combine_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T, D, k,
                                                static_cast<const bf16*>(ys), y, target, dy, inv_n,
-                                               sq_partial);
+                                               sq_partial, dbg);
   else
     combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(ye), gate, slot_of, T, D,
                                                 k, static_cast<const float*>(ys), y, target, dy,
-                                                inv_n, sq_partial);
+                                                inv_n, sq_partial, dbg);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
                                  int T, int D, int k, const void* ys, const float* target,
                                  double* sq_partial, void* dye, float* dgate, void* dy_lp,
-                                 cudaStream_t st, float inv_n) {
+                                 cudaStream_t st, float inv_n, int* dbg) {
   // the shared branch exists only for bf16 layers and comes with both Ys and dY
   const bool shared = ys != nullptr;
   if (k > 8 || (shared && (dy_lp == nullptr || dtype != 1))) return cudaErrorInvalidValue;
@@ -654,15 +663,15 @@ cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, c
   if (dtype == 1 && shared)
     combine_train_kernel<bf16, true><<<grid, 32 * CT_WARPS, 0, st>>>(
         static_cast<const bf16*>(ye), gate, slot_of, T, D, k, static_cast<const bf16*>(ys), target,
-        inv_n, sq_partial, static_cast<bf16*>(dye), dgate, static_cast<bf16*>(dy_lp));
+        inv_n, sq_partial, static_cast<bf16*>(dye), dgate, static_cast<bf16*>(dy_lp), dbg);
   else if (dtype == 1)
     combine_train_kernel<bf16, false><<<grid, 32 * CT_WARPS, 0, st>>>(
         static_cast<const bf16*>(ye), gate, slot_of, T, D, k, nullptr, target, inv_n, sq_partial,
-        static_cast<bf16*>(dye), dgate, nullptr);
+        static_cast<bf16*>(dye), dgate, nullptr, dbg);
   else
     combine_train_kernel<float, false><<<grid, 32 * CT_WARPS, 0, st>>>(
         static_cast<const float*>(ye), gate, slot_of, T, D, k, nullptr, target, inv_n,
-        sq_partial, static_cast<float*>(dye), dgate, nullptr);
+        sq_partial, static_cast<float*>(dye), dgate, nullptr, dbg);
   return cudaGetLastError();
 }
 
@@ -676,42 +685,44 @@ cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const flo
 
 cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
                                const int* slot_of, int T, int D, int k, void* dye, float* dgate,
-                               cudaStream_t st) {
+                               cudaStream_t st, int* dbg) {
   if (T == 0) return cudaSuccess;
   int grid = (T + 7) / 8;
   if (dtype == 1) {
     if (k <= 8)
       combine_bwd_kernel<bf16, 8><<<grid, 256, 0, st>>>(dy, static_cast<const bf16*>(ye), gate,
                                                         slot_of, T, D, k, static_cast<bf16*>(dye),
-                                                        dgate);
+                                                        dgate, dbg);
     else
       combine_bwd_kernel<bf16, 32><<<grid, 256, 0, st>>>(dy, static_cast<const bf16*>(ye), gate,
                                                          slot_of, T, D, k, static_cast<bf16*>(dye),
-                                                         dgate);
+                                                         dgate, dbg);
   } else {
     if (k <= 8)
       combine_bwd_kernel<float, 8><<<grid, 256, 0, st>>>(dy, static_cast<const float*>(ye), gate,
                                                          slot_of, T, D, k,
-                                                         static_cast<float*>(dye), dgate);
+                                                         static_cast<float*>(dye), dgate, dbg);
     else
       combine_bwd_kernel<float, 32><<<grid, 256, 0, st>>>(dy, static_cast<const float*>(ye), gate,
                                                           slot_of, T, D, k,
-                                                          static_cast<float*>(dye), dgate);
+                                                          static_cast<float*>(dye), dgate, dbg);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const int* slot_of,
-                                    int T, int D, int k, const void* extra, cudaStream_t st) {
+                                    int T, int D, int k, const void* extra, cudaStream_t st,
+                                    int* dbg) {
   if (T == 0) return cudaSuccess;
   const int grid = (T + 7) / 8;
   if (dtype == 1)
     scatter_back_add_kernel<bf16><<<grid, 256, 0, st>>>(dx, static_cast<const bf16*>(dxe), slot_of,
-                                                         T, D, k, static_cast<const bf16*>(extra));
+                                                         T, D, k, static_cast<const bf16*>(extra),
+                                                         dbg);
   else
     scatter_back_add_kernel<float><<<grid, 256, 0, st>>>(dx, static_cast<const float*>(dxe),
                                                           slot_of, T, D, k,
-                                                          static_cast<const float*>(extra));
+                                                          static_cast<const float*>(extra), dbg);
   return cudaGetLastError();
 }
 

@@ -206,15 +206,17 @@ moe_status moe_ep_combine(const moe_config* cfg, const moe_ep_config* ep,
       KL("combine_fused", launch_combine_train(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate),
                                                P.at<int>(L.slot_of), c.T, c.D, c.k, nullptr,
                                                y_target, P.at<double>(L.sq), P.at<void>(L.dye),
-                                               P.at<float>(L.dgate), nullptr, st, inv_n));
+                                               P.at<float>(L.dgate), nullptr, st, inv_n,
+                                               P.at<int>(L.status)));
     } else {
       KL("combine_loss", launch_combine(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate),
                                         P.at<int>(L.slot_of), c.T, c.D, c.k, nullptr, nullptr,
                                         y_target, P.at<float>(L.dy), P.at<double>(L.sq), st,
-                                        inv_n));
+                                        inv_n, P.at<int>(L.status)));
       KL("combine_bwd", launch_combine_bwd(c.dtype, P.at<float>(L.dy), P.at<void>(L.ye),
                                            P.at<float>(L.gate), P.at<int>(L.slot_of), c.T, c.D,
-                                           c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st));
+                                           c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st,
+                                           P.at<int>(L.status)));
     }
   }
   // losses from the statistics of all ranks: this rank's squared errors over

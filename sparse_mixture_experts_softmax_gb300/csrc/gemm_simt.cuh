@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
           float s = v;
           for (int jj = 0; jj < g.k; ++jj) {
             const int slot = g.slot_of[(size_t)r * g.k + jj];
-            if (slot < 0) continue;   // dropped by the expert capacity
+            // dropped by the expert capacity (or, in a MOE_DEBUG build, out of range)
+            if (!use_slot(slot, (long long)g.M * g.k, g.status)) continue;
             s += ld_rt(g.src, (size_t)slot * g.N + c, g.src_type);
           }
           static_cast<float*>(g.C)[ci] = s;

@@ -41,7 +41,8 @@ cudaError_t launch_router_fwd(int dtype, const void* x, const float* wg, const f
                               float* psum_partial, cudaStream_t st);
 cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* gate,
                               const float* dgate, const float* aux_row, const RouterArgs& a,
-                              float* dlogits, void* dlogits_lp, cudaStream_t st);
+                              float* dlogits, void* dlogits_lp, cudaStream_t st,
+                              int* dbg = nullptr);
 // selection from precomputed logits (bias already added) and the bf16 weight cast
 cudaError_t launch_router_select(const float* logits, const RouterArgs& a, float* scores, int* idx,
                                  float* gate, float* psum_partial, cudaStream_t st);
@@ -57,8 +58,10 @@ constexpr int ROUTE_CHUNK_MAX = 1024;
 constexpr int ROUTE_TARGET_CHUNKS = 608;   // four per SM
 int route_chunk(long long R);
 int route_chunks(long long R);
+// dbg: the status word a MOE_DEBUG build records an out-of-range routing
+// index in (unused by release builds), or nullptr; see common.cuh.
 cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_counts,
-                               cudaStream_t st);
+                               cudaStream_t st, int* dbg = nullptr);
 // Rows an expert may keep under a capacity factor cf > 0: ceil(cf * T * k / E)
 // (computed in double), else INT_MAX (no limit).
 inline int expert_capacity_rows(float cf, int T, int k, int E) {
@@ -73,16 +76,17 @@ cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int cap, in
                               int* offsets, cudaStream_t st);
 cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, int cap,
                                  const int* chunk_base, const int* offsets, int* src_tok,
-                                 int* slot_of, cudaStream_t st);
+                                 int* slot_of, cudaStream_t st, int* dbg = nullptr);
 cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, int k, int D,
-                          void* xe, cudaStream_t st);
+                          void* xe, cudaStream_t st, int* dbg = nullptr);
 int combine_blocks(int T);
 // ys: the shared-expert branch's output [T, D] added to Y, or nullptr.
 // inv_n: the MSE normaliser 1 / (tokens D); 0 takes 1 / (T D) (a single
 // device; an expert-parallel rank passes the one over all ranks' tokens).
 cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const int* slot_of,
                            int T, int D, int k, const void* ys, float* y, const float* target,
-                           float* dy, double* sq_partial, cudaStream_t st, float inv_n = 0.f);
+                           float* dy, double* sq_partial, cudaStream_t st, float inv_n = 0.f,
+                           int* dbg = nullptr);
 cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
                                    int n_ps, const int* counts, int T, int D, int E, int k,
                                    float alpha, float* d_loss, float* aux_row, cudaStream_t st);
@@ -91,13 +95,14 @@ cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const flo
 cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, const int* slot_of,
                                  int T, int D, int k, const void* ys, const float* target,
                                  double* sq_partial, void* dye, float* dgate, void* dy_lp,
-                                 cudaStream_t st, float inv_n = 0.f);
+                                 cudaStream_t st, float inv_n = 0.f, int* dbg = nullptr);
 cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const float* gate,
                                const int* slot_of, int T, int D, int k, void* dye, float* dgate,
-                               cudaStream_t st);
+                               cudaStream_t st, int* dbg = nullptr);
 // extra: a [T, D] row block (cfg dtype) added to dX after the expert rows, or nullptr.
 cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const int* slot_of,
-                                    int T, int D, int k, const void* extra, cudaStream_t st);
+                                    int T, int D, int k, const void* extra, cudaStream_t st,
+                                    int* dbg = nullptr);
 cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets, int E, int N,
                                   float* out, cudaStream_t st);
 cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,

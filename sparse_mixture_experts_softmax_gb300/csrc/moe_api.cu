@@ -237,7 +237,8 @@ moe_status route_tokens(const moe_config& c, const ExpertW& w, const void* x, co
     KL("router_fwd", launch_router_fwd(c.dtype, x, w.w_gate, w.logit_bias, ra, P.at<float>(L.scores),
                                        P.at<int>(L.idx), P.at<float>(L.gate), P.at<float>(L.psum), st));
   }
-  KL("route_count", launch_route_count(P.at<int>(L.idx), R, c.E, P.at<int>(L.chunk), st));
+  int* dbg = P.at<int>(L.status);
+  KL("route_count", launch_route_count(P.at<int>(L.idx), R, c.E, P.at<int>(L.chunk), st, dbg));
   // with a capacity factor each expert keeps its first `cap` assignments in
   // token order; dropped ones get slot -1 and are skipped downstream
   const int cap = expert_capacity_rows(c.capacity_factor, c.T, c.k, c.E);
@@ -245,8 +246,9 @@ moe_status route_tokens(const moe_config& c, const ExpertW& w, const void* x, co
                                      P.at<int>(L.counts), P.at<int>(L.offsets), st));
   KL("route_scatter", launch_route_scatter(P.at<int>(L.idx), R, c.k, c.E, cap, P.at<int>(L.chunk),
                                            P.at<int>(L.offsets), P.at<int>(L.src_tok),
-                                           P.at<int>(L.slot_of), st));
-  KL("gather", launch_gather(c.dtype, x, P.at<int>(L.slot_of), c.T, c.k, c.D, P.at<void>(L.xe), st));
+                                           P.at<int>(L.slot_of), st, dbg));
+  KL("gather", launch_gather(c.dtype, x, P.at<int>(L.slot_of), c.T, c.k, c.D, P.at<void>(L.xe), st,
+                             dbg));
   return MOE_OK;
 }
 
@@ -264,7 +266,8 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
   const bool lp = c.dtype == MOE_BF16;
   KL("router_bwd", launch_router_bwd(P.at<float>(L.scores), P.at<int>(L.idx), P.at<float>(L.gate),
                        P.at<float>(L.dgate), c.aux_alpha != 0.f ? P.at<float>(L.aux_row) : nullptr,
-                       ra, P.at<float>(L.dlogits), lp ? P.at<void>(L.dl_lp) : nullptr, st));
+                       ra, P.at<float>(L.dlogits), lp ? P.at<void>(L.dl_lp) : nullptr, st,
+                       P.at<int>(L.status)));
   if (lp) {
     // tensor-core router products: dW_g = dlogits^T x (split over token
     // chunks, fixed-order sum) and dX = dlogits W_g + scatter-back of dXe.
@@ -316,7 +319,7 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
     dg.epi = EPI_STORE;
     KL("gemm_router_dx", launch_gemm_tc(dg, st));
     KL("scatter_back", launch_scatter_back_add(c.dtype, dx, P.at<void>(L.dxe), P.at<int>(L.slot_of),
-                                               c.T, c.D, c.k, extra_dx, st));
+                                               c.T, c.D, c.k, extra_dx, st, P.at<int>(L.status)));
     return MOE_OK;
   }
   // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
@@ -366,6 +369,7 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
   dg.C = dx;
   dg.ldc = c.D;
   dg.epi = EPI_SCATTER_ADD;
+  dg.status = P.at<int>(L.status);
   dg.slot_of = P.at<int>(L.slot_of);
   dg.k = c.k;
   dg.src = P.at<void>(L.dxe);
@@ -468,11 +472,12 @@ moe_status run_forward(const moe_config& c, const ExpertW& w, const void* x, flo
                                              P.at<int>(L.slot_of), c.T, c.D, c.k, ys, target,
                                              P.at<double>(L.sq), P.at<void>(L.dye),
                                              P.at<float>(L.dgate),
-                                             shared ? P.at<void>(L.dy_lp) : nullptr, st));
+                                             shared ? P.at<void>(L.dy_lp) : nullptr, st, 0.f,
+                                             P.at<int>(L.status)));
   } else {
     KL("combine_loss", launch_combine(c.dtype, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of), c.T,
                       c.D, c.k, ys, y, target, train ? P.at<float>(L.dy) : nullptr,
-                      train ? P.at<double>(L.sq) : nullptr, st));
+                      train ? P.at<double>(L.sq) : nullptr, st, 0.f, P.at<int>(L.status)));
   }
   if (train)
     KL("finalize_losses", launch_finalize_losses(P.at<double>(L.sq), combine_blocks(c.T), P.at<float>(L.psum),
@@ -494,7 +499,8 @@ moe_status run_backward(const moe_config& c, const ExpertW& w, const void* x, co
                               P.at<float>(L.aux_row), st));
   if (dy != nullptr)
     KL("combine_bwd", launch_combine_bwd(c.dtype, dy, P.at<void>(L.ye), P.at<float>(L.gate), P.at<int>(L.slot_of),
-                          c.T, c.D, c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st));
+                          c.T, c.D, c.k, P.at<void>(L.dye), P.at<float>(L.dgate), st,
+                          P.at<int>(L.status)));
   RET_IF(experts_backward(c, w, expert_rows(c, P), gr, sgd, st));
 
   if (c.n_shared > 0) {
@@ -1131,6 +1137,35 @@ const char* moe_status_string(moe_status s) {
 }
 
 int32_t moe_last_launch_count(void) { return g_launches; }
+
+int32_t moe_build_flags(void) {
+#ifdef MOE_DEBUG
+  return MOE_BUILD_DEBUG_CHECKS;
+#else
+  return 0;
+#endif
+}
+
+moe_status moe_debug_poke_routing(const moe_config* cfg, void* workspace, size_t workspace_bytes,
+                                  int32_t field, int64_t index, int32_t value, void* stream) {
+#ifndef MOE_DEBUG
+  (void)cfg; (void)workspace; (void)workspace_bytes; (void)field; (void)index; (void)value;
+  (void)stream;
+  return MOE_ERR_UNSUPPORTED;   // a release build never corrupts its own state
+#else
+  RET_IF(validate_config(cfg));
+  const moe_config& c = *cfg;
+  RET_IF(check_ws(c, workspace, workspace_bytes));
+  if (field != 0 && field != 1) return MOE_ERR_INVALID_ARG;
+  if (index < 0 || index >= (int64_t)c.T * c.k) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(c);
+  char* at = static_cast<char*>(workspace) + (field == 0 ? L.idx : L.slot_of) + (size_t)index * 4;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(cudaMemcpyAsync(at, &value, sizeof(value), cudaMemcpyHostToDevice, st));
+  CK(cudaStreamSynchronize(st));
+  return MOE_OK;
+#endif
+}
 
 void moe_profile_enable(int32_t on) {
   g_prof = on != 0;

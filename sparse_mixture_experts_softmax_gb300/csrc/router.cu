@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(256)
 router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
                   const float* __restrict__ gate, const float* __restrict__ dgate,
                   const float* __restrict__ aux_row, RouterArgs a,
-                  float* __restrict__ dlogits, bf16* __restrict__ dlogits_lp) {
+                  float* __restrict__ dlogits, bf16* __restrict__ dlogits_lp, int* dbg) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= a.T) return;
@@ -437,6 +437,9 @@ router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
   float S = 0.f, inner = 0.f;
   for (int j = 0; j < k; ++j) {
     int e = idx[(size_t)t * k + j];
+    // an expert id only selects a lane and a register here (never an
+    // address); a MOE_DEBUG build still reports and skips one out of range
+    if (kDebugChecks && !valid_expert(e, E, dbg)) continue;
     float sv = __shfl_sync(0xffffffffu, s[0], e & 31);
 #pragma unroll
     for (int c = 1; c < NC; ++c) {
@@ -448,6 +451,7 @@ router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
   }
   for (int j = 0; j < k; ++j) {
     int e = idx[(size_t)t * k + j];
+    if (kDebugChecks && !valid_expert(e, E, dbg)) continue;
     float dsel = (dgate[(size_t)t * k + j] - inner) / S;
 #pragma unroll
     for (int c = 0; c < NC; ++c)
@@ -520,14 +524,14 @@ cudaError_t launch_router_fwd(int dtype, const void* x, const float* wg, const f
 
 cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* gate,
                               const float* dgate, const float* aux_row, const RouterArgs& a,
-                              float* dlogits, void* dlogits_lp, cudaStream_t st) {
+                              float* dlogits, void* dlogits_lp, cudaStream_t st, int* dbg) {
   if (a.T == 0) return cudaSuccess;
   dim3 grid((a.T + 7) / 8);
   bf16* lp = static_cast<bf16*>(dlogits_lp);
-  if (a.E <= 32) router_bwd_kernel<1><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
-  else if (a.E <= 64) router_bwd_kernel<2><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
-  else if (a.E <= 128) router_bwd_kernel<4><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
-  else router_bwd_kernel<8><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp);
+  if (a.E <= 32) router_bwd_kernel<1><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
+  else if (a.E <= 64) router_bwd_kernel<2><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
+  else if (a.E <= 128) router_bwd_kernel<4><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
+  else router_bwd_kernel<8><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
   return cudaGetLastError();
 }
 

@@ -165,3 +165,52 @@ def test_status_strings(L):
     for s in range(7):
         assert B.moe_status_string(s)
     assert "workspace" in B.moe_status_string(B.MOE_ERR_WORKSPACE_TOO_SMALL)
+
+
+def test_expert_parallel_validation(L):
+    """The expert-parallel phases check their requests on the host."""
+    cfg = _cfg(E=8, act="swiglu", has_bias=False, dtype="bf16")
+    assert B.moe_ep_workspace_size(cfg, B.moe_ep_config(2, 0, 128)) > 0
+    assert B.moe_ep_workspace_size(cfg, B.moe_ep_config(3, 0, 128)) == 0   # 3 does not divide E
+    assert B.moe_ep_workspace_size(cfg, B.moe_ep_config(2, 2, 128)) == 0   # rank out of range
+    assert B.moe_ep_workspace_size(cfg, B.moe_ep_config(2, 0, 10)) == 0    # T_total < T
+    cap = _cfg(E=8, act="swiglu", has_bias=False, dtype="bf16", capacity_factor=1.0)
+    assert B.moe_ep_workspace_size(cap, B.moe_ep_config(2, 0, 128)) == 0   # no capacity here
+    # the source-side workspace holds no expert-MLP buffers
+    assert B.moe_ep_workspace_size(cfg, B.moe_ep_config(2, 0, 128)) < B.moe_workspace_size(cfg)
+    offs = B.moe_ep_buffer_offsets(cfg, B.moe_ep_config(2, 1, 128))
+    assert offs == sorted(offs) and offs[0] % 256 == 0
+    good = lambda i: _Fake(0x10000 * (i + 1))  # noqa: E731
+    ws = _Fake(0x900000, 1 << 40)
+    ep = B.moe_ep_config(2, 0, 128)
+    w = B.make_weights(good(1), None, None)
+    assert _status(B.moe_ep_route, cfg, ep, w, good(2), None, ws) == B.MOE_ERR_INVALID_ARG
+    assert _status(B.moe_ep_route, cfg, ep, w, good(2), _Fake(0x30004), ws) == B.MOE_ERR_ALIGNMENT
+    small = _Fake(0x900000, 1024)
+    assert _status(B.moe_ep_route, cfg, ep, w, good(2), good(3), small) \
+        == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    # received rows beyond what every rank could route are refused
+    rows = B.make_ep_rows(128 * 2 + 1, good(4), good(5), good(6), good(7), good(8), good(9),
+                          status=good(10))
+    wx = B.make_weights(None, good(1), good(2), good(3))
+    assert _status(B.moe_ep_expert_forward, cfg, ep, wx, rows) == B.MOE_ERR_INVALID_ARG
+
+
+def test_debug_variant_and_poke_refusal(L):
+    """The release library reports no debug checks and refuses the fault
+    injection entry point before touching the device; the MOE_DEBUG variant
+    (built beside it) exports the same symbols and reports its checks."""
+    assert B.moe_build_flags() == 0
+    ws = _Fake(0x900000, 1 << 40)
+    assert _status(B.moe_debug_poke_routing, _cfg(), ws, 1, 0, 5) == B.MOE_ERR_UNSUPPORTED
+    from sparse_mixture_experts_softmax_gb300.build import LIB_DEBUG
+    if not os.path.exists(LIB_DEBUG):
+        build_library(debug=True)
+    dbg = ctypes.CDLL(LIB_DEBUG)
+    for n in _declared():
+        assert hasattr(dbg, n), n
+    with B.use_library(debug=True):
+        assert B.moe_build_flags() == B.MOE_BUILD_DEBUG_CHECKS
+        # host-side validation of the injection itself, before any device work
+        assert _status(B.moe_debug_poke_routing, _cfg(), ws, 2, 0, 5) == B.MOE_ERR_INVALID_ARG
+        assert _status(B.moe_debug_poke_routing, _cfg(), ws, 1, 64 * 2, 5) == B.MOE_ERR_INVALID_ARG
