@@ -43,11 +43,11 @@ FFMA_PER_SM_PER_CLK = 128
 # from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # same per-expert shapes at 8 experts, scaled by 16.  Valid only for the GEMM
 # source it was taken from: reported as null once gemm_tc.cu changes.
-GEMM_TRAFFIC = {"bytes_per_step": 122.2e9, "workload": "large",
-                "gemm_source_sha256_prefix": "ec7490d4efc27450"}
+GEMM_TRAFFIC = {"bytes_per_step": 106.7e9, "workload": "large",
+                "gemm_source_sha256_prefix": "07a5919a591b33ca", "gradients_stored": False}
 
 
-def gemm_traffic(wl: W.Workload):
+def gemm_traffic(wl: W.Workload, store_grads: bool = False):
     import hashlib
     src = os.path.join(ROOT, "sparse_mixture_experts_softmax_gb300", "csrc", "gemm_tc.cu")
     try:
@@ -56,6 +56,8 @@ def gemm_traffic(wl: W.Workload):
     except OSError:
         return None
     if wl.name != GEMM_TRAFFIC["workload"] or not sha.startswith(GEMM_TRAFFIC["gemm_source_sha256_prefix"]):
+        return None
+    if store_grads != GEMM_TRAFFIC["gradients_stored"]:
         return None
     return GEMM_TRAFFIC["bytes_per_step"]
 
@@ -463,7 +465,7 @@ def main():
         peak = GB300_SMS * FFMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
         bound, unit = "alu", "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": gemm_traffic(wl),
+                "frac": achieved / peak, "traffic": gemm_traffic(wl, args.store_grads),
                 "traffic_unit": "DRAM bytes per step of the GEMM family",
                 "traffic_measured_in_this_run": False,
                 "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of every "

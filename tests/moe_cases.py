@@ -96,11 +96,16 @@ def validated_relu_decisions(cfg: O.OracleConfig, st: dict, w: dict, h_kernel) -
     pre-activation within accumulation error of zero can fall on the kernel's
     side of zero differently from the float64 one.  Where the signs of the
     kernel's stored H (expert-major rows, the layer dtype) and the oracle's
-    differ, check that the oracle's value is within a bound far above fp32
-    accumulation error of zero (2^-14 * sum |x w| (+ |b|)), then let the
-    oracle's backward take the kernel's decision (h set to a signed tiny value
-    there; the forward values already computed are unchanged).  Returns the
-    number of decisions taken from the kernel."""
+    differ, check that the oracle's value lies within the fp32 accumulation
+    error bound of zero, then let the oracle's backward take the kernel's
+    decision (h set to a signed tiny value there; the forward values already
+    computed are unchanged).  The bound: a sum of D products in fp32 (exact
+    products of bf16 operands, or fused multiply-adds of fp32 ones) is within
+    D u sum |x w| of its exact value, u = 2^-24; it is doubled for an adder
+    that keeps one guard bit fewer (the tensor cores' accumulation order is
+    not the oracle's), and the bias add is one more term: (D + 1) 2^-23
+    (sum |x w| + |b|).  Returns the number of decisions taken from the
+    kernel."""
     if cfg.act != "relu":
         return 0
     hk = np.asarray(h_kernel, dtype=np.float64)
@@ -117,7 +122,8 @@ def validated_relu_decisions(cfg: O.OracleConfig, st: dict, w: dict, h_kernel) -
         scale = np.abs(st["xe"][lo:hi]) @ np.abs(w["w1"][e]).T
         if cfg.has_bias:
             scale = scale + np.abs(w["b1"][e])
-        assert np.all(np.abs(h64[differ]) <= 2.0 ** -14 * scale[differ]), \
+        bound = (cfg.D + 1) * 2.0 ** -23 * scale[differ]
+        assert np.all(np.abs(h64[differ]) <= bound), \
             f"expert {e}: ReLU decisions differ beyond rounding of a zero pre-activation"
         h_new = h64.copy()
         h_new[differ] = np.where(hk[lo:hi][differ] > 0.0, 1e-300, -1e-300)

@@ -64,6 +64,25 @@ def test_flip_within_rounding_is_taken_from_the_kernel():
     assert not diff[0].any() and not diff[2].any()
 
 
+def test_bound_grows_with_the_reduction_length():
+    """A flip at |h| just inside (D + 1) 2^-23 sum |x w| is taken, just outside
+    it fails: the bound is the fp32 accumulation error of a D-term sum."""
+    cfg, w, x = _case()
+    for factor, ok in ((0.9, True), (1.1, False)):
+        st = O.forward(cfg, w, x)
+        lo = int(st["offsets"][1])
+        scale = np.abs(st["xe"][lo]) @ np.abs(w["w1"][1][3]) + abs(w["b1"][1][3])
+        h = factor * (cfg.D + 1) * 2.0 ** -23 * scale
+        st["experts"][1]["h"][0, 3] = -h
+        hk = _kernel_h(st)
+        hk[lo, 3] = h
+        if ok:
+            assert validated_relu_decisions(cfg, st, w, hk) == 1
+        else:
+            with pytest.raises(AssertionError):
+                validated_relu_decisions(cfg, st, w, hk)
+
+
 def test_flip_beyond_rounding_fails():
     cfg, w, x = _case()
     st = O.forward(cfg, w, x)
