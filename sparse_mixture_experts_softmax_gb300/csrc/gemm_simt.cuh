@@ -3,8 +3,13 @@
 // "Trainable MoE in CUDA", Part 1 (matmul variants, bias add) and Part 5
 // (expert MLP forward and backward over each expert's slice of rows).
 //
-// Tile 128x128x8, 256 threads, 8x8 outputs per thread, register-prefetched
-// double buffering.  Three operand forms (see GemmArgs in kernels.h):
+// Tile 128x128x16, 256 threads (two blocks per SM), 8x8 outputs per thread,
+// register-prefetched double buffering.  Each operand tile is fetched with
+// 128-bit loads along its contiguous dimension (K for x W^T / dY W operands,
+// M or N for the ragged-K weight gradients) wherever the leading dimension
+// keeps them 16-byte aligned, and written to shared memory k-major (a
+// transpose in registers for the K-contiguous ones).  Three operand forms
+// (see GemmArgs in kernels.h):
 //   FORM 0  C[r,n] = sum_k A[r,k] B_e[n,k]   ragged M (x W^T)
 //   FORM 1  C[r,n] = sum_k A[r,k] B_e[k,n]   ragged M (x W)
 //   FORM 2  C_e[m,n] = sum_{r in e} A[r,m] B[r,n]   ragged K (weight gradients)
@@ -16,7 +21,7 @@
 namespace moe {
 namespace simt {
 
-constexpr int BM = 128, BN = 128, BK = 8, NT = 256;
+constexpr int BM = 128, BN = 128, BK = 16, NT = 256;
 
 template <typename T>
 __device__ __forceinline__ float ld_f(const void* p, size_t i) {
@@ -28,6 +33,24 @@ __device__ __forceinline__ float ld_rt(const void* p, size_t i, int type) {
 __device__ __forceinline__ void st_rt(void* p, size_t i, float v, int type) {
   if (type == 1) static_cast<bf16*>(p)[i] = __float2bfloat16_rn(v);
   else static_cast<float*>(p)[i] = v;
+}
+
+// Four consecutive elements of row `row` of a row-major matrix (leading
+// dimension ld), columns col0 .. col0 + 3; entries with row >= row_lim or
+// column >= col_lim read as zero.  One 128-bit load when `vec` (fp32, 16-byte
+// aligned rows and col0) and the four are in range.
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p, long long ld, int row, int row_lim, int col0,
+                                        int col_lim, bool vec) {
+  if (row >= row_lim) return make_float4(0.f, 0.f, 0.f, 0.f);
+  const T* q = p + (size_t)row * ld + col0;
+  if constexpr (sizeof(T) == 4) {
+    if (vec && col0 + 3 < col_lim) return *reinterpret_cast<const float4*>(q);
+  }
+  float v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = (col0 + i < col_lim) ? to_f(q[i]) : 0.f;
+  return make_float4(v[0], v[1], v[2], v[3]);
 }
 
 __device__ __forceinline__ int seg_lo(const GemmArgs& g, int e, int total) {
@@ -42,7 +65,7 @@ __device__ __forceinline__ int seg_hi(const GemmArgs& g, int e, int total) {
 }
 
 template <typename TA, typename TB, int FORM, int EPI>
-__global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
+__global__ void __launch_bounds__(NT, 2) gemm_simt_kernel(const GemmArgs g) {
   constexpr bool AK = FORM != 2;   // A element (m, k) has k contiguous
   constexpr bool BKC = FORM == 0;  // B element (k, n) has k contiguous
   constexpr bool RAGK = FORM == 2;
@@ -103,37 +126,42 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmArgs g) {
     const int mlim = RAGK ? g.M : hi;
     if (kend <= kbeg) continue;
 
-    float ra[4], rb[4];
+    // 512 four-element vectors per operand tile, two per thread
+    const bool vec_a = (g.lda % 4) == 0 && (AK ? (kbeg % 4) == 0 : true);
+    const bool vec_b = (g.ldb % 4) == 0 && (BKC ? (kbeg % 4) == 0 : true);
+    float4 ra[2], rb[2];
     auto load_tiles = [&](int k0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int l = tid + q * NT;
-        int m, kk;
-        if (AK) { m = l / BK; kk = l % BK; } else { m = l % BM; kk = l / BM; }
-        const int gm = m0 + m, gk = k0 + kk;
-        float v = 0.f;
-        if (gm < mlim && gk < kend)
-          v = to_f(AK ? A[(size_t)gm * g.lda + gk] : A[(size_t)gk * g.lda + gm]);
-        ra[q] = v;
-        int n, kb;
-        if (BKC) { n = l / BK; kb = l % BK; } else { n = l % BN; kb = l / BN; }
-        const int gn = n0 + n, gk2 = k0 + kb;
-        float w = 0.f;
-        if (gn < g.N && gk2 < kend)
-          w = to_f(BKC ? B[(size_t)gn * g.ldb + gk2] : B[(size_t)gk2 * g.ldb + gn]);
-        rb[q] = w;
+      for (int h = 0; h < 2; ++h) {
+        const int q = tid + h * NT;
+        if (AK) ra[h] = load4(A, g.lda, m0 + (q >> 2), mlim, k0 + (q & 3) * 4, kend, vec_a);
+        else ra[h] = load4(A, g.lda, k0 + (q >> 5), kend, m0 + (q & 31) * 4, mlim, vec_a);
+        if (BKC) rb[h] = load4(B, g.ldb, n0 + (q >> 2), g.N, k0 + (q & 3) * 4, kend, vec_b);
+        else rb[h] = load4(B, g.ldb, k0 + (q >> 5), kend, n0 + (q & 31) * 4, g.N, vec_b);
       }
     };
     auto store_tiles = [&](int buf) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int l = tid + q * NT;
-        int m, kk;
-        if (AK) { m = l / BK; kk = l % BK; } else { m = l % BM; kk = l / BM; }
-        As[buf][kk][m] = ra[q];
-        int n, kb;
-        if (BKC) { n = l / BK; kb = l % BK; } else { n = l % BN; kb = l / BN; }
-        Bs[buf][kb][n] = rb[q];
+      for (int h = 0; h < 2; ++h) {
+        const int q = tid + h * NT;
+        if (AK) {
+          const int m = q >> 2, kq = (q & 3) * 4;
+          As[buf][kq][m] = ra[h].x;
+          As[buf][kq + 1][m] = ra[h].y;
+          As[buf][kq + 2][m] = ra[h].z;
+          As[buf][kq + 3][m] = ra[h].w;
+        } else {
+          *reinterpret_cast<float4*>(&As[buf][q >> 5][(q & 31) * 4]) = ra[h];
+        }
+        if (BKC) {
+          const int n = q >> 2, kq = (q & 3) * 4;
+          Bs[buf][kq][n] = rb[h].x;
+          Bs[buf][kq + 1][n] = rb[h].y;
+          Bs[buf][kq + 2][n] = rb[h].z;
+          Bs[buf][kq + 3][n] = rb[h].w;
+        } else {
+          *reinterpret_cast<float4*>(&Bs[buf][q >> 5][(q & 31) * 4]) = rb[h];
+        }
       }
     };
 
