@@ -117,3 +117,27 @@ def test_side_draws_do_not_move_the_main_draws():
     cb = extra["corr_bias"]
     assert cb.shape == (base.E,) and float(cb.abs().max()) <= 0.1
     assert extra["ws1"].shape == (base.F, base.D) and extra["ws2"].shape == (base.D, base.F)
+
+
+def test_skewed_layer_realised_load():
+    """The skewed layer's configuration asks for the top 3 experts to take ~40%
+    of the tokens and 4 experts to receive none.  A share of the T k routed
+    assignments cannot exceed 3/8 for three experts (a token holds at most one
+    of its k slots per expert), so the realised share is asserted against that
+    ceiling: the oracle's routing of 2048 of the layer's tokens puts 0.32 to
+    0.375 of the assignments on the three busiest experts (0.340 with these
+    draws; the bench line reports 0.338 for the timed step's 32768 tokens)
+    and none on the four excluded ones."""
+    from oracle import moe_oracle as O
+    wl = W.WORKLOADS["skewed"].with_tokens(2048)
+    inp = W.make_inputs(wl, seed=0, with_target=False)
+    cfg = O.OracleConfig(T=wl.T, D=wl.D, F=wl.F, E=wl.E, k=wl.k, act=wl.act, score=wl.score,
+                         has_bias=False, aux_alpha=wl.aux_alpha)
+    x = inp["x"].to(torch.bfloat16).double().numpy()
+    wg = inp["w_gate"].to(torch.bfloat16).double().numpy()
+    lb = inp["logit_bias"].double().numpy()
+    idx = O.route(cfg, O.router_scores(cfg, O.router_logits(x, wg, lb)))
+    counts = np.bincount(idx.ravel(), minlength=wl.E)
+    share = np.sort(counts)[::-1][:3].sum() / float(wl.T * wl.k)
+    assert 0.32 <= share <= 3 / 8
+    assert (counts == 0).sum() == wl.zipf_empty == 4
