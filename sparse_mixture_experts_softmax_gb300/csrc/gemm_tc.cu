@@ -259,6 +259,24 @@ __device__ __forceinline__ void unpack4_bf16(uint2 q, float* v) {
   v[3] = __high2float(h[1]);
 }
 
+// Activations of the epilogues.  Every value they produce is stored in bf16
+// (8 significant bits), so the sigmoid uses the hardware's approximate
+// exponential and division (__expf, __fdividef: relative errors of a few fp32
+// ulps, far below the bf16 rounding that follows) and is evaluated once per
+// element; tanh is 2 sigmoid(2u) - 1.  The CUDA-core GEMMs of fp32 layers keep
+// the IEEE-accurate functions of common.cuh.
+__device__ __forceinline__ float sigmoid_epi(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float gelu_epi(float h) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float t = 2.0f * sigmoid_epi(2.0f * c * (h + a * h * h * h)) - 1.0f;
+  return 0.5f * h * (1.0f + t);
+}
+__device__ __forceinline__ float gelu_grad_epi(float h) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float t = 2.0f * sigmoid_epi(2.0f * c * (h + a * h * h * h)) - 1.0f;
+  return 0.5f * (1.0f + t) + 0.5f * h * (1.0f - t * t) * c * (1.0f + 3.0f * a * h * h);
+}
+
 // Side inputs of one epilogue chunk in the coalesced layout (four rows per
 // lane): H or H1 / H3 for the backward epilogues, fp32 master weights for the
 // fused SGD.  Members an epilogue does not use are never touched.
@@ -675,7 +693,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           } else if (EPI == EPI_ACT_FWD) {
             float a[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = p.act == 0 ? fmaxf(x[i], 0.f) : gelu_tanh_f(x[i]);
+            for (int i = 0; i < 4; ++i) a[i] = p.act == 0 ? fmaxf(x[i], 0.f) : gelu_epi(x[i]);
             st_ef(static_cast<bf16*>(p.out1) + o, pack4_bf16(x), pol);
             st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(a), pol);
           } else if (EPI == EPI_ACT_BWD) {
@@ -683,7 +701,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             unpack4_bf16(use.h1[j], h);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_tanh_grad_f(h[i]);
+              dh[i] = p.act == 0 ? (h[i] > 0.f ? x[i] : 0.f) : x[i] * gelu_grad_epi(h[i]);
             st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(dh), pol);
           } else if (EPI == EPI_SWIGLU_BWD) {
             float h1[4], h3[4], d1[4], d3[4];
@@ -691,8 +709,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             unpack4_bf16(use.h3[j], h3);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              d1[i] = x[i] * h3[i] * silu_grad_f(h1[i]);
-              d3[i] = x[i] * silu_f(h1[i]);
+              // SiLU(h) = h s, SiLU'(h) = s (1 + h (1 - s)), s = sigmoid(h)
+              const float sg = sigmoid_epi(h1[i]);
+              d1[i] = x[i] * h3[i] * (sg * (1.0f + h1[i] * (1.0f - sg)));
+              d3[i] = x[i] * (h1[i] * sg);
             }
             st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(d1), pol);
             st_ef(static_cast<bf16*>(p.out1) + o, pack4_bf16(d3), pol);
@@ -700,7 +720,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             const float h3[4] = {acc3[j].x, acc3[j].y, acc3[j].z, acc3[j].w};
             float a[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = silu_f(x[i]) * h3[i];
+            for (int i = 0; i < 4; ++i) a[i] = (x[i] * sigmoid_epi(x[i])) * h3[i];
             st_ef(static_cast<bf16*>(p.out1) + o, pack4_bf16(x), pol);
             st_ef(static_cast<bf16*>(p.out2) + o, pack4_bf16(h3), pol);
             st_ef(static_cast<bf16*>(p.C) + o, pack4_bf16(a), pol);
