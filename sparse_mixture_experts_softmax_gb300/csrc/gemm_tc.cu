@@ -50,14 +50,24 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BYTES = BN * BK * 2;    // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_EPI_WARPS = 8;
+// Epilogue warps: EPI_PARTS per TMEM lane quarter, each draining an equal
+// share of the tile's columns.
+#ifndef MOE_EPI_PARTS
+#define MOE_EPI_PARTS 2
+#endif
+constexpr int EPI_PARTS = MOE_EPI_PARTS;
+constexpr int NUM_EPI_WARPS = 4 * EPI_PARTS;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 256;
 constexpr int CHUNK = 16;                // accumulator columns per epilogue step
 constexpr int STG_BYTES = 32 * CHUNK * 4; // epilogue staging buffer of one warp
-constexpr size_t SMEM_BYTES =
-    (size_t)STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES + 1024;   // + alignment slack
+// Dynamic shared memory: the stage ring and the epilogue staging buffers.  The
+// ring needs 1024-byte alignment (128-byte swizzle): the declaration asks for
+// it, and the static shared memory (barriers, segment tables) is padded in
+// front of it to 3 KB.  Both must fit the 227 KB a block may opt into.
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES;
+static_assert(SMEM_BYTES + 3072 <= 232448, "shared memory of one block");
 constexpr long long WAIT_LIMIT_NS = 2000000000ll;   // default bound of every wait
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
@@ -589,9 +599,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     // ------------------------------------------------------------ epilogue
     float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + (warp - 2) * STG_BYTES);
     // TMEM lane quarter of this warp (a warp may only read lanes
-    // 32 (warp % 4) .. +31) and which half of the tile's columns it takes
+    // 32 (warp % 4) .. +31) and which share of the tile's columns it takes
     const int lane_base = (warp & 3) * 32;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const int row = lane_base + lane;
     const uint64_t pol = policy_evict_first();
     int buf = 0;
@@ -605,7 +615,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         // step leaves W as it is; its bf16 copy is still rewritten from W)
         if (FORM == FORM_TN && rok) {
           const size_t o = (size_t)T.e * p.sCe + (size_t)r * p.ldc;
-          const int nb = T.n0 + half * (BN / 2), ne = min(nb + BN / 2, p.N);
+          const int nb = T.n0 + part * (BN / EPI_PARTS), ne = min(nb + BN / EPI_PARTS, p.N);
           if (p.C != nullptr) {
             float* c = static_cast<float*>(p.C) + o;
             for (int n = nb; n < ne; n += 4)
@@ -630,7 +640,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       const int cq = lane & 3;
       const int row0 = T.m0 + lane_base + (lane >> 2);
       const int ncols = EPI == EPI_SWIGLU_UP ? 128 : BN;
-      const int c_begin = half * (ncols / 2), c_end = c_begin + ncols / 2;
+      const int c_begin = part * (ncols / EPI_PARTS), c_end = c_begin + ncols / EPI_PARTS;
       const size_t wbase = (size_t)T.e * p.sCe;
       // side inputs are fetched PF chunks ahead into a ring of PF + 1
       // register buffers (the first PF while the accumulator is still being
@@ -729,7 +739,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       };
       // chunks per warp: 8 (SwiGLU-up tiles: 4), a multiple of NB; chunk i
       // reads buffer i % NB and fills buffer (i + PF) % NB with chunk i + PF
-      static_assert(((EPI == EPI_SWIGLU_UP ? 64 : BN / 2) / CHUNK) % NB == 0, "whole rings");
+      static_assert(((EPI == EPI_SWIGLU_UP ? 128 : BN) / EPI_PARTS / CHUNK) % NB == 0, "whole rings");
 #pragma unroll 1
       for (int cc = c_begin; cc < c_end; cc += NB * CHUNK) {
 #pragma unroll
