@@ -70,6 +70,21 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// allowed to start before its predecessor in the stream has finished (so its
+// launch and its on-chip set-up overlap the predecessor's tail); it waits for
+// the predecessor's completion and memory before its first global access.
+// The short kernels then let their successor be launched at once; the GEMMs
+// do not (pdl_wait): a successor launched at their start would hold SM
+// resources for the whole GEMM while it waits, and the GEMM steps measured
+// slower that way.  Their blocks count as triggered when they exit.  A kernel
+// launched without the attribute passes these instructions at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+  pdl_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Routing indices before use.  A release build trusts the dispatch that
 // wrote them: a slot s >= 0 is used, -1 (an assignment dropped by the expert
 // capacity) is skipped; an expert id outside [0, E) is skipped.  A MOE_DEBUG

@@ -14,6 +14,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 route_count_kernel(const int* __restrict__ idx, long long R, int chunk, int E,
                    int* __restrict__ chunk_counts, int* dbg) {
+  pdl_begin();
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -40,6 +41,7 @@ constexpr int SCAN_THREADS = 1024;
 __global__ void __launch_bounds__(SCAN_THREADS)
 route_scan_kernel(int* __restrict__ cc, int nchunks, int E, int cap, int* __restrict__ counts,
                   int* __restrict__ offsets) {
+  pdl_begin();
   __shared__ int part[SCAN_THREADS];   // (group, expert): the range's sum, then its base
   __shared__ int tot[256];
   __shared__ int scan[257];
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(32)
 route_scatter_kernel(const int* __restrict__ idx, long long R, int chunk, int k, int E, int cap,
                      const int* __restrict__ chunk_base, const int* __restrict__ offsets,
                      int* __restrict__ src_tok, int* __restrict__ slot_of, int* dbg) {
+  pdl_begin();
   __shared__ int cursor[256];
   __shared__ int off[256];
   const int lane = threadIdx.x;
@@ -138,6 +141,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 gather_kernel(const T* __restrict__ x, const int* __restrict__ slot_of, int Tn, int k, int D,
               T* __restrict__ xe, int* dbg) {
+  pdl_begin();
   constexpr int VN = 16 / sizeof(T);
   const long long R = (long long)Tn * k;
   const int lane = threadIdx.x & 31;
@@ -177,6 +181,7 @@ combine_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
                float* __restrict__ y,
                const float* __restrict__ target, float* __restrict__ dy, float inv_n,
                double* __restrict__ sq_partial, int* dbg) {
+  pdl_begin();
   constexpr int VN = Vec<T>::N;
   const long long R = (long long)Tn * k;
   __shared__ float wpart[8];
@@ -258,6 +263,7 @@ combine_train_kernel(const T* __restrict__ ye, const float* __restrict__ gate,
                      const T* __restrict__ ys, const float* __restrict__ target, float inv_n,
                      double* __restrict__ sq_partial, T* __restrict__ dye,
                      float* __restrict__ dgate, bf16* __restrict__ dy_lp, int* dbg) {
+  pdl_begin();
   constexpr int VN = Vec<T>::N;
   constexpr int MAXK = 8;
   const long long R = (long long)Tn * k;
@@ -358,6 +364,7 @@ finalize_losses_kernel(const double* __restrict__ sq_partial, int n_sq,
                        const float* __restrict__ psum, int n_ps, const int* __restrict__ counts,
                        int T, int D, int E, int k, float alpha, float* __restrict__ d_loss,
                        float* __restrict__ aux_row) {
+  pdl_begin();
   __shared__ double sq_warp[FL_THREADS / 32];
   __shared__ float col[FL_THREADS];
   __shared__ float term_warp[FL_THREADS / 32];
@@ -422,6 +429,7 @@ __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const float* __restrict__ dy, const T* __restrict__ ye,
                    const float* __restrict__ gate, const int* __restrict__ slot_of, int Tn, int D,
                    int k, T* __restrict__ dye, float* __restrict__ dgate, int* dbg) {
+  pdl_begin();
   constexpr int VN = Vec<T>::N;
   const long long R = (long long)Tn * k;
   const int lane = threadIdx.x & 31;
@@ -475,6 +483,7 @@ __global__ void __launch_bounds__(256)
 scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
                         const int* __restrict__ slot_of, int Tn, int D, int k,
                         const T* __restrict__ extra, int* dbg) {
+  pdl_begin();
   constexpr int VN = Vec<T>::N;
   const long long R = (long long)Tn * k;
   const int lane = threadIdx.x & 31;
@@ -513,6 +522,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 segment_colsum_kernel(const T* __restrict__ src, const int* __restrict__ offsets, int N,
                       float* __restrict__ out) {
+  pdl_begin();
   __shared__ float part[8][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int e = blockIdx.y;
@@ -533,6 +543,7 @@ segment_colsum_kernel(const T* __restrict__ src, const int* __restrict__ offsets
 
 __global__ void __launch_bounds__(256)
 sum_partials_kernel(const float* __restrict__ p, int nparts, long long n, float* __restrict__ out) {
+  pdl_begin();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     float s = 0.f;
@@ -552,6 +563,7 @@ struct SgdList {
   int count;
 };
 __global__ void __launch_bounds__(256) sgd_kernel(const SgdList L, float lr) {
+  pdl_begin();
   const long long total = L.end4[L.count - 1];
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -598,13 +610,13 @@ cudaError_t launch_route_count(const int* idx, long long R, int E, int* chunk_co
                                cudaStream_t st, int* dbg) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
-  route_count_kernel<<<nc, 256, 0, st>>>(idx, R, route_chunk(R), E, chunk_counts, dbg);
+  MOE_LAUNCH(launch_pdl(route_count_kernel, dim3(nc), dim3(256), 0, st, idx, R, route_chunk(R), E, chunk_counts, dbg));
   return cudaGetLastError();
 }
 
 cudaError_t launch_route_scan(int* chunk_counts, int nchunks, int E, int cap, int* counts,
                               int* offsets, cudaStream_t st) {
-  route_scan_kernel<<<1, SCAN_THREADS, 0, st>>>(chunk_counts, nchunks, E, cap, counts, offsets);
+  MOE_LAUNCH(launch_pdl(route_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, st, chunk_counts, nchunks, E, cap, counts, offsets));
   return cudaGetLastError();
 }
 
@@ -613,8 +625,8 @@ cudaError_t launch_route_scatter(const int* idx, long long R, int k, int E, int 
                                  int* slot_of, cudaStream_t st, int* dbg) {
   int nc = route_chunks(R);
   if (nc == 0) return cudaSuccess;
-  route_scatter_kernel<<<nc, 32, 0, st>>>(idx, R, route_chunk(R), k, E, cap, chunk_base, offsets,
-                                          src_tok, slot_of, dbg);
+  MOE_LAUNCH(launch_pdl(route_scatter_kernel, dim3(nc), dim3(32), 0, st, idx, R, route_chunk(R), k, E, cap, chunk_base, offsets,
+                                          src_tok, slot_of, dbg));
   return cudaGetLastError();
 }
 
@@ -623,11 +635,11 @@ cudaError_t launch_gather(int dtype, const void* x, const int* slot_of, int T, i
   if (T == 0) return cudaSuccess;
   int grid = grid_for(T, 8, 152 * 16);
   if (dtype == 1)
-    gather_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(x), slot_of, T, k, D,
-                                              static_cast<bf16*>(xe), dbg);
+    MOE_LAUNCH(launch_pdl(gather_kernel<bf16>, dim3(grid), dim3(256), 0, st, static_cast<const bf16*>(x), slot_of, T, k, D,
+                                              static_cast<bf16*>(xe), dbg));
   else
-    gather_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), slot_of, T, k, D,
-                                               static_cast<float*>(xe), dbg);
+    MOE_LAUNCH(launch_pdl(gather_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(x), slot_of, T, k, D,
+                                               static_cast<float*>(xe), dbg));
   return cudaGetLastError();
 }
 
@@ -640,13 +652,13 @@ cudaError_t launch_combine(int dtype, const void* ye, const float* gate, const i
   if (inv_n == 0.f) inv_n = 1.0f / ((float)T * (float)D);
   int grid = combine_blocks(T);
   if (dtype == 1)
-    combine_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(ye), gate, slot_of, T, D, k,
+    MOE_LAUNCH(launch_pdl(combine_kernel<bf16>, dim3(grid), dim3(256), 0, st, static_cast<const bf16*>(ye), gate, slot_of, T, D, k,
                                                static_cast<const bf16*>(ys), y, target, dy, inv_n,
-                                               sq_partial, dbg);
+                                               sq_partial, dbg));
   else
-    combine_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(ye), gate, slot_of, T, D,
+    MOE_LAUNCH(launch_pdl(combine_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(ye), gate, slot_of, T, D,
                                                 k, static_cast<const float*>(ys), y, target, dy,
-                                                inv_n, sq_partial, dbg);
+                                                inv_n, sq_partial, dbg));
   return cudaGetLastError();
 }
 
@@ -661,25 +673,25 @@ cudaError_t launch_combine_train(int dtype, const void* ye, const float* gate, c
   if (inv_n == 0.f) inv_n = 1.0f / ((float)T * (float)D);
   const int grid = combine_blocks(T);
   if (dtype == 1 && shared)
-    combine_train_kernel<bf16, true><<<grid, 32 * CT_WARPS, 0, st>>>(
+    MOE_LAUNCH(launch_pdl(combine_train_kernel<bf16, true>, dim3(grid), dim3(32 * CT_WARPS), 0, st,
         static_cast<const bf16*>(ye), gate, slot_of, T, D, k, static_cast<const bf16*>(ys), target,
-        inv_n, sq_partial, static_cast<bf16*>(dye), dgate, static_cast<bf16*>(dy_lp), dbg);
+        inv_n, sq_partial, static_cast<bf16*>(dye), dgate, static_cast<bf16*>(dy_lp), dbg));
   else if (dtype == 1)
-    combine_train_kernel<bf16, false><<<grid, 32 * CT_WARPS, 0, st>>>(
+    MOE_LAUNCH(launch_pdl(combine_train_kernel<bf16, false>, dim3(grid), dim3(32 * CT_WARPS), 0, st,
         static_cast<const bf16*>(ye), gate, slot_of, T, D, k, nullptr, target, inv_n, sq_partial,
-        static_cast<bf16*>(dye), dgate, nullptr, dbg);
+        static_cast<bf16*>(dye), dgate, nullptr, dbg));
   else
-    combine_train_kernel<float, false><<<grid, 32 * CT_WARPS, 0, st>>>(
+    MOE_LAUNCH(launch_pdl(combine_train_kernel<float, false>, dim3(grid), dim3(32 * CT_WARPS), 0, st,
         static_cast<const float*>(ye), gate, slot_of, T, D, k, nullptr, target, inv_n,
-        sq_partial, static_cast<float*>(dye), dgate, nullptr, dbg);
+        sq_partial, static_cast<float*>(dye), dgate, nullptr, dbg));
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize_losses(const double* sq_partial, int n_sq, const float* psum_partial,
                                    int n_ps, const int* counts, int T, int D, int E, int k,
                                    float alpha, float* d_loss, float* aux_row, cudaStream_t st) {
-  finalize_losses_kernel<<<1, FL_THREADS, 0, st>>>(sq_partial, n_sq, psum_partial, n_ps, counts, T,
-                                                   D, E, k, alpha, d_loss, aux_row);
+  MOE_LAUNCH(launch_pdl(finalize_losses_kernel, dim3(1), dim3(FL_THREADS), 0, st, sq_partial, n_sq, psum_partial, n_ps, counts, T,
+                                                   D, E, k, alpha, d_loss, aux_row));
   return cudaGetLastError();
 }
 
@@ -690,22 +702,22 @@ cudaError_t launch_combine_bwd(int dtype, const float* dy, const void* ye, const
   int grid = (T + 7) / 8;
   if (dtype == 1) {
     if (k <= 8)
-      combine_bwd_kernel<bf16, 8><<<grid, 256, 0, st>>>(dy, static_cast<const bf16*>(ye), gate,
+      MOE_LAUNCH(launch_pdl(combine_bwd_kernel<bf16, 8>, dim3(grid), dim3(256), 0, st, dy, static_cast<const bf16*>(ye), gate,
                                                         slot_of, T, D, k, static_cast<bf16*>(dye),
-                                                        dgate, dbg);
+                                                        dgate, dbg));
     else
-      combine_bwd_kernel<bf16, 32><<<grid, 256, 0, st>>>(dy, static_cast<const bf16*>(ye), gate,
+      MOE_LAUNCH(launch_pdl(combine_bwd_kernel<bf16, 32>, dim3(grid), dim3(256), 0, st, dy, static_cast<const bf16*>(ye), gate,
                                                          slot_of, T, D, k, static_cast<bf16*>(dye),
-                                                         dgate, dbg);
+                                                         dgate, dbg));
   } else {
     if (k <= 8)
-      combine_bwd_kernel<float, 8><<<grid, 256, 0, st>>>(dy, static_cast<const float*>(ye), gate,
+      MOE_LAUNCH(launch_pdl(combine_bwd_kernel<float, 8>, dim3(grid), dim3(256), 0, st, dy, static_cast<const float*>(ye), gate,
                                                          slot_of, T, D, k,
-                                                         static_cast<float*>(dye), dgate, dbg);
+                                                         static_cast<float*>(dye), dgate, dbg));
     else
-      combine_bwd_kernel<float, 32><<<grid, 256, 0, st>>>(dy, static_cast<const float*>(ye), gate,
+      MOE_LAUNCH(launch_pdl(combine_bwd_kernel<float, 32>, dim3(grid), dim3(256), 0, st, dy, static_cast<const float*>(ye), gate,
                                                           slot_of, T, D, k,
-                                                          static_cast<float*>(dye), dgate, dbg);
+                                                          static_cast<float*>(dye), dgate, dbg));
   }
   return cudaGetLastError();
 }
@@ -716,13 +728,13 @@ cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const
   if (T == 0) return cudaSuccess;
   const int grid = (T + 7) / 8;
   if (dtype == 1)
-    scatter_back_add_kernel<bf16><<<grid, 256, 0, st>>>(dx, static_cast<const bf16*>(dxe), slot_of,
+    MOE_LAUNCH(launch_pdl(scatter_back_add_kernel<bf16>, dim3(grid), dim3(256), 0, st, dx, static_cast<const bf16*>(dxe), slot_of,
                                                          T, D, k, static_cast<const bf16*>(extra),
-                                                         dbg);
+                                                         dbg));
   else
-    scatter_back_add_kernel<float><<<grid, 256, 0, st>>>(dx, static_cast<const float*>(dxe),
+    MOE_LAUNCH(launch_pdl(scatter_back_add_kernel<float>, dim3(grid), dim3(256), 0, st, dx, static_cast<const float*>(dxe),
                                                           slot_of, T, D, k,
-                                                          static_cast<const float*>(extra), dbg);
+                                                          static_cast<const float*>(extra), dbg));
   return cudaGetLastError();
 }
 
@@ -730,16 +742,16 @@ cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets
                                   float* out, cudaStream_t st) {
   dim3 grid((N + 31) / 32, E);
   if (dtype == 1)
-    segment_colsum_kernel<bf16><<<grid, 256, 0, st>>>(static_cast<const bf16*>(src), offsets, N, out);
+    MOE_LAUNCH(launch_pdl(segment_colsum_kernel<bf16>, dim3(grid), dim3(256), 0, st, static_cast<const bf16*>(src), offsets, N, out));
   else
-    segment_colsum_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(src), offsets, N,
-                                                       out);
+    MOE_LAUNCH(launch_pdl(segment_colsum_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(src), offsets, N,
+                                                       out));
   return cudaGetLastError();
 }
 
 cudaError_t launch_sum_partials(const float* partials, int nparts, long long n, float* out,
                                 cudaStream_t st) {
-  sum_partials_kernel<<<grid_for(n, 256, 152 * 8), 256, 0, st>>>(partials, nparts, n, out);
+  MOE_LAUNCH(launch_pdl(sum_partials_kernel, dim3(grid_for(n, 256, 152 * 8)), dim3(256), 0, st, partials, nparts, n, out));
   return cudaGetLastError();
 }
 
@@ -759,7 +771,7 @@ cudaError_t launch_sgd(const SgdTensor* tensors, int count, float lr, cudaStream
   }
   if (n == 0) return cudaSuccess;
   L.count = n;
-  sgd_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, st>>>(L, lr);
+  MOE_LAUNCH(launch_pdl(sgd_kernel, dim3(grid_for(total, 256, 152 * 16)), dim3(256), 0, st, L, lr));
   return cudaGetLastError();
 }
 

@@ -62,18 +62,44 @@ constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 256;
 constexpr int CHUNK = 16;                // accumulator columns per epilogue step
 constexpr int STG_BYTES = 32 * CHUNK * 4; // epilogue staging buffer of one warp
-// Dynamic shared memory: the stage ring and the epilogue staging buffers.  The
-// ring needs 1024-byte alignment (128-byte swizzle): the declaration asks for
-// it, and the static shared memory (barriers, segment tables) is padded in
-// front of it to 3 KB.  Both must fit the 227 KB a block may opt into.
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES;
-static_assert(SMEM_BYTES + 3072 <= 232448, "shared memory of one block");
 constexpr long long WAIT_LIMIT_NS = 2000000000ll;   // default bound of every wait
 
 enum Form { FORM_NT = 0, FORM_NN = 1, FORM_TN = 2 };
 constexpr int EPI_STORE_F32_TAG = 100;   // TN: fp32 weight-gradient tile store
 constexpr int EPI_ROWS_F32_TAG = 101;    // fp32 row store (+ bias[n]): router logits, router dX
 constexpr int EPI_SGD_F32_TAG = 102;     // TN: fp32 weight-gradient store + fused SGD step
+
+// The activation backward's side inputs (H, or H1 and H3) can come by TMA
+// into a ring of SIDE_SLOTS buffers per epilogue warp, each one 16-column
+// chunk of the warp's 32 rows (2 KB: bf16 H1 then H3), so that the data in
+// flight costs no registers.  Such an instantiation (SIDE = true) runs the
+// operand ring with 3 stages to make room, which pays only at short reduction
+// lengths: the host picks it for K <= SIDE_TMA_MAX_K.  Other instantiations
+// keep 4 stages and fetch side inputs into registers (a ring of PF + 1
+// register buffers).
+constexpr int SIDE_SLOTS = 4;
+constexpr int SIDE_SLOT_BYTES = 2048;
+constexpr int SIDE_TMA_MAX_K = 2048;
+// The MMAs of a tile whose columns run past N use a smaller N (see the
+// MMA issuer); 0 keeps N = 256 on every tile.
+#ifndef MOE_TC_TRIM_N
+#define MOE_TC_TRIM_N 1
+#endif
+template <bool SIDE>
+__host__ __device__ constexpr int stages_of() { return SIDE ? 3 : STAGES; }
+
+// Dynamic shared memory: the stage ring, the epilogue staging buffers and the
+// side-input rings.  The stage ring needs 1024-byte alignment (128-byte
+// swizzle): the declaration asks for it, and the static shared memory
+// (barriers, segment tables) is padded in front of it to 3 KB.  All of it
+// must fit the 227 KB a block may opt into.
+template <bool SIDE>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return (size_t)stages_of<SIDE>() * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES +
+         (SIDE ? (size_t)NUM_EPI_WARPS * SIDE_SLOTS * SIDE_SLOT_BYTES : 0);
+}
+static_assert(smem_bytes<false>() + 3072 <= 232448, "shared memory of one block");
+static_assert(smem_bytes<true>() + 3072 <= 232448, "shared memory of one block");
 
 struct TcParams {
   int M, N, E;          // ragged-M: M = total rows; TN: output rows per expert
@@ -419,15 +445,19 @@ __device__ __forceinline__ Tile map_tile(int t, const TcParams& p, const int* of
   return T;
 }
 
-template <int FORM, int EPI>
+template <int FORM, int EPI, bool SIDE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB0x, const __grid_constant__ CUtensorMap tmA1,
-               const __grid_constant__ CUtensorMap tmB1, const TcParams p) {
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
+               const __grid_constant__ CUtensorMap tmS1, const TcParams p) {
+  static_assert(!SIDE || EPI == EPI_ACT_BWD || EPI == EPI_SWIGLU_BWD, "side ring: activation backward");
+  constexpr int NST = stages_of<SIDE>();   // operand ring stages of this instantiation
   // stage ring in dynamic shared memory (1024-byte aligned for the 128-byte
   // swizzle); barriers, the TMEM address slot and the segment tables static
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_mb[STAGES], empty_mb[STAGES], tfull_mb[2], tempty_mb[2], drain_mb;
+  __shared__ __align__(8) uint64_t side_mb[NUM_EPI_WARPS * SIDE_SLOTS];   // side-input ring
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_word;
   __shared__ int offs[MAX_E + 1];
@@ -438,10 +468,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full_mb[s]), 1);
       mbar_init(smem_u32(&empty_mb[s]), 1);
     }
+    if (SIDE)
+      for (int s = 0; s < NUM_EPI_WARPS * SIDE_SLOTS; ++s) mbar_init(smem_u32(&side_mb[s]), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_mb[b]), 1);
       mbar_init(smem_u32(&tempty_mb[b]), NUM_EPI_WARPS);
@@ -451,6 +483,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
+  pdl_wait();   // the previous kernel's outputs (segment offsets, operands) are visible from here
   for (int i = tid; i <= p.E; i += NUM_THREADS)
     offs[i] = p.offsets ? p.offsets[i] : min(i * p.seg_len, p.seg_rows);
   tc_fence_before();
@@ -497,8 +530,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             const int k0 = kb * BK;
             tma_load_2d(a_dst, &tmA0, fb, k0, T.m0);
             if (EPI == EPI_SWIGLU_UP) {
-              tma_load_3d(b_dst, &tmB0, fb, k0, T.n0, T.e);
-              tma_load_3d(b_dst + BM * BK * 2, &tmB0x, fb, k0, T.n0, T.e);
+              // 64-row boxes of W1 and W3 for the same output columns side
+              // by side: accumulator columns 128 h + [0, 64) hold W1 x and
+              // 128 h + [64, 128) W3 x of output columns 64 h + [0, 64)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                tma_load_3d(b_dst + (2 * h) * (64 * BK * 2), &tmB0, fb, k0, T.n0 + 64 * h, T.e);
+                tma_load_3d(b_dst + (2 * h + 1) * (64 * BK * 2), &tmB0x, fb, k0, T.n0 + 64 * h, T.e);
+              }
             } else {
               tma_load_3d(b_dst, &tmB0, fb, k0, T.n0, T.e);
               tma_load_3d(b_dst + BM * BK * 2, &tmB0, fb, k0, T.n0 + 128, T.e);
@@ -520,11 +559,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           }
           issued |= 1 << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          if (++s == NST) { s = 0; ph ^= 1u; }
         }
       }
       // drain: every stage's last load must have landed before the CTA exits
-      for (int q = 0; q < STAGES; ++q)
+      for (int q = 0; q < NST; ++q)
           if (issued & (1 << q)) drain_wait(smem_u32(&full_mb[q]), (last_par >> q) & 1u, p.wait_ns);
     }
     __syncwarp();
@@ -545,6 +584,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      // A tile whose columns run past N multiplies only the B rows it needs:
+      // N of the MMA rounded up to 16 (a SwiGLU tile keeps its W1 / W3
+      // halves at columns 0 and 64 of each 128).  The accumulator columns
+      // past it keep stale values that the epilogue never stores.
+      uint32_t id_t = idesc;
+      if (MOE_TC_TRIM_N) {
+        const int v = min(EPI == EPI_SWIGLU_UP ? 128 : BN, p.N - T.n0);
+        const int nv = EPI != EPI_SWIGLU_UP ? (v + 15) & ~15
+                       : v <= 64 ? 64 + ((v + 15) & ~15) : 192 + ((v - 64 + 15) & ~15);
+        id_t = (idesc & ~(0x3Fu << 17)) | ((uint32_t)(nv >> 3) << 17);
+      }
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&full_mb[s]), ph, abort_flag, p.status, p.wait_ns))) {
           ok = false;
@@ -556,9 +606,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           const int valid = T.kend - (T.kbeg + kb * BK);
           if (valid < BK) {
             // rows past the expert's last row: zero them in both operands
-            // (the two A and the four B boxes, each BK rows of 128 bytes;
-            // whole rows are invariant under the 128-byte swizzle).  Zeroing
-            // A alone is not enough: rows past the last kept row of an
+            // (the two A and four B boxes, each BK rows of 128 bytes; whole
+            // rows are invariant under the 128-byte swizzle).  Zeroing A
+            // alone is not enough: rows past the last kept row of an
             // expert capacity are never written, and 0 * NaN is NaN.
             const int nchunk = (BK - valid) * 8;   // 16-byte chunks per box
             for (int j = 0; j < 6; ++j) {
@@ -577,13 +627,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             else adesc = smem_desc(a_base + kk * 32, 16, 1024);
             if (FORM == FORM_NT) bdesc = smem_desc(b_base + kk * 32, 16, 1024);
             else bdesc = smem_desc(b_base + kk * 2048, 64 * BK * 2, 1024);
-            mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(d_tmem, adesc, bdesc, id_t, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&empty_mb[s]));
         }
         any_mma = true;
         __syncwarp();
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
+        if (++s == NST) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
       if (lane == 0) mma_commit(smem_u32(&tfull_mb[buf]));
@@ -597,7 +647,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + (warp - 2) * STG_BYTES);
+    float* stg = reinterpret_cast<float*>(smem + NST * STAGE_BYTES + (warp - 2) * STG_BYTES);
     // TMEM lane quarter of this warp (a warp may only read lanes
     // 32 (warp % 4) .. +31) and which share of the tile's columns it takes
     const int lane_base = (warp & 3) * 32;
@@ -606,6 +656,55 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const uint64_t pol = policy_evict_first();
     int buf = 0;
     uint32_t aph = 0;
+    // Side-input ring (SIDE): this warp's chunks form one sequence
+    // over its tiles (NCH chunks of 16 columns per tile); chunk g goes to slot
+    // g % SIDE_SLOTS, loaded by TMA SIDE_SLOTS chunks ahead of its use, the
+    // next tile's first chunks while this tile's last ones are processed.
+    constexpr int NCH = (BN / EPI_PARTS) / CHUNK;
+    const size_t side_off = (size_t)NST * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES +
+                            (size_t)(warp - 2) * SIDE_SLOTS * SIDE_SLOT_BYTES;
+    const uint32_t side_bar0 = smem_u32(&side_mb[(warp - 2) * SIDE_SLOTS]);
+    int side_t = blockIdx.x, side_i = 0;   // issue cursor: tile, chunk within it
+    long long side_iss = 0, side_con = 0;  // chunks issued / consumed
+    auto side_skip_empty = [&]() {
+      while (side_t < total && map_tile<FORM>(side_t, p, offs, tpre).nkb == 0) side_t += gridDim.x;
+    };
+    auto side_issue = [&](int slot) {
+      const Tile Ti = map_tile<FORM>(side_t, p, offs, tpre);
+      const int n = Ti.n0 + part * (BN / EPI_PARTS) + side_i * CHUNK;   // a multiple of 16
+      if (lane == 0) {
+        const uint32_t bar = side_bar0 + 8u * (uint32_t)slot;
+        const uint32_t dst = smem_u32(smem + side_off + (size_t)slot * SIDE_SLOT_BYTES);
+        // the lanes' reads of this slot's previous contents come first
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(bar, EPI == EPI_SWIGLU_BWD ? 2048u : 1024u);
+        tma_load_2d(dst, &tmS0, bar, n, Ti.m0 + lane_base);
+        if (EPI == EPI_SWIGLU_BWD) tma_load_2d(dst + 1024, &tmS1, bar, n, Ti.m0 + lane_base);
+      }
+      ++side_iss;
+      if (++side_i == NCH) {
+        side_i = 0;
+        side_t += gridDim.x;
+        side_skip_empty();
+      }
+    };
+    // the slot's rows in the coalesced layout: lane l takes columns
+    // 4 (l % 4) .. +3 of rows l / 4 + 8 j (box rows of 16 bf16 values)
+    auto side_read = [&](int slot, Side& d) {
+      const uint8_t* sp = smem + side_off + (size_t)slot * SIDE_SLOT_BYTES;
+      const int rr = lane >> 2, cq4 = lane & 3;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        d.h1[j] = *reinterpret_cast<const uint2*>(sp + (rr + 8 * j) * 32 + cq4 * 8);
+        if (EPI == EPI_SWIGLU_BWD)
+          d.h3[j] = *reinterpret_cast<const uint2*>(sp + 1024 + (rr + 8 * j) * 32 + cq4 * 8);
+      }
+    };
+    bool side_fail = false;
+    if (SIDE) {
+      side_skip_empty();
+      for (int q = 0; q < SIDE_SLOTS && side_t < total; ++q) side_issue(q);
+    }
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
       const int r = T.m0 + row;
@@ -655,19 +754,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         if (EPI == EPI_SGD_F32_TAG) load_f32x4_rows(p.sgd_w + wbase, p.ldc, row0, T.row_hi, n, p.N, d.w);
       };
       Side sd[NB];
+      if (!SIDE) {
 #pragma unroll
-      for (int q = 0; q < PF; ++q)
-        if (c_begin + q * CHUNK < c_end) load_side(T.n0 + c_begin + q * CHUNK + 4 * cq, sd[q]);
+        for (int q = 0; q < PF; ++q)
+          if (c_begin + q * CHUNK < c_end) load_side(T.n0 + c_begin + q * CHUNK + 4 * cq, sd[q]);
+      }
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tfull_mb[buf]), aph, abort_flag, p.status, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(buf * BN);
       auto chunk = [&](int cc, const Side& use, Side& fill) {
         const int n = T.n0 + cc + 4 * cq;
-        if (cc + PF * CHUNK < c_end) load_side(n + PF * CHUNK, fill);
+        if (!SIDE && cc + PF * CHUNK < c_end) load_side(n + PF * CHUNK, fill);
         float4 acc[4], acc3[4];
-        stage_chunk(stg, lane, t_row + cc, acc);
-        if (EPI == EPI_SWIGLU_UP) stage_chunk(stg, lane, t_row + 128 + cc, acc3);
+        if (EPI == EPI_SWIGLU_UP) {
+          // output columns 64 h + c: W1 x at accumulator column 128 h + c,
+          // W3 x at 128 h + 64 + c
+          const int c1 = cc + (cc & ~63);
+          stage_chunk(stg, lane, t_row + c1, acc);
+          stage_chunk(stg, lane, t_row + c1 + 64, acc3);
+        } else {
+          stage_chunk(stg, lane, t_row + cc, acc);
+        }
         constexpr bool BIAS_EPI = EPI == EPI_STORE || EPI == EPI_ROWS_F32_TAG || EPI == EPI_ACT_FWD;
         const bool add_bias = BIAS_EPI && p.bias != nullptr && n < p.N;
         float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -740,16 +848,42 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       // chunks per warp: 8 (SwiGLU-up tiles: 4), a multiple of NB; chunk i
       // reads buffer i % NB and fills buffer (i + PF) % NB with chunk i + PF
       static_assert(((EPI == EPI_SWIGLU_UP ? 128 : BN) / EPI_PARTS / CHUNK) % NB == 0, "whole rings");
+      if (SIDE) {
+        // side inputs from the TMA ring; each consumed slot is refilled with
+        // the chunk SIDE_SLOTS further on
 #pragma unroll 1
-      for (int cc = c_begin; cc < c_end; cc += NB * CHUNK) {
+        for (int i = 0; i < NCH; ++i) {
+          const int slot = (int)(side_con % SIDE_SLOTS);
+          const uint32_t par = (uint32_t)((side_con / SIDE_SLOTS) & 1);
+          if (!__all_sync(0xffffffffu, wait_bar(side_bar0 + 8u * (uint32_t)slot, par, abort_flag,
+                                                p.status, p.wait_ns))) {
+            side_fail = true;
+            break;
+          }
+          Side cur;
+          side_read(slot, cur);
+          chunk(c_begin + i * CHUNK, cur, cur);
+          __syncwarp();
+          ++side_con;
+          if (side_t < total) side_issue(slot);
+        }
+        if (side_fail) break;
+      } else {
+#pragma unroll 1
+        for (int cc = c_begin; cc < c_end; cc += NB * CHUNK) {
 #pragma unroll
-        for (int q = 0; q < NB; ++q) chunk(cc + q * CHUNK, sd[q], sd[(q + PF) % NB]);
+          for (int q = 0; q < NB; ++q) chunk(cc + q * CHUNK, sd[q], sd[(q + PF) % NB]);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_mb[buf]));
       if (++buf == 2) { buf = 0; aph ^= 1u; }
     }
+    // side loads still in flight (an aborted CTA) land before the CTA exits
+    for (long long g = side_con; g < side_iss; ++g)
+      drain_wait(side_bar0 + 8u * (uint32_t)(g % SIDE_SLOTS), (uint32_t)((g / SIDE_SLOTS) & 1),
+                 p.wait_ns);
   }
 
   tc_fence_before();
@@ -796,6 +930,24 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor map without swizzle for the epilogues' side inputs: [rows, cols]
+// row-major, `ld` elements between rows, fp32 (elem 4) or bf16 (elem 2), box
+// of 16 columns x 32 rows (out-of-range parts read as zeros).
+bool make_side_map(CUtensorMap* m, const void* ptr, int elem, uint64_t cols, uint64_t rows,
+                   uint64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[2] = {cols, rows};
+  const cuuint64_t st[1] = {ld * (uint64_t)elem};
+  const cuuint32_t b[2] = {16, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, elem == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  2, const_cast<void*>(ptr), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // SMs of the current device (cached per device ordinal): the persistent grid.
 int sm_count() {
   static std::atomic<int> cached[64];
@@ -814,17 +966,18 @@ int sm_count() {
   return n;
 }
 
-template <int FORM, int EPI>
+template <int FORM, int EPI, bool SIDE = false>
 cudaError_t launch_inst(const CUtensorMap* maps, const TcParams& p, int tiles_upper,
                         cudaStream_t st) {
   static std::atomic<unsigned long long> attr_done{0};
-  cudaError_t e = ensure_dynamic_smem(tc_gemm_kernel<FORM, EPI>, (int)SMEM_BYTES, attr_done);
+  constexpr size_t SMEM = smem_bytes<SIDE>();
+  cudaError_t e = ensure_dynamic_smem(tc_gemm_kernel<FORM, EPI, SIDE>, (int)SMEM, attr_done);
   if (e != cudaSuccess) return e;
   int grid = sm_count();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) return cudaSuccess;
-  tc_gemm_kernel<FORM, EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(maps[0], maps[1], maps[2],
-                                                                   maps[3], maps[4], p);
+  MOE_LAUNCH(launch_pdl(tc_gemm_kernel<FORM, EPI, SIDE>, dim3(grid), dim3(NUM_THREADS), SMEM, st,
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p));
   return cudaGetLastError();
 }
 
@@ -844,7 +997,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
       (g.epi == EPI_SWIGLU_BWD && (g.aux0 == nullptr || g.aux1 == nullptr || g.out1 == nullptr)) ||
       (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)) || g.epi == EPI_SCATTER_ADD)
     return cudaErrorInvalidValue;
-  CUtensorMap maps[5];
+  CUtensorMap maps[7];   // operands (5), then the epilogue's side inputs (2)
   TcParams p{};
   p.M = g.M;
   p.N = g.N;
@@ -878,10 +1031,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     const uint32_t ab[2] = {BK, BM};
     const uint64_t bd[3] = {(uint64_t)g.K0, (uint64_t)g.N, (uint64_t)g.E};
     const uint64_t bs[2] = {(uint64_t)g.ldb * 2, (uint64_t)g.sBe * 2};
-    const uint32_t bb[3] = {BK, 128, 1};
+    const bool swiglu = g.epi == EPI_SWIGLU_UP;
+    const uint32_t bb[3] = {BK, swiglu ? 64u : 128u, 1};
     if (!make_map(&maps[0], g.A0, 2, ad, as, ab) || !make_map(&maps[1], g.B0, 3, bd, bs, bb))
       return cudaErrorInvalidValue;
-    const bool swiglu = g.epi == EPI_SWIGLU_UP;
     if (swiglu) {
       if (!make_map(&maps[2], g.B0x, 3, bd, bs, bb)) return cudaErrorInvalidValue;
     } else {
@@ -889,6 +1042,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     }
     maps[3] = maps[0];
     maps[4] = maps[1];
+    maps[5] = maps[6] = maps[0];
     p.ntile_n = swiglu ? 128 : BN;
     p.nN = (g.N + p.ntile_n - 1) / p.ntile_n;
     p.nM = 0;
@@ -924,10 +1078,25 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     }
     p.ntile_n = BN;
     p.nN = (g.N + BN - 1) / BN;
+    maps[5] = maps[6] = maps[0];
+    // the activation backward at a short reduction length: side inputs by TMA
+    const bool side = (g.epi == EPI_SWIGLU_BWD || g.epi == EPI_ACT_BWD) &&
+                      g.K0 + (p.K1 > 0 ? g.K1 : 0) <= SIDE_TMA_MAX_K;
     tiles_upper = (int)(((R + BM - 1) / BM + g.E) * p.nN);
+    if (side) {
+      // H (H1) and H3 [R, N] bf16, leading dimension ld_aux
+      if (!make_side_map(&maps[5], g.aux0, 2, (uint64_t)g.N, R, (uint64_t)g.ld_aux) ||
+          (g.epi == EPI_SWIGLU_BWD &&
+           !make_side_map(&maps[6], g.aux1, 2, (uint64_t)g.N, R, (uint64_t)g.ld_aux)))
+        return cudaErrorInvalidValue;
+    }
     switch (g.epi) {
-      case EPI_SWIGLU_BWD: return launch_inst<FORM_NN, EPI_SWIGLU_BWD>(maps, p, tiles_upper, st);
-      case EPI_ACT_BWD: return launch_inst<FORM_NN, EPI_ACT_BWD>(maps, p, tiles_upper, st);
+      case EPI_SWIGLU_BWD:
+        if (side) return launch_inst<FORM_NN, EPI_SWIGLU_BWD, true>(maps, p, tiles_upper, st);
+        return launch_inst<FORM_NN, EPI_SWIGLU_BWD>(maps, p, tiles_upper, st);
+      case EPI_ACT_BWD:
+        if (side) return launch_inst<FORM_NN, EPI_ACT_BWD, true>(maps, p, tiles_upper, st);
+        return launch_inst<FORM_NN, EPI_ACT_BWD>(maps, p, tiles_upper, st);
       case EPI_STORE:
         if (g.c_type == 0) return launch_inst<FORM_NN, EPI_ROWS_F32_TAG>(maps, p, tiles_upper, st);
         return launch_inst<FORM_NN, EPI_STORE>(maps, p, tiles_upper, st);
@@ -950,6 +1119,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
     return cudaErrorInvalidValue;
   maps[2] = maps[3] = maps[0];
   maps[4] = maps[1];
+  maps[5] = maps[6] = maps[0];
   p.ntile_n = BN;
   p.nM = (g.M + BM - 1) / BM;
   p.nN = (g.N + BN - 1) / BN;

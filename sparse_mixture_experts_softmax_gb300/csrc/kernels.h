@@ -3,6 +3,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <utility>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -26,6 +27,35 @@ inline cudaError_t ensure_dynamic_smem(Kernel* kernel, int bytes,
   if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
+
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+// Launches `kernel` on `st` with programmatic stream serialization allowed:
+// it may start while the previous kernel of the stream finishes, and waits
+// for it (pdl_begin in common.cuh) before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = MOE_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Returns the launch's error from the enclosing launcher, if any.
+#define MOE_LAUNCH(expr)                          \
+  do {                                            \
+    cudaError_t _le = (expr);                     \
+    if (_le != cudaSuccess) return _le;           \
+  } while (0)
 
 struct RouterArgs {
   int T, D, E, k;

@@ -74,6 +74,7 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
                   const float* __restrict__ logit_bias, RouterArgs a,
                   float* __restrict__ scores, int* __restrict__ idx, float* __restrict__ gate,
                   float* __restrict__ psum_partial) {
+  pdl_begin();
   constexpr int EP = 16 * NJ;
   constexpr int NC = (EP + 31) / 32;   // scores per lane
   // dynamic shared memory: the logits tile ls aliases the staging tiles xs/ws
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(256)
 router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __restrict__ scores,
                      int* __restrict__ idx, float* __restrict__ gate,
                      float* __restrict__ psum_partial) {
+  pdl_begin();
   constexpr int EP = 32 * NC;
   __shared__ float rows[8][EP];
   __shared__ float wsum[8][EP];
@@ -407,6 +409,7 @@ router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __re
 // Round-to-nearest-even bf16 copy of an fp32 tensor (the router weight).
 __global__ void __launch_bounds__(256)
 cast_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst, long long n) {
+  pdl_begin();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
     dst[i] = __float2bfloat16_rn(src[i]);
@@ -422,6 +425,7 @@ router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
                   const float* __restrict__ gate, const float* __restrict__ dgate,
                   const float* __restrict__ aux_row, RouterArgs a,
                   float* __restrict__ dlogits, bf16* __restrict__ dlogits_lp, int* dbg) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= a.T) return;
@@ -497,8 +501,8 @@ static cudaError_t launch_fwd_nj(const void* x, const float* wg, const float* lb
   static std::atomic<unsigned long long> attr_done{0};   // per instantiation and device
   cudaError_t e = ensure_dynamic_smem(router_fwd_kernel<XT, NJ>, (int)smem, attr_done);
   if (e != cudaSuccess) return e;
-  router_fwd_kernel<XT, NJ><<<grid, RT_THREADS, smem, st>>>(
-      static_cast<const XT*>(x), wg, lb, a, scores, idx, gate, psum);
+  MOE_LAUNCH(launch_pdl(router_fwd_kernel<XT, NJ>, dim3(grid), dim3(RT_THREADS), smem, st,
+      static_cast<const XT*>(x), wg, lb, a, scores, idx, gate, psum));
   return cudaGetLastError();
 }
 
@@ -528,10 +532,10 @@ cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* 
   if (a.T == 0) return cudaSuccess;
   dim3 grid((a.T + 7) / 8);
   bf16* lp = static_cast<bf16*>(dlogits_lp);
-  if (a.E <= 32) router_bwd_kernel<1><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
-  else if (a.E <= 64) router_bwd_kernel<2><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
-  else if (a.E <= 128) router_bwd_kernel<4><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
-  else router_bwd_kernel<8><<<grid, 256, 0, st>>>(scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg);
+  if (a.E <= 32) MOE_LAUNCH(launch_pdl(router_bwd_kernel<1>, dim3(grid), dim3(256), 0, st, scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg));
+  else if (a.E <= 64) MOE_LAUNCH(launch_pdl(router_bwd_kernel<2>, dim3(grid), dim3(256), 0, st, scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg));
+  else if (a.E <= 128) MOE_LAUNCH(launch_pdl(router_bwd_kernel<4>, dim3(grid), dim3(256), 0, st, scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg));
+  else MOE_LAUNCH(launch_pdl(router_bwd_kernel<8>, dim3(grid), dim3(256), 0, st, scores, idx, gate, dgate, aux_row, a, dlogits, lp, dbg));
   return cudaGetLastError();
 }
 
@@ -539,10 +543,10 @@ cudaError_t launch_router_select(const float* logits, const RouterArgs& a, float
                                  float* gate, float* psum_partial, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   dim3 grid(router_fwd_blocks(a.T));
-  if (a.E <= 32) router_select_kernel<1><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
-  else if (a.E <= 64) router_select_kernel<2><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
-  else if (a.E <= 128) router_select_kernel<4><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
-  else router_select_kernel<8><<<grid, 256, 0, st>>>(logits, a, scores, idx, gate, psum_partial);
+  if (a.E <= 32) MOE_LAUNCH(launch_pdl(router_select_kernel<1>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  else if (a.E <= 64) MOE_LAUNCH(launch_pdl(router_select_kernel<2>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  else if (a.E <= 128) MOE_LAUNCH(launch_pdl(router_select_kernel<4>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  else MOE_LAUNCH(launch_pdl(router_select_kernel<8>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
   return cudaGetLastError();
 }
 
@@ -550,7 +554,7 @@ cudaError_t launch_cast_bf16(const float* src, void* dst, long long n, cudaStrea
   if (n == 0) return cudaSuccess;
   long long blocks = (n + 255) / 256;
   if (blocks > 152 * 8) blocks = 152 * 8;
-  cast_bf16_kernel<<<(int)blocks, 256, 0, st>>>(src, static_cast<bf16*>(dst), n);
+  MOE_LAUNCH(launch_pdl(cast_bf16_kernel, dim3((int)blocks), dim3(256), 0, st, src, static_cast<bf16*>(dst), n));
   return cudaGetLastError();
 }
 

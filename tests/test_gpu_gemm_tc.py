@@ -29,6 +29,7 @@ CASES = [
     ([128, 256, 0, 0, 77], 256, 64),
     ([5], 512, 200),
     ([1000, 24, 0, 333], 1408, 2048),
+    ([5000, 0, 3100, 100, 2600], 704, 1000),
 ]
 
 
@@ -177,3 +178,4 @@ def test_caller_offsets_are_clamped(form, raw):
                 assert _rel(C[e], ref) <= 1e-4, e
         assert torch.all(buf[E * Mo * N:] == 7.0)
     assert st.item() == 0
+
