@@ -56,11 +56,21 @@ inline size_t esize(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // split-K factor of the router weight gradient dW_g = dlogits^T x
-inline int dwg_splits(int T) {
-  int s = T / 2048;
-  if (s < 1) s = 1;
-  if (s > 32) s = 32;
-  return s;
+// Token chunks of the router weight gradient dW_g = dlogits^T x: each chunk
+// is one ragged-K segment of the grouped GEMM and a fixed-order sum adds the
+// partial products.  Enough chunks that chunks x output tiles fill two waves
+// of 152 SMs (output tiles of 128 x 256 on the tensor-core path, 128 x 128 on
+// the CUDA-core one), at least one per 2048 tokens, each at least 64
+// tokens, at most 64 chunks.
+inline int dwg_splits(const moe_config& c) {
+  const bool tc = c.dtype == MOE_BF16;
+  const long long bn = tc ? 256 : 128;
+  const long long tiles = (((long long)c.E + 127) / 128) * (((long long)c.D + bn - 1) / bn);
+  long long s = (2 * 152 + tiles - 1) / tiles;
+  if (s < c.T / 2048) s = c.T / 2048;
+  if (s > c.T / 64) s = c.T / 64;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : (int)s;
 }
 
 struct Layout {
@@ -117,7 +127,7 @@ inline Layout make_layout(const moe_config& c, bool expert_buffers = true) {
   L.dh3 = expert_buffers && swiglu ? take(R * F * es) : 0;
   L.dxe = take(R * D * es);
   L.dlogits = take(T * E * 4);
-  L.dwg_part = take((size_t)dwg_splits(c.T) * E * D * 4);
+  L.dwg_part = take((size_t)dwg_splits(c) * E * D * 4);
   L.dx = take(T * D * 4);
   const bool lp = c.dtype == MOE_BF16;
   L.logits = lp ? take(T * E * 4) : 0;
@@ -237,7 +247,6 @@ inline GemmArgs gemm_base(const moe_config& c, const Ptrs& P) {
   g.a_type = g.b_type = g.c_type = c.dtype;
   g.offsets = P.at<int>(P.L->offsets);
   g.E = c.E;
-  g.src_type = c.dtype;
   g.act = c.act == MOE_ACT_GELU_TANH ? 1 : 0;
   return g;
 }
@@ -273,7 +282,6 @@ inline GemmArgs rows_gemm(const moe_config& c, const ExpertRows& r) {
   g.a_type = g.b_type = g.c_type = c.dtype;
   g.offsets = r.offsets;
   g.E = r.E;
-  g.src_type = c.dtype;
   g.act = c.act == MOE_ACT_GELU_TANH ? 1 : 0;
   return g;
 }

@@ -64,17 +64,8 @@ __device__ __forceinline__ int seg_hi(const GemmArgs& g, int e, int total) {
   return (int)(v < total ? v : total);
 }
 
-// Tuning knobs: fragments read one step ahead (MOE_SIMT_FRAG_DB) and the
-// blocks per SM the registers are sized for (MOE_SIMT_MIN_BLOCKS).
-#ifndef MOE_SIMT_FRAG_DB
-#define MOE_SIMT_FRAG_DB 0
-#endif
-#ifndef MOE_SIMT_MIN_BLOCKS
-#define MOE_SIMT_MIN_BLOCKS 2
-#endif
-
 template <typename TA, typename TB, int FORM, int EPI>
-__global__ void __launch_bounds__(NT, MOE_SIMT_MIN_BLOCKS) gemm_simt_kernel(const GemmArgs g) {
+__global__ void __launch_bounds__(NT, 2) gemm_simt_kernel(const GemmArgs g) {
   pdl_begin();
   constexpr bool AK = FORM != 2;   // A element (m, k) has k contiguous
   constexpr bool BKC = FORM == 0;  // B element (k, n) has k contiguous
@@ -183,9 +174,9 @@ __global__ void __launch_bounds__(NT, MOE_SIMT_MIN_BLOCKS) gemm_simt_kernel(cons
     for (int k0 = kbeg; k0 < kend; k0 += BK) {
       const bool more = k0 + BK < kend;
       if (more) load_tiles(k0 + BK);
-      // this thread's A / B fragments of step kk: rows ty*4 + {0..3, 64..67},
-      // columns tx*4 + {0..3, 64..67} of the 128 x 128 tile
-      auto frag = [&](int kk, float (&a)[8], float (&b)[8]) {
+#pragma unroll
+      for (int kk = 0; kk < BK; ++kk) {
+        float a[8], b[8];
         const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
         const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
         const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
@@ -194,30 +185,11 @@ __global__ void __launch_bounds__(NT, MOE_SIMT_MIN_BLOCKS) gemm_simt_kernel(cons
         a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
         b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
         b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
-      };
-#if MOE_SIMT_FRAG_DB
-      // fragments of step kk + 1 are read while step kk's products issue
-      float fa[2][8], fb[2][8];
-      frag(0, fa[0], fb[0]);
-#pragma unroll
-      for (int kk = 0; kk < BK; ++kk) {
-        if (kk + 1 < BK) frag(kk + 1, fa[(kk + 1) & 1], fb[(kk + 1) & 1]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(fa[kk & 1][i], fb[kk & 1][j], acc[i][j]);
-      }
-#else
-#pragma unroll
-      for (int kk = 0; kk < BK; ++kk) {
-        float a[8], b[8];
-        frag(kk, a, b);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
           for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
       }
-#endif
       if (more) {
         store_tiles(buf ^ 1);
         __syncthreads();
@@ -267,17 +239,6 @@ __global__ void __launch_bounds__(NT, MOE_SIMT_MIN_BLOCKS) gemm_simt_kernel(cons
           float h3 = ld_rt(g.aux1, ai, g.c_type);
           st_rt(g.C, ci, v * h3 * silu_grad_f(h1), g.c_type);
           st_rt(g.out1, ci, v * silu_f(h1), g.c_type);
-          break;
-        }
-        case EPI_SCATTER_ADD: {
-          float s = v;
-          for (int jj = 0; jj < g.k; ++jj) {
-            const int slot = g.slot_of[(size_t)r * g.k + jj];
-            // dropped by the expert capacity (or, in a MOE_DEBUG build, out of range)
-            if (!use_slot(slot, (long long)g.M * g.k, g.status)) continue;
-            s += ld_rt(g.src, (size_t)slot * g.N + c, g.src_type);
-          }
-          static_cast<float*>(g.C)[ci] = s;
           break;
         }
       }

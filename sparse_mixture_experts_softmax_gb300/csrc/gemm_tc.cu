@@ -995,7 +995,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st) {
   if ((g.epi == EPI_SWIGLU_UP && (g.B0x == nullptr || g.out1 == nullptr || g.out2 == nullptr)) ||
       (g.epi == EPI_ACT_FWD && g.out1 == nullptr) || (g.epi == EPI_ACT_BWD && g.aux0 == nullptr) ||
       (g.epi == EPI_SWIGLU_BWD && (g.aux0 == nullptr || g.aux1 == nullptr || g.out1 == nullptr)) ||
-      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)) || g.epi == EPI_SCATTER_ADD)
+      (g.A1 != nullptr && (g.B1 == nullptr || g.K1 <= 0)))
     return cudaErrorInvalidValue;
   CUtensorMap maps[7];   // operands (5), then the epilogue's side inputs (2)
   TcParams p{};

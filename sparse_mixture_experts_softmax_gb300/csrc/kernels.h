@@ -157,7 +157,6 @@ enum Epi {
   EPI_SWIGLU_FWD = 2,   // acc = H3; H1 read from aux0;  out1 = H3;  C = SiLU(H1) * H3
   EPI_ACT_BWD = 3,      // acc = dA; H from aux0;  C = dA * act'(H)
   EPI_SWIGLU_BWD = 4,   // acc = dA; H1 aux0, H3 aux1;  C = dH1;  out1 = dH3
-  EPI_SCATTER_ADD = 5,  // C(fp32) = acc + sum_j src[slot_of[r, j], n]  (CUDA-core GEMM only)
   EPI_SWIGLU_UP = 6     // tcgen05 only: B0 = W1, B0x = W3 in one N = 2 x 128 tile;
                         //   out1 = H1, out2 = H3, C = SiLU(H1) * H3
 };
@@ -193,10 +192,6 @@ struct GemmArgs {
   const void* aux1;
   void* out1;
   long long ld_aux;
-  const int* slot_of;
-  int k;
-  const void* src;
-  int src_type;
   const void* B0x;              // second B operand of EPI_SWIGLU_UP (W3)
   void* out2;                   // second extra output (H3 of EPI_SWIGLU_UP)
   int* status;                  // device status word (bounded-wait timeouts), tcgen05 only

@@ -274,7 +274,7 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
     // W_g's bf16 copy is the forward's, still in the workspace: the backward
     // runs with the forward's weights, and a training step updates W_g only
     // after the backward.
-    const int S = dwg_splits(c.T);
+    const int S = dwg_splits(c);
     GemmArgs rg{};
     rg.a_type = rg.b_type = MOE_BF16;
     rg.c_type = MOE_F32;
@@ -323,7 +323,7 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
     return MOE_OK;
   }
   // dW_g = dlogits^T x (split over token chunks, then a fixed-order sum)
-  const int S = dwg_splits(c.T);
+  const int S = dwg_splits(c);
   GemmArgs rg{};
   rg.a_type = MOE_F32;
   rg.b_type = c.dtype;
@@ -347,7 +347,8 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
   rg.epi = EPI_STORE;
   KL("gemm_router_dwg", launch_gemm_simt(rg, st));
   KL("router_dwg_sum", launch_sum_partials(P.at<float>(L.dwg_part), S, (long long)c.E * c.D, dw_gate, st));
-  // dX = dlogits W_g + sum_j dXe[slot(t, j)]
+  // dX = dlogits W_g, then each token's expert rows added in j order (the
+  // HBM-bound scatter-back pass)
   GemmArgs dg{};
   dg.a_type = MOE_F32;
   dg.b_type = MOE_F32;
@@ -368,13 +369,11 @@ moe_status router_backward(const moe_config& c, const ExpertW& w, const void* x,
   dg.seg_len = c.T;
   dg.C = dx;
   dg.ldc = c.D;
-  dg.epi = EPI_SCATTER_ADD;
+  dg.epi = EPI_STORE;
   dg.status = P.at<int>(L.status);
-  dg.slot_of = P.at<int>(L.slot_of);
-  dg.k = c.k;
-  dg.src = P.at<void>(L.dxe);
-  dg.src_type = c.dtype;
   KL("gemm_router_dx", launch_gemm_simt(dg, st));
+  KL("scatter_back", launch_scatter_back_add(c.dtype, dx, P.at<void>(L.dxe), P.at<int>(L.slot_of),
+                                             c.T, c.D, c.k, extra_dx, st, P.at<int>(L.status)));
   return MOE_OK;
 }
 
