@@ -80,6 +80,16 @@ constexpr int EPI_SGD_F32_TAG = 102;     // TN: fp32 weight-gradient store + fus
 constexpr int SIDE_SLOTS = 4;
 constexpr int SIDE_SLOT_BYTES = 2048;
 constexpr int SIDE_TMA_MAX_K = 2048;
+// 1: weight-gradient tiles in size order and snake order over the grid when
+// the largest expert has more than SNAKE_SKEW times the mean rows (see
+// sched_tile).  0 (the default): always round-robin in expert order.  The
+// skewed schedule shortens the weight-gradient launches of a skewed layer by
+// a fifth, but the run-time choice slows those of balanced layers by 2-4%,
+// the layers the default build is tuned for.
+#ifndef MOE_TC_SNAKE
+#define MOE_TC_SNAKE 0
+#endif
+constexpr int SNAKE_SKEW = 2;
 // The MMAs of a tile whose columns run past N use a smaller N (see the
 // MMA issuer); 0 keeps N = 256 on every tile.
 #ifndef MOE_TC_TRIM_N
@@ -426,8 +436,10 @@ __device__ __forceinline__ Tile map_tile(int t, const TcParams& p, const int* of
     T.nkb0 = (p.K0 + BK - 1) / BK;
     T.nkb = T.nkb0 + (p.K1 > 0 ? (p.K1 + BK - 1) / BK : 0);
   } else {
+    // ragged K: experts in order of decreasing row count (tpre holds that
+    // order for this form)
     const int per = p.nM * p.nN;
-    T.e = t / per;
+    T.e = tpre[t / per];
     const int rem = t % per;
     if (p.m_fast) {
       T.m0 = (rem % p.nM) * BM;
@@ -443,6 +455,22 @@ __device__ __forceinline__ Tile map_tile(int t, const TcParams& p, const int* of
     T.nkb0 = T.nkb;
   }
   return T;
+}
+
+// The i-th tile of this CTA's persistent schedule, or -1 past its last.
+// Tiles are dealt round by round over the grid.  A weight-gradient tile
+// (ragged K) costs in proportion to its expert's rows: when those are
+// skewed (`snake`), the tiles come largest expert first and are dealt in
+// alternating direction, so that the sums of tile costs of the CTAs stay
+// close to their mean.
+template <int FORM>
+__device__ __forceinline__ int sched_tile(int i, int total, bool snake) {
+  const int base = i * (int)gridDim.x;
+  if (base >= total) return -1;
+  const int pos = (FORM == FORM_TN && snake && (i & 1)) ? (int)gridDim.x - 1 - (int)blockIdx.x
+                                                       : (int)blockIdx.x;
+  const int t = base + pos;
+  return t < total ? t : -1;
 }
 
 template <int FORM, int EPI, bool SIDE>
@@ -462,6 +490,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
   __shared__ int abort_word;
   __shared__ int offs[MAX_E + 1];
   __shared__ int tpre[MAX_E + 1];
+  __shared__ int snake_word;
   volatile int* abort_flag = &abort_word;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t drain_bar = smem_u32(&drain_mb);
@@ -504,8 +533,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       tpre[0] = 0;
       for (int e = 0; e < p.E; ++e) tpre[e + 1] = tpre[e] + (offs[e + 1] - offs[e] + BM - 1) / BM;
     }
+    int mx = 0;
+    for (int e = 0; e < p.E; ++e) mx = max(mx, offs[e + 1] - offs[e]);
+    snake_word = (FORM == FORM_TN && MOE_TC_SNAKE &&
+                  (long long)mx * p.E > (long long)SNAKE_SKEW * offs[p.E]) ? 1 : 0;
   }
   __syncthreads();
+  const bool snake = snake_word != 0;
+  if (FORM == FORM_TN) {
+    // tpre[rank] = expert: by decreasing row count, ties by id, when the
+    // loads are skewed; else in id order
+    for (int e = tid; e < p.E; e += NUM_THREADS) {
+      int rank = e;
+      if (snake) {
+        const int re = offs[e + 1] - offs[e];
+        rank = 0;
+        for (int j = 0; j < p.E; ++j) {
+          const int rj = offs[j + 1] - offs[j];
+          rank += (rj > re || (rj == re && j < e)) ? 1 : 0;
+        }
+      }
+      tpre[rank] = e;
+    }
+    __syncthreads();
+  }
   const uint32_t tmem_base = tmem_slot;
   const int total = (FORM != FORM_TN) ? tpre[p.E] * p.nN : p.E * p.nM * p.nN;
 
@@ -518,7 +569,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       int issued = 0;
       uint32_t last_par = 0;
       bool ok = p.stall == 0;   // a stalled self-test issues nothing: the MMA waits run out
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int it = 0, t; ok && (t = sched_tile<FORM>(it, total, snake)) >= 0; ++it) {
         const Tile T = map_tile<FORM>(t, p, offs, tpre);
         for (int kb = 0; kb < T.nkb; ++kb) {
           if (!wait_bar(smem_u32(&empty_mb[s]), ph ^ 1u, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
@@ -575,7 +626,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     int buf = 0;
     uint32_t aph = 0;
     bool ok = true, any_mma = false;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int it = 0, t; ok && (t = sched_tile<FORM>(it, total, snake)) >= 0; ++it) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
       if (T.nkb == 0) continue;
       if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&tempty_mb[buf]), aph ^ 1u, abort_flag, p.status, p.wait_ns))) {
@@ -664,10 +715,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const size_t side_off = (size_t)NST * STAGE_BYTES + NUM_EPI_WARPS * STG_BYTES +
                             (size_t)(warp - 2) * SIDE_SLOTS * SIDE_SLOT_BYTES;
     const uint32_t side_bar0 = smem_u32(&side_mb[(warp - 2) * SIDE_SLOTS]);
-    int side_t = blockIdx.x, side_i = 0;   // issue cursor: tile, chunk within it
+    int side_it = 0, side_i = 0;           // issue cursor: schedule position, chunk
+    int side_t = sched_tile<FORM>(0, total, snake);   // its tile (-1: none left)
     long long side_iss = 0, side_con = 0;  // chunks issued / consumed
     auto side_skip_empty = [&]() {
-      while (side_t < total && map_tile<FORM>(side_t, p, offs, tpre).nkb == 0) side_t += gridDim.x;
+      while (side_t >= 0 && map_tile<FORM>(side_t, p, offs, tpre).nkb == 0)
+        side_t = sched_tile<FORM>(++side_it, total, snake);
     };
     auto side_issue = [&](int slot) {
       const Tile Ti = map_tile<FORM>(side_t, p, offs, tpre);
@@ -684,7 +737,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       ++side_iss;
       if (++side_i == NCH) {
         side_i = 0;
-        side_t += gridDim.x;
+        side_t = sched_tile<FORM>(++side_it, total, snake);
         side_skip_empty();
       }
     };
@@ -703,9 +756,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     bool side_fail = false;
     if (SIDE) {
       side_skip_empty();
-      for (int q = 0; q < SIDE_SLOTS && side_t < total; ++q) side_issue(q);
+      for (int q = 0; q < SIDE_SLOTS && side_t >= 0; ++q) side_issue(q);
     }
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int it = 0, t; (t = sched_tile<FORM>(it, total, snake)) >= 0; ++it) {
       const Tile T = map_tile<FORM>(t, p, offs, tpre);
       const int r = T.m0 + row;
       const bool rok = r < T.row_hi;
@@ -865,7 +918,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           chunk(c_begin + i * CHUNK, cur, cur);
           __syncwarp();
           ++side_con;
-          if (side_t < total) side_issue(slot);
+          if (side_t >= 0) side_issue(slot);
         }
         if (side_fail) break;
       } else {

@@ -60,7 +60,11 @@ def test_ragged_m_forms(form, counts, N, K):
 
 @pytest.mark.parametrize("counts,Mo,N", [([300, 0, 129, 1, 570], 1024, 704),
                                          ([64, 65, 0, 127], 704, 256),
-                                         ([2000, 3], 512, 2048)])
+                                         ([2000, 3], 512, 2048),
+                                         # skewed loads: the largest expert holds more than
+                                         # twice the mean rows (the case a MOE_TC_SNAKE
+                                         # build deals in size order), empty experts
+                                         ([4000, 0, 10, 3000, 0, 1, 64, 65, 128, 500], 512, 768)])
 def test_ragged_k_form(counts, Mo, N):
     g = torch.Generator(device="cuda")
     g.manual_seed(2)
