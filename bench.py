@@ -43,8 +43,8 @@ FFMA_PER_SM_PER_CLK = 128
 # from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # same per-expert shapes at 8 experts, scaled by 16.  Valid only for the GEMM
 # source it was taken from: reported as null once gemm_tc.cu changes.
-GEMM_TRAFFIC = {"bytes_per_step": 107.2e9, "workload": "large",
-                "gemm_source_sha256_prefix": "a7985172f2ca89b4", "gradients_stored": False}
+GEMM_TRAFFIC = {"bytes_per_step": 107.4e9, "workload": "large",
+                "gemm_source_sha256_prefix": "f575d8870daa70d5", "gradients_stored": False}
 
 
 def gemm_traffic(wl: W.Workload, store_grads: bool = False):
