@@ -463,14 +463,20 @@ def main():
     peaks = load_peaks()
     rows_kept = int(layer.routing()["offsets"][-1].item())   # T k unless a capacity drops
     eflops = expert_flops_per_step(wl, rows_kept)
-    if lp:
-        achieved = eflops / (gemm_ms / 1e3) / 1e12
+    # fp32 layers on the tensor cores do six bf16 term products per fp32
+    # product (csrc/gemm_f32x3.cu): their roofline counts that tensor work
+    path = B.moe_expert_gemm_path(layer.cfg)
+    f32x3 = (not lp) and path == B.GEMM_TENSOR_F32X3
+    work = 6.0 if f32x3 else 1.0
+    mhz = clk.get("sm_max_mhz") or 2070.0
+    ffma_peak = GB300_SMS * FFMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
+    if lp or f32x3:
+        achieved = work * eflops / (gemm_ms / 1e3) / 1e12
         peak = float(peaks["bf16_tflops_sustained"])
         bound, unit = "tensor", "TFLOP/s"
     else:
         achieved = eflops / (gemm_ms / 1e3) / 1e12
-        mhz = clk.get("sm_max_mhz") or 2070.0
-        peak = GB300_SMS * FFMA_PER_SM_PER_CLK * 2 * mhz * 1e6 / 1e12
+        peak = ffma_peak
         bound, unit = "alu", "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": gemm_traffic(wl, args.store_grads),
@@ -481,20 +487,31 @@ def main():
                                    "(profiles/tc_gemm_large_e8_traffic.md); null when the GEMM "
                                    "source differs from the one captured"),
                 "kernel": "grouped expert GEMMs (all launches of one step)",
-                "peak_source": f"{peaks['source']} ({'bf16_tflops_sustained' if lp else 'FFMA at max clock'})"}
-    if lp:
+                "peak_source": f"{peaks['source']} "
+                               f"({'bf16_tflops_sustained' if (lp or f32x3) else 'FFMA at max clock'})"}
+    if lp or f32x3:
         burst = float(peaks["bf16_tflops"])
         roofline["peak_burst"] = burst
         roofline["frac_of_burst"] = achieved / burst
+    if f32x3:
+        eff = eflops / (gemm_ms / 1e3) / 1e12
+        roofline["kernel"] = ("grouped expert GEMMs of an fp32 layer on the tensor cores: each fp32 "
+                              "operand split into three bf16 terms, six term products per fp32 "
+                              "product (counted in `achieved`), operand expansion and activation "
+                              "passes included in the time")
+        roofline["fp32_effective_tflops"] = eff
+        roofline["fp32_effective_vs_ffma_peak"] = eff / ffma_peak
+    roofline["gemm_path"] = {B.GEMM_CUDA_CORES: "cuda_cores", B.GEMM_TENSOR_BF16: "tensor_bf16",
+                             B.GEMM_TENSOR_F32X3: "tensor_fp32_three_term_split"}.get(path, "?")
     # each expert-GEMM launch on its own (FLOPs per step / its time per step)
     launches_tc = {}
     for name, fl in gemm_launch_flops(wl, rows_kept).items():
         ms = per_kernel.get(name, 0.0)
         if ms > 0:
-            tf = fl / (ms / 1e3) / 1e12
+            tf = work * fl / (ms / 1e3) / 1e12
             launches_tc[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                                  "frac": round(tf / peak, 4)}
-            if lp:
+            if lp or f32x3:
                 launches_tc[name]["frac_of_burst"] = round(tf / float(peaks["bf16_tflops"]), 4)
     hb = hbm_bytes(wl, rows_kept)
     hbm = {}

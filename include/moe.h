@@ -322,6 +322,20 @@ MOE_API moe_status moe_selftest_wait_timeout(int32_t form, int32_t M, int32_t N,
 #define MOE_BUILD_DEBUG_CHECKS 1
 MOE_API int32_t moe_build_flags(void);
 
+/* Which units run the expert GEMMs of a layer (host call, no device work):
+ * MOE_GEMM_TENSOR_BF16 for bf16 layers (tcgen05 with bf16 operands);
+ * MOE_GEMM_TENSOR_F32X3 for fp32 layers whose workspace holds the scratch
+ * of the tensor-core path, where each fp32 operand is split into three bf16
+ * terms and the six leading term products are summed in fp32 (the GEMMs with
+ * a bias, ReLU / GELU or no epilogue; SwiGLU's activation GEMMs stay on the
+ * CUDA cores); MOE_GEMM_CUDA_CORES for the other fp32 layers (D F below
+ * 65536, or a scratch past 1 GiB); a negative moe_status on an invalid
+ * configuration. */
+#define MOE_GEMM_CUDA_CORES 0
+#define MOE_GEMM_TENSOR_BF16 1
+#define MOE_GEMM_TENSOR_F32X3 2
+MOE_API int32_t moe_expert_gemm_path(const moe_config* cfg);
+
 /* Fault injection for the MOE_DEBUG variant's tests, on the host side: writes
  * `value` into entry `index` (0 <= index < T k) of the routing state the last
  * forward left in `workspace`: field 0 the expert ids idx [T,k], field 1 the

@@ -85,7 +85,22 @@ typedef struct {
   void* dx;                /* [rows, D] input gradients, to be sent back     */
   int32_t* status;         /* device int32: 0, or MOE_ERR_TIMEOUT if a
                               bounded device wait expired (caller zeroes it) */
+  void* f32_scratch;       /* fp32 layers: moe_ep_f32_scratch_size bytes of
+                              device scratch (16-byte aligned) for the expert
+                              GEMMs on the tensor cores, or NULL (CUDA-core
+                              GEMMs); ignored by bf16 layers                 */
+  size_t f32_scratch_bytes;
 } moe_ep_rows;
+
+/* Scratch bytes that let the expert GEMMs of an fp32 layer over `rows`
+ * received rows run on the tensor cores (each fp32 operand split into three
+ * bf16 terms, the six leading term products summed in fp32): the same
+ * arithmetic as the single-device step, which takes its scratch from its
+ * workspace; without it (or when the answer is 0) they run on the CUDA cores
+ * and results may differ from the single-device step's in the last bits.
+ * 0 for bf16 layers and on an invalid request. */
+MOE_API size_t moe_ep_f32_scratch_size(const moe_config* cfg, const moe_ep_config* ep,
+                                       int32_t rows);
 
 /* Workspace bytes of one rank's source-side state (routing, its tokens'
  * expert-major rows x_e / y_e / dy_e / dx_e, router buffers); 0 on an

@@ -64,7 +64,8 @@ class moe_ep_config(ctypes.Structure):
 
 class moe_ep_rows(ctypes.Structure):
     _fields_ = [("rows", c_int32)] + [(n, c_void_p) for n in (
-        "offsets", "x", "h1", "h3", "a", "y", "dy", "dh1", "dh3", "dx", "status")]
+        "offsets", "x", "h1", "h3", "a", "y", "dy", "dh1", "dh3", "dx", "status",
+        "f32_scratch")] + [("f32_scratch_bytes", ctypes.c_size_t)]
 
 
 class MoEError(RuntimeError):
@@ -155,6 +156,8 @@ def _load(path: str) -> ctypes.CDLL:
                                                                             c_void_p]
     L.moe_ep_workspace_size.argtypes = [P(moe_config), P(moe_ep_config)]
     L.moe_ep_workspace_size.restype = c_size_t
+    L.moe_ep_f32_scratch_size.argtypes = [P(moe_config), P(moe_ep_config), c_int32]
+    L.moe_ep_f32_scratch_size.restype = c_size_t
     L.moe_ep_buffer_offsets.argtypes = [P(moe_config), P(moe_ep_config), P(c_size_t)]
     L.moe_ep_route.argtypes = [P(moe_config), P(moe_ep_config), P(moe_weights), c_void_p,
                                c_void_p, c_void_p, c_size_t, c_void_p]
@@ -182,6 +185,8 @@ def _load(path: str) -> ctypes.CDLL:
         getattr(L, fn).restype = c_int32
     L.moe_build_flags.argtypes = []
     L.moe_build_flags.restype = c_int32
+    L.moe_expert_gemm_path.argtypes = [P(moe_config)]
+    L.moe_expert_gemm_path.restype = c_int32
     L.moe_debug_poke_routing.argtypes = [P(moe_config), c_void_p, c_size_t, c_int32,
                                          ctypes.c_int64, c_int32, c_void_p]
     L.moe_debug_poke_routing.restype = c_int32
@@ -369,9 +374,15 @@ def moe_selftest_wait_timeout(form, M, N, K, E, offsets, A, B, C, dev_status, li
 # ---- expert-parallel phases (include/moe_ep.h)
 
 def make_ep_rows(rows: int, offsets, x=None, h1=None, h3=None, a=None, y=None, dy=None,
-                 dh1=None, dh3=None, dx=None, status=None) -> moe_ep_rows:
+                 dh1=None, dh3=None, dx=None, status=None, f32_scratch=None) -> moe_ep_rows:
+    nbytes = 0 if f32_scratch is None else f32_scratch.numel() * f32_scratch.element_size()
     return moe_ep_rows(int(rows), _ptr(offsets), _ptr(x), _ptr(h1), _ptr(h3), _ptr(a), _ptr(y),
-                       _ptr(dy), _ptr(dh1), _ptr(dh3), _ptr(dx), _ptr(status))
+                       _ptr(dy), _ptr(dh1), _ptr(dh3), _ptr(dx), _ptr(status), _ptr(f32_scratch),
+                       nbytes)
+
+
+def moe_ep_f32_scratch_size(cfg, ep, rows: int) -> int:
+    return int(lib().moe_ep_f32_scratch_size(ctypes.byref(cfg), ctypes.byref(ep), int(rows)))
 
 
 def moe_ep_workspace_size(cfg, ep) -> int:
@@ -437,6 +448,13 @@ def moe_ep_router_update(cfg, w_gate, dw_gate, lr, stream=None):
 
 def moe_build_flags() -> int:
     return int(lib().moe_build_flags())
+
+
+GEMM_CUDA_CORES, GEMM_TENSOR_BF16, GEMM_TENSOR_F32X3 = 0, 1, 2
+
+
+def moe_expert_gemm_path(cfg) -> int:
+    return int(lib().moe_expert_gemm_path(ctypes.byref(cfg)))
 
 
 def moe_debug_poke_routing(cfg, workspace, field: int, index: int, value: int, stream=None):

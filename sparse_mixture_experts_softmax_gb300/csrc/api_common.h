@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -85,8 +86,31 @@ struct Layout {
   // runs after the GEMMs; bf16 layers apply it inside the GEMM epilogues and
   // store nothing)
   size_t g_wg, g_b1, g_b2, g_w1, g_w3, g_w2;
+  // fp32 layers: expanded operands of the expert GEMMs on the tensor cores
+  size_t f32x3, f32x3_bytes;
   size_t total;
 };
+
+// Scratch of the fp32 expert GEMMs on the tensor cores (gemm_f32x3.cu) for R
+// expert rows over E experts: the largest pair of expanded operands among
+// the layer's expert GEMMs (six bf16 terms, 12 bytes, per fp32 value).  0,
+// and the CUDA-core GEMMs serve, for bf16 layers, for layers with D F below
+// F32X3_MIN_DF (their few-microsecond GEMMs would pay more for the operand
+// expansion launches than they gain) and past F32X3_MAX_BYTES.  The choice
+// depends on the layer alone, so an expert-parallel rank makes the one the
+// single-device step makes.
+constexpr size_t F32X3_MAX_BYTES = (size_t)1 << 30;
+constexpr size_t F32X3_MIN_DF = (size_t)1 << 16;
+inline size_t f32x3_scratch(const moe_config& c, size_t R, size_t E) {
+  if (c.dtype != MOE_F32 || (size_t)c.D * (size_t)c.F < F32X3_MIN_DF) return 0;
+  const size_t D = (size_t)c.D, F = (size_t)c.F, u = 12;
+  auto r = [](size_t b) { return (b + 255) & ~(size_t)255; };
+  size_t m = r(R * D * u) + r(E * F * D * u);                          // up (K = D)
+  m = std::max(m, r(R * F * u) + r(E * D * F * u));                   // down, dXe (K = F)
+  if (c.act == MOE_ACT_SWIGLU) m = std::max(m, 2 * (r(R * F * u) + r(E * D * F * u)));   // dXe, 2 pairs
+  m = std::max(m, r(R * D * u) + r(R * F * u) + r((E + 1) * 4));      // dW (6R rows)
+  return m > F32X3_MAX_BYTES ? 0 : m;
+}
 
 // expert_buffers = false: the source-side workspace of an expert-parallel
 // rank, without the buffers of the expert MLPs (H, A, dH and the fp32
@@ -152,6 +176,8 @@ inline Layout make_layout(const moe_config& c, bool expert_buffers = true) {
     L.g_w3 = swiglu ? take(E * F * D * 4) : 0;
     L.g_w2 = take(E * D * F * 4);
   }
+  L.f32x3_bytes = expert_buffers ? f32x3_scratch(c, R, E) : 0;
+  L.f32x3 = L.f32x3_bytes ? take(L.f32x3_bytes) : 0;
   L.total = o;
   return L;
 }
@@ -252,9 +278,20 @@ inline GemmArgs gemm_base(const moe_config& c, const Ptrs& P) {
 }
 
 
-// Expert GEMMs: tcgen05 tensor cores for bf16 layers, CUDA cores for fp32.
-inline cudaError_t run_gemm(const moe_config& c, const GemmArgs& g, cudaStream_t st) {
+// Expert GEMMs: tcgen05 tensor cores for bf16 layers; for fp32 layers the
+// tensor cores through the three-term split where the rows carry scratch for
+// it and the GEMM is of a form it takes, else the CUDA cores.
+inline cudaError_t run_gemm(const moe_config& c, const GemmArgs& g, cudaStream_t st,
+                            void* f32x3 = nullptr, size_t f32x3_bytes = 0) {
   if (c.dtype == MOE_BF16) return launch_gemm_tc(g, st);
+  if (f32x3 != nullptr) {
+    int kernels = 0;
+    const cudaError_t e = launch_gemm_f32x3(g, f32x3, f32x3_bytes, st, &kernels);
+    if (e != cudaErrorNotSupported) {
+      g_launches += kernels > 0 ? kernels - 1 : 0;   // the caller counts one
+      return e;
+    }
+  }
   return launch_gemm_simt(g, st);
 }
 
@@ -274,6 +311,8 @@ struct ExpertRows {
   const int* offsets;    // [E + 1] device: segment e = rows [offsets[e], offsets[e + 1])
   int* status;           // device status word of the bounded waits
   void *xe, *h1, *h3, *a, *ye, *dye, *dh1, *dh3, *dxe;
+  void* f32x3;           // fp32 layers: scratch of the tensor-core GEMMs, or nullptr
+  size_t f32x3_bytes;
 };
 
 inline GemmArgs rows_gemm(const moe_config& c, const ExpertRows& r) {

@@ -79,6 +79,11 @@ moe_status rows_of(const moe_config& c, const moe_ep_config& ep, const moe_ep_ro
   e.dh1 = r.dh1;
   e.dh3 = r.dh3;
   e.dxe = r.dx;
+  if (c.dtype == MOE_F32 && r.f32_scratch != nullptr && r.f32_scratch_bytes > 0) {
+    if (!aligned16(r.f32_scratch)) return MOE_ERR_ALIGNMENT;
+    e.f32x3 = r.f32_scratch;
+    e.f32x3_bytes = r.f32_scratch_bytes;
+  }
   *out = e;
   return MOE_OK;
 }
@@ -90,6 +95,12 @@ extern "C" {
 size_t moe_ep_workspace_size(const moe_config* cfg, const moe_ep_config* ep) {
   if (ep_check(cfg, ep) != MOE_OK) return 0;
   return ep_layout(*cfg).total;
+}
+
+size_t moe_ep_f32_scratch_size(const moe_config* cfg, const moe_ep_config* ep, int32_t rows) {
+  if (ep_check(cfg, ep) != MOE_OK || rows < 0 || (long long)rows > (long long)ep->T_total * cfg->k)
+    return 0;
+  return f32x3_scratch(*cfg, (size_t)rows, (size_t)(cfg->E / ep->n_ranks));
 }
 
 moe_status moe_ep_buffer_offsets(const moe_config* cfg, const moe_ep_config* ep, size_t* out4) {

@@ -1,0 +1,294 @@
+// fp32 expert GEMMs on the bf16 tensor cores.  Course "Trainable MoE in
+// CUDA", Part 1 (matmul variants) and Part 5 (expert MLP forward and
+// backward); the fp32 layers keep their fp32 tolerance.
+//
+// Each fp32 operand value is split into three bf16 terms,
+//   x1 = RN(x),  x2 = RN(x - x1),  x3 = RN(x - x1 - x2),
+// (both differences are exact in fp32), which together hold x to about
+// 2^-24 of |x|.  A product a b is then the fp32-accumulated sum of the six
+// term products of order up to a2 b2:
+//   a1 b1 + a1 b2 + a2 b1 + a1 b3 + a2 b2 + a3 b1,
+// each exact in fp32 (8 x 8 significant bits); the three left out are below
+// 2^-26 of |a b|.  The six products of a dot product over K become one bf16
+// GEMM over 6 K: the A side lays its terms out along the reduction as
+// [a1 a1 a2 a1 a2 a3], the B side as [b1 b2 b1 b3 b2 b1].  So the
+// tensor-core grouped GEMM (gemm_tc.cu) runs unchanged on operands expanded
+// here:
+//   ragged M, A [M, K] K-major          -> A' [M, 6K]
+//   ragged M, B [E, N, K] K-major (NT)  -> B' [E, N, 6K]
+//   ragged M, B [E, K, N] N-major (NN)  -> B' [E, 6K, N]
+//   ragged K, A [R, M] and B [R, N]     -> [6R, M] and [6R, N]: expert e's
+//            rows [o_e, o_e+1) become six blocks of its rows at 6 o_e
+//            (offsets scaled by 6).
+// The GEMM stores fp32 (+ bias); the activation and its backward, which the
+// CUDA-core GEMM applies in its epilogue, run as elementwise passes over that
+// output with the same functions.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+// a launch counted in n_k (kernels launched by this call)
+#define MOE_LAUNCH_N(expr) \
+  do {                     \
+    MOE_LAUNCH(expr);      \
+    ++n_k;                 \
+  } while (0)
+
+namespace moe {
+namespace {
+
+// The three bf16 terms of x.
+__device__ __forceinline__ void split3(float x, bf16 (&t)[3]) {
+  t[0] = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(t[0]);
+  t[1] = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(t[1]);
+  t[2] = __float2bfloat16_rn(r2);
+}
+
+// Term index of reduction block b (0..5) on side A (0) or B (1).
+__device__ __forceinline__ int term_of(int side, int b) {
+  // A: 1 1 2 1 2 3    B: 1 2 1 3 2 1   (0-based below)
+  const int a = (0x210100 >> (4 * b)) & 0xF;
+  const int bb = (0x012010 >> (4 * b)) & 0xF;
+  return side == 0 ? a : bb;
+}
+
+// Four consecutive values -> their term `which` as four packed bf16.
+__device__ __forceinline__ uint2 pack_term(const bf16 (&t)[4][3], int which) {
+  __nv_bfloat162 lo, hi;
+  lo.x = t[0][which];
+  lo.y = t[1][which];
+  hi.x = t[2][which];
+  hi.y = t[3][which];
+  uint2 q;
+  q.x = *reinterpret_cast<uint32_t*>(&lo);
+  q.y = *reinterpret_cast<uint32_t*>(&hi);
+  return q;
+}
+
+__device__ __forceinline__ void split4(float4 v, bf16 (&t)[4][3]) {
+  split3(v.x, t[0]);
+  split3(v.y, t[1]);
+  split3(v.z, t[2]);
+  split3(v.w, t[3]);
+}
+
+// Rows of K values (row stride ldx) -> rows of 6K (the blocks side by side).
+__global__ void expand_cols_kernel(const float* __restrict__ X, long long ldx, long long rows, int K,
+                                   bf16* __restrict__ Y, int side) {
+  pdl_begin();
+  const int kq = K / 4;
+  const long long n = rows * kq;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / kq;
+    const int k = (int)(i - r * kq) * 4;
+    bf16 t[4][3];
+    split4(*reinterpret_cast<const float4*>(X + r * ldx + k), t);
+    bf16* y = Y + r * 6LL * K + k;
+#pragma unroll
+    for (int b = 0; b < 6; ++b)
+      *reinterpret_cast<uint2*>(y + (long long)b * K) = pack_term(t, term_of(side, b));
+  }
+}
+
+// [E][K][N] (row stride N) -> [E][6K][N]: the six K blocks one below the other.
+__global__ void expand_rows_kernel(const float* __restrict__ X, long long E, int K, int N,
+                                   bf16* __restrict__ Y, int side) {
+  pdl_begin();
+  const int nq = N / 4;
+  const long long n = E * K * (long long)nq;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / nq;          // e * K + k
+    const int c = (int)(i - row * nq) * 4;
+    const long long e = row / K;
+    const int k = (int)(row - e * K);
+    bf16 t[4][3];
+    split4(*reinterpret_cast<const float4*>(X + row * N + c), t);
+#pragma unroll
+    for (int b = 0; b < 6; ++b)
+      *reinterpret_cast<uint2*>(Y + ((e * 6 + b) * K + k) * N + c) = pack_term(t, term_of(side, b));
+  }
+}
+
+// Row segments [R][M] (row stride ldx, segment e = rows [o_e, o_e+1)) ->
+// [6R][M]: segment e's six blocks of its rows starting at row 6 o_e.  Rows
+// past o_E belong to no segment and are not written.
+__global__ void expand_segments_kernel(const float* __restrict__ X, long long ldx, long long R, int M,
+                                       const int* __restrict__ offsets, int E,
+                                       bf16* __restrict__ Y, int side) {
+  pdl_begin();
+  const int mq = M / 4;
+  const long long n = R * mq;
+  const int end = offsets[E];
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / mq;
+    if (r >= end) continue;
+    const int c = (int)(i - r * mq) * 4;
+    int lo = 0, hi = E;   // the segment holding r: largest e with offsets[e] <= r
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (offsets[mid] <= r) lo = mid; else hi = mid;
+    }
+    const long long o = offsets[lo], rows = offsets[lo + 1] - o, j = r - o;
+    bf16 t[4][3];
+    split4(*reinterpret_cast<const float4*>(X + r * ldx + c), t);
+#pragma unroll
+    for (int b = 0; b < 6; ++b)
+      *reinterpret_cast<uint2*>(Y + (6 * o + b * rows + j) * M + c) = pack_term(t, term_of(side, b));
+  }
+}
+
+__global__ void scale_offsets_kernel(const int* __restrict__ in, int n, int* __restrict__ out) {
+  pdl_begin();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    out[i] = 6 * in[i];
+}
+
+// A = act(H) over the expert rows of the GEMM output (rows [0, *end) of
+// N values, row stride ld).
+__global__ void act_fwd_kernel(const float* __restrict__ H, float* __restrict__ A,
+                               const int* __restrict__ end, int N, long long ld, int act) {
+  pdl_begin();
+  const long long n = (long long)*end * N;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / N, o = r * ld + (i - r * N);
+    const float h = H[o];
+    A[o] = act == 0 ? fmaxf(h, 0.f) : gelu_tanh_f(h);
+  }
+}
+
+// dH = dA * act'(H), in place over dA (expert rows only).
+__global__ void act_bwd_kernel(float* __restrict__ dA, const float* __restrict__ H,
+                               const int* __restrict__ end, int N, long long ld, long long ld_h,
+                               int act) {
+  pdl_begin();
+  const long long n = (long long)*end * N;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / N, c = i - r * N, o = r * ld + c;
+    const float v = dA[o], h = H[r * ld_h + c];
+    dA[o] = act == 0 ? (h > 0.f ? v : 0.f) : v * gelu_tanh_grad_f(h);
+  }
+}
+
+int grid_of(long long n) {
+  const long long b = (n + 255) / 256;
+  return (int)(b < 152 * 16 ? (b < 1 ? 1 : b) : 152 * 16);
+}
+
+size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t gemm_f32x3_scratch_bytes(const GemmArgs& g) {
+  if (g.ragged_k)
+    return up256((size_t)6 * g.K0 * g.M * 2) + up256((size_t)6 * g.K0 * g.N * 2) +
+           up256((size_t)(g.E + 1) * 4);
+  const size_t per = up256((size_t)g.M * 6 * g.K0 * 2) + up256((size_t)g.E * g.N * 6 * g.K0 * 2);
+  const size_t pair = (g.A1 != nullptr && g.K1 > 0)
+                          ? up256((size_t)g.M * 6 * g.K1 * 2) + up256((size_t)g.E * g.N * 6 * g.K1 * 2)
+                          : 0;
+  return per + pair;
+}
+
+cudaError_t launch_gemm_f32x3(const GemmArgs& g, void* scratch, size_t scratch_bytes, cudaStream_t st,
+                              int* kernels) {
+  int n_k = 0;
+  if (kernels) *kernels = 0;
+  if (g.M == 0 || g.N == 0 || g.E == 0) return cudaSuccess;
+  if (g.a_type != 0 || g.b_type != 0 || g.c_type != 0 || g.offsets == nullptr || g.sgd_w != nullptr)
+    return cudaErrorNotSupported;
+  const bool fwd = g.epi == EPI_ACT_FWD, bwd = g.epi == EPI_ACT_BWD;
+  if (g.epi != EPI_STORE && !fwd && !bwd) return cudaErrorNotSupported;
+  if (g.ragged_k && g.epi != EPI_STORE) return cudaErrorNotSupported;
+  if (scratch == nullptr || scratch_bytes < gemm_f32x3_scratch_bytes(g)) return cudaErrorNotSupported;
+  char* s = static_cast<char*>(scratch);
+  auto take = [&](size_t bytes) {
+    char* p = s;
+    s += up256(bytes);
+    return p;
+  };
+  GemmArgs t = g;
+  t.a_type = t.b_type = 1;
+  t.bias = (g.epi == EPI_ACT_BWD) ? nullptr : g.bias;
+  t.epi = EPI_STORE;
+  if (g.ragged_k) {
+    // weight gradient: A [R, M], B [R, N], segments of rows
+    if (g.lda % 4 || g.ldb % 4 || g.M % 4 || g.N % 4) return cudaErrorNotSupported;
+    const long long R = g.K0;
+    bf16* A = reinterpret_cast<bf16*>(take((size_t)6 * R * g.M * 2));
+    bf16* B = reinterpret_cast<bf16*>(take((size_t)6 * R * g.N * 2));
+    int* off6 = reinterpret_cast<int*>(take((size_t)(g.E + 1) * 4));
+    MOE_LAUNCH_N(launch_pdl(scale_offsets_kernel, dim3(1), dim3(256), 0, st, g.offsets, g.E + 1, off6));
+    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.M / 4))), dim3(256), 0, st,
+                          static_cast<const float*>(g.A0), g.lda, R, g.M, g.offsets, g.E, A, 0));
+    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.N / 4))), dim3(256), 0, st,
+                          static_cast<const float*>(g.B0), g.ldb, R, g.N, g.offsets, g.E, B, 1));
+    t.A0 = A;
+    t.lda = g.M;
+    t.B0 = B;
+    t.ldb = g.N;
+    t.K0 = (int)(6 * R);
+    t.offsets = off6;
+    const cudaError_t e = launch_gemm_tc(t, st);
+    if (kernels) *kernels = n_k + 1;
+    return e;
+  }
+  // ragged M: A [M, K] K-major; B per expert K-major (NT) or N-major (NN),
+  // its rows packed (row stride K or N, expert stride N K)
+  if (!g.a_kcontig) return cudaErrorNotSupported;
+  const int pairs = (g.A1 != nullptr && g.K1 > 0) ? 2 : 1;
+  if (pairs == 2 && g.K0 != g.K1) return cudaErrorNotSupported;   // one row stride for both
+  for (int q = 0; q < pairs; ++q) {
+    const int K = q == 0 ? g.K0 : g.K1;
+    const float* Aq = static_cast<const float*>(q == 0 ? g.A0 : g.A1);
+    const float* Bq = static_cast<const float*>(q == 0 ? g.B0 : g.B1);
+    const long long ldb_want = g.b_kcontig ? K : g.N;
+    if (K % 4 || g.lda % 4 || g.N % 8 || g.ldb != ldb_want || g.sBe != (long long)g.N * K)
+      return cudaErrorNotSupported;
+    bf16* A = reinterpret_cast<bf16*>(take((size_t)g.M * 6 * K * 2));
+    bf16* B = reinterpret_cast<bf16*>(take((size_t)g.E * g.N * 6 * K * 2));
+    MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.M * (K / 4))), dim3(256), 0,
+                          st, Aq, g.lda, (long long)g.M, K, A, 0));
+    if (g.b_kcontig)
+      MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.E * g.N * (K / 4))),
+                            dim3(256), 0, st, Bq, (long long)K, (long long)g.E * g.N, K, B, 1));
+    else
+      MOE_LAUNCH_N(launch_pdl(expand_rows_kernel, dim3(grid_of((long long)g.E * K * (g.N / 4))),
+                            dim3(256), 0, st, Bq, (long long)g.E, K, g.N, B, 1));
+    if (q == 0) {
+      t.A0 = A;
+      t.B0 = B;
+      t.K0 = 6 * K;
+    } else {
+      t.A1 = A;
+      t.B1 = B;
+      t.K1 = 6 * K;
+    }
+    t.lda = 6LL * K;   // both pairs have the same K in every caller (F for dXe)
+    t.ldb = g.b_kcontig ? 6LL * K : g.N;
+    t.sBe = (long long)g.N * 6 * K;
+  }
+  if (fwd) t.C = g.out1;   // H = acc + bias, then A = act(H)
+  cudaError_t e = launch_gemm_tc(t, st);
+  if (e != cudaSuccess) return e;
+  ++n_k;
+  if (fwd)
+    MOE_LAUNCH_N(launch_pdl(act_fwd_kernel, dim3(grid_of((long long)g.M * g.N)), dim3(256), 0, st,
+                          static_cast<const float*>(g.out1), static_cast<float*>(g.C),
+                          g.offsets + g.E, g.N, g.ldc, g.act));
+  if (bwd)
+    MOE_LAUNCH_N(launch_pdl(act_bwd_kernel, dim3(grid_of((long long)g.M * g.N)), dim3(256), 0, st,
+                          static_cast<float*>(g.C), static_cast<const float*>(g.aux0),
+                          g.offsets + g.E, g.N, g.ldc, g.ld_aux, g.act));
+  if (kernels) *kernels = n_k;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

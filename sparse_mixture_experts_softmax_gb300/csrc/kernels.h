@@ -214,6 +214,15 @@ inline cudaError_t launch_gemm_simt(const GemmArgs& g, cudaStream_t st) {
 
 // tcgen05 / TMA grouped GEMM for bf16 operands (gemm_tc.cu).
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t st);
+
+// fp32 operands on the bf16 tensor cores through a three-term bf16 split of
+// each operand (gemm_f32x3.cu): scratch for the expanded operands, and the
+// launch; cudaErrorNotSupported (before any launch) for forms, epilogues or
+// strides it does not take, and when the scratch is missing or too small.
+// `kernels` (optional) receives the number of kernels launched.
+size_t gemm_f32x3_scratch_bytes(const GemmArgs& g);
+cudaError_t launch_gemm_f32x3(const GemmArgs& g, void* scratch, size_t scratch_bytes,
+                              cudaStream_t st, int* kernels = nullptr);
 // Device status word values written by kernels (0 = ok).
 constexpr int DEV_STATUS_TIMEOUT = 6;
 

@@ -44,23 +44,23 @@ moe_status experts_forward(const moe_config& c, const ExpertW& w, const ExpertRo
     g.out1 = r.h1;
     g.out2 = r.h3;
     g.C = r.a;
-    KL("gemm_up", run_gemm(c, g, st));
+    KL("gemm_up", run_gemm(c, g, st, r.f32x3, r.f32x3_bytes));
   } else if (c.act == MOE_ACT_SWIGLU) {
     g.epi = EPI_STORE;
     g.C = r.h1;
-    KL("gemm_up", run_gemm(c, g, st));
+    KL("gemm_up", run_gemm(c, g, st, r.f32x3, r.f32x3_bytes));
     g.B0 = w.w3;
     g.epi = EPI_SWIGLU_FWD;
     g.aux0 = r.h1;
     g.out1 = r.h3;
     g.C = r.a;
-    KL("gemm_up_w3", run_gemm(c, g, st));
+    KL("gemm_up_w3", run_gemm(c, g, st, r.f32x3, r.f32x3_bytes));
   } else {
     g.epi = EPI_ACT_FWD;
     g.bias = w.b1;
     g.out1 = r.h1;
     g.C = r.a;
-    KL("gemm_up", run_gemm(c, g, st));
+    KL("gemm_up", run_gemm(c, g, st, r.f32x3, r.f32x3_bytes));
   }
   // expert down-projection (+ bias)
   GemmArgs d = rows_gemm(c, r);
@@ -79,7 +79,7 @@ moe_status experts_forward(const moe_config& c, const ExpertW& w, const ExpertRo
   d.epi = EPI_STORE;
   d.bias = w.b2;
   d.C = r.ye;
-  KL("gemm_down", run_gemm(c, d, st));
+  KL("gemm_down", run_gemm(c, d, st, r.f32x3, r.f32x3_bytes));
 
   return MOE_OK;
 }
@@ -113,7 +113,7 @@ moe_status experts_backward(const moe_config& c, const ExpertW& w, const ExpertR
   } else {
     g.epi = EPI_ACT_BWD;
   }
-  KL("gemm_dA", run_gemm(c, g, st));
+  KL("gemm_dA", run_gemm(c, g, st, r.f32x3, r.f32x3_bytes));
   // dW2_e = dYe_e^T A_e  (ragged K)
   GemmArgs w2g = rows_gemm(c, r);
   w2g.ragged_k = true;
@@ -136,7 +136,7 @@ moe_status experts_backward(const moe_config& c, const ExpertW& w, const ExpertR
     w2g.sgd_wlp = sgd->w2_lp;
     w2g.sgd_lr = sgd->lr;
   }
-  KL("gemm_dw2", run_gemm(c, w2g, st));
+  KL("gemm_dw2", run_gemm(c, w2g, st, r.f32x3, r.f32x3_bytes));
   if (gr.db2) KL("bias_grad", launch_segment_colsum(c.dtype, r.dye, r.offsets, r.E, c.D, gr.db2, st));
   // dXe = dH1 W1_e (+ dH3 W3_e)
   GemmArgs xg = rows_gemm(c, r);
@@ -159,7 +159,7 @@ moe_status experts_backward(const moe_config& c, const ExpertW& w, const ExpertR
   xg.ldc = c.D;
   xg.epi = EPI_STORE;
   xg.C = r.dxe;
-  KL("gemm_dxe", run_gemm(c, xg, st));
+  KL("gemm_dxe", run_gemm(c, xg, st, r.f32x3, r.f32x3_bytes));
   // dW1_e = dH1_e^T Xe_e (dW3 likewise)
   GemmArgs w1g = rows_gemm(c, r);
   w1g.ragged_k = true;
@@ -182,7 +182,7 @@ moe_status experts_backward(const moe_config& c, const ExpertW& w, const ExpertR
     w1g.sgd_wlp = sgd->w1_lp;
     w1g.sgd_lr = sgd->lr;
   }
-  KL("gemm_dw1", run_gemm(c, w1g, st));
+  KL("gemm_dw1", run_gemm(c, w1g, st, r.f32x3, r.f32x3_bytes));
   if (swiglu) {
     w1g.A0 = r.dh3;
     w1g.C = gr.dw3;
@@ -190,7 +190,7 @@ moe_status experts_backward(const moe_config& c, const ExpertW& w, const ExpertR
       w1g.sgd_w = sgd->w3;
       w1g.sgd_wlp = sgd->w3_lp;
     }
-    KL("gemm_dw3", run_gemm(c, w1g, st));
+    KL("gemm_dw3", run_gemm(c, w1g, st, r.f32x3, r.f32x3_bytes));
   }
   if (gr.db1) KL("bias_grad", launch_segment_colsum(c.dtype, r.dh1, r.offsets, r.E, c.F, gr.db1, st));
   return MOE_OK;
@@ -399,6 +399,8 @@ ExpertRows expert_rows(const moe_config& c, const Ptrs& P) {
   r.dh1 = P.at<void>(L.dh1);
   r.dh3 = L.dh3 ? P.at<void>(L.dh3) : nullptr;
   r.dxe = P.at<void>(L.dxe);
+  r.f32x3 = L.f32x3_bytes ? P.at<void>(L.f32x3) : nullptr;
+  r.f32x3_bytes = L.f32x3_bytes;
   return r;
 }
 
@@ -1136,6 +1138,13 @@ const char* moe_status_string(moe_status s) {
 }
 
 int32_t moe_last_launch_count(void) { return g_launches; }
+
+int32_t moe_expert_gemm_path(const moe_config* cfg) {
+  const moe_status v = validate_config(cfg);
+  if (v != MOE_OK) return -(int32_t)v;
+  if (cfg->dtype == MOE_BF16) return MOE_GEMM_TENSOR_BF16;
+  return make_layout(*cfg).f32x3_bytes > 0 ? MOE_GEMM_TENSOR_F32X3 : MOE_GEMM_CUDA_CORES;
+}
 
 int32_t moe_build_flags(void) {
 #ifdef MOE_DEBUG

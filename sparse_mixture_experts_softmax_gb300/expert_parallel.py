@@ -302,10 +302,15 @@ class EPRank:
         self.r_dh1 = torch.empty(n, c.F, dtype=dt, device=dev)
         self.r_dh3 = torch.empty(n, c.F, dtype=dt, device=dev) if swiglu else None
         self.r_dx = torch.empty(n, c.D, dtype=dt, device=dev)
+        # fp32 layers: scratch that puts the expert GEMMs on the tensor cores,
+        # as the single-device step's workspace does
+        nbytes = B.moe_ep_f32_scratch_size(c, self.ep, rows)
+        self.r_f32 = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
 
     def ep_rows(self):
         return B.make_ep_rows(self.rows, self.r_offsets, self.r_x, self.r_h1, self.r_h3, self.r_a,
-                              self.r_y, self.r_dy, self.r_dh1, self.r_dh3, self.r_dx, self.status)
+                              self.r_y, self.r_dy, self.r_dh1, self.r_dh3, self.r_dx, self.status,
+                              self.r_f32)
 
 
 def train_step(ranks: List[EPRank], transport, xs: Dict[int, torch.Tensor],

@@ -214,3 +214,34 @@ def test_debug_variant_and_poke_refusal(L):
         # host-side validation of the injection itself, before any device work
         assert _status(B.moe_debug_poke_routing, _cfg(), ws, 2, 0, 5) == B.MOE_ERR_INVALID_ARG
         assert _status(B.moe_debug_poke_routing, _cfg(), ws, 1, 64 * 2, 5) == B.MOE_ERR_INVALID_ARG
+
+
+def test_expert_gemm_path(L):
+    """Which units run a layer's expert GEMMs: bf16 layers the tensor cores;
+    fp32 layers with D F >= 65536 the tensor cores through the three-term
+    bf16 split while its scratch (12 bytes per expanded fp32 value, the
+    largest operand pair of the layer) stays within 1 GiB, else the CUDA
+    cores; the scratch is part of the workspace exactly when that path is
+    taken."""
+    bf = _cfg(dtype="bf16", D=64, F=64, E=8, has_bias=False, act="swiglu")
+    assert B.moe_expert_gemm_path(bf) == B.GEMM_TENSOR_BF16
+    assert B.moe_expert_gemm_path(_cfg()) == B.GEMM_CUDA_CORES        # D F = 2048: too small
+    assert B.moe_expert_gemm_path(_cfg(D=256, F=256)) == B.GEMM_TENSOR_F32X3
+    # R = 65536 rows of D = F = 1024 over 64 experts: 805 MB + 805 MB of operands
+    big = _cfg(T=8192, k=8, E=64, D=1024, F=1024)
+    assert B.moe_expert_gemm_path(big) == B.GEMM_CUDA_CORES
+    assert B.moe_expert_gemm_path(_cfg(k=0)) < 0
+    # dense fp32 layer of the benchmarks: R = 8192, D = 512, F = 1024, E = 8
+    dense = _cfg(T=4096, k=2, E=8, D=512, F=1024, act="gelu_tanh")
+    assert B.moe_expert_gemm_path(dense) == B.GEMM_TENSOR_F32X3
+    R, D, F, E = 8192, 512, 1024, 8
+    want = 12 * (R * F + E * D * F)          # down / dXe: the largest pair
+    assert B.moe_workspace_size(dense) > want
+    # expert-parallel ranks size their own scratch by the rows they received
+    ep = B.moe_ep_config(2, 0, 4096)
+    r, el = 4096, E // 2
+    assert B.moe_ep_f32_scratch_size(dense, ep, r) == max(
+        12 * (r * D + el * F * D), 12 * (r * F + el * D * F),
+        12 * (r * D + r * F) + 256)     # dW: six blocks of rows of both operands, scaled offsets
+    assert B.moe_ep_f32_scratch_size(dense, ep, 4096 * 2 + 1) == 0     # more than T_total k rows
+    assert B.moe_ep_f32_scratch_size(bf, B.moe_ep_config(2, 0, 64), 8) == 0

@@ -1,5 +1,5 @@
 """The ctypes mirrors in the binding must lay out every struct of
-``include/moe.h`` exactly as a C compiler does, and carry the header's enum
+``include/moe.h`` and ``include/moe_ep.h`` exactly as a C compiler does, and carry the header's enum
 values.  A C probe is compiled against the header with the host compiler
 (gcc or cc) and prints each struct's size and each field's offset, and each
 enum constant.  Host code only: no GPU, no CUDA library needed.
@@ -24,6 +24,8 @@ STRUCTS = {
     "moe_weights": B.moe_weights,
     "moe_grads": B.moe_grads,
     "moe_params": B.moe_params,
+    "moe_ep_config": B.moe_ep_config,
+    "moe_ep_rows": B.moe_ep_rows,
 }
 
 ENUMS = {
@@ -43,11 +45,14 @@ ENUMS = {
     "MOE_GROUP_MAX": B.GROUP_SCORE["max"],
     "MOE_F32": B.DTYPE["f32"],
     "MOE_BF16": B.DTYPE["bf16"],
+    "MOE_GEMM_CUDA_CORES": B.GEMM_CUDA_CORES,
+    "MOE_GEMM_TENSOR_BF16": B.GEMM_TENSOR_BF16,
+    "MOE_GEMM_TENSOR_F32X3": B.GEMM_TENSOR_F32X3,
 }
 
 
 def _probe_source() -> str:
-    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe.h"', "int main(void) {"]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe_ep.h"', "int main(void) {"]
     for name, cls in STRUCTS.items():
         lines.append(f'  printf("size {name} %zu\\n", sizeof({name}));')
         for field, ftype in cls._fields_:
