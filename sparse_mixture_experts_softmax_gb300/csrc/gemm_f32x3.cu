@@ -55,42 +55,49 @@ __device__ __forceinline__ int term_of(int side, int b) {
   return side == 0 ? a : bb;
 }
 
-// Four consecutive values -> their term `which` as four packed bf16.
-__device__ __forceinline__ uint2 pack_term(const bf16 (&t)[4][3], int which) {
-  __nv_bfloat162 lo, hi;
-  lo.x = t[0][which];
-  lo.y = t[1][which];
-  hi.x = t[2][which];
-  hi.y = t[3][which];
-  uint2 q;
-  q.x = *reinterpret_cast<uint32_t*>(&lo);
-  q.y = *reinterpret_cast<uint32_t*>(&hi);
-  return q;
+// Eight consecutive values -> their term `which` as eight packed bf16.
+__device__ __forceinline__ uint4 pack_term(const bf16 (&t)[8][3], int which) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h;
+    h.x = t[2 * i][which];
+    h.y = t[2 * i + 1][which];
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ void split4(float4 v, bf16 (&t)[4][3]) {
-  split3(v.x, t[0]);
-  split3(v.y, t[1]);
-  split3(v.z, t[2]);
-  split3(v.w, t[3]);
+// The terms of eight consecutive fp32 values at p (16-byte aligned).
+__device__ __forceinline__ void split8(const float* p, bf16 (&t)[8][3]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  split3(a.x, t[0]);
+  split3(a.y, t[1]);
+  split3(a.z, t[2]);
+  split3(a.w, t[3]);
+  split3(b.x, t[4]);
+  split3(b.y, t[5]);
+  split3(b.z, t[6]);
+  split3(b.w, t[7]);
 }
 
 // Rows of K values (row stride ldx) -> rows of 6K (the blocks side by side).
 __global__ void expand_cols_kernel(const float* __restrict__ X, long long ldx, long long rows, int K,
                                    bf16* __restrict__ Y, int side) {
   pdl_begin();
-  const int kq = K / 4;
+  const int kq = K / 8;
   const long long n = rows * kq;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const long long r = i / kq;
-    const int k = (int)(i - r * kq) * 4;
-    bf16 t[4][3];
-    split4(*reinterpret_cast<const float4*>(X + r * ldx + k), t);
+    const int k = (int)(i - r * kq) * 8;
+    bf16 t[8][3];
+    split8(X + r * ldx + k, t);
     bf16* y = Y + r * 6LL * K + k;
 #pragma unroll
     for (int b = 0; b < 6; ++b)
-      *reinterpret_cast<uint2*>(y + (long long)b * K) = pack_term(t, term_of(side, b));
+      *reinterpret_cast<uint4*>(y + (long long)b * K) = pack_term(t, term_of(side, b));
   }
 }
 
@@ -98,19 +105,19 @@ __global__ void expand_cols_kernel(const float* __restrict__ X, long long ldx, l
 __global__ void expand_rows_kernel(const float* __restrict__ X, long long E, int K, int N,
                                    bf16* __restrict__ Y, int side) {
   pdl_begin();
-  const int nq = N / 4;
+  const int nq = N / 8;
   const long long n = E * K * (long long)nq;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const long long row = i / nq;          // e * K + k
-    const int c = (int)(i - row * nq) * 4;
+    const int c = (int)(i - row * nq) * 8;
     const long long e = row / K;
     const int k = (int)(row - e * K);
-    bf16 t[4][3];
-    split4(*reinterpret_cast<const float4*>(X + row * N + c), t);
+    bf16 t[8][3];
+    split8(X + row * N + c, t);
 #pragma unroll
     for (int b = 0; b < 6; ++b)
-      *reinterpret_cast<uint2*>(Y + ((e * 6 + b) * K + k) * N + c) = pack_term(t, term_of(side, b));
+      *reinterpret_cast<uint4*>(Y + ((e * 6 + b) * K + k) * N + c) = pack_term(t, term_of(side, b));
   }
 }
 
@@ -121,25 +128,25 @@ __global__ void expand_segments_kernel(const float* __restrict__ X, long long ld
                                        const int* __restrict__ offsets, int E,
                                        bf16* __restrict__ Y, int side) {
   pdl_begin();
-  const int mq = M / 4;
+  const int mq = M / 8;
   const long long n = R * mq;
   const int end = offsets[E];
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const long long r = i / mq;
     if (r >= end) continue;
-    const int c = (int)(i - r * mq) * 4;
+    const int c = (int)(i - r * mq) * 8;
     int lo = 0, hi = E;   // the segment holding r: largest e with offsets[e] <= r
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (offsets[mid] <= r) lo = mid; else hi = mid;
     }
     const long long o = offsets[lo], rows = offsets[lo + 1] - o, j = r - o;
-    bf16 t[4][3];
-    split4(*reinterpret_cast<const float4*>(X + r * ldx + c), t);
+    bf16 t[8][3];
+    split8(X + r * ldx + c, t);
 #pragma unroll
     for (int b = 0; b < 6; ++b)
-      *reinterpret_cast<uint2*>(Y + (6 * o + b * rows + j) * M + c) = pack_term(t, term_of(side, b));
+      *reinterpret_cast<uint4*>(Y + (6 * o + b * rows + j) * M + c) = pack_term(t, term_of(side, b));
   }
 }
 
@@ -220,15 +227,15 @@ cudaError_t launch_gemm_f32x3(const GemmArgs& g, void* scratch, size_t scratch_b
   t.epi = EPI_STORE;
   if (g.ragged_k) {
     // weight gradient: A [R, M], B [R, N], segments of rows
-    if (g.lda % 4 || g.ldb % 4 || g.M % 4 || g.N % 4) return cudaErrorNotSupported;
+    if (g.lda % 4 || g.ldb % 4 || g.M % 8 || g.N % 8) return cudaErrorNotSupported;
     const long long R = g.K0;
     bf16* A = reinterpret_cast<bf16*>(take((size_t)6 * R * g.M * 2));
     bf16* B = reinterpret_cast<bf16*>(take((size_t)6 * R * g.N * 2));
     int* off6 = reinterpret_cast<int*>(take((size_t)(g.E + 1) * 4));
     MOE_LAUNCH_N(launch_pdl(scale_offsets_kernel, dim3(1), dim3(256), 0, st, g.offsets, g.E + 1, off6));
-    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.M / 4))), dim3(256), 0, st,
+    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.M / 8))), dim3(256), 0, st,
                           static_cast<const float*>(g.A0), g.lda, R, g.M, g.offsets, g.E, A, 0));
-    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.N / 4))), dim3(256), 0, st,
+    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.N / 8))), dim3(256), 0, st,
                           static_cast<const float*>(g.B0), g.ldb, R, g.N, g.offsets, g.E, B, 1));
     t.A0 = A;
     t.lda = g.M;
@@ -250,17 +257,17 @@ cudaError_t launch_gemm_f32x3(const GemmArgs& g, void* scratch, size_t scratch_b
     const float* Aq = static_cast<const float*>(q == 0 ? g.A0 : g.A1);
     const float* Bq = static_cast<const float*>(q == 0 ? g.B0 : g.B1);
     const long long ldb_want = g.b_kcontig ? K : g.N;
-    if (K % 4 || g.lda % 4 || g.N % 8 || g.ldb != ldb_want || g.sBe != (long long)g.N * K)
+    if (K % 8 || g.lda % 4 || g.N % 8 || g.ldb != ldb_want || g.sBe != (long long)g.N * K)
       return cudaErrorNotSupported;
     bf16* A = reinterpret_cast<bf16*>(take((size_t)g.M * 6 * K * 2));
     bf16* B = reinterpret_cast<bf16*>(take((size_t)g.E * g.N * 6 * K * 2));
-    MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.M * (K / 4))), dim3(256), 0,
+    MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.M * (K / 8))), dim3(256), 0,
                           st, Aq, g.lda, (long long)g.M, K, A, 0));
     if (g.b_kcontig)
-      MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.E * g.N * (K / 4))),
+      MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.E * g.N * (K / 8))),
                             dim3(256), 0, st, Bq, (long long)K, (long long)g.E * g.N, K, B, 1));
     else
-      MOE_LAUNCH_N(launch_pdl(expand_rows_kernel, dim3(grid_of((long long)g.E * K * (g.N / 4))),
+      MOE_LAUNCH_N(launch_pdl(expand_rows_kernel, dim3(grid_of((long long)g.E * K * (g.N / 8))),
                             dim3(256), 0, st, Bq, (long long)g.E, K, g.N, B, 1));
     if (q == 0) {
       t.A0 = A;
