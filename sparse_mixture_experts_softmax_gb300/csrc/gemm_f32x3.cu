@@ -11,7 +11,10 @@
 // each exact in fp32 (8 x 8 significant bits); the three left out are below
 // 2^-26 of |a b|.  The six products of a dot product over K become one bf16
 // GEMM over 6 K: the A side lays its terms out along the reduction as
-// [a1 a1 a2 a1 a2 a3], the B side as [b1 b2 b1 b3 b2 b1].  So the
+// [a3 a2 a1 a2 a1 a1], the B side as [b1 b2 b3 b1 b2 b1], the smallest
+// products first: the tensor cores' fp32 accumulation rounds more coarsely
+// than IEEE additions, and with a1 b1 last the partial sums stay small while
+// the other five blocks are added.  So the
 // tensor-core grouped GEMM (gemm_tc.cu) runs unchanged on operands expanded
 // here:
 //   ragged M, A [M, K] K-major          -> A' [M, 6K]
@@ -49,9 +52,9 @@ __device__ __forceinline__ void split3(float x, bf16 (&t)[3]) {
 
 // Term index of reduction block b (0..5) on side A (0) or B (1).
 __device__ __forceinline__ int term_of(int side, int b) {
-  // A: 1 1 2 1 2 3    B: 1 2 1 3 2 1   (0-based below)
-  const int a = (0x210100 >> (4 * b)) & 0xF;
-  const int bb = (0x012010 >> (4 * b)) & 0xF;
+  // A: 3 2 1 2 1 1    B: 1 2 3 1 2 1   (0-based below, nibble b)
+  const int a = (0x001012 >> (4 * b)) & 0xF;
+  const int bb = (0x010210 >> (4 * b)) & 0xF;
   return side == 0 ? a : bb;
 }
 

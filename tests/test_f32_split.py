@@ -4,8 +4,8 @@
 
 * the three bf16 terms of an fp32 value are exact differences and hold the
   value to 2^-24 of its magnitude;
-* the reduction over six K blocks laid out as A' = [a1 a1 a2 a1 a2 a3],
-  B' = [b1 b2 b1 b3 b2 b1] gives the fp32 operands' dot product to a few
+* the reduction over six K blocks laid out as A' = [a3 a2 a1 a2 a1 a1],
+  B' = [b1 b2 b3 b1 b2 b1] gives the fp32 operands' dot product to a few
   2^-24 of sum |a b| (the three dropped term products are below 2^-26 of
   |a b| each), far inside the fp32 layers' 1e-4 tolerance, while the plain
   bf16 product (one block) misses it by ~1e-3;
@@ -16,8 +16,8 @@
 import numpy as np
 import torch
 
-A_TERMS = [0, 0, 1, 0, 1, 2]
-B_TERMS = [0, 1, 0, 2, 1, 0]
+A_TERMS = [2, 1, 0, 1, 0, 0]      # a3 a2 a1 a2 a1 a1: smallest products first
+B_TERMS = [0, 1, 2, 0, 1, 0]      # b1 b2 b3 b1 b2 b1
 
 
 def _terms(x: torch.Tensor):
@@ -68,9 +68,9 @@ def test_wrong_pairing_is_detected():
     b = torch.randn(16, 256, generator=g)
     exact = (a.double() * b.double()).sum(-1)
     scale = (a.double() * b.double()).abs().sum(-1)
-    # (swapping the first two B blocks is not a mistake: A's first two blocks
-    # are both a1, so the same six products are formed)
-    for bad_b in ([0, 1, 0, 2, 1, 1], [0, 1, 0, 2, 2, 0], [0, 1, 1, 2, 1, 0], [0, 0, 1, 2, 1, 0]):
+    # (swapping B's last two blocks would not be a mistake: A's last two
+    # blocks are both a1, so the same six products are formed)
+    for bad_b in ([0, 1, 2, 0, 1, 1], [0, 1, 2, 0, 2, 0], [0, 2, 2, 0, 1, 0], [1, 1, 2, 0, 1, 0]):
         B = _expand(b, bad_b).double()
         wrong = (_expand(a, A_TERMS).double() * B).sum(-1)
         assert torch.max((wrong - exact).abs() / scale) > 4 * 2.0 ** -24, bad_b
