@@ -411,11 +411,13 @@ def test_all_routing_options_together():
     assert int((layer.routing()["slot_of"] < 0).sum().item()) > 0
 
 
-def test_cuda_graph_replay_matches_eager():
+@pytest.mark.parametrize("name", ["dense_bf16", "dense_f32"])
+def test_cuda_graph_replay_matches_eager(name):
     """After one eager call, a training step captures into a CUDA graph (no
     host synchronisation or allocation inside); three replays give the same
-    bits as three eager steps."""
-    wl = W.WORKLOADS["dense_bf16"].with_tokens(1000)
+    bits as three eager steps (the fp32 layer with its GEMMs on the tensor
+    cores through the three-term split, the operand expansion included)."""
+    wl = W.WORKLOADS[name].with_tokens(1000)
     inp = W.make_inputs(wl, seed=8)
     a = make_layer(wl, inp)
     b = make_layer(wl, inp)
@@ -455,8 +457,17 @@ def test_wide_routing_bf16(E, k, T):
     assert max(errs.values()) <= 2e-2
 
 
-def test_empty_tokens():
+# tiny: CUDA-core GEMMs; the 256 x 256 fp32 layer: the tensor-core path
+# through the three-term split
+SPLIT_F32 = dict(D=256, F=256, act="gelu_tanh")
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_empty_tokens(split):
+    import dataclasses
     wl = W.WORKLOADS["tiny"]
+    if split:
+        wl = dataclasses.replace(wl, **SPLIT_F32)
     inp = W.make_inputs(wl, seed=0)
     layer = make_layer(wl.with_tokens(0), {**inp, "x": inp["x"][:0], "target": inp["target"][:0]})
     x = torch.empty(0, wl.D, device="cuda")
@@ -467,12 +478,14 @@ def test_empty_tokens():
     assert torch.all(layer.dw1 == 0)
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("T,k,E", [(1, 1, 1), (1, 2, 4), (37, 4, 4), (130, 1, 3)])
-def test_edge_shapes(T, k, E):
-    """Single token, single expert, k = E, odd token counts."""
+def test_edge_shapes(T, k, E, split):
+    """Single token, single expert, k = E, odd token counts; on the CUDA-core
+    GEMMs and on the tensor-core path of fp32 layers."""
     base = W.WORKLOADS["tiny"]
     import dataclasses
-    wl = dataclasses.replace(base, T=T, k=k, E=E)
+    wl = dataclasses.replace(base, T=T, k=k, E=E, **(SPLIT_F32 if split else {}))
     errs, _, _ = _one_step_parity(wl, seed=11)
     assert max(errs.values()) <= 1e-4
 
