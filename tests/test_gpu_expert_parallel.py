@@ -40,6 +40,10 @@ CASES = {
     # fp32 GELU experts with biases, two ranks
     "gelu_f32_g2": (dataclasses.replace(W.WORKLOADS["dense_f32"], name="ep_gelu", T=769),
                     (640, 129), True),
+    # fp32 SwiGLU experts (GEMMs through the three-term split on the tensor
+    # cores, two-pair dXe included), two ranks
+    "swiglu_f32_g2": (dataclasses.replace(W.WORKLOADS["dense_f32"], name="ep_swiglu_f32",
+                                          act="swiglu", has_bias=False, T=500), (300, 200), True),
     # grouped sigmoid routing over eight ranks (8 local experts each)
     "grouped_bf16_g8": (dataclasses.replace(W.WORKLOADS["grouped"], name="ep_grouped", D=256,
                                             F=128, T=900),

@@ -462,6 +462,18 @@ def test_wide_routing_bf16(E, k, T):
 SPLIT_F32 = dict(D=256, F=256, act="gelu_tanh")
 
 
+def test_swiglu_f32_split_step():
+    """An fp32 SwiGLU layer wide enough for the tensor-core path: H1 = X W1^T,
+    dXe over both pairs (dH1 W1 + dH3 W3) and the weight gradients through the
+    three-term split; the W3 product with the SwiGLU epilogue and the SwiGLU
+    backward on the CUDA cores."""
+    import dataclasses
+    wl = dataclasses.replace(W.WORKLOADS["tiny"], name="swiglu_f32_split", T=300, D=256, F=512,
+                             E=8, k=2, act="swiglu", has_bias=False)
+    errs, _, _ = _one_step_parity(wl, seed=17)
+    assert max(errs.values()) <= 1e-4
+
+
 @pytest.mark.parametrize("split", [False, True])
 def test_empty_tokens(split):
     import dataclasses
