@@ -50,12 +50,12 @@ __device__ __forceinline__ void split3(float x, bf16 (&t)[3]) {
   t[2] = __float2bfloat16_rn(r2);
 }
 
-// Term index of reduction block b (0..5) on side A (0) or B (1).
-__device__ __forceinline__ int term_of(int side, int b) {
+// Term index of reduction block b (0..5) on side A (0) or B (1); constant
+// once the block loop is unrolled, so the terms stay in registers.
+template <int SIDE>
+__device__ __forceinline__ constexpr int term_of(int b) {
   // A: 3 2 1 2 1 1    B: 1 2 3 1 2 1   (0-based below, nibble b)
-  const int a = (0x001012 >> (4 * b)) & 0xF;
-  const int bb = (0x010210 >> (4 * b)) & 0xF;
-  return side == 0 ? a : bb;
+  return ((SIDE == 0 ? 0x001012 : 0x010210) >> (4 * b)) & 0xF;
 }
 
 // Eight consecutive values -> their term `which` as eight packed bf16.
@@ -85,72 +85,80 @@ __device__ __forceinline__ void split8(const float* p, bf16 (&t)[8][3]) {
   split3(b.w, t[7]);
 }
 
-// Rows of K values (row stride ldx) -> rows of 6K (the blocks side by side).
-__global__ void expand_cols_kernel(const float* __restrict__ X, long long ldx, long long rows, int K,
-                                   bf16* __restrict__ Y, int side) {
-  pdl_begin();
-  const int kq = K / 8;
-  const long long n = rows * kq;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long r = i / kq;
-    const int k = (int)(i - r * kq) * 8;
-    bf16 t[8][3];
-    split8(X + r * ldx + k, t);
-    bf16* y = Y + r * 6LL * K + k;
-#pragma unroll
-    for (int b = 0; b < 6; ++b)
-      *reinterpret_cast<uint4*>(y + (long long)b * K) = pack_term(t, term_of(side, b));
-  }
-}
+// One operand's expansion.  kind 0: rows of K values (row stride ldx) ->
+// rows of 6K, the blocks side by side.  kind 1: [E][K][N] (row stride N) ->
+// [E][6K][N], the six K blocks one below the other.  kind 2: row segments
+// [R][M] (row stride ldx, segment e = rows [o_e, o_e+1)) -> [6R][M], segment
+// e's six blocks of its rows starting at row 6 o_e; rows past o_E belong to
+// no segment and are not written.  Eight values per work item.
+struct ExpandJob {
+  const float* X;
+  long long ldx;
+  long long rows;        // kind 0: rows; kind 1: E; kind 2: R
+  int K;                 // kind 0 and 1: reduction length; kind 2: M (row length)
+  int N;                 // kind 1: row length
+  const int* offsets;    // kind 2: [E + 1]
+  int E;
+  bf16* Y;
+  int kind;
+  long long items;       // eight-value work items
+  int blocks;            // blocks of the launch given to this job
+};
 
-// [E][K][N] (row stride N) -> [E][6K][N]: the six K blocks one below the other.
-__global__ void expand_rows_kernel(const float* __restrict__ X, long long E, int K, int N,
-                                   bf16* __restrict__ Y, int side) {
-  pdl_begin();
-  const int nq = N / 8;
-  const long long n = E * K * (long long)nq;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / nq;          // e * K + k
-    const int c = (int)(i - row * nq) * 8;
-    const long long e = row / K;
-    const int k = (int)(row - e * K);
+template <int SIDE>
+__device__ __forceinline__ void run_job(const ExpandJob& j, long long first, long long stride) {
+  const int end = j.kind == 2 ? j.offsets[j.E] : 0;
+  for (long long i = first; i < j.items; i += stride) {
     bf16 t[8][3];
-    split8(X + row * N + c, t);
+    if (j.kind == 0) {
+      const int kq = j.K / 8;
+      const long long r = i / kq;
+      const int k = (int)(i - r * kq) * 8;
+      split8(j.X + r * j.ldx + k, t);
+      bf16* y = j.Y + r * 6LL * j.K + k;
 #pragma unroll
-    for (int b = 0; b < 6; ++b)
-      *reinterpret_cast<uint4*>(Y + ((e * 6 + b) * K + k) * N + c) = pack_term(t, term_of(side, b));
-  }
-}
-
-// Row segments [R][M] (row stride ldx, segment e = rows [o_e, o_e+1)) ->
-// [6R][M]: segment e's six blocks of its rows starting at row 6 o_e.  Rows
-// past o_E belong to no segment and are not written.
-__global__ void expand_segments_kernel(const float* __restrict__ X, long long ldx, long long R, int M,
-                                       const int* __restrict__ offsets, int E,
-                                       bf16* __restrict__ Y, int side) {
-  pdl_begin();
-  const int mq = M / 8;
-  const long long n = R * mq;
-  const int end = offsets[E];
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long r = i / mq;
-    if (r >= end) continue;
-    const int c = (int)(i - r * mq) * 8;
-    int lo = 0, hi = E;   // the segment holding r: largest e with offsets[e] <= r
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (offsets[mid] <= r) lo = mid; else hi = mid;
+      for (int b = 0; b < 6; ++b)
+        *reinterpret_cast<uint4*>(y + (long long)b * j.K) = pack_term(t, term_of<SIDE>(b));
+    } else if (j.kind == 1) {
+      const int nq = j.N / 8;
+      const long long row = i / nq;          // e * K + k
+      const int c = (int)(i - row * nq) * 8;
+      const long long e = row / j.K;
+      const int k = (int)(row - e * j.K);
+      split8(j.X + row * j.N + c, t);
+#pragma unroll
+      for (int b = 0; b < 6; ++b)
+        *reinterpret_cast<uint4*>(j.Y + ((e * 6 + b) * j.K + k) * j.N + c) =
+            pack_term(t, term_of<SIDE>(b));
+    } else {
+      const int M = j.K, mq = M / 8;
+      const long long r = i / mq;
+      if (r >= end) continue;
+      const int c = (int)(i - r * mq) * 8;
+      int lo = 0, hi = j.E;   // the segment holding r: largest e with offsets[e] <= r
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (j.offsets[mid] <= r) lo = mid; else hi = mid;
+      }
+      const long long o = j.offsets[lo], rows = j.offsets[lo + 1] - o, jr = r - o;
+      split8(j.X + r * j.ldx + c, t);
+#pragma unroll
+      for (int b = 0; b < 6; ++b)
+        *reinterpret_cast<uint4*>(j.Y + (6 * o + b * rows + jr) * M + c) =
+            pack_term(t, term_of<SIDE>(b));
     }
-    const long long o = offsets[lo], rows = offsets[lo + 1] - o, j = r - o;
-    bf16 t[8][3];
-    split8(X + r * ldx + c, t);
-#pragma unroll
-    for (int b = 0; b < 6; ++b)
-      *reinterpret_cast<uint4*>(Y + (6 * o + b * rows + j) * M + c) = pack_term(t, term_of(side, b));
   }
+}
+
+// A GEMM's two operand expansions in one launch: blocks [0, a.blocks) take
+// job a (side A), the rest job b (side B).
+__global__ void expand_pair_kernel(const ExpandJob a, const ExpandJob b) {
+  pdl_begin();
+  if ((int)blockIdx.x < a.blocks)
+    run_job<0>(a, (long long)blockIdx.x * blockDim.x + threadIdx.x, (long long)a.blocks * blockDim.x);
+  else
+    run_job<1>(b, (long long)(blockIdx.x - a.blocks) * blockDim.x + threadIdx.x,
+            (long long)b.blocks * blockDim.x);
 }
 
 __global__ void scale_offsets_kernel(const int* __restrict__ in, int n, int* __restrict__ out) {
@@ -190,6 +198,14 @@ __global__ void act_bwd_kernel(float* __restrict__ dA, const float* __restrict__
 int grid_of(long long n) {
   const long long b = (n + 255) / 256;
   return (int)(b < 152 * 16 ? (b < 1 ? 1 : b) : 152 * 16);
+}
+
+ExpandJob job(int kind, const void* X, long long ldx, long long rows, int K, int N,
+              const int* offsets, int E, bf16* Y) {
+  ExpandJob j{static_cast<const float*>(X), ldx, rows, K, N, offsets, E, Y, kind, 0, 0};
+  j.items = kind == 0 ? rows * (K / 8) : kind == 1 ? rows * K * (long long)(N / 8) : rows * (K / 8);
+  j.blocks = grid_of(j.items);
+  return j;
 }
 
 size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -236,10 +252,9 @@ cudaError_t launch_gemm_f32x3(const GemmArgs& g, void* scratch, size_t scratch_b
     bf16* B = reinterpret_cast<bf16*>(take((size_t)6 * R * g.N * 2));
     int* off6 = reinterpret_cast<int*>(take((size_t)(g.E + 1) * 4));
     MOE_LAUNCH_N(launch_pdl(scale_offsets_kernel, dim3(1), dim3(256), 0, st, g.offsets, g.E + 1, off6));
-    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.M / 8))), dim3(256), 0, st,
-                          static_cast<const float*>(g.A0), g.lda, R, g.M, g.offsets, g.E, A, 0));
-    MOE_LAUNCH_N(launch_pdl(expand_segments_kernel, dim3(grid_of(R * (g.N / 8))), dim3(256), 0, st,
-                          static_cast<const float*>(g.B0), g.ldb, R, g.N, g.offsets, g.E, B, 1));
+    const ExpandJob ja = job(2, g.A0, g.lda, R, g.M, 0, g.offsets, g.E, A);
+    const ExpandJob jb = job(2, g.B0, g.ldb, R, g.N, 0, g.offsets, g.E, B);
+    MOE_LAUNCH_N(launch_pdl(expand_pair_kernel, dim3(ja.blocks + jb.blocks), dim3(256), 0, st, ja, jb));
     t.A0 = A;
     t.lda = g.M;
     t.B0 = B;
@@ -264,14 +279,10 @@ cudaError_t launch_gemm_f32x3(const GemmArgs& g, void* scratch, size_t scratch_b
       return cudaErrorNotSupported;
     bf16* A = reinterpret_cast<bf16*>(take((size_t)g.M * 6 * K * 2));
     bf16* B = reinterpret_cast<bf16*>(take((size_t)g.E * g.N * 6 * K * 2));
-    MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.M * (K / 8))), dim3(256), 0,
-                          st, Aq, g.lda, (long long)g.M, K, A, 0));
-    if (g.b_kcontig)
-      MOE_LAUNCH_N(launch_pdl(expand_cols_kernel, dim3(grid_of((long long)g.E * g.N * (K / 8))),
-                            dim3(256), 0, st, Bq, (long long)K, (long long)g.E * g.N, K, B, 1));
-    else
-      MOE_LAUNCH_N(launch_pdl(expand_rows_kernel, dim3(grid_of((long long)g.E * K * (g.N / 8))),
-                            dim3(256), 0, st, Bq, (long long)g.E, K, g.N, B, 1));
+    const ExpandJob ja = job(0, Aq, g.lda, g.M, K, 0, nullptr, 0, A);
+    const ExpandJob jb = g.b_kcontig ? job(0, Bq, K, (long long)g.E * g.N, K, 0, nullptr, 0, B)
+                                     : job(1, Bq, g.N, g.E, K, g.N, nullptr, 0, B);
+    MOE_LAUNCH_N(launch_pdl(expand_pair_kernel, dim3(ja.blocks + jb.blocks), dim3(256), 0, st, ja, jb));
     if (q == 0) {
       t.A0 = A;
       t.B0 = B;
