@@ -1,6 +1,8 @@
 // Token dispatch and combine (course "Trainable MoE in CUDA", Part 4), the
 // losses (Parts 6 and 7) and the SGD update (Part 7).  No floating-point
 // atomics: every reduction has a fixed order, so results are bit-reproducible.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -517,28 +519,82 @@ scatter_back_add_kernel(float* __restrict__ dx, const T* __restrict__ dxe,
   }
 }
 
-// out[e, n] = sum over rows of segment e of src[r, n] (fixed order), for db.
-template <typename T>
-__global__ void __launch_bounds__(256)
+// out[e, n] = sum over rows of segment e of src[r, n], for db.  A cluster of
+// CS_SPLIT CTAs shares one column block of one segment: CTA z sums rows
+// [lo + n z / S, lo + n (z+1) / S) (8 warps, rows w, w+8, ... with four
+// accumulators per thread), the warps' sums are added in warp order, and CTA
+// 0 adds the CTAs' sums in rank order through distributed shared memory.
+// The order depends on the segment's rows alone, so a segment gives the same
+// bits wherever it sits.  VEC: one 16-byte load per row for the thread's
+// V = 16 / sizeof(T) columns (N a multiple of V, src 16-byte aligned).
+constexpr int CS_SPLIT = 8;
+template <typename T, bool VEC>
+__global__ void __cluster_dims__(1, 1, CS_SPLIT) __launch_bounds__(256)
 segment_colsum_kernel(const T* __restrict__ src, const int* __restrict__ offsets, int N,
                       float* __restrict__ out) {
   pdl_begin();
-  __shared__ float part[8][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  namespace cg = cooperative_groups;
+  constexpr int V = 16 / (int)sizeof(T), COLS = 32 * V;
+  __shared__ float part[8][COLS];
+  __shared__ float csum[COLS];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int e = blockIdx.y;
-  const int n = blockIdx.x * 32 + tx;
-  const int lo = offsets[e], hi = offsets[e + 1];
-  float s = 0.f;
-  if (n < N)
-    for (int r = lo + ty; r < hi; r += 8) s += to_f(src[(size_t)r * N + n]);
-  part[ty][tx] = s;
-  __syncthreads();
-  if (ty == 0 && n < N) {
-    float acc = 0.f;
+  const int z = (int)blockIdx.z;   // the cluster spans z: z is the CTA's rank in it
+  const int c0 = blockIdx.x * COLS + lane * V;
+  const int lo = offsets[e], n = offsets[e + 1] - lo;
+  const int r0 = lo + (int)((long long)n * z / CS_SPLIT);
+  const int r1 = lo + (int)((long long)n * (z + 1) / CS_SPLIT);
+
+  float acc[4][V];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc += part[i][tx];
-    out[(size_t)e * N + n] = acc;
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[j][v] = 0.f;
+  auto add_row = [&](float (&a)[V], int r) {
+    const T* p = src + (size_t)r * N + c0;
+    if (VEC) {
+      const uint4 q = *reinterpret_cast<const uint4*>(p);
+      const T* h = reinterpret_cast<const T*>(&q);
+#pragma unroll
+      for (int v = 0; v < V; ++v) a[v] += to_f(h[v]);
+    } else {
+#pragma unroll
+      for (int v = 0; v < V; ++v)
+        if (c0 + v < N) a[v] += to_f(p[v]);
+    }
+  };
+  if (c0 < N) {
+    int r = r0 + w;
+    for (; r + 24 < r1; r += 32) {
+      add_row(acc[0], r);
+      add_row(acc[1], r + 8);
+      add_row(acc[2], r + 16);
+      add_row(acc[3], r + 24);
+    }
+    for (; r < r1; r += 8) add_row(acc[0], r);
   }
+#pragma unroll
+  for (int v = 0; v < V; ++v) part[w][lane * V + v] = (acc[0][v] + acc[1][v]) + (acc[2][v] + acc[3][v]);
+  __syncthreads();
+  for (int c = threadIdx.x; c < COLS; c += blockDim.x) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += part[i][c];
+    csum[c] = s;
+  }
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();   // every CTA's csum is complete
+  if (z == 0) {
+    for (int c = threadIdx.x; c < COLS; c += blockDim.x) {
+      const int col = blockIdx.x * COLS + c;
+      if (col >= N) continue;
+      float s = 0.f;
+#pragma unroll
+      for (int q = 0; q < CS_SPLIT; ++q) s += cluster.map_shared_rank(csum, q)[c];
+      out[(size_t)e * N + col] = s;
+    }
+  }
+  cluster.sync();   // the other CTAs keep their shared memory until CTA 0 has read it
 }
 
 __global__ void __launch_bounds__(256)
@@ -740,12 +796,23 @@ cudaError_t launch_scatter_back_add(int dtype, float* dx, const void* dxe, const
 
 cudaError_t launch_segment_colsum(int dtype, const void* src, const int* offsets, int E, int N,
                                   float* out, cudaStream_t st) {
-  dim3 grid((N + 31) / 32, E);
-  if (dtype == 1)
-    MOE_LAUNCH(launch_pdl(segment_colsum_kernel<bf16>, dim3(grid), dim3(256), 0, st, static_cast<const bf16*>(src), offsets, N, out));
-  else
-    MOE_LAUNCH(launch_pdl(segment_colsum_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<const float*>(src), offsets, N,
-                                                       out));
+  if (E == 0 || N == 0) return cudaSuccess;
+  const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  if (dtype == 1) {
+    const dim3 grid((N + 255) / 256, E, CS_SPLIT);
+    const bf16* s = static_cast<const bf16*>(src);
+    if (aligned && N % 8 == 0)
+      MOE_LAUNCH(launch_pdl(segment_colsum_kernel<bf16, true>, grid, dim3(256), 0, st, s, offsets, N, out));
+    else
+      MOE_LAUNCH(launch_pdl(segment_colsum_kernel<bf16, false>, grid, dim3(256), 0, st, s, offsets, N, out));
+  } else {
+    const dim3 grid((N + 127) / 128, E, CS_SPLIT);
+    const float* s = static_cast<const float*>(src);
+    if (aligned && N % 4 == 0)
+      MOE_LAUNCH(launch_pdl(segment_colsum_kernel<float, true>, grid, dim3(256), 0, st, s, offsets, N, out));
+    else
+      MOE_LAUNCH(launch_pdl(segment_colsum_kernel<float, false>, grid, dim3(256), 0, st, s, offsets, N, out));
+  }
   return cudaGetLastError();
 }
 

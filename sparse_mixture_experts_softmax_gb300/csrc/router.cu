@@ -11,15 +11,22 @@ namespace moe {
 
 namespace {
 
-constexpr int RT_TOK = 64;    // tokens per block
+// Tokens per block: 64, or 16 when 64-token blocks would not fill two
+// blocks per SM (152 SMs), so that short batches still spread over the GPU.
+constexpr int RT_TOK = 64;
+constexpr int RT_TOK_SMALL = 16;
 constexpr int RT_BK = 32;     // D chunk staged in shared memory
 constexpr int RT_THREADS = 256;
 
-template <int NJ>
+__host__ __device__ constexpr int router_tok_per_block(int T) {
+  return T >= RT_TOK * 2 * 152 ? RT_TOK : RT_TOK_SMALL;
+}
+
+template <int NJ, int TB>
 struct RouterSmem {
   static constexpr int EP = 16 * NJ;
-  static constexpr int stage_floats = RT_BK * (RT_TOK + 1) + RT_BK * (EP + 1);
-  static constexpr int logit_floats = RT_TOK * (EP + 1);
+  static constexpr int stage_floats = RT_BK * (TB + 1) + RT_BK * (EP + 1);
+  static constexpr int logit_floats = TB * (EP + 1);
   static constexpr int main_floats = stage_floats > logit_floats ? stage_floats : logit_floats;
   static constexpr size_t bytes = sizeof(float) * (size_t)(main_floats + (RT_THREADS / 32) * EP);
 };
@@ -66,9 +73,10 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
   return c;
 }
 
-// Logits for RT_TOK tokens x E_pad experts (E_pad = 16*NJ), then one warp per
-// token for score, selection and renormalisation.
-template <typename XT, int NJ>
+// Logits for TB tokens x E_pad experts (E_pad = 16*NJ), then one warp per
+// token for score, selection and renormalisation.  Each logit is one fp32
+// accumulation over d in ascending order, whatever TB is.
+template <typename XT, int NJ, int TB>
 __global__ void __launch_bounds__(RT_THREADS)
 router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
                   const float* __restrict__ logit_bias, RouterArgs a,
@@ -77,51 +85,71 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
   pdl_begin();
   constexpr int EP = 16 * NJ;
   constexpr int NC = (EP + 31) / 32;   // scores per lane
+  constexpr int TI = TB / 16;          // tokens per thread in the logits tile
+  constexpr int XPT = TB * RT_BK / RT_THREADS, WPT = EP * RT_BK / RT_THREADS;
+  static_assert(TB % 16 == 0 && XPT * RT_THREADS == TB * RT_BK && WPT * RT_THREADS == EP * RT_BK,
+                "staging splits evenly over the threads");
   // dynamic shared memory: the logits tile ls aliases the staging tiles xs/ws
   extern __shared__ __align__(16) float rsm[];
-  float(*xs)[RT_TOK + 1] = reinterpret_cast<float(*)[RT_TOK + 1]>(rsm);
-  float(*ws)[EP + 1] = reinterpret_cast<float(*)[EP + 1]>(rsm + RT_BK * (RT_TOK + 1));
+  float(*xs)[TB + 1] = reinterpret_cast<float(*)[TB + 1]>(rsm);
+  float(*ws)[EP + 1] = reinterpret_cast<float(*)[EP + 1]>(rsm + RT_BK * (TB + 1));
   float(*ls)[EP + 1] = reinterpret_cast<float(*)[EP + 1]>(rsm);
-  float(*wsum)[EP] = reinterpret_cast<float(*)[EP]>(rsm + RouterSmem<NJ>::main_floats);
+  float(*wsum)[EP] = reinterpret_cast<float(*)[EP]>(rsm + RouterSmem<NJ, TB>::main_floats);
 
   const int T = a.T, D = a.D, E = a.E;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int t0 = blockIdx.x * RT_TOK;
+  const int t0 = blockIdx.x * TB;
 
-  float acc[4][NJ];
+  float acc[TI][NJ];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < TI; ++i)
 #pragma unroll
     for (int j = 0; j < NJ; ++j) acc[i][j] = 0.f;
 
-  for (int d0 = 0; d0 < D; d0 += RT_BK) {
-    for (int l = tid; l < RT_TOK * RT_BK; l += RT_THREADS) {
-      int tk = l / RT_BK, dd = l % RT_BK;
-      int t = t0 + tk, d = d0 + dd;
-      xs[dd][tk] = (t < T && d < D) ? to_f(x[(size_t)t * D + d]) : 0.f;
+  // the next D chunk is read into registers while the current one is used
+  float xr[XPT], wr[WPT];
+  auto fetch = [&](int d0) {
+#pragma unroll
+    for (int u = 0; u < XPT; ++u) {
+      const int l = tid + u * RT_THREADS, tk = l / RT_BK, d = d0 + l % RT_BK, t = t0 + tk;
+      xr[u] = (t < T && d < D) ? to_f(x[(size_t)t * D + d]) : 0.f;
     }
-    for (int l = tid; l < EP * RT_BK; l += RT_THREADS) {
-      int e = l / RT_BK, dd = l % RT_BK;
-      int d = d0 + dd;
-      ws[dd][e] = (e < E && d < D) ? wg[(size_t)e * D + d] : 0.f;
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const int l = tid + u * RT_THREADS, e = l / RT_BK, d = d0 + l % RT_BK;
+      wr[u] = (e < E && d < D) ? wg[(size_t)e * D + d] : 0.f;
+    }
+  };
+  fetch(0);
+  for (int d0 = 0; d0 < D; d0 += RT_BK) {
+#pragma unroll
+    for (int u = 0; u < XPT; ++u) {
+      const int l = tid + u * RT_THREADS;
+      xs[l % RT_BK][l / RT_BK] = xr[u];
+    }
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const int l = tid + u * RT_THREADS;
+      ws[l % RT_BK][l / RT_BK] = wr[u];
     }
     __syncthreads();
+    if (d0 + RT_BK < D) fetch(d0 + RT_BK);
 #pragma unroll 8
     for (int kk = 0; kk < RT_BK; ++kk) {
-      float av[4], bv[NJ];
+      float av[TI], bv[NJ];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = xs[kk][ty + 16 * i];
+      for (int i = 0; i < TI; ++i) av[i] = xs[kk][ty + 16 * i];
 #pragma unroll
       for (int j = 0; j < NJ; ++j) bv[j] = ws[kk][tx + 16 * j];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < TI; ++i)
 #pragma unroll
         for (int j = 0; j < NJ; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < TI; ++i)
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       int e = tx + 16 * j;
@@ -131,7 +159,7 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
   __syncthreads();
 
   const int warp = tid >> 5, lane = tid & 31;
-  constexpr int TOK_PER_WARP = RT_TOK / (RT_THREADS / 32);
+  constexpr int TOK_PER_WARP = TB / (RT_THREADS / 32);
   float colsum[NC];
 #pragma unroll
   for (int c = 0; c < NC; ++c) colsum[c] = 0.f;
@@ -271,7 +299,7 @@ router_fwd_kernel(const XT* __restrict__ x, const float* __restrict__ wg,
 // layers compute logits = x W_g^T + logit_bias on the tensor cores).  One warp
 // per token; a warp-private shared row serves the group-limited selection.
 // Per-block column sums of the scores feed the aux loss.
-template <int NC>
+template <int NC, int TB>
 __global__ void __launch_bounds__(256)
 router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __restrict__ scores,
                      int* __restrict__ idx, float* __restrict__ gate,
@@ -286,8 +314,8 @@ router_select_kernel(const float* __restrict__ logits, RouterArgs a, float* __re
   float colsum[NC];
 #pragma unroll
   for (int c = 0; c < NC; ++c) colsum[c] = 0.f;
-  for (int tt = 0; tt < RT_TOK / 8; ++tt) {
-    const int t = blockIdx.x * RT_TOK + warp * (RT_TOK / 8) + tt;
+  for (int tt = 0; tt < TB / 8; ++tt) {
+    const int t = blockIdx.x * TB + warp * (TB / 8) + tt;
     if (t >= T) break;
     float s[NC];
     if (a.score == 0) {
@@ -490,20 +518,32 @@ router_bwd_kernel(const float* __restrict__ scores, const int* __restrict__ idx,
 
 }  // namespace
 
-int router_fwd_blocks(int T) { return (T + RT_TOK - 1) / RT_TOK; }
+int router_fwd_blocks(int T) {
+  const int tb = router_tok_per_block(T);
+  return (T + tb - 1) / tb;
+}
+
+template <typename XT, int NJ, int TB>
+static cudaError_t launch_fwd_tb(const void* x, const float* wg, const float* lb,
+                                 const RouterArgs& a, float* scores, int* idx, float* gate,
+                                 float* psum, cudaStream_t st) {
+  dim3 grid((a.T + TB - 1) / TB);
+  const size_t smem = RouterSmem<NJ, TB>::bytes;
+  static std::atomic<unsigned long long> attr_done{0};   // per instantiation and device
+  cudaError_t e = ensure_dynamic_smem(router_fwd_kernel<XT, NJ, TB>, (int)smem, attr_done);
+  if (e != cudaSuccess) return e;
+  MOE_LAUNCH(launch_pdl(router_fwd_kernel<XT, NJ, TB>, dim3(grid), dim3(RT_THREADS), smem, st,
+      static_cast<const XT*>(x), wg, lb, a, scores, idx, gate, psum));
+  return cudaGetLastError();
+}
 
 template <typename XT, int NJ>
 static cudaError_t launch_fwd_nj(const void* x, const float* wg, const float* lb,
                                  const RouterArgs& a, float* scores, int* idx, float* gate,
                                  float* psum, cudaStream_t st) {
-  dim3 grid(router_fwd_blocks(a.T));
-  const size_t smem = RouterSmem<NJ>::bytes;
-  static std::atomic<unsigned long long> attr_done{0};   // per instantiation and device
-  cudaError_t e = ensure_dynamic_smem(router_fwd_kernel<XT, NJ>, (int)smem, attr_done);
-  if (e != cudaSuccess) return e;
-  MOE_LAUNCH(launch_pdl(router_fwd_kernel<XT, NJ>, dim3(grid), dim3(RT_THREADS), smem, st,
-      static_cast<const XT*>(x), wg, lb, a, scores, idx, gate, psum));
-  return cudaGetLastError();
+  if (router_tok_per_block(a.T) == RT_TOK)
+    return launch_fwd_tb<XT, NJ, RT_TOK>(x, wg, lb, a, scores, idx, gate, psum, st);
+  return launch_fwd_tb<XT, NJ, RT_TOK_SMALL>(x, wg, lb, a, scores, idx, gate, psum, st);
 }
 
 template <typename XT>
@@ -539,15 +579,23 @@ cudaError_t launch_router_bwd(const float* scores, const int* idx, const float* 
   return cudaGetLastError();
 }
 
+template <int TB>
+static cudaError_t launch_select_tb(const float* logits, const RouterArgs& a, float* scores, int* idx,
+                                   float* gate, float* psum_partial, cudaStream_t st) {
+  dim3 grid((a.T + TB - 1) / TB);
+  if (a.E <= 32) MOE_LAUNCH(launch_pdl(router_select_kernel<1, TB>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  else if (a.E <= 64) MOE_LAUNCH(launch_pdl(router_select_kernel<2, TB>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  else if (a.E <= 128) MOE_LAUNCH(launch_pdl(router_select_kernel<4, TB>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  else MOE_LAUNCH(launch_pdl(router_select_kernel<8, TB>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_select(const float* logits, const RouterArgs& a, float* scores, int* idx,
                                  float* gate, float* psum_partial, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  dim3 grid(router_fwd_blocks(a.T));
-  if (a.E <= 32) MOE_LAUNCH(launch_pdl(router_select_kernel<1>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
-  else if (a.E <= 64) MOE_LAUNCH(launch_pdl(router_select_kernel<2>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
-  else if (a.E <= 128) MOE_LAUNCH(launch_pdl(router_select_kernel<4>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
-  else MOE_LAUNCH(launch_pdl(router_select_kernel<8>, dim3(grid), dim3(256), 0, st, logits, a, scores, idx, gate, psum_partial));
-  return cudaGetLastError();
+  if (router_tok_per_block(a.T) == RT_TOK)
+    return launch_select_tb<RT_TOK>(logits, a, scores, idx, gate, psum_partial, st);
+  return launch_select_tb<RT_TOK_SMALL>(logits, a, scores, idx, gate, psum_partial, st);
 }
 
 cudaError_t launch_cast_bf16(const float* src, void* dst, long long n, cudaStream_t st) {
