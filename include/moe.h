@@ -186,7 +186,11 @@ typedef struct {
 
 /* Bytes of device workspace the forward / backward / train step need for one
  * configuration: routing state, expert-major activations saved for the
- * backward, and reduction partials.  0 on an invalid configuration. */
+ * backward, and reduction partials.  0 on an invalid configuration.  The size
+ * is not monotone in T (the router's tokens per block and whether an fp32
+ * layer's GEMMs take the tensor-core scratch both depend on it), so a
+ * workspace is sized for the configuration of each call that uses it; a call
+ * given fewer bytes returns MOE_ERR_WORKSPACE_TOO_SMALL. */
 MOE_API size_t moe_workspace_size(const moe_config* cfg);
 
 /* Forward (course Parts 3, 4 and 5): router, dispatch, expert MLPs, combine.
